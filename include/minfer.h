@@ -1,0 +1,221 @@
+/*
+ * minfer.h -- C ABI of the GB300 (sm_103a) prefill library.
+ *
+ * One call, minfer_prefill, runs the prefill forward of a Qwen2-style decoder
+ * over a whole prompt: every token goes through every layer in one pass, K/V
+ * rows land in persistent per-layer regions at the rows named by a positions
+ * buffer, attention is causal (token t sees positions 0..=pos[t]), and only
+ * the last token's logits come back ("09 · Prefill: the first forward",
+ * sections 2.2-2.4; "05 · Graph build — the IR and the builder", section 2.5
+ * node list and section 2.8 tail rows).  Weights are Q8_0 (32 int8 codes and
+ * one fp16 scale per block) and every matmul input activation is quantized
+ * to Q8_0 on the fly (walkthrough index, master table, row "CPU matmul
+ * kernels").
+ *
+ * Conventions
+ *  - Every function returns MINFER_OK (0) or a negative MINFER_ERR_* code;
+ *    minfer_strerror() names it.
+ *  - "host" pointers are ordinary CPU memory, "device" pointers are CUDA
+ *    global memory on the current device.  Pointers are borrowed for the
+ *    duration of the call only, unless stated otherwise.
+ *  - Matrices use the GGUF convention of the pages ("05 · Graph build",
+ *    section 2.4): ne0 is the contiguous (input) dimension, ne1 the number of
+ *    rows (output dimension); memory is row-major [ne1][ne0].
+ *  - Arguments are validated on the host before any device write; a call
+ *    that fails validation leaves the KV regions and the logits untouched.
+ *  - A model and the KV handles made from it belong to the CUDA device that
+ *    was current at minfer_model_create; call them with that device current.
+ *    One call at a time per (model, kv) pair.
+ */
+#ifndef MINFER_H
+#define MINFER_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* ---------------------------------------------------------------- errors */
+#define MINFER_OK 0
+#define MINFER_ERR_ARG (-1)            /* null pointer, bad size, duplicate position */
+#define MINFER_ERR_POS_OOB (-2)        /* a position < 0 or >= the KV region's n_ctx */
+#define MINFER_ERR_TOKEN_OOB (-3)      /* a token id < 0 or >= n_vocab */
+#define MINFER_ERR_MISSING_TENSOR (-4) /* a tensor the forward needs was never set */
+#define MINFER_ERR_SHAPE (-5)          /* unknown tensor name or wrong ne0/ne1/type */
+#define MINFER_ERR_CUDA (-6)           /* a CUDA runtime/driver call failed */
+#define MINFER_ERR_OOM (-7)            /* device allocation failed */
+#define MINFER_ERR_DEVICE (-8)         /* a kernel gave up a bounded wait (status word set) */
+#define MINFER_ERR_STATE (-9)          /* call order violated (e.g. prefill before finalize) */
+
+/* ---------------------------------------------------------------- tensors */
+#define MINFER_F32 0  /* float32 values */
+#define MINFER_Q8_0 8 /* blocks of 34 bytes: uint16 fp16 scale bits (little endian),
+                         then 32 int8 codes; a row of ne0 values holds ceil(ne0/32)
+                         blocks, the missing tail elements of a partial block are 0 */
+
+typedef struct minfer_hparams {
+  int n_layer;       /* transformer layers */
+  int n_embd;        /* hidden width H */
+  int n_head;        /* query heads */
+  int n_head_kv;     /* key/value heads; n_head % n_head_kv == 0 */
+  int head_dim;      /* dims per head (even, <= 128, multiple of 16) */
+  int n_ff;          /* FFN width F */
+  int n_vocab;       /* vocabulary V */
+  int max_seq_len;   /* upper clamp of n_ctx ("09 · Prefill", section 2.5) */
+  float rope_theta;  /* RoPE frequency base */
+  float rms_eps;     /* RMSNorm epsilon */
+  int tied_embeddings; /* 1: lm_head reuses token_embd.weight */
+} minfer_hparams;
+
+typedef struct minfer_tensor {
+  const char* name; /* GGUF names: token_embd.weight, output_norm.weight, output.weight,
+                       blk.{i}.{attn_norm.weight, attn_q.weight, attn_q.bias,
+                       attn_k.weight, attn_k.bias, attn_v.weight, attn_v.bias,
+                       attn_output.weight, ffn_norm.weight, ffn_gate.weight,
+                       ffn_up.weight, ffn_down.weight} */
+  int type;         /* MINFER_F32 (vectors and matrices) or MINFER_Q8_0 (matrices) */
+  int64_t ne0, ne1; /* ne0 contiguous; ne1 = 1 for vectors */
+  const void* data; /* host memory, borrowed during the call */
+} minfer_tensor;
+
+typedef struct minfer_model minfer_model;
+typedef struct minfer_kv minfer_kv;
+
+/* ---------------------------------------------------------------- model */
+
+/* Create an empty model on the current device.  *out is owned by the caller
+ * and released with minfer_free. */
+int minfer_model_create(const minfer_hparams* hp, minfer_model** out);
+
+/* Copy one tensor to the device.  F32 matrices are quantized to Q8_0 on the
+ * device (same block rule as the activations); Q8_0 matrices are taken as
+ * given.  Matrices are repacked into the tensor-core layout.  Host data may
+ * be freed on return.  MINFER_ERR_SHAPE for an unknown name or a shape or
+ * type that does not match hp. */
+int minfer_model_set_tensor(minfer_model* m, const minfer_tensor* t);
+
+/* Check that every tensor is present (MINFER_ERR_MISSING_TENSOR otherwise,
+ * the pages' "missing weight name is an execution-time error", "05 · Graph
+ * build", section 3.4 item 8) and make the model ready for prefill. */
+int minfer_model_finalize(minfer_model* m);
+
+/* create + set every tensor + finalize in one call. */
+int minfer_load_weights(const minfer_hparams* hp, const minfer_tensor* tensors, int n,
+                        minfer_model** out);
+
+void minfer_free(minfer_model* m);
+
+/* ---------------------------------------------------------------- KV regions */
+
+/* Per-layer K and V regions of n_ctx rows x (n_head_kv * head_dim) f32,
+ * zero-filled, sized once ("09 · Prefill", section 2.5: n_ctx clamped to
+ * max_seq_len, regions never resized).  *out owned by the caller. */
+int minfer_kv_create(minfer_model* m, int n_ctx, minfer_kv** out);
+int minfer_kv_n_ctx(const minfer_kv* kv);
+void minfer_kv_free(minfer_kv* kv);
+
+/* Copy rows [row0, row0 + nrows) of layer `layer`'s K (which = 0) or V
+ * (which = 1) region to/from host memory (nrows x n_head_kv*head_dim f32).
+ * Synchronous.  For tests, snapshots and canaries. */
+int minfer_kv_read(const minfer_kv* kv, int layer, int which, int row0, int nrows, float* out);
+int minfer_kv_write(minfer_kv* kv, int layer, int which, int row0, int nrows, const float* in);
+
+/* ---------------------------------------------------------------- prefill */
+
+/* The prefill forward ("09 · Prefill", section 3.2, forward_cached: preflight,
+ * fill inputs, execute, one copy of the logits out).
+ *   token_ids[n_tokens], positions[n_tokens]: host int32; positions distinct
+ *     and within [0, n_ctx) of kv.
+ *   logits_out: host, n_vocab floats, caller-owned; written exactly once on
+ *     success with the last token's logits.
+ * K/V rows positions[t] of every layer are overwritten; every other row is
+ * left untouched.  Synchronous: returns when the logits are in logits_out. */
+int minfer_prefill(minfer_model* m, const int32_t* token_ids, const int32_t* positions,
+                   int n_tokens, minfer_kv* kv, float* logits_out);
+
+/* Same forward with device-resident inputs and output, enqueued on `stream`
+ * (a cudaStream_t, or NULL for the model's own stream) without a host sync.
+ * d_token_ids, d_positions: device int32[n_tokens]; d_logits: device
+ * float[n_vocab].  Positions and ids are validated on the device: when one is
+ * out of range or a position repeats, no K/V row and no logit is written and
+ * the error is reported by the next minfer_sync_status.  The launch sequence
+ * is recorded once per (n_tokens, kv) as a CUDA graph and replayed. */
+int minfer_prefill_device(minfer_model* m, const int32_t* d_token_ids,
+                          const int32_t* d_positions, int n_tokens, minfer_kv* kv,
+                          float* d_logits, void* stream);
+
+/* Wait for the work enqueued by minfer_prefill_device on `stream` and return
+ * its status (MINFER_OK, MINFER_ERR_POS_OOB, MINFER_ERR_TOKEN_OOB,
+ * MINFER_ERR_ARG or MINFER_ERR_DEVICE). */
+int minfer_sync_status(minfer_model* m, void* stream);
+
+/* ---------------------------------------------------------------- debug hooks */
+
+/* Register a host buffer that the next prefill calls fill with hidden states:
+ * (n_layer + 1) slots of [n_tokens][n_embd] f32, slot 0 the embedding, slot
+ * l + 1 the output of layer l; the last layer carries only the last token
+ * (written to row 0 of its slot).  NULL disables.  The buffer is borrowed
+ * until disabled ("09 · Prefill", section 4: per-layer dumps for
+ * CPU-vs-GPU comparison). */
+int minfer_set_dump(minfer_model* m, float* host_hidden, int max_tokens);
+
+/* Per-kernel device time of the prefill calls since the last reset, measured
+ * with CUDA events around each launch: kernel class k in [0, n) gets its
+ * name, its launch count and its total milliseconds.  enable = 1 turns the
+ * events on (they add a few microseconds per launch), 0 off. */
+int minfer_profile_enable(minfer_model* m, int enable);
+int minfer_profile_read(minfer_model* m, int k, const char** name, int64_t* launches,
+                        double* total_ms);
+
+/* ---------------------------------------------------------------- single stages
+ * Each stage of the forward on its own, device pointers, synchronous, for
+ * parity tests.  Codes are int8 [rows][nb*32] (nb = ceil(n/32)), scale bits
+ * uint16 fp16 [rows][nb].  They run the same kernels as minfer_prefill. */
+
+/* Q8_0-quantize rows of x [rows][n] (walkthrough index, "CPU matmul kernels"). */
+int minfer_op_quantize(const float* d_x, int64_t rows, int64_t n, int8_t* d_q, uint16_t* d_d);
+
+/* RMSNorm then Q8_0 ("05 · Graph build", section 2.5: rms_norm, eps). */
+int minfer_op_rmsnorm_quantize(const float* d_x, const float* d_w, int64_t rows, int64_t n,
+                               float eps, int8_t* d_q, uint16_t* d_d);
+
+/* y[M][N] = Q8_0(x) . Q8_0(W)^T on the tensor-core GEMM; optional per-block
+ * int32 dots out [M][N][nb] (d_dots may be NULL). x codes [M][nb*32], W codes
+ * [N][nb*32]; K = n columns. */
+int minfer_op_gemm(const int8_t* d_xq, const uint16_t* d_xd, int64_t M, const int8_t* d_wq,
+                   const uint16_t* d_wd, int64_t N, int64_t K, float* d_y, int32_t* d_dots);
+
+/* Fused gate/up GEMM + SwiGLU + Q8_0: s = silu(x.Wg^T) * (x.Wu^T), then
+ * quantized; Wg, Wu [F][nb*32]; outputs codes [M][ceil(F/32)*32] and scale
+ * bits [M][ceil(F/32)]. ("05 · Graph build", section 2.5: SwiGLU). */
+int minfer_op_gemm_swiglu(const int8_t* d_xq, const uint16_t* d_xd, int64_t M,
+                          const int8_t* d_gq, const uint16_t* d_gd, const int8_t* d_uq,
+                          const uint16_t* d_ud, int64_t F, int64_t K, int8_t* d_sq,
+                          uint16_t* d_sd);
+
+/* Causal GQA attention of query rows q [nt][n_head*head_dim] (already
+ * rotated) over K/V regions [n_ctx][n_head_kv*head_dim]; token t sees region
+ * rows 0..=pos[t] with scale 1/sqrt(head_dim) ("09 · Prefill", section 2.2;
+ * "05 · Graph build", section 2.5). o [nt][n_head*head_dim] f32. */
+int minfer_op_attention(const float* d_q, const int32_t* d_pos, int nt, const float* d_k,
+                        const float* d_v, int n_ctx, int n_head, int n_head_kv, int head_dim,
+                        float* d_o);
+
+/* RoPE (NeoX half-split pairs, theta^(-2i/hd)) of the Q and K parts of
+ * qkv [nt][(nh + 2 nkv) hd] plus bias, and the KV store: K/V regions row
+ * pos[t] <- rotated K[t], V[t] ("09 · Prefill", section 2.2). q_out
+ * [nt][nh*hd] f32. Positions must be valid for n_ctx. */
+int minfer_op_rope_store(const float* d_qkv, const float* d_bias, const int32_t* d_pos, int nt,
+                         int n_head, int n_head_kv, int head_dim, float theta, int n_ctx,
+                         float* d_q_out, float* d_k, float* d_v);
+
+/* ---------------------------------------------------------------- misc */
+const char* minfer_strerror(int code);
+/* Device-side status of the last failed call (a MINFER device code, 0 if none). */
+int minfer_device_status(minfer_model* m);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* MINFER_H */

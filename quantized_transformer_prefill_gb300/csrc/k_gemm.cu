@@ -1,0 +1,447 @@
+// k_gemm.cu -- Q8_0 x Q8_0 block-scaled GEMM on the 5th-generation tensor
+// cores (tcgen05.mma kind::f16 with TMEM accumulators, TMA-fed).
+//
+// What it computes (walkthrough index, master table, row "CPU matmul
+// kernels": quantized weight x on-the-fly Q8_0 activations; "05 · Graph
+// build", section 2.5: one matmul per projection):
+//     y[m][n] = sum_b  da[m][b] * dw[n][b] * sum_{i<32} qa[m][32b+i] * qw[n][32b+i]
+//
+// How: the int8 codes are stored as fp16 (every integer in [-127, 127] is
+// exact in fp16, each product is exact in f32 and a 32-term block sum stays
+// below 2^24), so a kind::f16 MMA with f32 accumulation over one 32-wide
+// block returns that block's integer dot exactly.  Each K block is
+// accumulated into its own TMEM slot; epilogue warps read the slot back
+// (tcgen05.ld), scale it by da * dw in f32 registers and add it to the
+// running f32 sum.  This keeps the per-block scales of Q8_0 exact where a
+// dequantize-first scheme would round the operands.
+//
+// Warp roles (320 threads, one CTA per SM, persistent over output tiles):
+//   warp 0     TMA producer: A/B code tiles (128-byte swizzle) and the two
+//              blocks' scale rows per 64-wide K stage
+//   warp 1     TMEM allocator and MMA issuer (one thread)
+//   warps 2-9  epilogue: warp w reads TMEM lane quadrant w % 4 (32 rows of
+//              the 128-row tile); warps 2-5 take the left half of the N
+//              tile, warps 6-9 the right half
+// Rings: STAGES smem stages (full/empty mbarriers; a stage is free once the
+// MMAs that read it completed and all epilogue warps read its scales) and
+// NSLOT TMEM slots of BN columns (tfull/tempty).  Every wait is bounded; on
+// timeout the kernel records a status code, drains its own TMA loads and
+// MMAs, frees TMEM and returns.
+#include <algorithm>
+#include <cstdio>
+#include <cudaTypedefs.h>
+
+#include "common.cuh"
+#include "kernels.h"
+
+namespace minfer {
+
+namespace {
+
+constexpr int kBM = 128;
+constexpr int kBK = 64;  // fp16 elements per stage: two Q8_0 blocks
+constexpr int kEpiWarps = 8;
+constexpr int kThreads = 64 + 32 * kEpiWarps;
+
+template <int BN>
+struct Cfg {
+  static constexpr int STAGES = BN == 256 ? 4 : 6;
+  static constexpr int NSLOT = 512 / BN;
+  static constexpr int CPW = BN / 2;  // columns per epilogue thread
+  static constexpr int A_BYTES = kBM * kBK * 2;
+  static constexpr int B_BYTES = BN * kBK * 2;
+  static constexpr int SA_BYTES = 2 * kBM * 4;
+  static constexpr int SB_BYTES = 2 * BN * 4;
+  static constexpr uint32_t STAGE_TX = A_BYTES + B_BYTES + SA_BYTES + SB_BYTES;
+  static constexpr int OFF_A = 0;
+  static constexpr int OFF_B = OFF_A + STAGES * A_BYTES;
+  static constexpr int OFF_SA = OFF_B + STAGES * B_BYTES;
+  static constexpr int OFF_SB = OFF_SA + STAGES * SA_BYTES;
+  static constexpr int OFF_BAR = OFF_SB + STAGES * SB_BYTES;
+  static constexpr int NBAR = 2 * STAGES + 2 * NSLOT;
+  static constexpr int OFF_TMEM = OFF_BAR + NBAR * 8;
+  static constexpr int SMEM = OFF_TMEM + 16 + 1024;  // + slack to align the base to 1024
+  static_assert(OFF_B % 1024 == 0 && OFF_SA % 1024 == 0, "swizzled tiles need 1024-B alignment");
+};
+
+struct Args {
+  int M, N, nb, n_stages;
+  int m_tiles, n_tiles, splits, stages_per_split;
+  int epi;
+  float* out;
+  int64_t ldo, split_stride;
+  __half* q_out;
+  int64_t ldq;
+  float* qs_out;
+  int64_t ldqs;
+  int64_t n_out_cols;
+  int32_t* dots;
+  int* err;
+};
+
+__device__ __forceinline__ float silu_mul(float g, float u) {
+  return __fmul_rn(__fdiv_rn(g, __fadd_rn(1.0f, expf(-g))), u);
+}
+
+template <int BN>
+__global__ void __launch_bounds__(kThreads, 1)
+    gemm_q8_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                   const __grid_constant__ CUtensorMap tmSA,
+                   const __grid_constant__ CUtensorMap tmSB, const Args p) {
+  using C = Cfg<BN>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~uintptr_t(1023));
+  uint8_t* sA = smem + C::OFF_A;
+  uint8_t* sB = smem + C::OFF_B;
+  float* sSA = reinterpret_cast<float*>(smem + C::OFF_SA);
+  float* sSB = reinterpret_cast<float*>(smem + C::OFF_SB);
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + C::OFF_BAR);
+  uint64_t* empty = full + C::STAGES;
+  uint64_t* tfull = empty + C::STAGES;
+  uint64_t* tempty = tfull + C::NSLOT;
+  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(smem + C::OFF_TMEM);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < C::STAGES; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], 1 + kEpiWarps);
+    }
+    for (int k = 0; k < C::NSLOT; ++k) {
+      mbar_init(&tfull[k], 1);
+      mbar_init(&tempty[k], kEpiWarps);
+    }
+    fence_barrier_init();
+    tma_prefetch_desc(&tmA);
+    tma_prefetch_desc(&tmB);
+    tma_prefetch_desc(&tmSA);
+    tma_prefetch_desc(&tmSB);
+  }
+  if (warp == 1) {
+    tmem_alloc(tmem_holder, 512);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_holder;
+
+  const int total = p.m_tiles * p.n_tiles * p.splits;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      int it = 0;
+      bool ok = true;
+      for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
+        const int mt = t % p.m_tiles;
+        const int rest = t / p.m_tiles;
+        const int ntile = rest % p.n_tiles;
+        const int sp = rest / p.n_tiles;
+        const int s0 = sp * p.stages_per_split;
+        const int s1 = min(p.n_stages, s0 + p.stages_per_split);
+        for (int s = s0; s < s1; ++s, ++it) {
+          const int st = it % C::STAGES;
+          const uint32_t ph = ((it / C::STAGES) & 1) ^ 1;
+          if (!mbar_wait(&empty[st], ph, p.err, kDevTimeoutTmaEmpty)) { ok = false; break; }
+          mbar_arrive_expect_tx(&full[st], C::STAGE_TX);
+          tma_load_2d(sA + st * C::A_BYTES, &tmA, &full[st], s * kBK, mt * kBM);
+          tma_load_2d(sB + st * C::B_BYTES, &tmB, &full[st], s * kBK, ntile * BN);
+          tma_load_2d(sSA + st * (C::SA_BYTES / 4), &tmSA, &full[st], mt * kBM, 2 * s);
+          tma_load_2d(sSB + st * (C::SB_BYTES / 4), &tmSB, &full[st], ntile * BN, 2 * s);
+        }
+      }
+      if (!ok) {
+        // drain the loads that may still be in flight before the CTA exits
+        for (int j = max(0, it - C::STAGES); j < it; ++j)
+          mbar_wait(&full[j % C::STAGES], (j / C::STAGES) & 1, p.err, kDevTimeoutDrain);
+      }
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      constexpr uint32_t idesc = idesc_f16_f32(kBM, BN);
+      int it = 0, sit = 0;
+      bool ok = true;
+      for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
+        const int rest = t / p.m_tiles;
+        const int sp = rest / p.n_tiles;
+        const int s0 = sp * p.stages_per_split;
+        const int s1 = min(p.n_stages, s0 + p.stages_per_split);
+        for (int s = s0; s < s1 && ok; ++s, ++it) {
+          const int st = it % C::STAGES;
+          if (!mbar_wait(&full[st], (it / C::STAGES) & 1, p.err, kDevTimeoutMmaFull)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t a_base = smem_u32(sA + st * C::A_BYTES);
+          const uint32_t b_base = smem_u32(sB + st * C::B_BYTES);
+#pragma unroll
+          for (int blk = 0; blk < 2; ++blk) {
+            const int slot = sit % C::NSLOT;
+            if (!mbar_wait(&tempty[slot], ((sit / C::NSLOT) & 1) ^ 1, p.err, kDevTimeoutMmaSlot)) {
+              ok = false;
+              break;
+            }
+            tc_fence_after();
+            const uint32_t d = tmem_base + (uint32_t)(slot * BN);
+#pragma unroll
+            for (int k16 = 0; k16 < 2; ++k16) {
+              const uint32_t koff = (uint32_t)(blk * 64 + k16 * 32);  // bytes along K
+              tc_mma_f16(d, smem_desc_sw128(a_base + koff), smem_desc_sw128(b_base + koff), idesc,
+                         (uint32_t)k16);
+            }
+            tc_commit(&tfull[slot]);
+            ++sit;
+          }
+          if (ok) tc_commit(&empty[st]);
+        }
+      }
+      // every MMA issued must have landed before TMEM is released
+      if (sit > 0) {
+        const int j = sit - 1;
+        mbar_wait(&tfull[j % C::NSLOT], (j / C::NSLOT) & 1, p.err, kDevTimeoutDrain);
+      }
+    }
+  } else {
+    // ------------------------------------------------------------ epilogue
+    const int ew = warp - 2;
+    const int quad = warp & 3;
+    const int half = ew >> 2;
+    const int row = quad * 32 + lane;
+    int it = 0, sit = 0;
+    bool ok = true;
+    for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
+      const int mt = t % p.m_tiles;
+      const int rest = t / p.m_tiles;
+      const int ntile = rest % p.n_tiles;
+      const int sp = rest / p.n_tiles;
+      const int s0 = sp * p.stages_per_split;
+      const int s1 = min(p.n_stages, s0 + p.stages_per_split);
+      const int m = mt * kBM + row;
+      const int ncol0 = ntile * BN + half * C::CPW;
+
+      float2 acc[C::CPW / 2];
+#pragma unroll
+      for (int j = 0; j < C::CPW / 2; ++j) acc[j] = make_float2(0.f, 0.f);
+
+      for (int s = s0; s < s1 && ok; ++s, ++it) {
+        const int st = it % C::STAGES;
+        if (!mbar_wait(&full[st], (it / C::STAGES) & 1, p.err, kDevTimeoutEpilogue)) {
+          ok = false;
+          break;
+        }
+#pragma unroll 1
+        for (int blk = 0; blk < 2; ++blk) {
+          const int slot = sit % C::NSLOT;
+          if (!mbar_wait(&tfull[slot], (sit / C::NSLOT) & 1, p.err, kDevTimeoutEpilogue)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const float da = sSA[st * 2 * kBM + blk * kBM + row];
+          const float* dw = sSB + st * 2 * BN + blk * BN + half * C::CPW;
+          const uint32_t taddr =
+              tmem_base + ((uint32_t)(quad * 32) << 16) + (uint32_t)(slot * BN + half * C::CPW);
+          const int b = 2 * s + blk;
+#pragma unroll
+          for (int c = 0; c < C::CPW; c += 32) {
+            uint32_t r[32];
+            tmem_ld32(taddr + c, r);
+            tmem_wait_ld();
+            if (c + 32 >= C::CPW) {
+              // slot fully read: hand it back to the MMA issuer
+              tc_fence_before();
+              __syncwarp();
+              if (lane == 0) mbar_arrive(&tempty[slot]);
+            }
+            if (p.epi == kEpiDots && m < p.M && b < p.nb) {
+#pragma unroll
+              for (int j = 0; j < 32; ++j) {
+                const int n = ncol0 + c + j;
+                if (n < p.N)
+                  p.dots[((int64_t)m * p.N + n) * p.nb + b] = __float2int_rn(__uint_as_float(r[j]));
+              }
+            }
+            const float2 da2 = make_float2(da, da);
+#pragma unroll
+            for (int j = 0; j < 32; j += 2) {
+              const float2 w2 = *reinterpret_cast<const float2*>(dw + c + j);
+              const float2 sc = __fmul2_rn(da2, w2);
+              const float2 v = make_float2(__uint_as_float(r[j]), __uint_as_float(r[j + 1]));
+              acc[(c + j) / 2] = __ffma2_rn(v, sc, acc[(c + j) / 2]);
+            }
+          }
+          ++sit;
+        }
+        if (!ok) break;
+        // this stage's scales are consumed
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&empty[st]);
+      }
+      if (!ok) break;
+
+      // ---------------------------------------------------------- store
+      if (m < p.M) {
+        if (p.epi == kEpiSwiGLU) {
+          // columns come in groups of 64: 32 gate then 32 up rows of W
+#pragma unroll
+          for (int g0 = 0; g0 < C::CPW; g0 += 64) {
+            const int64_t j0 = (int64_t)(ncol0 + g0) / 2;  // first SwiGLU output of the group
+            if (j0 >= p.n_out_cols) continue;
+            float sv[32];
+            float amax = 0.f;
+#pragma unroll
+            for (int i = 0; i < 32; ++i) {
+              const float gg = (i & 1) ? acc[(g0 + i) / 2].y : acc[(g0 + i) / 2].x;
+              const float uu = (i & 1) ? acc[(g0 + 32 + i) / 2].y : acc[(g0 + 32 + i) / 2].x;
+              sv[i] = silu_mul(gg, uu);
+              amax = fmaxf(amax, fabsf(sv[i]));
+            }
+            const float d = __fdiv_rn(amax, 127.0f);
+            const float id = q8_inv(d);
+            __half* dst = p.q_out + (int64_t)m * p.ldq + j0;
+#pragma unroll
+            for (int i = 0; i < 32; i += 8) {
+              __align__(16) __half hq[8];
+#pragma unroll
+              for (int k = 0; k < 8; ++k) hq[k] = __float2half_rn(q8_code(sv[i + k], id));
+              *reinterpret_cast<uint4*>(dst + i) = *reinterpret_cast<const uint4*>(hq);
+            }
+            p.qs_out[(j0 / 32) * p.ldqs + m] = __half2float(__float2half_rn(d));
+          }
+        } else {
+          float* dst = p.out + (int64_t)sp * p.split_stride + (int64_t)m * p.ldo + ncol0;
+          if (ncol0 + C::CPW <= p.N && (p.ldo & 3) == 0) {
+#pragma unroll
+            for (int j = 0; j < C::CPW; j += 4)
+              *reinterpret_cast<float4*>(dst + j) =
+                  make_float4(acc[j / 2].x, acc[j / 2].y, acc[j / 2 + 1].x, acc[j / 2 + 1].y);
+          } else {
+#pragma unroll
+            for (int j = 0; j < C::CPW; ++j)
+              if (ncol0 + j < p.N) dst[j] = (j & 1) ? acc[j / 2].y : acc[j / 2].x;
+          }
+        }
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == 1) tmem_dealloc(tmem_base, 512);
+}
+
+// ------------------------------------------------------------------ host side
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  if (!fn) {
+    cudaDriverEntryPointQueryResult q;
+    void* ptr = nullptr;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
+  }
+  return fn;
+}
+
+int make_map(CUtensorMap* map, const void* base, CUtensorMapDataType dt, uint64_t inner,
+             uint64_t outer, uint64_t row_bytes, uint32_t box_inner, uint32_t box_outer,
+             CUtensorMapSwizzle sw) {
+  auto fn = encode_fn();
+  if (!fn) return -1;
+  const cuuint64_t dims[2] = {inner, outer};
+  const cuuint64_t strides[1] = {row_bytes};
+  const cuuint32_t box[2] = {box_inner, box_outer};
+  const cuuint32_t es[2] = {1, 1};
+  CUresult r = fn(map, dt, 2, const_cast<void*>(base), dims, strides, box, es,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, sw, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? 0 : -2;
+}
+
+template <int BN>
+cudaError_t launch_bn(const GemmLaunch& g, const GemmMaps& maps, int num_sms, cudaStream_t st) {
+  using C = Cfg<BN>;
+  static bool attr_set = false;
+  if (!attr_set) {
+    cudaError_t e = cudaFuncSetAttribute(gemm_q8_kernel<BN>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
+    if (e != cudaSuccess) return e;
+    attr_set = true;
+  }
+  Args a;
+  a.M = (int)g.M;
+  a.N = (int)g.N;
+  a.nb = g.B.nb;
+  a.n_stages = (g.B.nb + 1) / 2;
+  a.m_tiles = (int)((g.M + kBM - 1) / kBM);
+  a.n_tiles = (int)((g.N + BN - 1) / BN);
+  a.splits = std::max(1, std::min(g.plan.splits, a.n_stages));
+  a.stages_per_split = (a.n_stages + a.splits - 1) / a.splits;
+  a.splits = (a.n_stages + a.stages_per_split - 1) / a.stages_per_split;
+  a.epi = g.epi;
+  a.out = g.out;
+  a.ldo = g.ldo;
+  a.split_stride = g.split_stride;
+  a.q_out = g.q_out;
+  a.ldq = g.ldq;
+  a.qs_out = g.qs_out;
+  a.ldqs = g.ldqs;
+  a.n_out_cols = g.n_out_cols;
+  a.dots = g.dots;
+  a.err = g.err;
+  const int total = a.m_tiles * a.n_tiles * a.splits;
+  const int grid = std::max(1, std::min(total, num_sms));
+  gemm_q8_kernel<BN><<<grid, kThreads, C::SMEM, st>>>(maps.a, maps.b, maps.sa, maps.sb, a);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+GemmPlan gemm_plan(int64_t M, int64_t N, int nb, int num_sms, bool allow_split) {
+  GemmPlan p;
+  const int64_t mt = (M + kBM - 1) / kBM;
+  const int stages = (nb + 1) / 2;
+  // wide N: 256-column tiles when they still fill the machine
+  p.bn = (mt * ((N + 255) / 256) >= num_sms) ? 256 : 128;
+  const int64_t tiles = mt * ((N + p.bn - 1) / p.bn);
+  p.splits = 1;
+  if (allow_split && tiles < num_sms) {
+    // split K so that every SM gets work, keeping >= 4 stages per split
+    int s = (int)std::min<int64_t>(num_sms / std::max<int64_t>(tiles, 1), stages / 4);
+    p.splits = std::max(1, s);
+  }
+  return p;
+}
+
+int gemm_make_maps(const GemmOperand& A, const GemmOperand& B, int bn, GemmMaps* maps) {
+  const uint64_t kpad = (uint64_t)B.nb * 32;
+  int r = 0;
+  r |= make_map(&maps->a, A.codes, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, kpad, (uint64_t)A.rows,
+                kpad * 2, kBK, kBM, CU_TENSOR_MAP_SWIZZLE_128B);
+  r |= make_map(&maps->b, B.codes, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, kpad, (uint64_t)B.rows,
+                kpad * 2, kBK, (uint32_t)bn, CU_TENSOR_MAP_SWIZZLE_128B);
+  r |= make_map(&maps->sa, A.scales, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, (uint64_t)A.rows_pad,
+                (uint64_t)A.nb, (uint64_t)A.rows_pad * 4, kBM, 2, CU_TENSOR_MAP_SWIZZLE_NONE);
+  r |= make_map(&maps->sb, B.scales, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, (uint64_t)B.rows_pad,
+                (uint64_t)B.nb, (uint64_t)B.rows_pad * 4, (uint32_t)bn, 2,
+                CU_TENSOR_MAP_SWIZZLE_NONE);
+  return r ? -1 : 0;
+}
+
+cudaError_t gemm_launch(const GemmLaunch& g, const GemmMaps& maps, int num_sms,
+                        cudaStream_t stream) {
+  if (g.A.nb != g.B.nb) return cudaErrorInvalidValue;
+  if (g.plan.bn == 256) return launch_bn<256>(g, maps, num_sms, stream);
+  return launch_bn<128>(g, maps, num_sms, stream);
+}
+
+}  // namespace minfer

@@ -1,0 +1,435 @@
+// k_rows.cu -- the memory-bound kernels of the prefill: embedding gather,
+// residual-add + RMSNorm + Q8_0 activation quantization, RoPE + KV store,
+// input validation, the one-row tail (GEMV, SwiGLU + quantize) and the
+// load-time weight quantize/repack kernels.
+//
+// Q8_0 of a 32-element block (walkthrough index, master table, row "CPU
+// matmul kernels": on-the-fly Q8_0 activations; block = 32 int8 codes + one
+// fp16 scale): d = amax / 127 (f32), codes = round-half-away(x * (1/d))
+// clamped to +-127, stored scale = fp16(d) round-to-nearest-even.  One warp
+// owns one block, one lane one element, so amax is a 5-step shuffle max.
+#include <cstdint>
+
+#include "common.cuh"
+#include "kernels.h"
+
+namespace minfer {
+
+namespace {
+
+constexpr int kRowThreads = 128;
+constexpr int kMaxPerThread = 32;  // rows up to 4096 elements
+
+// ---------------------------------------------------------------- error-free sums
+// Knuth's TwoSum and the fma-based TwoProduct: the pair (hi, lo) carries the
+// sum of squares to about 48 bits, so the per-row RMS matches a float64
+// accumulation.
+__device__ __forceinline__ void two_sum(float a, float b, float& s, float& e) {
+  s = __fadd_rn(a, b);
+  const float bb = __fsub_rn(s, a);
+  e = __fadd_rn(__fsub_rn(a, __fsub_rn(s, bb)), __fsub_rn(b, bb));
+}
+
+__device__ __forceinline__ void ff_add(float& hi, float& lo, float bhi, float blo) {
+  float s, e;
+  two_sum(hi, bhi, s, e);
+  e = __fadd_rn(e, __fadd_rn(lo, blo));
+  hi = __fadd_rn(s, e);
+  lo = __fsub_rn(e, __fsub_rn(hi, s));
+}
+
+// ---------------------------------------------------------------- row quant
+// One CTA (128 threads) per row.  Thread i holds elements i + 128 k; in step
+// k, warp w holds block 4k + w, lane = element within the block.
+template <bool kGemvOut>
+__global__ void __launch_bounds__(kRowThreads) row_quant_kernel(const RowQuantArgs a) {
+  __shared__ float red_hi[kRowThreads / 32], red_lo[kRowThreads / 32];
+  __shared__ float s_scale;
+  const int64_t r = blockIdx.x;
+  const int64_t hr = a.row_offset + r;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int64_t n = a.n;
+  const int per = (int)((n + kRowThreads - 1) / kRowThreads);
+  float* hrow = a.h + hr * n;
+
+  float x[kMaxPerThread];
+#pragma unroll
+  for (int i = 0; i < kMaxPerThread; ++i) {
+    x[i] = 0.f;
+    if (i < per) {
+      const int64_t k = tid + (int64_t)kRowThreads * i;
+      if (k < n) {
+        float v = hrow[k];
+        if (a.nsplit > 0) {
+          float o = a.partials[hr * n + k];
+          for (int s = 1; s < a.nsplit; ++s) o = __fadd_rn(o, a.partials[s * a.split_stride + hr * n + k]);
+          v = __fadd_rn(v, o);
+          hrow[k] = v;
+        }
+        x[i] = v;
+      }
+    }
+  }
+
+  float scale = 1.0f;
+  if (a.norm_w) {
+    float hi = 0.f, lo = 0.f;
+#pragma unroll
+    for (int i = 0; i < kMaxPerThread; ++i) {
+      if (i < per) {
+        const float p = __fmul_rn(x[i], x[i]);
+        const float e = fmaf(x[i], x[i], -p);
+        ff_add(hi, lo, p, e);
+      }
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      const float bhi = __shfl_xor_sync(0xffffffffu, hi, o);
+      const float blo = __shfl_xor_sync(0xffffffffu, lo, o);
+      ff_add(hi, lo, bhi, blo);
+    }
+    if (lane == 0) { red_hi[warp] = hi; red_lo[warp] = lo; }
+    __syncthreads();
+    if (tid == 0) {
+      float h2 = red_hi[0], l2 = red_lo[0];
+      for (int w = 1; w < kRowThreads / 32; ++w) ff_add(h2, l2, red_hi[w], red_lo[w]);
+      const double ss = (double)h2 + (double)l2;
+      s_scale = (float)(1.0 / sqrt(ss / (double)n + (double)a.eps));
+    }
+    __syncthreads();
+    scale = s_scale;
+  }
+
+  const int nb = (int)((n + 31) / 32);
+#pragma unroll
+  for (int i = 0; i < kMaxPerThread; ++i) {
+    if (i < per) {
+      const int64_t k = tid + (int64_t)kRowThreads * i;
+      const int b = 4 * i + warp;
+      float y = x[i];
+      if (a.norm_w) y = (k < n) ? __fmul_rn(__fmul_rn(y, scale), a.norm_w[k]) : 0.f;
+      const float amax = warp_max(fabsf(y));
+      if (b < nb) {
+        const float d = __fdiv_rn(amax, 127.0f);
+        const float code = q8_code(y, q8_inv(d));
+        const __half d16 = __float2half_rn(d);
+        if (kGemvOut) {
+          a.q8[r * (int64_t)nb * 32 + k] = (int8_t)code;
+          if (lane == 0) {
+            a.s8[r * nb + b] = __half2float(d16);
+            if (a.s8_bits) a.s8_bits[r * nb + b] = __half_as_ushort(d16);
+          }
+        } else {
+          a.q16[r * a.ldq + k] = __float2half_rn(code);
+          if (lane == 0) a.s16[(int64_t)b * a.ldqs + r] = __half2float(d16);
+        }
+      }
+    }
+  }
+}
+
+// ---------------------------------------------------------------- embedding
+__global__ void embed_kernel(const int8_t* __restrict__ q, const float* __restrict__ s,
+                             int64_t kpad, int nb, const int32_t* __restrict__ ids, int64_t H,
+                             float* __restrict__ h, int n_vocab) {
+  const int t = blockIdx.x;
+  int id = ids[t];
+  id = id < 0 ? 0 : (id >= n_vocab ? n_vocab - 1 : id);  // invalid ids are reported by validation
+  const int8_t* qr = q + (int64_t)id * kpad;
+  const float* sr = s + (int64_t)id * nb;
+  for (int64_t k = threadIdx.x; k < H; k += blockDim.x)
+    h[(int64_t)t * H + k] = __fmul_rn(sr[k / 32], (float)qr[k]);
+}
+
+// ---------------------------------------------------------------- validation
+__global__ void validate_kernel(const int32_t* __restrict__ ids, const int32_t* __restrict__ pos,
+                                int nt, int n_vocab, int n_ctx, uint32_t* seen, int* status) {
+  __shared__ int code;
+  if (threadIdx.x == 0) code = 0;
+  const int words = (n_ctx + 31) / 32;
+  for (int i = threadIdx.x; i < words; i += blockDim.x) seen[i] = 0u;
+  __syncthreads();
+  for (int t = threadIdx.x; t < nt; t += blockDim.x) {
+    const int p = pos[t];
+    const int id = ids[t];
+    if (p < 0 || p >= n_ctx) {
+      atomicCAS(&code, 0, MINFER_ERR_POS_OOB);
+    } else {
+      const uint32_t bit = 1u << (p & 31);
+      if (atomicOr(&seen[p >> 5], bit) & bit) atomicCAS(&code, 0, MINFER_ERR_ARG);
+    }
+    if (id < 0 || id >= n_vocab) atomicCAS(&code, 0, MINFER_ERR_TOKEN_OOB);
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) *status = code;
+}
+
+// ---------------------------------------------------------------- RoPE + KV store
+// NeoX half-split pairs (x_i, x_{i + hd/2}) rotated by the per-position
+// cos/sin table ("09 · Prefill", section 2.2: the positions buffer is the
+// rotation angle's input and names the K/V row written).  The products and
+// the differences are separate IEEE roundings, as written.
+__global__ void rope_store_kernel(const RopeStoreArgs a) {
+  const int t = blockIdx.x;
+  const int p_in = a.pos[t];
+  // an out-of-range position is reported by validation; it only selects a
+  // table row here (clamped) and never a region row
+  const bool write_kv = ((a.status == nullptr) || (*a.status == 0)) && p_in >= 0 && p_in < a.n_ctx;
+  const int p = (p_in >= 0 && p_in < a.n_ctx) ? p_in : 0;
+  const int half = a.hd / 2;
+  const int W = (a.nh + 2 * a.nkv) * a.hd;
+  const int64_t row = (int64_t)t * W;
+  const int npairs = (a.nh + a.nkv) * half;
+  const float* cs = a.cos_t + (int64_t)p * half;
+  const float* sn = a.sin_t + (int64_t)p * half;
+  auto load = [&](int e) -> float {
+    float o = a.partials[row + e];
+    for (int s = 1; s < a.nsplit; ++s) o = __fadd_rn(o, a.partials[s * a.split_stride + row + e]);
+    return a.bias ? __fadd_rn(o, a.bias[e]) : o;
+  };
+  for (int pi = threadIdx.x; pi < npairs; pi += blockDim.x) {
+    const int head = pi / half, i = pi % half;
+    const int e0 = head * a.hd + i;
+    const float x0 = load(e0), x1 = load(e0 + half);
+    const float c = cs[i], s = sn[i];
+    const float v0 = __fsub_rn(__fmul_rn(x0, c), __fmul_rn(x1, s));
+    const float v1 = __fadd_rn(__fmul_rn(x0, s), __fmul_rn(x1, c));
+    if (head < a.nh) {
+      a.q_out[(int64_t)t * a.nh * a.hd + e0] = v0;
+      a.q_out[(int64_t)t * a.nh * a.hd + e0 + half] = v1;
+    } else if (write_kv) {
+      const int64_t kw = (int64_t)a.nkv * a.hd;
+      const int ke = (head - a.nh) * a.hd + i;
+      a.kreg[(int64_t)p * kw + ke] = v0;
+      a.kreg[(int64_t)p * kw + ke + half] = v1;
+    }
+  }
+  if (write_kv) {
+    const int kw = a.nkv * a.hd;
+    const int v0e = (a.nh + a.nkv) * a.hd;
+    for (int e = threadIdx.x; e < kw; e += blockDim.x) a.vreg[(int64_t)p * kw + e] = load(v0e + e);
+  }
+}
+
+// ---------------------------------------------------------------- one-row GEMV
+// One warp per output row.  Lane l reads 16 code bytes of each 512-byte chunk
+// (half of a Q8_0 block); dp4a gives the integer partial, the lane pair adds
+// up the block's exact int32 dot, the even lane scales it by dw * da.
+__global__ void gemv_kernel(const GemvArgs a) {
+  const int lane = threadIdx.x & 31;
+  const int64_t n = (int64_t)blockIdx.x * (blockDim.x / 32) + (threadIdx.x >> 5);
+  if (n >= a.N) return;
+  const int8_t* wr = a.wq + n * a.kpad;
+  const float* wsr = a.ws + n * a.nb;
+  float acc = 0.f;
+  for (int64_t c = 0; c < a.kpad; c += 512) {
+    const int64_t k = c + 16 * lane;
+    int isum = 0;
+    if (k < a.kpad) {
+      const int4 w = *reinterpret_cast<const int4*>(wr + k);
+      const int4 x = *reinterpret_cast<const int4*>(a.xq + k);
+      isum = __dp4a(w.x, x.x, isum);
+      isum = __dp4a(w.y, x.y, isum);
+      isum = __dp4a(w.z, x.z, isum);
+      isum = __dp4a(w.w, x.w, isum);
+    }
+    isum += __shfl_xor_sync(0xffffffffu, isum, 1);
+    if (!(lane & 1) && k < a.kpad) {
+      const int b = (int)(k / 32);
+      acc = fmaf((float)isum, __fmul_rn(wsr[b], a.xs[b]), acc);
+    }
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
+  if (lane == 0) {
+    if (a.status && *a.status != 0) return;
+    a.y[n] = a.resid ? __fadd_rn(a.resid[n], acc) : acc;
+  }
+}
+
+__global__ void swiglu_quant_row_kernel(const float* __restrict__ gu, int64_t F, int8_t* q,
+                                        float* s) {
+  const int lane = threadIdx.x & 31;
+  const int64_t nb = (F + 31) / 32;
+  for (int64_t b = threadIdx.x >> 5; b < nb; b += blockDim.x >> 5) {
+    const int64_t j = b * 32 + lane;
+    float v = 0.f;
+    if (j < F) {
+      const float g = gu[j], u = gu[F + j];
+      v = __fmul_rn(__fdiv_rn(g, __fadd_rn(1.0f, expf(-g))), u);
+    }
+    const float amax = warp_max(fabsf(v));
+    const float d = __fdiv_rn(amax, 127.0f);
+    q[j] = (int8_t)q8_code(v, q8_inv(d));
+    if (lane == 0) s[b] = __half2float(__float2half_rn(d));
+  }
+}
+
+// ---------------------------------------------------------------- load-time kernels
+__global__ void quantize_rows_kernel(const float* __restrict__ x, int64_t rows, int64_t n,
+                                     int8_t* q, uint16_t* dbits) {
+  const int lane = threadIdx.x & 31;
+  const int64_t nb = (n + 31) / 32;
+  const int64_t total = rows * nb;
+  for (int64_t w = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5; w < total;
+       w += ((int64_t)gridDim.x * blockDim.x) >> 5) {
+    const int64_t r = w / nb, b = w % nb;
+    const int64_t k = b * 32 + lane;
+    const float v = k < n ? x[r * n + k] : 0.f;
+    const float amax = warp_max(fabsf(v));
+    const float d = __fdiv_rn(amax, 127.0f);
+    q[r * nb * 32 + k] = (int8_t)q8_code(v, q8_inv(d));
+    if (lane == 0) dbits[r * nb + b] = __half_as_ushort(__float2half_rn(d));
+  }
+}
+
+__global__ void unpack_q8_0_kernel(const uint8_t* __restrict__ blocks, int64_t rows, int64_t n,
+                                   int8_t* q, uint16_t* dbits) {
+  const int64_t nb = (n + 31) / 32;
+  const int64_t total = rows * nb;
+  for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < total;
+       i += (int64_t)gridDim.x * blockDim.x) {
+    const int64_t r = i / nb, b = i % nb;
+    const uint8_t* p = blocks + 34 * i;
+    dbits[i] = (uint16_t)(p[0] | (p[1] << 8));
+    for (int k = 0; k < 32; ++k) q[(r * nb + b) * 32 + k] = (b * 32 + k < n) ? (int8_t)p[2 + k] : 0;
+  }
+}
+
+__global__ void repack_gemm_kernel(const RepackArgs a) {
+  const int64_t kpad = (int64_t)a.nb * 32;
+  const int64_t total = a.rows * kpad;
+  for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < total;
+       i += (int64_t)gridDim.x * blockDim.x) {
+    const int64_t r = i / kpad, k = i % kpad;
+    const int64_t dr = a.interleave ? ((r / 32) * 64 + a.which * 32 + (r % 32)) : (a.dst_row0 + r);
+    a.dst_codes[dr * kpad + k] = __float2half_rn((float)a.q[i]);
+    if ((k & 31) == 0) {
+      const int b = (int)(k / 32);
+      a.dst_scales[(int64_t)b * a.dst_rows_pad + dr] =
+          __half2float(__ushort_as_half(a.dbits[r * a.nb + b]));
+    }
+  }
+}
+
+__global__ void repack_gemv_kernel(const int8_t* __restrict__ q, const uint16_t* __restrict__ dbits,
+                                   int64_t rows, int nb, int8_t* dst_q, float* dst_s) {
+  const int64_t kpad = (int64_t)nb * 32;
+  const int64_t total = rows * kpad;
+  for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < total;
+       i += (int64_t)gridDim.x * blockDim.x) {
+    dst_q[i] = q[i];
+    if ((i & 31) == 0) dst_s[i / 32] = __half2float(__ushort_as_half(dbits[i / 32]));
+  }
+}
+
+__global__ void plane_to_q8_kernel(const __half* __restrict__ codes, const float* __restrict__ scales,
+                                   int64_t rows, int64_t rows_pad, int nb, int8_t* q,
+                                   uint16_t* dbits) {
+  const int64_t kpad = (int64_t)nb * 32;
+  const int64_t total = rows * kpad;
+  for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < total;
+       i += (int64_t)gridDim.x * blockDim.x) {
+    const int64_t r = i / kpad, k = i % kpad;
+    q[i] = (int8_t)__half2float(codes[i]);
+    if ((k & 31) == 0)
+      dbits[r * nb + k / 32] = __half_as_ushort(__float2half_rn(scales[(k / 32) * rows_pad + r]));
+  }
+}
+
+__global__ void sum_splits_kernel(const float* __restrict__ p, int nsplit, int64_t stride,
+                                  int64_t count, float* out) {
+  for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < count;
+       i += (int64_t)gridDim.x * blockDim.x) {
+    float o = p[i];
+    for (int s = 1; s < nsplit; ++s) o = __fadd_rn(o, p[s * stride + i]);
+    out[i] = o;
+  }
+}
+
+int grid_for(int64_t work, int threads) {
+  int64_t g = (work + threads - 1) / threads;
+  if (g > 152 * 32) g = 152 * 32;
+  return (int)(g < 1 ? 1 : g);
+}
+
+}  // namespace
+
+cudaError_t row_quant_launch(const RowQuantArgs& a, cudaStream_t st) {
+  if (a.rows <= 0) return cudaSuccess;
+  if (a.n > (int64_t)kRowThreads * kMaxPerThread) return cudaErrorInvalidValue;
+  if (a.q8) row_quant_kernel<true><<<(unsigned)a.rows, kRowThreads, 0, st>>>(a);
+  else row_quant_kernel<false><<<(unsigned)a.rows, kRowThreads, 0, st>>>(a);
+  return cudaGetLastError();
+}
+
+cudaError_t embed_launch(const int8_t* q, const float* s, int64_t kpad, int nb, const int32_t* ids,
+                         int nt, int64_t H, int n_vocab, float* h, cudaStream_t st) {
+  embed_kernel<<<nt, 128, 0, st>>>(q, s, kpad, nb, ids, H, h, n_vocab);
+  return cudaGetLastError();
+}
+
+cudaError_t validate_launch(const int32_t* ids, const int32_t* pos, int nt, int n_vocab, int n_ctx,
+                            uint32_t* seen, int* status, cudaStream_t st) {
+  validate_kernel<<<1, 1024, 0, st>>>(ids, pos, nt, n_vocab, n_ctx, seen, status);
+  return cudaGetLastError();
+}
+
+cudaError_t rope_store_launch(const RopeStoreArgs& a, cudaStream_t st) {
+  if (a.nt <= 0) return cudaSuccess;
+  rope_store_kernel<<<a.nt, 128, 0, st>>>(a);
+  return cudaGetLastError();
+}
+
+cudaError_t gemv_launch(const GemvArgs& a, cudaStream_t st) {
+  const int warps = 8;
+  gemv_kernel<<<(unsigned)((a.N + warps - 1) / warps), 32 * warps, 0, st>>>(a);
+  return cudaGetLastError();
+}
+
+cudaError_t swiglu_quant_row_launch(const float* gu, int64_t F, int8_t* q, float* s,
+                                    cudaStream_t st) {
+  swiglu_quant_row_kernel<<<1, 1024, 0, st>>>(gu, F, q, s);
+  return cudaGetLastError();
+}
+
+cudaError_t quantize_rows_launch(const float* x, int64_t rows, int64_t n, int8_t* q,
+                                 uint16_t* dbits, cudaStream_t st) {
+  const int64_t nb = (n + 31) / 32;
+  quantize_rows_kernel<<<grid_for(rows * nb * 32, 256), 256, 0, st>>>(x, rows, n, q, dbits);
+  return cudaGetLastError();
+}
+
+cudaError_t unpack_q8_0_launch(const uint8_t* blocks, int64_t rows, int64_t n, int8_t* q,
+                               uint16_t* dbits, cudaStream_t st) {
+  const int64_t nb = (n + 31) / 32;
+  unpack_q8_0_kernel<<<grid_for(rows * nb, 256), 256, 0, st>>>(blocks, rows, n, q, dbits);
+  return cudaGetLastError();
+}
+
+cudaError_t repack_gemm_launch(const RepackArgs& a, cudaStream_t st) {
+  repack_gemm_kernel<<<grid_for(a.rows * a.nb * 32, 256), 256, 0, st>>>(a);
+  return cudaGetLastError();
+}
+
+cudaError_t repack_gemv_launch(const int8_t* q, const uint16_t* dbits, int64_t rows, int nb,
+                               int8_t* dst_q, float* dst_s, cudaStream_t st) {
+  repack_gemv_kernel<<<grid_for(rows * nb * 32, 256), 256, 0, st>>>(q, dbits, rows, nb, dst_q, dst_s);
+  return cudaGetLastError();
+}
+
+cudaError_t gemm_plane_to_q8_launch(const __half* codes, const float* scales, int64_t rows,
+                                    int64_t rows_pad, int nb, int8_t* q, uint16_t* dbits,
+                                    cudaStream_t st) {
+  plane_to_q8_kernel<<<grid_for(rows * nb * 32, 256), 256, 0, st>>>(codes, scales, rows, rows_pad,
+                                                                    nb, q, dbits);
+  return cudaGetLastError();
+}
+
+cudaError_t sum_splits_launch(const float* p, int nsplit, int64_t stride, int64_t count, float* out,
+                              cudaStream_t st) {
+  sum_splits_kernel<<<grid_for(count, 256), 256, 0, st>>>(p, nsplit, stride, count, out);
+  return cudaGetLastError();
+}
+
+}  // namespace minfer

@@ -1,0 +1,191 @@
+// kernels.h -- host-side launchers of the sm_103a kernels (one translation
+// unit per kernel family) and the device data layouts they share.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace minfer {
+
+// ---------------------------------------------------------------- layouts
+//
+// GEMM operand planes (tensor-core path):
+//   codes  fp16 [rows][kpad]   integer values -127..127 held exactly in fp16,
+//                              kpad = nb * 32, zero beyond the real columns
+//   scales f32  [nb][rows_pad] f32 value of each block's fp16 scale, stored
+//                              block-major ("transposed") so a tile's scales
+//                              are one contiguous box per block
+// GEMV planes (one-row tail):
+//   codes  int8 [rows][kpad], scales f32 [rows][nb]
+
+struct GemmOperand {
+  const __half* codes = nullptr;  // [rows][kpad]
+  const float* scales = nullptr;  // [nb][rows_pad]
+  int64_t rows = 0, rows_pad = 0;
+  int nb = 0;
+};
+
+enum GemmEpilogue : int {
+  kEpiF32 = 0,     // out[split][m][n] = sum over the split's K blocks
+  kEpiSwiGLU = 1,  // interleaved gate/up columns -> silu(g)*u -> Q8_0 codes + scales
+  kEpiDots = 2,    // debug: also write every block's int32 dot to dots[m][n][b]
+};
+
+struct GemmPlan {
+  int bn = 128;
+  int splits = 1;
+};
+
+// Choose the N tile and the split-K factor for an M x N x nb problem.
+GemmPlan gemm_plan(int64_t M, int64_t N, int nb, int num_sms, bool allow_split);
+
+// y = A . B^T on the tensor cores.  A: activations (rows = M), B: weights
+// (rows = N).  Epilogue kEpiF32 writes split s to out + s * split_stride.
+// kEpiSwiGLU expects B rows interleaved in groups of 32 gate / 32 up rows and
+// writes codes [M][ldq] fp16 and scales [nbF][ldqs] f32.
+struct GemmLaunch {
+  GemmOperand A, B;
+  int64_t M = 0, N = 0;
+  int epi = kEpiF32;
+  GemmPlan plan;
+  float* out = nullptr;
+  int64_t ldo = 0, split_stride = 0;
+  __half* q_out = nullptr;
+  int64_t ldq = 0;
+  float* qs_out = nullptr;
+  int64_t ldqs = 0;
+  int64_t n_out_cols = 0;  // kEpiSwiGLU: padded count of SwiGLU outputs
+  int32_t* dots = nullptr;
+  int* err = nullptr;
+};
+
+// Tensor maps are built once per (buffer, shape) and cached by the caller.
+struct GemmMaps {
+  CUtensorMap a, b, sa, sb;
+};
+int gemm_make_maps(const GemmOperand& A, const GemmOperand& B, int bn, GemmMaps* maps);
+cudaError_t gemm_launch(const GemmLaunch& g, const GemmMaps& maps, int num_sms,
+                        cudaStream_t stream);
+
+// ---------------------------------------------------------------- row kernels
+// RMSNorm (optional) then Q8_0 of rows; optionally first h += sum of split
+// partials.  Writes fp16 codes [rows][ldq] + f32 scales [nb][ldqs] (GEMM
+// layout) or int8 codes + f32 scales [rows][nb] (GEMV layout).
+struct RowQuantArgs {
+  float* h = nullptr;             // [rows][n] residual stream (read; written if nsplit > 0)
+  const float* partials = nullptr;  // [nsplit][rows][n]
+  int nsplit = 0;
+  int64_t split_stride = 0;
+  const float* norm_w = nullptr;  // nullptr: no RMSNorm
+  float eps = 0.f;
+  int64_t rows = 0, n = 0;
+  int64_t row_offset = 0;  // first row of h / partials processed
+  __half* q16 = nullptr;   // GEMM codes [rows][ldq]
+  int64_t ldq = 0;
+  float* s16 = nullptr;    // GEMM scales [nb][ldqs]
+  int64_t ldqs = 0;
+  int8_t* q8 = nullptr;    // GEMV codes [rows][nb*32]
+  float* s8 = nullptr;     // GEMV scales [rows][nb]
+  uint16_t* s8_bits = nullptr;  // optional fp16 bits [rows][nb] (tests)
+};
+cudaError_t row_quant_launch(const RowQuantArgs& a, cudaStream_t stream);
+
+// h[t][:] = dequantized tok_embd row ids[t] (int8 codes + f32 scales).
+cudaError_t embed_launch(const int8_t* emb_q, const float* emb_s, int64_t kpad, int nb,
+                         const int32_t* ids, int nt, int64_t H, int n_vocab, float* h,
+                         cudaStream_t stream);
+
+// Device validation of ids/positions: writes MINFER error code into *status
+// (0 when valid).  seen: n_ctx-bit scratch bitmap, cleared here first.
+cudaError_t validate_launch(const int32_t* ids, const int32_t* pos, int nt, int n_vocab,
+                            int n_ctx, uint32_t* seen, int* status, cudaStream_t stream);
+
+// RoPE + KV store.  qkv = bias + sum of nsplit partials [nt][nq + 2 nkv] ...
+struct RopeStoreArgs {
+  const float* partials = nullptr;
+  int nsplit = 1;
+  int64_t split_stride = 0;
+  const float* bias = nullptr;  // [(nh + 2 nkv) hd]
+  const int32_t* pos = nullptr;
+  int nt = 0, nh = 0, nkv = 0, hd = 0;
+  int n_ctx = 0;                 // rows of the regions and of the cos/sin tables
+  const float* cos_t = nullptr;  // [n_ctx][hd/2]
+  const float* sin_t = nullptr;
+  float* q_out = nullptr;  // [nt][nh*hd]
+  float* kreg = nullptr;   // [n_ctx][nkv*hd]
+  float* vreg = nullptr;
+  const int* status = nullptr;  // skip all writes to the regions when *status != 0
+};
+cudaError_t rope_store_launch(const RopeStoreArgs& a, cudaStream_t stream);
+
+// Causal GQA attention of query rows [r0, r1).
+struct AttnArgs {
+  const float* q = nullptr;  // [nt][nh*hd]
+  const int32_t* pos = nullptr;
+  int r0 = 0, r1 = 0;
+  const float* k = nullptr;  // [n_ctx][nkv*hd]
+  const float* v = nullptr;
+  int nh = 0, nkv = 0, hd = 0;
+  int n_ctx = 0;       // positions are clamped into [0, n_ctx) before any region read
+  float* o = nullptr;  // [nt][nh*hd]
+};
+cudaError_t attention_launch(const AttnArgs& a, cudaStream_t stream);
+
+// One-row quantized GEMV: y[n] = sum_b dw[n][b] * da[b] * dot_b (+ resid[n]).
+// W int8 [N][kpad] + f32 scales [N][nb]; x int8 [kpad] + f32 scales [nb].
+struct GemvArgs {
+  const int8_t* wq = nullptr;
+  const float* ws = nullptr;
+  int64_t N = 0;
+  int nb = 0;
+  int64_t kpad = 0;
+  const int8_t* xq = nullptr;
+  const float* xs = nullptr;
+  float* y = nullptr;
+  const float* resid = nullptr;  // y = resid + W.x when set (may alias y)
+  const int* status = nullptr;   // skip writing y when *status != 0
+};
+cudaError_t gemv_launch(const GemvArgs& a, cudaStream_t stream);
+
+// s = silu(g) * u for one row of F outputs (g = y[0:F], u = y[F:2F]) -> Q8_0
+// int8 codes [nbF*32] + f32 scales [nbF].
+cudaError_t swiglu_quant_row_launch(const float* gu, int64_t F, int8_t* q, float* s,
+                                    cudaStream_t stream);
+
+// ---------------------------------------------------------------- load-time kernels
+// f32 rows -> Q8_0 (int8 codes [rows][nb*32] + fp16 scale bits [rows][nb]).
+cudaError_t quantize_rows_launch(const float* x, int64_t rows, int64_t n, int8_t* q,
+                                 uint16_t* dbits, cudaStream_t stream);
+// 34-byte Q8_0 blocks -> int8 codes + fp16 bits.
+cudaError_t unpack_q8_0_launch(const uint8_t* blocks, int64_t rows, int64_t n, int8_t* q,
+                               uint16_t* dbits, cudaStream_t stream);
+// int8 codes + fp16 bits (rows [src_row0, +rows)) -> GEMM planes: fp16 codes
+// at dst rows given by row_map (row r -> dst_row(r)) and f32 scales [nb][dst_rows_pad].
+struct RepackArgs {
+  const int8_t* q = nullptr;
+  const uint16_t* dbits = nullptr;
+  int64_t rows = 0;
+  int nb = 0;
+  __half* dst_codes = nullptr;  // [dst_rows][nb*32]
+  float* dst_scales = nullptr;  // [nb][dst_rows_pad]
+  int64_t dst_rows_pad = 0;
+  int64_t dst_row0 = 0;     // destination row of source row 0 (plain layout)
+  int interleave = 0;       // 1: gate (which=0) / up (which=1) interleave in groups of 32
+  int which = 0;
+};
+cudaError_t repack_gemm_launch(const RepackArgs& a, cudaStream_t stream);
+// int8 codes + fp16 bits -> GEMV planes (int8 codes copy + f32 scales [rows][nb]).
+cudaError_t repack_gemv_launch(const int8_t* q, const uint16_t* dbits, int64_t rows, int nb,
+                               int8_t* dst_q, float* dst_s, cudaStream_t stream);
+// GEMM planes -> canonical int8 codes / fp16 bits (tests).
+cudaError_t gemm_plane_to_q8_launch(const __half* codes, const float* scales, int64_t rows,
+                                    int64_t rows_pad, int nb, int8_t* q, uint16_t* dbits,
+                                    cudaStream_t stream);
+
+// Split-partials sum: out[m][n] = sum_s partials[s][m][n].
+cudaError_t sum_splits_launch(const float* partials, int nsplit, int64_t split_stride,
+                              int64_t count, float* out, cudaStream_t stream);
+
+}  // namespace minfer

@@ -1,0 +1,1360 @@
+// minfer.cu -- host side of the prefill library: weight loading and repacking,
+// KV regions, the launch sequence of one prefill forward (recorded once per
+// shape as a CUDA graph and replayed), and the C ABI of include/minfer.h.
+//
+// The forward follows the node list of "05 · Graph build — the IR and the
+// builder", section 2.5, with the tail rows of section 2.8 and the call
+// contract of "09 · Prefill: the first forward", section 3.2 (preflight,
+// fill inputs, execute, one copy of the logits out):
+//
+//   validate ids/positions                          (device status word)
+//   h = embed(ids)
+//   x = Q8_0(rmsnorm(h) * attn_norm[0])
+//   per layer l < L-1:
+//     [Q|K|V] = x . Wqkv + b        tensor-core GEMM (split-K partials)
+//     RoPE(Q, K); K/V rows pos[t]  <- K, V
+//     a = attention(Q, regions)     all rows
+//     o = Q8_0(a) . Wo              GEMM
+//     h += o; x = Q8_0(rmsnorm(h) * ffn_norm)
+//     s = Q8_0(silu(x.Wg) * x.Wu)   GEMM with SwiGLU + quantize epilogue
+//     d = s . Wd                    GEMM
+//     h += d; x = Q8_0(rmsnorm(h) * attn_norm[l+1])
+//   last layer: QKV GEMM, RoPE and KV store on all rows (the regions must hold
+//   every prompt row); attention, o-projection, FFN, final norm and lm_head
+//   on the last row only, as one-row int8 GEMVs.  Rows other than the last
+//   never reach the logits ("05 · Graph build", section 2.8), so cutting
+//   them before the last attention changes no output.
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <cmath>
+#include <cstdio>
+#include <cstdlib>
+#include <cstring>
+#include <map>
+#include <mutex>
+#include <string>
+#include <vector>
+
+#include "../../include/minfer.h"
+#include "kernels.h"
+
+using namespace minfer;
+
+namespace {
+
+#define CK(x)                                                   \
+  do {                                                          \
+    cudaError_t e_ = (x);                                       \
+    if (e_ != cudaSuccess) {                                    \
+      record_cuda_error(e_, #x, __LINE__);                      \
+      return e_ == cudaErrorMemoryAllocation ? MINFER_ERR_OOM : MINFER_ERR_CUDA; \
+    }                                                           \
+  } while (0)
+
+thread_local char g_last_error[512] = "";
+
+void record_cuda_error(cudaError_t e, const char* what, int line) {
+  snprintf(g_last_error, sizeof g_last_error, "%s (%s) at minfer.cu:%d: %s",
+           cudaGetErrorName(e), cudaGetErrorString(e), line, what);
+}
+
+int64_t rup(int64_t x, int64_t m) { return (x + m - 1) / m * m; }
+
+template <typename T>
+int dalloc(T** p, size_t count) {
+  *p = nullptr;
+  if (count == 0) return MINFER_OK;
+  cudaError_t e = cudaMalloc(reinterpret_cast<void**>(p), count * sizeof(T));
+  if (e != cudaSuccess) {
+    record_cuda_error(e, "cudaMalloc", __LINE__);
+    *p = nullptr;
+    return MINFER_ERR_OOM;
+  }
+  e = cudaMemset(*p, 0, count * sizeof(T));
+  if (e != cudaSuccess) {
+    record_cuda_error(e, "cudaMemset", __LINE__);
+    return MINFER_ERR_CUDA;
+  }
+  return MINFER_OK;
+}
+
+template <typename T>
+void dfree(T*& p) {
+  if (p) cudaFree(p);
+  p = nullptr;
+}
+
+// A weight in the tensor-core layout.
+struct GemmW {
+  __half* codes = nullptr;
+  float* scales = nullptr;
+  int64_t rows = 0, rows_pad = 0;
+  int nb = 0;
+  GemmOperand op() const {
+    GemmOperand o;
+    o.codes = codes;
+    o.scales = scales;
+    o.rows = rows;
+    o.rows_pad = rows_pad;
+    o.nb = nb;
+    return o;
+  }
+  int alloc(int64_t r, int n_blocks) {
+    rows = r;
+    rows_pad = rup(r, 128);
+    nb = n_blocks;
+    int rc = dalloc(&codes, (size_t)rows * nb * 32);
+    if (rc) return rc;
+    return dalloc(&scales, (size_t)nb * rows_pad);
+  }
+  void release() {
+    dfree(codes);
+    dfree(scales);
+  }
+};
+
+// A weight in the one-row GEMV layout.
+struct GemvW {
+  int8_t* q = nullptr;
+  float* s = nullptr;
+  int64_t rows = 0;
+  int nb = 0;
+  int alloc(int64_t r, int n_blocks) {
+    rows = r;
+    nb = n_blocks;
+    int rc = dalloc(&q, (size_t)rows * nb * 32);
+    if (rc) return rc;
+    return dalloc(&s, (size_t)rows * nb);
+  }
+  void release() {
+    dfree(q);
+    dfree(s);
+  }
+};
+
+struct Layer {
+  float* attn_norm = nullptr;
+  float* ffn_norm = nullptr;
+  float* bqkv = nullptr;
+  GemmW wqkv, wo, wgu, wd;  // wo/wgu/wd unused on the last layer
+  GemvW wo_v, wgu_v, wd_v;  // last layer only
+};
+
+// Activation buffers for up to max_nt rows.
+struct Workspace {
+  int max_nt = 0;
+  int32_t* ids = nullptr;
+  int32_t* pos = nullptr;
+  float* h = nullptr;        // [nt][H]
+  __half* xa = nullptr;      // [nt][kx] codes (norm outputs and attention output)
+  float* xa_s = nullptr;     // [nbx][ntp]
+  __half* xf = nullptr;      // [nt][Fp] SwiGLU codes
+  float* xf_s = nullptr;     // [nbF][ntp]
+  float* part = nullptr;     // [splits][nt][max(qkvN, H)]
+  int64_t part_stride = 0;
+  float* qrot = nullptr;     // [nt][q]
+  float* att = nullptr;      // [nt][q]
+  float* h_last = nullptr;   // [H]
+  int8_t* t_q = nullptr;     // [max kpad] one-row codes
+  float* t_s = nullptr;      // [max nb]
+  float* gu = nullptr;       // [2F]
+  float* logits = nullptr;   // [V]
+  int ntp = 0;
+  void release() {
+    dfree(ids); dfree(pos); dfree(h); dfree(xa); dfree(xa_s); dfree(xf); dfree(xf_s);
+    dfree(part); dfree(qrot); dfree(att); dfree(h_last); dfree(t_q); dfree(t_s); dfree(gu);
+    dfree(logits);
+    max_nt = 0;
+  }
+};
+
+constexpr int kMaxSplits = 8;
+
+enum KClass : int {
+  kKValidate, kKEmbed, kKRowQuant, kKGemmQKV, kKRope, kKAttn, kKGemmO, kKGemmGU, kKGemmDown,
+  kKTailGemv, kKTailSwiglu, kKLmHead, kNumKClass
+};
+const char* kClassNames[kNumKClass] = {
+    "validate", "embed", "rmsnorm_quant", "gemm_qkv", "rope_kv_store", "attention", "gemm_o",
+    "gemm_gate_up_swiglu", "gemm_down", "tail_gemv", "tail_swiglu", "lm_head_gemv"};
+
+}  // namespace
+
+struct minfer_kv {
+  minfer_model* m = nullptr;
+  int n_ctx = 0;
+  float* regions = nullptr;  // [L][2][n_ctx][kvw]
+  float* cos_t = nullptr;    // [n_ctx][hd/2]
+  float* sin_t = nullptr;
+  uint32_t* seen = nullptr;  // n_ctx bits (duplicate-position check)
+  float* k(int l) const;
+  float* v(int l) const;
+};
+
+struct minfer_model {
+  int device = 0;
+  int num_sms = 148;
+  minfer_hparams hp{};
+  int64_t H = 0, q = 0, kvw = 0, F = 0, Fp = 0, V = 0, qkvN = 0;
+  int nbH = 0, nbq = 0, nbF = 0;
+  cudaStream_t stream = nullptr;
+  GemvW tok_embd, output;
+  float* out_norm = nullptr;
+  std::vector<Layer> layers;
+  std::map<std::string, bool> have;
+  bool finalized = false;
+  Workspace ws;
+  int* d_status = nullptr;
+  int* h_status = nullptr;  // pinned
+  // staging for loads
+  void* stage = nullptr;
+  size_t stage_bytes = 0;
+  int8_t* stage_q = nullptr;
+  uint16_t* stage_d = nullptr;
+  size_t stage_q_bytes = 0;
+  // graph cache
+  struct GraphKey {
+    int nt = 0;
+    const minfer_kv* kv = nullptr;
+    const void *ids = nullptr, *pos = nullptr, *logits = nullptr;
+    bool profile = false;
+    bool operator==(const GraphKey& o) const {
+      return nt == o.nt && kv == o.kv && ids == o.ids && pos == o.pos && logits == o.logits &&
+             profile == o.profile;
+    }
+  };
+  GraphKey gkey;
+  cudaGraphExec_t gexec = nullptr;
+  cudaGraph_t graph = nullptr;
+  // profiling
+  bool profile = false;
+  std::vector<cudaEvent_t> ev;  // pairs per launch
+  std::vector<int> ev_class;
+  int ev_used = 0;
+  double prof_ms[kNumKClass] = {};
+  int64_t prof_n[kNumKClass] = {};
+  // dumps
+  float* dump_host = nullptr;
+  int dump_max_nt = 0;
+  int last_device_status = 0;
+};
+
+float* minfer_kv::k(int l) const {
+  return regions + ((int64_t)l * 2 + 0) * n_ctx * m->kvw;
+}
+float* minfer_kv::v(int l) const {
+  return regions + ((int64_t)l * 2 + 1) * n_ctx * m->kvw;
+}
+
+namespace {
+
+std::mutex g_mu;
+
+// ------------------------------------------------------------------ loading
+
+int ensure_stage(minfer_model* m, size_t bytes, size_t q_elems, size_t nblocks) {
+  if (bytes > m->stage_bytes) {
+    if (m->stage) cudaFree(m->stage);
+    m->stage = nullptr;
+    CK(cudaMalloc(&m->stage, bytes));
+    m->stage_bytes = bytes;
+  }
+  if (q_elems > m->stage_q_bytes) {
+    dfree(m->stage_q);
+    dfree(m->stage_d);
+    int rc = dalloc(&m->stage_q, q_elems);
+    if (rc) return rc;
+    rc = dalloc(&m->stage_d, std::max<size_t>(nblocks, q_elems / 32));
+    if (rc) return rc;
+    m->stage_q_bytes = q_elems;
+  }
+  return MINFER_OK;
+}
+
+// Upload a matrix [ne1][ne0] (F32 or Q8_0 blocks) and leave its int8 codes
+// [ne1][nb*32] and fp16 bits [ne1][nb] in the model's staging buffers.
+int stage_matrix(minfer_model* m, const minfer_tensor* t) {
+  const int64_t nb = (t->ne0 + 31) / 32;
+  const size_t q_elems = (size_t)t->ne1 * nb * 32;
+  const size_t in_bytes =
+      t->type == MINFER_F32 ? (size_t)t->ne0 * t->ne1 * 4 : (size_t)t->ne1 * nb * 34;
+  int rc = ensure_stage(m, in_bytes, q_elems, (size_t)t->ne1 * nb);
+  if (rc) return rc;
+  CK(cudaMemcpyAsync(m->stage, t->data, in_bytes, cudaMemcpyHostToDevice, m->stream));
+  if (t->type == MINFER_F32)
+    CK(quantize_rows_launch(static_cast<const float*>(m->stage), t->ne1, t->ne0, m->stage_q,
+                            m->stage_d, m->stream));
+  else
+    CK(unpack_q8_0_launch(static_cast<const uint8_t*>(m->stage), t->ne1, t->ne0, m->stage_q,
+                          m->stage_d, m->stream));
+  return MINFER_OK;
+}
+
+int to_gemm(minfer_model* m, int64_t rows, int nb, GemmW& w, int64_t row0, int interleave,
+            int which) {
+  RepackArgs r;
+  r.q = m->stage_q;
+  r.dbits = m->stage_d;
+  r.rows = rows;
+  r.nb = nb;
+  r.dst_codes = w.codes;
+  r.dst_scales = w.scales;
+  r.dst_rows_pad = w.rows_pad;
+  r.dst_row0 = row0;
+  r.interleave = interleave;
+  r.which = which;
+  CK(repack_gemm_launch(r, m->stream));
+  return MINFER_OK;
+}
+
+int to_gemv(minfer_model* m, int64_t rows, int nb, GemvW& w, int64_t row0) {
+  CK(repack_gemv_launch(m->stage_q, m->stage_d, rows, nb, w.q + row0 * nb * 32, w.s + row0 * nb,
+                        m->stream));
+  return MINFER_OK;
+}
+
+int upload_vec(minfer_model* m, float* dst, const minfer_tensor* t) {
+  CK(cudaMemcpyAsync(dst, t->data, (size_t)t->ne0 * 4, cudaMemcpyHostToDevice, m->stream));
+  return MINFER_OK;
+}
+
+bool parse_layer(const char* name, int* layer, std::string* kind) {
+  if (strncmp(name, "blk.", 4) != 0) return false;
+  char* end = nullptr;
+  long l = strtol(name + 4, &end, 10);
+  if (!end || *end != '.' || end == name + 4) return false;
+  *layer = (int)l;
+  *kind = std::string(end + 1);
+  return true;
+}
+
+int model_alloc(minfer_model* m) {
+  const auto& hp = m->hp;
+  m->H = hp.n_embd;
+  m->q = (int64_t)hp.n_head * hp.head_dim;
+  m->kvw = (int64_t)hp.n_head_kv * hp.head_dim;
+  m->F = hp.n_ff;
+  m->V = hp.n_vocab;
+  m->nbH = (int)((m->H + 31) / 32);
+  m->nbq = (int)((m->q + 31) / 32);
+  m->nbF = (int)((m->F + 31) / 32);
+  m->Fp = (int64_t)m->nbF * 32;
+  m->qkvN = m->q + 2 * m->kvw;
+  int rc;
+  if ((rc = m->tok_embd.alloc(m->V, m->nbH))) return rc;
+  if (!hp.tied_embeddings && (rc = m->output.alloc(m->V, m->nbH))) return rc;
+  if ((rc = dalloc(&m->out_norm, m->H))) return rc;
+  m->layers.resize(hp.n_layer);
+  for (int l = 0; l < hp.n_layer; ++l) {
+    Layer& L = m->layers[l];
+    const bool last = l == hp.n_layer - 1;
+    if ((rc = dalloc(&L.attn_norm, m->H)) || (rc = dalloc(&L.ffn_norm, m->H)) ||
+        (rc = dalloc(&L.bqkv, m->qkvN)))
+      return rc;
+    if ((rc = L.wqkv.alloc(m->qkvN, m->nbH))) return rc;
+    if (!last) {
+      if ((rc = L.wo.alloc(m->H, m->nbq)) || (rc = L.wgu.alloc(2 * m->Fp, m->nbH)) ||
+          (rc = L.wd.alloc(m->H, m->nbF)))
+        return rc;
+    } else {
+      if ((rc = L.wo_v.alloc(m->H, m->nbq)) || (rc = L.wgu_v.alloc(2 * m->F, m->nbH)) ||
+          (rc = L.wd_v.alloc(m->H, m->nbF)))
+        return rc;
+    }
+  }
+  if ((rc = dalloc(&m->d_status, 4))) return rc;
+  CK(cudaMallocHost(&m->h_status, 4 * sizeof(int)));
+  return MINFER_OK;
+}
+
+void model_release(minfer_model* m) {
+  if (m->gexec) cudaGraphExecDestroy(m->gexec);
+  if (m->graph) cudaGraphDestroy(m->graph);
+  for (auto e : m->ev) cudaEventDestroy(e);
+  m->tok_embd.release();
+  m->output.release();
+  dfree(m->out_norm);
+  for (auto& L : m->layers) {
+    dfree(L.attn_norm); dfree(L.ffn_norm); dfree(L.bqkv);
+    L.wqkv.release(); L.wo.release(); L.wgu.release(); L.wd.release();
+    L.wo_v.release(); L.wgu_v.release(); L.wd_v.release();
+  }
+  m->ws.release();
+  dfree(m->d_status);
+  if (m->h_status) cudaFreeHost(m->h_status);
+  if (m->stage) cudaFree(m->stage);
+  dfree(m->stage_q);
+  dfree(m->stage_d);
+  if (m->stream) cudaStreamDestroy(m->stream);
+}
+
+int set_tensor(minfer_model* m, const minfer_tensor* t) {
+  if (!t || !t->name || !t->data) return MINFER_ERR_ARG;
+  const auto& hp = m->hp;
+  const std::string name(t->name);
+  const bool is_f32 = t->type == MINFER_F32, is_q8 = t->type == MINFER_Q8_0;
+  if (!is_f32 && !is_q8) return MINFER_ERR_SHAPE;
+  auto vec_ok = [&](int64_t n) { return is_f32 && t->ne0 == n && t->ne1 == 1; };
+  auto mat_ok = [&](int64_t in, int64_t out) { return t->ne0 == in && t->ne1 == out; };
+  int rc = MINFER_OK;
+  if (name == "token_embd.weight") {
+    if (!mat_ok(m->H, m->V)) return MINFER_ERR_SHAPE;
+    if ((rc = stage_matrix(m, t)) || (rc = to_gemv(m, m->V, m->nbH, m->tok_embd, 0))) return rc;
+  } else if (name == "output.weight") {
+    if (hp.tied_embeddings || !mat_ok(m->H, m->V)) return MINFER_ERR_SHAPE;
+    if ((rc = stage_matrix(m, t)) || (rc = to_gemv(m, m->V, m->nbH, m->output, 0))) return rc;
+  } else if (name == "output_norm.weight") {
+    if (!vec_ok(m->H)) return MINFER_ERR_SHAPE;
+    if ((rc = upload_vec(m, m->out_norm, t))) return rc;
+  } else {
+    int l;
+    std::string k;
+    if (!parse_layer(t->name, &l, &k) || l < 0 || l >= hp.n_layer) return MINFER_ERR_SHAPE;
+    Layer& L = m->layers[l];
+    const bool last = l == hp.n_layer - 1;
+    if (k == "attn_norm.weight") {
+      if (!vec_ok(m->H)) return MINFER_ERR_SHAPE;
+      rc = upload_vec(m, L.attn_norm, t);
+    } else if (k == "ffn_norm.weight") {
+      if (!vec_ok(m->H)) return MINFER_ERR_SHAPE;
+      rc = upload_vec(m, L.ffn_norm, t);
+    } else if (k == "attn_q.bias" || k == "attn_k.bias" || k == "attn_v.bias") {
+      const int64_t n = k == "attn_q.bias" ? m->q : m->kvw;
+      const int64_t off = k == "attn_q.bias" ? 0 : (k == "attn_k.bias" ? m->q : m->q + m->kvw);
+      if (!vec_ok(n)) return MINFER_ERR_SHAPE;
+      CK(cudaMemcpyAsync(L.bqkv + off, t->data, (size_t)n * 4, cudaMemcpyHostToDevice, m->stream));
+    } else if (k == "attn_q.weight" || k == "attn_k.weight" || k == "attn_v.weight") {
+      const int64_t n = k == "attn_q.weight" ? m->q : m->kvw;
+      const int64_t off = k == "attn_q.weight" ? 0 : (k == "attn_k.weight" ? m->q : m->q + m->kvw);
+      if (!mat_ok(m->H, n)) return MINFER_ERR_SHAPE;
+      if ((rc = stage_matrix(m, t)) || (rc = to_gemm(m, n, m->nbH, L.wqkv, off, 0, 0))) return rc;
+    } else if (k == "attn_output.weight") {
+      if (!mat_ok(m->q, m->H)) return MINFER_ERR_SHAPE;
+      if ((rc = stage_matrix(m, t))) return rc;
+      rc = last ? to_gemv(m, m->H, m->nbq, L.wo_v, 0) : to_gemm(m, m->H, m->nbq, L.wo, 0, 0, 0);
+    } else if (k == "ffn_gate.weight" || k == "ffn_up.weight") {
+      const int which = k == "ffn_gate.weight" ? 0 : 1;
+      if (!mat_ok(m->H, m->F)) return MINFER_ERR_SHAPE;
+      if ((rc = stage_matrix(m, t))) return rc;
+      rc = last ? to_gemv(m, m->F, m->nbH, L.wgu_v, which * m->F)
+                : to_gemm(m, m->F, m->nbH, L.wgu, 0, 1, which);
+    } else if (k == "ffn_down.weight") {
+      if (!mat_ok(m->F, m->H)) return MINFER_ERR_SHAPE;
+      if ((rc = stage_matrix(m, t))) return rc;
+      rc = last ? to_gemv(m, m->H, m->nbF, L.wd_v, 0) : to_gemm(m, m->H, m->nbF, L.wd, 0, 0, 0);
+    } else {
+      return MINFER_ERR_SHAPE;
+    }
+    if (rc) return rc;
+  }
+  CK(cudaStreamSynchronize(m->stream));  // host data may be freed on return
+  m->have[name] = true;
+  return MINFER_OK;
+}
+
+std::vector<std::string> required_names(const minfer_hparams& hp) {
+  std::vector<std::string> v = {"token_embd.weight", "output_norm.weight"};
+  if (!hp.tied_embeddings) v.push_back("output.weight");
+  const char* kinds[] = {"attn_norm.weight", "attn_q.weight", "attn_q.bias", "attn_k.weight",
+                         "attn_k.bias", "attn_v.weight", "attn_v.bias", "attn_output.weight",
+                         "ffn_norm.weight", "ffn_gate.weight", "ffn_up.weight", "ffn_down.weight"};
+  for (int l = 0; l < hp.n_layer; ++l)
+    for (const char* k : kinds) v.push_back("blk." + std::to_string(l) + "." + k);
+  return v;
+}
+
+// ------------------------------------------------------------------ workspace
+
+int ensure_workspace(minfer_model* m, int nt) {
+  Workspace& w = m->ws;
+  if (nt <= w.max_nt) return MINFER_OK;
+  if (m->gexec) {
+    cudaGraphExecDestroy(m->gexec);
+    m->gexec = nullptr;
+  }
+  if (m->graph) {
+    cudaGraphDestroy(m->graph);
+    m->graph = nullptr;
+  }
+  w.release();
+  const int64_t ntp = rup(nt, 128);
+  const int64_t kx = std::max<int64_t>((int64_t)m->nbH, m->nbq) * 32;
+  const int nbx = std::max(m->nbH, m->nbq);
+  const int64_t pw = std::max(m->qkvN, m->H);
+  int rc;
+  if ((rc = dalloc(&w.ids, nt)) || (rc = dalloc(&w.pos, nt)) || (rc = dalloc(&w.h, nt * m->H)) ||
+      (rc = dalloc(&w.xa, ntp * kx)) || (rc = dalloc(&w.xa_s, (size_t)nbx * ntp)) ||
+      (rc = dalloc(&w.xf, ntp * m->Fp)) || (rc = dalloc(&w.xf_s, (size_t)m->nbF * ntp)) ||
+      (rc = dalloc(&w.part, (size_t)kMaxSplits * nt * pw)) || (rc = dalloc(&w.qrot, nt * m->q)) ||
+      (rc = dalloc(&w.att, nt * m->q)) || (rc = dalloc(&w.h_last, m->H)) ||
+      (rc = dalloc(&w.t_q, std::max<int64_t>(kx, m->Fp))) ||
+      (rc = dalloc(&w.t_s, std::max(nbx, m->nbF))) || (rc = dalloc(&w.gu, 2 * m->F)) ||
+      (rc = dalloc(&w.logits, m->V)))
+    return rc;
+  w.part_stride = (int64_t)nt * pw;
+  w.ntp = (int)ntp;
+  w.max_nt = nt;
+  return MINFER_OK;
+}
+
+// ------------------------------------------------------------------ launch sequence
+
+struct Launcher {
+  minfer_model* m;
+  cudaStream_t st;
+  bool prof;
+  int begin(int cls) {
+    if (!prof) return MINFER_OK;
+    if (m->ev_used + 2 > (int)m->ev.size()) {
+      for (int i = 0; i < 64; ++i) {
+        cudaEvent_t e;
+        CK(cudaEventCreate(&e));
+        m->ev.push_back(e);
+        m->ev_class.push_back(-1);
+      }
+    }
+    m->ev_class[m->ev_used] = cls;
+    CK(cudaEventRecord(m->ev[m->ev_used], st));
+    return MINFER_OK;
+  }
+  int end() {
+    if (!prof) return MINFER_OK;
+    CK(cudaEventRecord(m->ev[m->ev_used + 1], st));
+    m->ev_used += 2;
+    return MINFER_OK;
+  }
+};
+
+#define LAUNCH(cls, call)            \
+  do {                               \
+    int rc_ = L.begin(cls);          \
+    if (rc_) return rc_;             \
+    CK(call);                        \
+    if ((rc_ = L.end())) return rc_; \
+  } while (0)
+
+int gemm_call(minfer_model* m, Launcher& L, int cls, const GemmOperand& A, const GemmW& W,
+              int64_t M, int epi, bool allow_split, float* out, int64_t ldo, __half* q_out,
+              int64_t ldq, float* qs_out, int64_t ldqs, int* nsplit_out) {
+  GemmLaunch g;
+  g.A = A;
+  g.B = W.op();
+  g.M = M;
+  g.N = W.rows;
+  g.epi = epi;
+  g.plan = gemm_plan(M, W.rows, W.nb, m->num_sms, allow_split);
+  g.plan.splits = std::min(g.plan.splits, kMaxSplits);
+  g.out = out;
+  g.ldo = ldo;
+  g.split_stride = m->ws.part_stride;
+  g.q_out = q_out;
+  g.ldq = ldq;
+  g.qs_out = qs_out;
+  g.ldqs = ldqs;
+  g.n_out_cols = m->Fp;
+  g.err = m->d_status + 1;
+  GemmMaps maps;
+  if (gemm_make_maps(g.A, g.B, g.plan.bn, &maps)) {
+    snprintf(g_last_error, sizeof g_last_error, "cuTensorMapEncodeTiled failed");
+    return MINFER_ERR_CUDA;
+  }
+  // the kernel may round the split count; recompute it the same way
+  const int stages = (W.nb + 1) / 2;
+  int splits = std::max(1, std::min(g.plan.splits, stages));
+  const int sps = (stages + splits - 1) / splits;
+  splits = (stages + sps - 1) / sps;
+  if (nsplit_out) *nsplit_out = splits;
+  LAUNCH(cls, gemm_launch(g, maps, m->num_sms, L.st));
+  return MINFER_OK;
+}
+
+void dump_hidden(minfer_model* m, cudaStream_t st, int slot, const float* src, int rows) {
+  if (!m->dump_host) return;
+  float* dst = m->dump_host + (int64_t)slot * m->dump_max_nt * m->H;
+  cudaMemcpyAsync(dst, src, (size_t)rows * m->H * 4, cudaMemcpyDeviceToHost, st);
+}
+
+// Enqueue one forward.  ids/pos/logits are device pointers.
+int enqueue_forward(minfer_model* m, minfer_kv* kv, const int32_t* ids, const int32_t* pos, int nt,
+                    float* logits, cudaStream_t st, bool prof, bool dumps) {
+  const auto& hp = m->hp;
+  Workspace& w = m->ws;
+  Launcher L{m, st, prof};
+  const int ntp = w.ntp;
+  GemmOperand xa;
+  xa.codes = w.xa;
+  xa.scales = w.xa_s;
+  xa.rows = nt;
+  xa.rows_pad = ntp;
+  xa.nb = m->nbH;
+  GemmOperand xo = xa;  // attention output operand (K = q)
+  xo.nb = m->nbq;
+  GemmOperand xf;
+  xf.codes = w.xf;
+  xf.scales = w.xf_s;
+  xf.rows = nt;
+  xf.rows_pad = ntp;
+  xf.nb = m->nbF;
+
+  CK(cudaMemsetAsync(m->d_status + 1, 0, sizeof(int), st));
+  LAUNCH(kKValidate, validate_launch(ids, pos, nt, (int)m->V, kv->n_ctx, kv->seen, m->d_status, st));
+  LAUNCH(kKEmbed, embed_launch(m->tok_embd.q, m->tok_embd.s, (int64_t)m->nbH * 32, m->nbH, ids, nt,
+                               m->H, (int)m->V, w.h, st));
+  if (dumps) dump_hidden(m, st, 0, w.h, nt);
+  {
+    RowQuantArgs r;
+    r.h = w.h;
+    r.norm_w = m->layers[0].attn_norm;
+    r.eps = hp.rms_eps;
+    r.rows = nt;
+    r.n = m->H;
+    r.q16 = w.xa;
+    r.ldq = (int64_t)m->nbH * 32;
+    r.s16 = w.xa_s;
+    r.ldqs = ntp;
+    LAUNCH(kKRowQuant, row_quant_launch(r, st));
+  }
+  for (int l = 0; l < hp.n_layer; ++l) {
+    Layer& Ly = m->layers[l];
+    const bool last = l == hp.n_layer - 1;
+    int ns = 1, rc;
+    if ((rc = gemm_call(m, L, kKGemmQKV, xa, Ly.wqkv, nt, kEpiF32, true, w.part, m->qkvN, nullptr,
+                        0, nullptr, 0, &ns)))
+      return rc;
+    {
+      RopeStoreArgs r;
+      r.partials = w.part;
+      r.nsplit = ns;
+      r.split_stride = w.part_stride;
+      r.bias = Ly.bqkv;
+      r.pos = pos;
+      r.nt = nt;
+      r.nh = hp.n_head;
+      r.nkv = hp.n_head_kv;
+      r.hd = hp.head_dim;
+      r.n_ctx = kv->n_ctx;
+      r.cos_t = kv->cos_t;
+      r.sin_t = kv->sin_t;
+      r.q_out = w.qrot;
+      r.kreg = kv->k(l);
+      r.vreg = kv->v(l);
+      r.status = m->d_status;
+      LAUNCH(kKRope, rope_store_launch(r, st));
+    }
+    AttnArgs at;
+    at.q = w.qrot;
+    at.pos = pos;
+    at.r0 = last ? nt - 1 : 0;
+    at.r1 = nt;
+    at.k = kv->k(l);
+    at.v = kv->v(l);
+    at.nh = hp.n_head;
+    at.nkv = hp.n_head_kv;
+    at.hd = hp.head_dim;
+    at.n_ctx = kv->n_ctx;
+    at.o = w.att;
+    LAUNCH(kKAttn, attention_launch(at, st));
+    if (!last) {
+      {
+        RowQuantArgs r;
+        r.h = w.att;
+        r.rows = nt;
+        r.n = m->q;
+        r.q16 = w.xa;
+        r.ldq = (int64_t)m->nbq * 32;
+        r.s16 = w.xa_s;
+        r.ldqs = ntp;
+        LAUNCH(kKRowQuant, row_quant_launch(r, st));
+      }
+      if ((rc = gemm_call(m, L, kKGemmO, xo, Ly.wo, nt, kEpiF32, true, w.part, m->H, nullptr, 0,
+                          nullptr, 0, &ns)))
+        return rc;
+      {
+        RowQuantArgs r;
+        r.h = w.h;
+        r.partials = w.part;
+        r.nsplit = ns;
+        r.split_stride = w.part_stride;
+        r.norm_w = Ly.ffn_norm;
+        r.eps = hp.rms_eps;
+        r.rows = nt;
+        r.n = m->H;
+        r.q16 = w.xa;
+        r.ldq = (int64_t)m->nbH * 32;
+        r.s16 = w.xa_s;
+        r.ldqs = ntp;
+        LAUNCH(kKRowQuant, row_quant_launch(r, st));
+      }
+      if ((rc = gemm_call(m, L, kKGemmGU, xa, Ly.wgu, nt, kEpiSwiGLU, false, nullptr, 0, w.xf,
+                          m->Fp, w.xf_s, ntp, nullptr)))
+        return rc;
+      if ((rc = gemm_call(m, L, kKGemmDown, xf, Ly.wd, nt, kEpiF32, true, w.part, m->H, nullptr, 0,
+                          nullptr, 0, &ns)))
+        return rc;
+      {
+        RowQuantArgs r;
+        r.h = w.h;
+        r.partials = w.part;
+        r.nsplit = ns;
+        r.split_stride = w.part_stride;
+        r.norm_w = m->layers[l + 1].attn_norm;
+        r.eps = hp.rms_eps;
+        r.rows = nt;
+        r.n = m->H;
+        r.q16 = w.xa;
+        r.ldq = (int64_t)m->nbH * 32;
+        r.s16 = w.xa_s;
+        r.ldqs = ntp;
+        LAUNCH(kKRowQuant, row_quant_launch(r, st));
+      }
+      if (dumps) dump_hidden(m, st, l + 1, w.h, nt);
+    } else {
+      // last row only: o-projection, FFN, final norm, lm_head as GEMVs
+      const int64_t last_row = nt - 1;
+      {
+        RowQuantArgs r;
+        r.h = w.att;
+        r.row_offset = last_row;
+        r.rows = 1;
+        r.n = m->q;
+        r.q8 = w.t_q;
+        r.s8 = w.t_s;
+        LAUNCH(kKRowQuant, row_quant_launch(r, st));
+      }
+      {
+        GemvArgs g;
+        g.wq = Ly.wo_v.q;
+        g.ws = Ly.wo_v.s;
+        g.N = m->H;
+        g.nb = m->nbq;
+        g.kpad = (int64_t)m->nbq * 32;
+        g.xq = w.t_q;
+        g.xs = w.t_s;
+        g.y = w.h_last;
+        g.resid = w.h + last_row * m->H;
+        LAUNCH(kKTailGemv, gemv_launch(g, st));
+      }
+      {
+        RowQuantArgs r;
+        r.h = w.h_last;
+        r.norm_w = Ly.ffn_norm;
+        r.eps = hp.rms_eps;
+        r.rows = 1;
+        r.n = m->H;
+        r.q8 = w.t_q;
+        r.s8 = w.t_s;
+        LAUNCH(kKRowQuant, row_quant_launch(r, st));
+      }
+      {
+        GemvArgs g;
+        g.wq = Ly.wgu_v.q;
+        g.ws = Ly.wgu_v.s;
+        g.N = 2 * m->F;
+        g.nb = m->nbH;
+        g.kpad = (int64_t)m->nbH * 32;
+        g.xq = w.t_q;
+        g.xs = w.t_s;
+        g.y = w.gu;
+        LAUNCH(kKTailGemv, gemv_launch(g, st));
+      }
+      LAUNCH(kKTailSwiglu, swiglu_quant_row_launch(w.gu, m->F, w.t_q, w.t_s, st));
+      {
+        GemvArgs g;
+        g.wq = Ly.wd_v.q;
+        g.ws = Ly.wd_v.s;
+        g.N = m->H;
+        g.nb = m->nbF;
+        g.kpad = (int64_t)m->nbF * 32;
+        g.xq = w.t_q;
+        g.xs = w.t_s;
+        g.y = w.h_last;
+        g.resid = w.h_last;
+        LAUNCH(kKTailGemv, gemv_launch(g, st));
+      }
+      if (dumps) dump_hidden(m, st, l + 1, w.h_last, 1);
+      {
+        RowQuantArgs r;
+        r.h = w.h_last;
+        r.norm_w = m->out_norm;
+        r.eps = hp.rms_eps;
+        r.rows = 1;
+        r.n = m->H;
+        r.q8 = w.t_q;
+        r.s8 = w.t_s;
+        LAUNCH(kKRowQuant, row_quant_launch(r, st));
+      }
+      {
+        const GemvW& out = hp.tied_embeddings ? m->tok_embd : m->output;
+        GemvArgs g;
+        g.wq = out.q;
+        g.ws = out.s;
+        g.N = m->V;
+        g.nb = m->nbH;
+        g.kpad = (int64_t)m->nbH * 32;
+        g.xq = w.t_q;
+        g.xs = w.t_s;
+        g.y = logits;
+        g.status = m->d_status;
+        LAUNCH(kKLmHead, gemv_launch(g, st));
+      }
+    }
+  }
+  return MINFER_OK;
+}
+
+// Run (record or replay) the forward on stream st.
+int run_forward(minfer_model* m, minfer_kv* kv, const int32_t* ids, const int32_t* pos, int nt,
+                float* logits, cudaStream_t st) {
+  int rc = ensure_workspace(m, nt);
+  if (rc) return rc;
+  const bool dumps = m->dump_host != nullptr && nt <= m->dump_max_nt;
+  if (dumps) {
+    // dumps copy to host memory mid-sequence: run eagerly
+    m->ev_used = 0;
+    rc = enqueue_forward(m, kv, ids, pos, nt, logits, st, m->profile, true);
+    return rc;
+  }
+  minfer_model::GraphKey key;
+  key.nt = nt;
+  key.kv = kv;
+  key.ids = ids;
+  key.pos = pos;
+  key.logits = logits;
+  key.profile = m->profile;
+  if (!m->gexec || !(key == m->gkey)) {
+    if (m->gexec) {
+      cudaGraphExecDestroy(m->gexec);
+      m->gexec = nullptr;
+    }
+    if (m->graph) {
+      cudaGraphDestroy(m->graph);
+      m->graph = nullptr;
+    }
+    m->ev_used = 0;
+    CK(cudaStreamBeginCapture(st, cudaStreamCaptureModeThreadLocal));
+    rc = enqueue_forward(m, kv, ids, pos, nt, logits, st, m->profile, false);
+    cudaGraph_t g = nullptr;
+    cudaError_t e = cudaStreamEndCapture(st, &g);
+    if (rc) {
+      if (g) cudaGraphDestroy(g);
+      return rc;
+    }
+    CK(e);
+    m->graph = g;
+    CK(cudaGraphInstantiate(&m->gexec, g, 0));
+    m->gkey = key;
+  }
+  CK(cudaGraphLaunch(m->gexec, st));
+  return MINFER_OK;
+}
+
+int finish_status(minfer_model* m, cudaStream_t st) {
+  CK(cudaMemcpyAsync(m->h_status, m->d_status, 2 * sizeof(int), cudaMemcpyDeviceToHost, st));
+  CK(cudaStreamSynchronize(st));
+  if (m->profile) {
+    for (int i = 0; i + 1 < m->ev_used; i += 2) {
+      float ms = 0.f;
+      if (cudaEventElapsedTime(&ms, m->ev[i], m->ev[i + 1]) == cudaSuccess) {
+        m->prof_ms[m->ev_class[i]] += ms;
+        m->prof_n[m->ev_class[i]] += 1;
+      }
+    }
+  }
+  if (m->h_status[1] != 0) {
+    m->last_device_status = m->h_status[1];
+    snprintf(g_last_error, sizeof g_last_error, "device wait timed out (code %d)", m->h_status[1]);
+    return MINFER_ERR_DEVICE;
+  }
+  return m->h_status[0];
+}
+
+void rope_tables(int n_ctx, int hd, float theta, std::vector<float>& c, std::vector<float>& s) {
+  // cos/sin of p * theta^(-2i/hd), evaluated in double and rounded to f32
+  const int half = hd / 2;
+  c.assign((size_t)n_ctx * half, 0.f);
+  s.assign((size_t)n_ctx * half, 0.f);
+  for (int i = 0; i < half; ++i) {
+    const double f = std::pow((double)theta, -2.0 * (double)i / (double)hd);
+    for (int p = 0; p < n_ctx; ++p) {
+      const double ang = (double)p * f;
+      c[(size_t)p * half + i] = (float)std::cos(ang);
+      s[(size_t)p * half + i] = (float)std::sin(ang);
+    }
+  }
+}
+
+int check_device(const minfer_model* m) {
+  int dev = -1;
+  CK(cudaGetDevice(&dev));
+  if (dev != m->device) return MINFER_ERR_STATE;
+  return MINFER_OK;
+}
+
+}  // namespace
+
+// ====================================================================== C ABI
+
+extern "C" {
+
+int minfer_model_create(const minfer_hparams* hp, minfer_model** out) {
+  if (!hp || !out) return MINFER_ERR_ARG;
+  *out = nullptr;
+  if (hp->n_layer <= 0 || hp->n_embd <= 0 || hp->n_head <= 0 || hp->n_head_kv <= 0 ||
+      hp->n_head % hp->n_head_kv != 0 || hp->head_dim <= 0 || hp->n_ff <= 0 || hp->n_vocab <= 0 ||
+      hp->max_seq_len <= 0)
+    return MINFER_ERR_ARG;
+  if (!(hp->head_dim == 64 || hp->head_dim == 128) || hp->n_head / hp->n_head_kv > 8 ||
+      hp->n_embd > 4096 || (int64_t)hp->n_head * hp->head_dim > 4096)
+    return MINFER_ERR_SHAPE;
+  minfer_model* m = new minfer_model();
+  m->hp = *hp;
+  cudaError_t e = cudaGetDevice(&m->device);
+  if (e == cudaSuccess) e = cudaDeviceGetAttribute(&m->num_sms, cudaDevAttrMultiProcessorCount, m->device);
+  if (e == cudaSuccess) e = cudaStreamCreateWithFlags(&m->stream, cudaStreamNonBlocking);
+  if (e != cudaSuccess) {
+    record_cuda_error(e, "model_create", __LINE__);
+    delete m;
+    return MINFER_ERR_CUDA;
+  }
+  int rc = model_alloc(m);
+  if (rc) {
+    model_release(m);
+    delete m;
+    return rc;
+  }
+  *out = m;
+  return MINFER_OK;
+}
+
+int minfer_model_set_tensor(minfer_model* m, const minfer_tensor* t) {
+  if (!m) return MINFER_ERR_ARG;
+  int rc = check_device(m);
+  if (rc) return rc;
+  return set_tensor(m, t);
+}
+
+int minfer_model_finalize(minfer_model* m) {
+  if (!m) return MINFER_ERR_ARG;
+  for (const auto& n : required_names(m->hp))
+    if (!m->have.count(n)) {
+      snprintf(g_last_error, sizeof g_last_error, "missing tensor %s", n.c_str());
+      return MINFER_ERR_MISSING_TENSOR;
+    }
+  // staging buffers are not needed after load
+  if (m->stage) cudaFree(m->stage);
+  m->stage = nullptr;
+  m->stage_bytes = 0;
+  dfree(m->stage_q);
+  dfree(m->stage_d);
+  m->stage_q_bytes = 0;
+  m->finalized = true;
+  return MINFER_OK;
+}
+
+int minfer_load_weights(const minfer_hparams* hp, const minfer_tensor* tensors, int n,
+                        minfer_model** out) {
+  if (!out || (n > 0 && !tensors)) return MINFER_ERR_ARG;
+  minfer_model* m = nullptr;
+  int rc = minfer_model_create(hp, &m);
+  if (rc) return rc;
+  for (int i = 0; i < n && !rc; ++i) rc = set_tensor(m, &tensors[i]);
+  if (!rc) rc = minfer_model_finalize(m);
+  if (rc) {
+    minfer_free(m);
+    return rc;
+  }
+  *out = m;
+  return MINFER_OK;
+}
+
+void minfer_free(minfer_model* m) {
+  if (!m) return;
+  cudaDeviceSynchronize();
+  model_release(m);
+  delete m;
+}
+
+int minfer_kv_create(minfer_model* m, int n_ctx, minfer_kv** out) {
+  if (!m || !out || n_ctx <= 0) return MINFER_ERR_ARG;
+  *out = nullptr;
+  int rc = check_device(m);
+  if (rc) return rc;
+  minfer_kv* kv = new minfer_kv();
+  kv->m = m;
+  kv->n_ctx = std::min(n_ctx, m->hp.max_seq_len);
+  std::vector<float> c, s;
+  rope_tables(kv->n_ctx, m->hp.head_dim, m->hp.rope_theta, c, s);
+  if ((rc = dalloc(&kv->regions, (size_t)m->hp.n_layer * 2 * kv->n_ctx * m->kvw)) ||
+      (rc = dalloc(&kv->cos_t, c.size())) || (rc = dalloc(&kv->sin_t, s.size())) ||
+      (rc = dalloc(&kv->seen, (size_t)(kv->n_ctx + 31) / 32))) {
+    minfer_kv_free(kv);
+    return rc;
+  }
+  if (cudaMemcpy(kv->cos_t, c.data(), c.size() * 4, cudaMemcpyHostToDevice) != cudaSuccess ||
+      cudaMemcpy(kv->sin_t, s.data(), s.size() * 4, cudaMemcpyHostToDevice) != cudaSuccess) {
+    minfer_kv_free(kv);
+    return MINFER_ERR_CUDA;
+  }
+  *out = kv;
+  return MINFER_OK;
+}
+
+int minfer_kv_n_ctx(const minfer_kv* kv) { return kv ? kv->n_ctx : 0; }
+
+void minfer_kv_free(minfer_kv* kv) {
+  if (!kv) return;
+  cudaDeviceSynchronize();
+  if (kv->m && kv->m->gkey.kv == kv && kv->m->gexec) {
+    cudaGraphExecDestroy(kv->m->gexec);
+    kv->m->gexec = nullptr;
+    if (kv->m->graph) cudaGraphDestroy(kv->m->graph);
+    kv->m->graph = nullptr;
+    kv->m->gkey = minfer_model::GraphKey();
+  }
+  dfree(kv->regions);
+  dfree(kv->cos_t);
+  dfree(kv->sin_t);
+  dfree(kv->seen);
+  delete kv;
+}
+
+int minfer_kv_read(const minfer_kv* kv, int layer, int which, int row0, int nrows, float* out) {
+  if (!kv || !out || layer < 0 || layer >= kv->m->hp.n_layer || (which != 0 && which != 1) ||
+      row0 < 0 || nrows < 0 || row0 + nrows > kv->n_ctx)
+    return MINFER_ERR_ARG;
+  const float* src = (which ? kv->v(layer) : kv->k(layer)) + (int64_t)row0 * kv->m->kvw;
+  CK(cudaDeviceSynchronize());
+  CK(cudaMemcpy(out, src, (size_t)nrows * kv->m->kvw * 4, cudaMemcpyDeviceToHost));
+  return MINFER_OK;
+}
+
+int minfer_kv_write(minfer_kv* kv, int layer, int which, int row0, int nrows, const float* in) {
+  if (!kv || !in || layer < 0 || layer >= kv->m->hp.n_layer || (which != 0 && which != 1) ||
+      row0 < 0 || nrows < 0 || row0 + nrows > kv->n_ctx)
+    return MINFER_ERR_ARG;
+  float* dst = (which ? kv->v(layer) : kv->k(layer)) + (int64_t)row0 * kv->m->kvw;
+  CK(cudaDeviceSynchronize());
+  CK(cudaMemcpy(dst, in, (size_t)nrows * kv->m->kvw * 4, cudaMemcpyHostToDevice));
+  return MINFER_OK;
+}
+
+int minfer_prefill(minfer_model* m, const int32_t* token_ids, const int32_t* positions,
+                   int n_tokens, minfer_kv* kv, float* logits_out) {
+  if (!m || !token_ids || !positions || !kv || !logits_out || n_tokens <= 0 || kv->m != m)
+    return MINFER_ERR_ARG;
+  if (!m->finalized) return MINFER_ERR_STATE;
+  int rc = check_device(m);
+  if (rc) return rc;
+  // host preflight: nothing is written when it fails
+  std::vector<uint8_t> seen((size_t)kv->n_ctx, 0);
+  for (int t = 0; t < n_tokens; ++t) {
+    const int p = positions[t];
+    if (p < 0 || p >= kv->n_ctx) return MINFER_ERR_POS_OOB;
+  }
+  for (int t = 0; t < n_tokens; ++t)
+    if (token_ids[t] < 0 || token_ids[t] >= m->hp.n_vocab) return MINFER_ERR_TOKEN_OOB;
+  for (int t = 0; t < n_tokens; ++t) {
+    if (seen[positions[t]]) return MINFER_ERR_ARG;
+    seen[positions[t]] = 1;
+  }
+  std::lock_guard<std::mutex> lk(g_mu);
+  if ((rc = ensure_workspace(m, n_tokens))) return rc;
+  cudaStream_t st = m->stream;
+  CK(cudaMemcpyAsync(m->ws.ids, token_ids, (size_t)n_tokens * 4, cudaMemcpyHostToDevice, st));
+  CK(cudaMemcpyAsync(m->ws.pos, positions, (size_t)n_tokens * 4, cudaMemcpyHostToDevice, st));
+  if ((rc = run_forward(m, kv, m->ws.ids, m->ws.pos, n_tokens, m->ws.logits, st))) return rc;
+  CK(cudaMemcpyAsync(logits_out, m->ws.logits, (size_t)m->V * 4, cudaMemcpyDeviceToHost, st));
+  return finish_status(m, st);
+}
+
+int minfer_prefill_device(minfer_model* m, const int32_t* d_token_ids, const int32_t* d_positions,
+                          int n_tokens, minfer_kv* kv, float* d_logits, void* stream) {
+  if (!m || !d_token_ids || !d_positions || !kv || !d_logits || n_tokens <= 0 || kv->m != m)
+    return MINFER_ERR_ARG;
+  if (!m->finalized) return MINFER_ERR_STATE;
+  int rc = check_device(m);
+  if (rc) return rc;
+  std::lock_guard<std::mutex> lk(g_mu);
+  cudaStream_t st = stream ? static_cast<cudaStream_t>(stream) : m->stream;
+  return run_forward(m, kv, d_token_ids, d_positions, n_tokens, d_logits, st);
+}
+
+int minfer_sync_status(minfer_model* m, void* stream) {
+  if (!m) return MINFER_ERR_ARG;
+  cudaStream_t st = stream ? static_cast<cudaStream_t>(stream) : m->stream;
+  return finish_status(m, st);
+}
+
+int minfer_set_dump(minfer_model* m, float* host_hidden, int max_tokens) {
+  if (!m || (host_hidden && max_tokens <= 0)) return MINFER_ERR_ARG;
+  m->dump_host = host_hidden;
+  m->dump_max_nt = host_hidden ? max_tokens : 0;
+  return MINFER_OK;
+}
+
+int minfer_profile_enable(minfer_model* m, int enable) {
+  if (!m) return MINFER_ERR_ARG;
+  m->profile = enable != 0;
+  for (int k = 0; k < kNumKClass; ++k) {
+    m->prof_ms[k] = 0.0;
+    m->prof_n[k] = 0;
+  }
+  return MINFER_OK;
+}
+
+int minfer_profile_read(minfer_model* m, int k, const char** name, int64_t* launches,
+                        double* total_ms) {
+  if (!m || k < 0 || k >= kNumKClass) return MINFER_ERR_ARG;
+  if (name) *name = kClassNames[k];
+  if (launches) *launches = m->prof_n[k];
+  if (total_ms) *total_ms = m->prof_ms[k];
+  return MINFER_OK;
+}
+
+// ---------------------------------------------------------------- single stages
+
+int minfer_op_quantize(const float* d_x, int64_t rows, int64_t n, int8_t* d_q, uint16_t* d_d) {
+  if (!d_x || !d_q || !d_d || rows <= 0 || n <= 0 || n > 4096) return MINFER_ERR_ARG;
+  RowQuantArgs r;
+  r.h = const_cast<float*>(d_x);
+  r.rows = rows;
+  r.n = n;
+  r.q8 = d_q;
+  float* s = nullptr;
+  int rc = dalloc(&s, (size_t)rows * ((n + 31) / 32));
+  if (rc) return rc;
+  r.s8 = s;
+  r.s8_bits = d_d;
+  cudaError_t e = row_quant_launch(r, 0);
+  if (e == cudaSuccess) e = cudaDeviceSynchronize();
+  dfree(s);
+  CK(e);
+  return MINFER_OK;
+}
+
+int minfer_op_rmsnorm_quantize(const float* d_x, const float* d_w, int64_t rows, int64_t n,
+                               float eps, int8_t* d_q, uint16_t* d_d) {
+  if (!d_x || !d_w || !d_q || !d_d || rows <= 0 || n <= 0 || n > 4096) return MINFER_ERR_ARG;
+  RowQuantArgs r;
+  r.h = const_cast<float*>(d_x);
+  r.norm_w = d_w;
+  r.eps = eps;
+  r.rows = rows;
+  r.n = n;
+  r.q8 = d_q;
+  float* s = nullptr;
+  int rc = dalloc(&s, (size_t)rows * ((n + 31) / 32));
+  if (rc) return rc;
+  r.s8 = s;
+  r.s8_bits = d_d;
+  cudaError_t e = row_quant_launch(r, 0);
+  if (e == cudaSuccess) e = cudaDeviceSynchronize();
+  dfree(s);
+  CK(e);
+  return MINFER_OK;
+}
+
+namespace {
+// Canonical int8 + fp16 bits -> GEMM planes (test helper).
+int planes_from_q8(const int8_t* q, const uint16_t* d, int64_t rows, int nb, GemmW& w,
+                   int interleave, int which, bool alloc) {
+  int rc;
+  if (alloc && (rc = w.alloc(interleave ? 2 * rup(rows, 32) : rows, nb))) return rc;
+  RepackArgs r;
+  r.q = q;
+  r.dbits = d;
+  r.rows = rows;
+  r.nb = nb;
+  r.dst_codes = w.codes;
+  r.dst_scales = w.scales;
+  r.dst_rows_pad = w.rows_pad;
+  r.interleave = interleave;
+  r.which = which;
+  CK(repack_gemm_launch(r, 0));
+  return MINFER_OK;
+}
+}  // namespace
+
+int minfer_op_gemm(const int8_t* d_xq, const uint16_t* d_xd, int64_t M, const int8_t* d_wq,
+                   const uint16_t* d_wd, int64_t N, int64_t K, float* d_y, int32_t* d_dots) {
+  if (!d_xq || !d_xd || !d_wq || !d_wd || !d_y || M <= 0 || N <= 0 || K <= 0) return MINFER_ERR_ARG;
+  const int nb = (int)((K + 31) / 32);
+  int num_sms = 148, dev = 0;
+  CK(cudaGetDevice(&dev));
+  CK(cudaDeviceGetAttribute(&num_sms, cudaDevAttrMultiProcessorCount, dev));
+  GemmW A, B;
+  float* part = nullptr;
+  int rc = planes_from_q8(d_xq, d_xd, M, nb, A, 0, 0, true);
+  if (!rc) rc = planes_from_q8(d_wq, d_wd, N, nb, B, 0, 0, true);
+  GemmLaunch g;
+  g.A = A.op();
+  g.B = B.op();
+  g.M = M;
+  g.N = N;
+  g.epi = d_dots ? kEpiDots : kEpiF32;
+  g.plan = gemm_plan(M, N, nb, num_sms, d_dots == nullptr);
+  g.plan.splits = std::min(g.plan.splits, kMaxSplits);
+  const int stages = (nb + 1) / 2;
+  int splits = std::max(1, std::min(g.plan.splits, stages));
+  const int sps = (stages + splits - 1) / splits;
+  splits = (stages + sps - 1) / sps;
+  if (!rc) rc = dalloc(&part, (size_t)splits * M * N);
+  int* err = nullptr;
+  if (!rc) rc = dalloc(&err, 1);
+  g.out = part;
+  g.ldo = N;
+  g.split_stride = M * N;
+  g.dots = d_dots;
+  g.err = err;
+  GemmMaps maps;
+  if (!rc && gemm_make_maps(g.A, g.B, g.plan.bn, &maps)) rc = MINFER_ERR_CUDA;
+  cudaError_t e = cudaSuccess;
+  if (!rc) e = gemm_launch(g, maps, num_sms, 0);
+  if (!rc && e == cudaSuccess) e = sum_splits_launch(part, splits, M * N, M * N, d_y, 0);
+  if (!rc && e == cudaSuccess) e = cudaDeviceSynchronize();
+  int herr = 0;
+  if (!rc && e == cudaSuccess) cudaMemcpy(&herr, err, 4, cudaMemcpyDeviceToHost);
+  A.release();
+  B.release();
+  dfree(part);
+  dfree(err);
+  if (rc) return rc;
+  CK(e);
+  return herr ? MINFER_ERR_DEVICE : MINFER_OK;
+}
+
+int minfer_op_gemm_swiglu(const int8_t* d_xq, const uint16_t* d_xd, int64_t M, const int8_t* d_gq,
+                          const uint16_t* d_gd, const int8_t* d_uq, const uint16_t* d_ud, int64_t F,
+                          int64_t K, int8_t* d_sq, uint16_t* d_sd) {
+  if (!d_xq || !d_xd || !d_gq || !d_gd || !d_uq || !d_ud || !d_sq || !d_sd || M <= 0 || F <= 0 ||
+      K <= 0)
+    return MINFER_ERR_ARG;
+  const int nb = (int)((K + 31) / 32);
+  const int nbF = (int)((F + 31) / 32);
+  const int64_t Fp = (int64_t)nbF * 32;
+  int num_sms = 148, dev = 0;
+  CK(cudaGetDevice(&dev));
+  CK(cudaDeviceGetAttribute(&num_sms, cudaDevAttrMultiProcessorCount, dev));
+  GemmW A, B;
+  int rc = planes_from_q8(d_xq, d_xd, M, nb, A, 0, 0, true);
+  if (!rc) rc = B.alloc(2 * Fp, nb);
+  if (!rc) rc = planes_from_q8(d_gq, d_gd, F, nb, B, 1, 0, false);
+  if (!rc) rc = planes_from_q8(d_uq, d_ud, F, nb, B, 1, 1, false);
+  const int64_t Mp = rup(M, 128);
+  __half* codes = nullptr;
+  float* scales = nullptr;
+  int* err = nullptr;
+  if (!rc) rc = dalloc(&codes, (size_t)M * Fp);
+  if (!rc) rc = dalloc(&scales, (size_t)nbF * Mp);
+  if (!rc) rc = dalloc(&err, 1);
+  GemmLaunch g;
+  g.A = A.op();
+  g.B = B.op();
+  g.M = M;
+  g.N = 2 * Fp;
+  g.epi = kEpiSwiGLU;
+  g.plan = gemm_plan(M, 2 * Fp, nb, num_sms, false);
+  g.q_out = codes;
+  g.ldq = Fp;
+  g.qs_out = scales;
+  g.ldqs = Mp;
+  g.n_out_cols = Fp;
+  g.err = err;
+  GemmMaps maps;
+  if (!rc && gemm_make_maps(g.A, g.B, g.plan.bn, &maps)) rc = MINFER_ERR_CUDA;
+  cudaError_t e = cudaSuccess;
+  if (!rc) e = gemm_launch(g, maps, num_sms, 0);
+  if (!rc && e == cudaSuccess) e = gemm_plane_to_q8_launch(codes, scales, M, Mp, nbF, d_sq, d_sd, 0);
+  if (!rc && e == cudaSuccess) e = cudaDeviceSynchronize();
+  int herr = 0;
+  if (!rc && e == cudaSuccess) cudaMemcpy(&herr, err, 4, cudaMemcpyDeviceToHost);
+  A.release();
+  B.release();
+  dfree(codes);
+  dfree(scales);
+  dfree(err);
+  if (rc) return rc;
+  CK(e);
+  return herr ? MINFER_ERR_DEVICE : MINFER_OK;
+}
+
+int minfer_op_attention(const float* d_q, const int32_t* d_pos, int nt, const float* d_k,
+                        const float* d_v, int n_ctx, int n_head, int n_head_kv, int head_dim,
+                        float* d_o) {
+  if (!d_q || !d_pos || !d_k || !d_v || !d_o || nt <= 0 || n_ctx <= 0 || n_head_kv <= 0 ||
+      n_head % n_head_kv != 0)
+    return MINFER_ERR_ARG;
+  AttnArgs a;
+  a.q = d_q;
+  a.pos = d_pos;
+  a.r0 = 0;
+  a.r1 = nt;
+  a.k = d_k;
+  a.v = d_v;
+  a.nh = n_head;
+  a.nkv = n_head_kv;
+  a.hd = head_dim;
+  a.n_ctx = n_ctx;
+  a.o = d_o;
+  CK(attention_launch(a, 0));
+  CK(cudaDeviceSynchronize());
+  return MINFER_OK;
+}
+
+int minfer_op_rope_store(const float* d_qkv, const float* d_bias, const int32_t* d_pos, int nt,
+                         int n_head, int n_head_kv, int head_dim, float theta, int n_ctx,
+                         float* d_q_out, float* d_k, float* d_v) {
+  if (!d_qkv || !d_pos || !d_q_out || !d_k || !d_v || nt <= 0 || n_ctx <= 0) return MINFER_ERR_ARG;
+  std::vector<float> c, s;
+  rope_tables(n_ctx, head_dim, theta, c, s);
+  float *dc = nullptr, *ds = nullptr;
+  int rc = dalloc(&dc, c.size());
+  if (!rc) rc = dalloc(&ds, s.size());
+  cudaError_t e = cudaSuccess;
+  if (!rc) e = cudaMemcpy(dc, c.data(), c.size() * 4, cudaMemcpyHostToDevice);
+  if (!rc && e == cudaSuccess) e = cudaMemcpy(ds, s.data(), s.size() * 4, cudaMemcpyHostToDevice);
+  RopeStoreArgs a;
+  a.partials = d_qkv;
+  a.nsplit = 1;
+  a.bias = d_bias;
+  a.pos = d_pos;
+  a.nt = nt;
+  a.nh = n_head;
+  a.nkv = n_head_kv;
+  a.hd = head_dim;
+  a.n_ctx = n_ctx;
+  a.cos_t = dc;
+  a.sin_t = ds;
+  a.q_out = d_q_out;
+  a.kreg = d_k;
+  a.vreg = d_v;
+  if (!rc && e == cudaSuccess) e = rope_store_launch(a, 0);
+  if (!rc && e == cudaSuccess) e = cudaDeviceSynchronize();
+  dfree(dc);
+  dfree(ds);
+  if (rc) return rc;
+  CK(e);
+  return MINFER_OK;
+}
+
+const char* minfer_strerror(int code) {
+  switch (code) {
+    case MINFER_OK: return "ok";
+    case MINFER_ERR_ARG: return "invalid argument";
+    case MINFER_ERR_POS_OOB: return "position out of range of the KV regions";
+    case MINFER_ERR_TOKEN_OOB: return "token id out of range of the vocabulary";
+    case MINFER_ERR_MISSING_TENSOR: return "missing tensor";
+    case MINFER_ERR_SHAPE: return "unknown tensor or wrong shape/type";
+    case MINFER_ERR_CUDA: return g_last_error[0] ? g_last_error : "CUDA error";
+    case MINFER_ERR_OOM: return "device out of memory";
+    case MINFER_ERR_DEVICE: return "device-side wait timed out";
+    case MINFER_ERR_STATE: return "call order or device violated";
+    default: return "unknown error";
+  }
+}
+
+int minfer_device_status(minfer_model* m) { return m ? m->last_device_status : 0; }
+
+}  // extern "C"
