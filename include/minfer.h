@@ -160,6 +160,14 @@ int minfer_sync_status(minfer_model* m, void* stream);
  * CPU-vs-GPU comparison). */
 int minfer_set_dump(minfer_model* m, float* host_hidden, int max_tokens);
 
+/* Copy a named activation buffer of the last prefill to host memory
+ * (synchronous, debugging): "h" f32 [nt][n_embd], "att" f32 [nt][n_head*hd]
+ * (attention output; the last layer writes only its last row), "xf" fp16
+ * codes [nt][ceil(n_ff/32)*32] (quantized SwiGLU output of the layer before
+ * last), "xf_s" f32 scales [ceil(n_ff/32)][ceil(nt/128)*128].  bytes is the
+ * host buffer size; MINFER_ERR_ARG for an unknown name or a short buffer. */
+int minfer_debug_read(minfer_model* m, const char* buffer, void* host, int64_t bytes);
+
 /* Per-kernel device time of the prefill calls since the last reset, measured
  * with CUDA events around each launch: kernel class k in [0, n) gets its
  * name, its launch count and its total milliseconds.  enable = 1 turns the

@@ -73,6 +73,7 @@ def _lib_handle():
                 "orc_kv_write": ([P, I, I, I, I, P, I64], I),
                 "orc_prefill": ([P, P, P, P, I, I, P, P], I),
                 "orc_argmax": ([P, I64], I64),
+                "orc_set_attention_f32": ([I], I),
             }
             for name, (args, res) in sig.items():
                 fn = getattr(L, name)
@@ -180,6 +181,11 @@ def swiglu(g, u) -> np.ndarray:
     s = np.zeros_like(g)
     _lib_handle().orc_swiglu(pg, pu, g.size, s.ctypes.data)
     return s
+
+
+def set_attention_f32(on: bool) -> bool:
+    """Switch the attention between float64 (default) and float32 rounding."""
+    return bool(_lib_handle().orc_set_attention_f32(int(on)))
 
 
 def argmax(x: np.ndarray) -> int:

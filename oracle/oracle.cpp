@@ -231,6 +231,12 @@ void rope_apply(float* x, int64_t nt, int nheads, int hd, const int32_t* pos,
     }
 }
 
+/* Rounding variant of the attention, used only to measure how far two
+ * correct roundings of the same forward drift apart: 0 = float64 scores,
+ * softmax and weighted sum (the reference behaviour), 1 = the same steps in
+ * float32. */
+int g_attn_f32 = 0;
+
 /* Causal GQA attention (reading R5; [P09] section 2.2: token t attends to
  * positions 0..=pos[t]; [P05] section 2.5: scale 1/sqrt(head_dim), n_head_kv
  * groups).  q: [nt][nh*hd]; K,V regions: [n_ctx][nkv*hd]; o: [nt][nh*hd]. */
@@ -245,6 +251,27 @@ void attention(const float* q, int64_t nt, const int32_t* pos, const float* K, c
       const int g = h / group;
       const float* qv = q + t * (int64_t)nh * hd + (int64_t)h * hd;
       const int64_t nk = (int64_t)pos[t] + 1;
+      if (g_attn_f32) {
+        std::vector<float> sf(nk);
+        float mf = -INFINITY;
+        const float fscale = 1.0f / std::sqrt((float)hd);
+        for (int64_t j = 0; j < nk; ++j) {
+          const float* kr = K + j * kvw + (int64_t)g * hd;
+          float dot = 0.0f;
+          for (int d = 0; d < hd; ++d) dot = dot + qv[d] * kr[d];
+          sf[j] = dot * fscale;
+          mf = std::max(mf, sf[j]);
+        }
+        float denf = 0.0f;
+        for (int64_t j = 0; j < nk; ++j) { sf[j] = std::exp(sf[j] - mf); denf = denf + sf[j]; }
+        float* ovf = o + t * (int64_t)nh * hd + (int64_t)h * hd;
+        for (int d = 0; d < hd; ++d) {
+          float acc = 0.0f;
+          for (int64_t j = 0; j < nk; ++j) acc = acc + sf[j] * V[j * kvw + (int64_t)g * hd + d];
+          ovf[d] = acc / denf;
+        }
+        continue;
+      }
       std::vector<double> sc(nk);
       double mx = -INFINITY;
       for (int64_t j = 0; j < nk; ++j) {
@@ -301,6 +328,13 @@ struct orc_kv {
 };
 
 uint16_t orc_f32_to_f16(float f) { return f32_to_f16(f); }
+
+/* Select the attention rounding variant (see g_attn_f32); returns the old one. */
+int orc_set_attention_f32(int on) {
+  const int old = g_attn_f32;
+  g_attn_f32 = on ? 1 : 0;
+  return old;
+}
 float orc_f16_to_f32(uint16_t h) { return f16_to_f32(h); }
 
 /* Quantize rows x [rows][n] -> codes [rows][nb*32], scale bits [rows][nb]. */

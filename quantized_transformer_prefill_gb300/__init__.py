@@ -58,6 +58,7 @@ SIGNATURES = {
     "minfer_prefill_device": ([_P, _P, _P, _I, _P, _P, _P], _I),
     "minfer_sync_status": ([_P, _P], _I),
     "minfer_set_dump": ([_P, _P, _I], _I),
+    "minfer_debug_read": ([_P, ctypes.c_char_p, _P, _I64], _I),
     "minfer_profile_enable": ([_P, _I], _I),
     "minfer_profile_read": ([_P, _I, ctypes.POINTER(ctypes.c_char_p), ctypes.POINTER(_I64),
                              ctypes.POINTER(ctypes.c_double)], _I),
@@ -166,6 +167,11 @@ class Model:
         assert buf.dtype == np.float32 and buf.flags.c_contiguous
         self._dump = buf
         check(lib().minfer_set_dump(self.ptr, buf.ctypes.data, buf.shape[1]), "set_dump")
+
+    def debug_read(self, name: str, out: np.ndarray) -> np.ndarray:
+        check(lib().minfer_debug_read(self.ptr, name.encode(), out.ctypes.data, out.nbytes),
+              f"debug_read {name}")
+        return out
 
     def profile_enable(self, on: bool = True):
         check(lib().minfer_profile_enable(self.ptr, int(on)), "profile_enable")

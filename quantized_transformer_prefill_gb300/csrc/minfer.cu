@@ -516,12 +516,14 @@ struct Launcher {
       }
     }
     m->ev_class[m->ev_used] = cls;
-    CK(cudaEventRecord(m->ev[m->ev_used], st));
+    // external: under stream capture the record becomes a graph node that
+    // records the event on every replay
+    CK(cudaEventRecordWithFlags(m->ev[m->ev_used], st, cudaEventRecordExternal));
     return MINFER_OK;
   }
   int end() {
     if (!prof) return MINFER_OK;
-    CK(cudaEventRecord(m->ev[m->ev_used + 1], st));
+    CK(cudaEventRecordWithFlags(m->ev[m->ev_used + 1], st, cudaEventRecordExternal));
     m->ev_used += 2;
     return MINFER_OK;
   }
@@ -861,6 +863,7 @@ int finish_status(minfer_model* m, cudaStream_t st) {
         m->prof_n[m->ev_class[i]] += 1;
       }
     }
+    (void)cudaGetLastError();  // a failed timing query must not leak into the next launch check
   }
   if (m->h_status[1] != 0) {
     m->last_device_status = m->h_status[1];
@@ -1336,6 +1339,23 @@ int minfer_op_rope_store(const float* d_qkv, const float* d_bias, const int32_t*
   dfree(ds);
   if (rc) return rc;
   CK(e);
+  return MINFER_OK;
+}
+
+int minfer_debug_read(minfer_model* m, const char* buffer, void* host, int64_t bytes) {
+  if (!m || !buffer || !host || m->ws.max_nt == 0) return MINFER_ERR_ARG;
+  const Workspace& w = m->ws;
+  const std::string b(buffer);
+  const void* src = nullptr;
+  int64_t n = 0;
+  if (b == "h") { src = w.h; n = (int64_t)w.max_nt * m->H * 4; }
+  else if (b == "att") { src = w.att; n = (int64_t)w.max_nt * m->q * 4; }
+  else if (b == "xf") { src = w.xf; n = (int64_t)w.max_nt * m->Fp * 2; }
+  else if (b == "xf_s") { src = w.xf_s; n = (int64_t)m->nbF * w.ntp * 4; }
+  else return MINFER_ERR_ARG;
+  if (bytes < n) return MINFER_ERR_ARG;
+  CK(cudaDeviceSynchronize());
+  CK(cudaMemcpy(host, src, (size_t)n, cudaMemcpyDeviceToHost));
   return MINFER_OK;
 }
 

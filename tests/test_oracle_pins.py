@@ -421,3 +421,22 @@ def test_sizes_printed_on_pages(oracle_mod, synth_mod):
     m = oracle_mod.Model(small)
     kv = m.kv(16)
     assert kv.read(0, 0).nbytes == 16 * kvw * 4
+
+
+def test_attention_f32_variant_is_the_same_attention(oracle_mod):
+    """The float32 rounding variant (used only to measure the drift floor)
+    computes the same masked softmax attention to float32 accuracy."""
+    rng = np.random.default_rng(12)
+    nh, nkv, hd, n_ctx = 4, 2, 32, 40
+    pos = np.array([0, 3, 17, 39, 20], np.int32)
+    q = rng.normal(0, 1, (5, nh * hd)).astype(np.float32)
+    K = rng.normal(0, 1, (n_ctx, nkv * hd)).astype(np.float32)
+    V = rng.normal(0, 1, (n_ctx, nkv * hd)).astype(np.float32)
+    ref = _attention_brute(q, pos, K, V, nh, nkv, hd)
+    oracle_mod.set_attention_f32(True)
+    try:
+        o32 = oracle_mod.attention(q, pos, K, V, nh, nkv, hd)
+    finally:
+        oracle_mod.set_attention_f32(False)
+    assert np.allclose(o32, ref, rtol=2e-5, atol=2e-6)
+    assert not np.array_equal(o32, oracle_mod.attention(q, pos, K, V, nh, nkv, hd))
