@@ -6,15 +6,22 @@
 //     o[t, h] = sum_{j <= pos[t]} softmax_j(q[t,h] . K[j, g] / sqrt(hd)) V[j, g],
 //     g = h / (n_head / n_head_kv)
 //
-// Design: one CTA per (16 query rows, KV head g); warp w of the CTA serves
+// Design.  One CTA per (16 query rows, KV head g, key split): warp w serves
 // query head g * G + w, so the G heads that share a KV head share every K/V
-// tile staged in shared memory.  Scores and P.V run on the tensor cores
-// (mma.sync m16n8k16, fp16 operands, f32 accumulate) with each f32 operand
-// split into an fp16 pair hi + lo and the three significant cross products
-// (hi.hi + hi.lo + lo.hi) accumulated, which keeps about 22 significant bits
-// -- the precision the following Q8_0 quantization of the output needs.  The
-// softmax is online (running row max and sum in f32, reduced across the four
-// lanes that share a row with warp shuffles).
+// tile in shared memory.  K/V tiles come from fp16 hi/lo shadow planes of the
+// f32 regions (written next to the regions by the RoPE/store kernel), staged
+// with double-buffered cp.async.  Scores and P.V run on the tensor cores
+// (mma.sync m16n8k16, fp16 operands, f32 accumulate) with every f32 operand
+// split as hi + lo and the three significant cross products accumulated
+// (about 22 significant bits, the precision the Q8_0 quantization of the
+// output needs).  The softmax is online: running row max and sum in f32,
+// reduced across the four lanes of a row with warp shuffles.
+//
+// Short prompts have too few (rows, KV head) tiles to fill the GPU, so the
+// key range is split (the split-KV scheme of the pages' CUDA backend): each
+// split writes its unnormalized output and (max, sum) to scratch, and the
+// combine kernel merges the splits, normalizes, and quantizes each 32-block
+// of the output row to Q8_0 for the o-projection.
 #include <cstdint>
 
 #include "common.cuh"
@@ -24,6 +31,7 @@ namespace minfer {
 
 namespace {
 
+constexpr int kMaxSplitsSmem = 64;  // key splits one combine CTA can merge
 constexpr int kTileQ = 16;   // query rows per CTA
 constexpr int kTileKV = 32;  // keys per shared-memory tile
 
@@ -36,6 +44,27 @@ __device__ __forceinline__ void mma16816(float (&d)[4], const uint32_t (&a)[4], 
       : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
 }
 
+// Four 8x8 b16 matrices, transposed on the way into registers.
+__device__ __forceinline__ void ldsm_x4_t(uint32_t saddr, uint32_t& r0, uint32_t& r1, uint32_t& r2,
+                                          uint32_t& r3) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+               : "r"(saddr));
+}
+
+__device__ __forceinline__ void cp_async16(uint32_t saddr, const void* g, bool valid) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(saddr), "l"(g),
+               "r"(valid ? 16 : 0)
+               : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() {
+  asm volatile("cp.async.commit_group;" ::: "memory");
+}
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+  asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
+
 // f32 pair -> (hi, lo) fp16x2 words with x = hi + lo to ~22 bits.
 __device__ __forceinline__ void split2(float x0, float x1, uint32_t& hi, uint32_t& lo) {
   const __half h0 = __float2half_rn(x0), h1 = __float2half_rn(x1);
@@ -46,19 +75,23 @@ __device__ __forceinline__ void split2(float x0, float x1, uint32_t& hi, uint32_
 }
 
 template <int HD>
-__global__ void __launch_bounds__(256) attn_kernel(const AttnArgs a) {
-  constexpr int KS = HD + 8;       // K tile row stride (halves)
-  constexpr int VS = kTileKV + 8;  // V^T tile row stride (halves)
-  __shared__ __align__(16) __half sKh[kTileKV * KS];
-  __shared__ __align__(16) __half sKl[kTileKV * KS];
-  __shared__ __align__(16) __half sVh[HD * VS];
-  __shared__ __align__(16) __half sVl[HD * VS];
+struct Tile {
+  static constexpr int RS = HD + 8;            // row stride (halves), conflict-free
+  static constexpr int PLANE = kTileKV * RS;   // halves per plane
+  static constexpr int STAGE = 4 * PLANE;      // Kh, Kl, Vh, Vl
+  static constexpr int BYTES = 2 * STAGE * 2;  // two stages, 2 B per half
+};
+
+template <int HD>
+__global__ void __launch_bounds__(256) attn_split_kernel(const AttnArgs a) {
+  using T = Tile<HD>;
+  extern __shared__ __align__(16) __half smem_h[];
   __shared__ int s_maxp;
 
   const int G = a.nh / a.nkv;
+  const int tile = (int)gridDim.x - 1 - (int)blockIdx.x;  // longest rows first
   const int g = blockIdx.y;
-  const int n_tiles = gridDim.x;
-  const int tile = n_tiles - 1 - (int)blockIdx.x;  // longest rows first
+  const int split = blockIdx.z;
   const int rbase = a.r0 + tile * kTileQ;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int h = g * G + warp;
@@ -68,19 +101,45 @@ __global__ void __launch_bounds__(256) attn_kernel(const AttnArgs a) {
 
   auto clamp_pos = [&](int r) -> int {
     if (r >= a.r1) return -1;
-    int p = a.pos[r];
+    const int p = a.pos[r];
     return p < 0 ? -1 : (p >= a.n_ctx ? a.n_ctx - 1 : p);
   };
-  const int ra = rbase + qr, rb = rbase + qr + 8;
-  const int pa = clamp_pos(ra), pb = clamp_pos(rb);
-
   if (threadIdx.x == 0) s_maxp = -1;
   __syncthreads();
   if (threadIdx.x < kTileQ) atomicMax(&s_maxp, clamp_pos(rbase + threadIdx.x));
   __syncthreads();
   const int maxp = s_maxp;
+  const int kbeg = split * a.ksplit;
+  if (kbeg > maxp) return;  // uniform across the CTA
+  const int kend = min(maxp + 1, kbeg + a.ksplit);
+  const int ntile = (kend - kbeg + kTileKV - 1) / kTileKV;
 
-  // Q fragments (A operand, row-major 16 x HD), split into fp16 hi/lo.
+  const int ra = rbase + qr, rb = rbase + qr + 8;
+  const int pa = clamp_pos(ra), pb = clamp_pos(rb);
+
+  // stage loader: 32 keys x HD of Kh, Kl, Vh, Vl in 16-byte chunks
+  const uint32_t sbase = smem_u32(smem_h);
+  auto load_tile = [&](int t, int stage) {
+    const int key0 = kbeg + t * kTileKV;
+    constexpr int CPR = HD / 8;  // 16-byte chunks per row
+    for (int c = threadIdx.x; c < 4 * kTileKV * CPR; c += blockDim.x) {
+      const int plane = c / (kTileKV * CPR);
+      const int rem = c % (kTileKV * CPR);
+      const int j = rem / CPR, ch = rem % CPR;
+      const int key = key0 + j;
+      const bool ok = key < a.n_ctx;
+      const __half* pbase =
+          plane == 0 ? a.shadow[0] : (plane == 1 ? a.shadow[1] : (plane == 2 ? a.shadow[2] : a.shadow[3]));
+      const __half* src = pbase + (int64_t)(ok ? key : 0) * kw + (int64_t)g * HD + ch * 8;
+      const uint32_t dst =
+          sbase + 2u * (uint32_t)(stage * T::STAGE + plane * T::PLANE + j * T::RS + ch * 8);
+      cp_async16(dst, src, ok);
+    }
+    cp_async_commit();
+  };
+  load_tile(0, 0);
+
+  // Q fragments (A operand, row-major 16 x HD), split into fp16 hi/lo
   uint32_t qh[HD / 16][4], ql[HD / 16][4];
   {
     const float* qa = a.q + (int64_t)ra * qw + (int64_t)h * HD;
@@ -89,10 +148,10 @@ __global__ void __launch_bounds__(256) attn_kernel(const AttnArgs a) {
 #pragma unroll
     for (int kk = 0; kk < HD / 16; ++kk) {
       const int c0 = kk * 16 + qc;
-      float2 x0 = va ? *reinterpret_cast<const float2*>(qa + c0) : make_float2(0.f, 0.f);
-      float2 x1 = vb ? *reinterpret_cast<const float2*>(qb + c0) : make_float2(0.f, 0.f);
-      float2 x2 = va ? *reinterpret_cast<const float2*>(qa + c0 + 8) : make_float2(0.f, 0.f);
-      float2 x3 = vb ? *reinterpret_cast<const float2*>(qb + c0 + 8) : make_float2(0.f, 0.f);
+      const float2 x0 = va ? *reinterpret_cast<const float2*>(qa + c0) : make_float2(0.f, 0.f);
+      const float2 x1 = vb ? *reinterpret_cast<const float2*>(qb + c0) : make_float2(0.f, 0.f);
+      const float2 x2 = va ? *reinterpret_cast<const float2*>(qa + c0 + 8) : make_float2(0.f, 0.f);
+      const float2 x3 = vb ? *reinterpret_cast<const float2*>(qb + c0 + 8) : make_float2(0.f, 0.f);
       split2(x0.x, x0.y, qh[kk][0], ql[kk][0]);
       split2(x1.x, x1.y, qh[kk][1], ql[kk][1]);
       split2(x2.x, x2.y, qh[kk][2], ql[kk][2]);
@@ -106,27 +165,23 @@ __global__ void __launch_bounds__(256) attn_kernel(const AttnArgs a) {
   float m_a = -INFINITY, m_b = -INFINITY, l_a = 0.f, l_b = 0.f;
   // scores are kept in log2 units: s2 = (q.k) / sqrt(hd) * log2(e)
   const float sc = __fmul_rn(__fdiv_rn(1.0f, __fsqrt_rn((float)HD)), 1.4426950408889634f);
+  const int mi = lane >> 3, mr = lane & 7;
 
-  for (int kv0 = 0; kv0 <= maxp; kv0 += kTileKV) {
-    __syncthreads();
-    // stage K (rows) and V (transposed) of head g, split into fp16 hi/lo
-    for (int e = threadIdx.x; e < kTileKV * HD; e += blockDim.x) {
-      const int j = e / HD, d = e % HD;
-      const int row = kv0 + j;
-      float kx = 0.f, vx = 0.f;
-      if (row < a.n_ctx) {
-        kx = a.k[(int64_t)row * kw + (int64_t)g * HD + d];
-        vx = a.v[(int64_t)row * kw + (int64_t)g * HD + d];
-      }
-      const __half kh = __float2half_rn(kx), vh = __float2half_rn(vx);
-      sKh[j * KS + d] = kh;
-      sKl[j * KS + d] = __float2half_rn(__fsub_rn(kx, __half2float(kh)));
-      sVh[d * VS + j] = vh;
-      sVl[d * VS + j] = __float2half_rn(__fsub_rn(vx, __half2float(vh)));
+  for (int t = 0; t < ntile; ++t) {
+    const int stage = t & 1;
+    if (t + 1 < ntile) {
+      load_tile(t + 1, stage ^ 1);
+      cp_async_wait<1>();
+    } else {
+      cp_async_wait<0>();
     }
     __syncthreads();
+    const __half* Kh = smem_h + stage * T::STAGE;
+    const __half* Kl = Kh + T::PLANE;
+    const uint32_t vh_base = sbase + 2u * (uint32_t)(stage * T::STAGE + 2 * T::PLANE);
+    const uint32_t vl_base = vh_base + 2u * (uint32_t)T::PLANE;
+    const int key0 = kbeg + t * kTileKV;
 
-    // S = Q K^T for 32 keys: 4 n-tiles of 8
     float s[4][4];
 #pragma unroll
     for (int nt = 0; nt < 4; ++nt) s[nt][0] = s[nt][1] = s[nt][2] = s[nt][3] = 0.f;
@@ -134,8 +189,8 @@ __global__ void __launch_bounds__(256) attn_kernel(const AttnArgs a) {
     for (int kk = 0; kk < HD / 16; ++kk) {
 #pragma unroll
       for (int nt = 0; nt < 4; ++nt) {
-        const __half* kh = sKh + (nt * 8 + qr) * KS + kk * 16 + qc;
-        const __half* kl = sKl + (nt * 8 + qr) * KS + kk * 16 + qc;
+        const __half* kh = Kh + (nt * 8 + qr) * T::RS + kk * 16 + qc;
+        const __half* kl = Kl + (nt * 8 + qr) * T::RS + kk * 16 + qc;
         const uint32_t bh0 = *reinterpret_cast<const uint32_t*>(kh);
         const uint32_t bh1 = *reinterpret_cast<const uint32_t*>(kh + 8);
         const uint32_t bl0 = *reinterpret_cast<const uint32_t*>(kl);
@@ -152,7 +207,7 @@ __global__ void __launch_bounds__(256) attn_kernel(const AttnArgs a) {
     for (int nt = 0; nt < 4; ++nt) {
 #pragma unroll
       for (int c = 0; c < 2; ++c) {
-        const int j = kv0 + nt * 8 + qc + c;
+        const int j = key0 + nt * 8 + qc + c;
         s[nt][c] = (j <= pa) ? __fmul_rn(s[nt][c], sc) : -INFINITY;
         s[nt][2 + c] = (j <= pb) ? __fmul_rn(s[nt][2 + c], sc) : -INFINITY;
         mx_a = fmaxf(mx_a, s[nt][c]);
@@ -175,7 +230,6 @@ __global__ void __launch_bounds__(256) attn_kernel(const AttnArgs a) {
       o[i][0] *= ca; o[i][1] *= ca;
       o[i][2] *= cb; o[i][3] *= cb;
     }
-    // P fragments (A operand of P.V), keys [16 ks, 16 ks + 16)
     uint32_t ph[2][4], pl[2][4];
 #pragma unroll
     for (int nt = 0; nt < 4; ++nt) {
@@ -189,55 +243,200 @@ __global__ void __launch_bounds__(256) attn_kernel(const AttnArgs a) {
       split2(p0, p1, ph[ks][hi8 * 2 + 0], pl[ks][hi8 * 2 + 0]);
       split2(p2, p3, ph[ks][hi8 * 2 + 1], pl[ks][hi8 * 2 + 1]);
     }
-    // O += P V
+    // O += P V: B fragments of V (keys x dims) by transposing ldmatrix
 #pragma unroll
     for (int ks = 0; ks < 2; ++ks) {
 #pragma unroll
-      for (int nd = 0; nd < HD / 8; ++nd) {
-        const __half* vh = sVh + (nd * 8 + qr) * VS + ks * 16 + qc;
-        const __half* vl = sVl + (nd * 8 + qr) * VS + ks * 16 + qc;
-        const uint32_t bh0 = *reinterpret_cast<const uint32_t*>(vh);
-        const uint32_t bh1 = *reinterpret_cast<const uint32_t*>(vh + 8);
-        const uint32_t bl0 = *reinterpret_cast<const uint32_t*>(vl);
-        const uint32_t bl1 = *reinterpret_cast<const uint32_t*>(vl + 8);
-        mma16816(o[nd], ph[ks], bh0, bh1);
-        mma16816(o[nd], ph[ks], bl0, bl1);
-        mma16816(o[nd], pl[ks], bh0, bh1);
+      for (int nd = 0; nd < HD / 8; nd += 2) {
+        const uint32_t off =
+            2u * (uint32_t)((ks * 16 + (mi & 1) * 8 + mr) * T::RS + nd * 8 + (mi >> 1) * 8);
+        uint32_t h0, h1, h2, h3, l0, l1, l2, l3;
+        ldsm_x4_t(vh_base + off, h0, h1, h2, h3);
+        ldsm_x4_t(vl_base + off, l0, l1, l2, l3);
+        mma16816(o[nd], ph[ks], h0, h1);
+        mma16816(o[nd], ph[ks], l0, l1);
+        mma16816(o[nd], pl[ks], h0, h1);
+        mma16816(o[nd + 1], ph[ks], h2, h3);
+        mma16816(o[nd + 1], ph[ks], l2, l3);
+        mma16816(o[nd + 1], pl[ks], h2, h3);
       }
     }
+    __syncthreads();  // the next prefetch overwrites this stage's buffer
   }
 
   l_a += __shfl_xor_sync(0xffffffffu, l_a, 1);
   l_a += __shfl_xor_sync(0xffffffffu, l_a, 2);
   l_b += __shfl_xor_sync(0xffffffffu, l_b, 1);
   l_b += __shfl_xor_sync(0xffffffffu, l_b, 2);
-  const float ia = l_a > 0.f ? __fdiv_rn(1.0f, l_a) : 0.f;
-  const float ib = l_b > 0.f ? __fdiv_rn(1.0f, l_b) : 0.f;
+  // partial: unnormalized o, running max (log2 units) and sum per row
+  const int nrows = a.r1 - a.r0;
   if (ra < a.r1) {
-    float* dst = a.o + (int64_t)ra * qw + (int64_t)h * HD + qc;
+    const int64_t base = ((int64_t)split * nrows + (ra - a.r0)) * a.nh + h;
+    float* dst = a.part_o + base * HD + qc;
 #pragma unroll
     for (int nd = 0; nd < HD / 8; ++nd)
-      *reinterpret_cast<float2*>(dst + nd * 8) = make_float2(o[nd][0] * ia, o[nd][1] * ia);
+      *reinterpret_cast<float2*>(dst + nd * 8) = make_float2(o[nd][0], o[nd][1]);
+    if ((lane & 3) == 0) *reinterpret_cast<float2*>(a.part_ml + base * 2) = make_float2(m_a, l_a);
   }
   if (rb < a.r1) {
-    float* dst = a.o + (int64_t)rb * qw + (int64_t)h * HD + qc;
+    const int64_t base = ((int64_t)split * nrows + (rb - a.r0)) * a.nh + h;
+    float* dst = a.part_o + base * HD + qc;
 #pragma unroll
     for (int nd = 0; nd < HD / 8; ++nd)
-      *reinterpret_cast<float2*>(dst + nd * 8) = make_float2(o[nd][2] * ib, o[nd][3] * ib);
+      *reinterpret_cast<float2*>(dst + nd * 8) = make_float2(o[nd][2], o[nd][3]);
+    if ((lane & 3) == 0) *reinterpret_cast<float2*>(a.part_ml + base * 2) = make_float2(m_b, l_b);
+  }
+}
+
+// One CTA of 256 threads per query row: per-head split weights
+// w_s = 2^(m_s - M) / L in shared memory, then every thread merges its
+// elements over the splits, and each warp quantizes its 32-block.
+constexpr int kCombThreads = 256;
+constexpr int kMaxHeads = 64;
+
+template <bool kGemvOut, int PER>
+__global__ void __launch_bounds__(kCombThreads) attn_combine_kernel(const AttnArgs a, const AttnOut out) {
+  __shared__ float s_w[kMaxHeads][kMaxSplitsSmem];
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int r = a.r0 + (int)blockIdx.x;
+  const int nrows = a.r1 - a.r0;
+  int p = a.pos[r];
+  p = p < 0 ? 0 : (p >= a.n_ctx ? a.n_ctx - 1 : p);
+  const int nsplit = min(p / a.ksplit + 1, kMaxSplitsSmem);
+  const int hd = a.hd;
+  const int q = a.nh * hd;
+  const int nb = q / 32;
+  if (tid < a.nh) {
+    const int h = tid;
+    float M = -INFINITY;
+    for (int s = 0; s < nsplit; ++s)
+      M = fmaxf(M, a.part_ml[(((int64_t)s * nrows + (r - a.r0)) * a.nh + h) * 2]);
+    float L = 0.f;
+    for (int s = 0; s < nsplit; ++s) {
+      const int64_t base = ((int64_t)s * nrows + (r - a.r0)) * a.nh + h;
+      const float m = a.part_ml[base * 2];
+      const float w = (m == -INFINITY) ? 0.f : exp2f(m - M);
+      s_w[h][s] = w;
+      L = fmaf(a.part_ml[base * 2 + 1], w, L);
+    }
+    const float inv = L > 0.f ? __fdiv_rn(1.0f, L) : 0.f;
+    for (int s = 0; s < nsplit; ++s) s_w[h][s] = __fmul_rn(s_w[h][s], inv);
+  }
+  __syncthreads();
+  float y[PER];
+#pragma unroll
+  for (int i = 0; i < PER; ++i) y[i] = 0.f;
+  for (int s = 0; s < nsplit; ++s) {
+    const float* po = a.part_o + ((int64_t)s * nrows + (r - a.r0)) * q;
+#pragma unroll
+    for (int i = 0; i < PER; ++i) {
+      const int k = tid + kCombThreads * i;
+      if (k < q) y[i] = fmaf(po[k], s_w[k / hd][s], y[i]);
+    }
+  }
+  const int64_t orow = r - out.row_base;
+#pragma unroll
+  for (int i = 0; i < PER; ++i) {
+    const int k = tid + kCombThreads * i;
+    const int b = 8 * i + warp;
+    if (b >= nb) continue;  // warp-uniform
+    if (out.f32) out.f32[(int64_t)r * q + k] = y[i];
+    const float amax = warp_max(fabsf(y[i]));
+    const float dd = __fdiv_rn(amax, 127.0f);
+    const float code = q8_code(y[i], q8_inv(dd));
+    const __half d16 = __float2half_rn(dd);
+    if (kGemvOut) {
+      out.q8[orow * (int64_t)nb * 32 + k] = (int8_t)code;
+      if (lane == 0) out.s8[orow * nb + b] = __half2float(d16);
+    } else {
+      out.q16[orow * out.ldq + k] = __float2half_rn(code);
+      if (lane == 0) out.s16[(int64_t)b * out.ldqs + orow] = __half2float(d16);
+    }
+  }
+}
+
+template <bool kGemvOut>
+cudaError_t combine_dispatch(const AttnArgs& a, const AttnOut& out, int rows, cudaStream_t st) {
+  const int per = (a.nh * a.hd + kCombThreads - 1) / kCombThreads;
+  if (per <= 4) attn_combine_kernel<kGemvOut, 4><<<rows, kCombThreads, 0, st>>>(a, out);
+  else if (per <= 8) attn_combine_kernel<kGemvOut, 8><<<rows, kCombThreads, 0, st>>>(a, out);
+  else if (per <= 16) attn_combine_kernel<kGemvOut, 16><<<rows, kCombThreads, 0, st>>>(a, out);
+  else return cudaErrorInvalidValue;
+  return cudaGetLastError();
+}
+
+// K/V rows of one layer -> fp16 hi/lo shadow planes (count f32 values each).
+__global__ void kv_shadow_kernel(const float* __restrict__ k, const float* __restrict__ v,
+                                 int64_t count, __half* kh, __half* kl, __half* vh, __half* vl) {
+  for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < count;
+       i += (int64_t)gridDim.x * blockDim.x) {
+    const float x = k[i], y = v[i];
+    const __half xh = __float2half_rn(x), yh = __float2half_rn(y);
+    kh[i] = xh;
+    kl[i] = __float2half_rn(__fsub_rn(x, __half2float(xh)));
+    vh[i] = yh;
+    vl[i] = __float2half_rn(__fsub_rn(y, __half2float(yh)));
   }
 }
 
 }  // namespace
 
-cudaError_t attention_launch(const AttnArgs& a, cudaStream_t st) {
+int attention_splits(int rows, int nkv, int n_ctx, int num_sms, int* ksplit) {
+  const int tiles = (rows + kTileQ - 1) / kTileQ;
+  if (tiles * nkv >= num_sms) {
+    *ksplit = (n_ctx + kTileKV - 1) / kTileKV * kTileKV;
+    return 1;
+  }
+  // 128 keys per split, fewer (longer) splits for very long regions
+  int ks = (n_ctx + kMaxSplitsSmem - 1) / kMaxSplitsSmem;
+  ks = ks < 128 ? 128 : (ks + kTileKV - 1) / kTileKV * kTileKV;
+  *ksplit = ks;
+  return (n_ctx + ks - 1) / ks;
+}
+
+cudaError_t attention_launch(const AttnArgs& a, const AttnOut& out, cudaStream_t st) {
   const int rows = a.r1 - a.r0;
   if (rows <= 0) return cudaSuccess;
   const int G = a.nh / a.nkv;
-  if (a.nh % a.nkv != 0 || G > 8) return cudaErrorInvalidValue;
-  dim3 grid((rows + kTileQ - 1) / kTileQ, a.nkv);
-  if (a.hd == 64) attn_kernel<64><<<grid, 32 * G, 0, st>>>(a);
-  else if (a.hd == 128) attn_kernel<128><<<grid, 32 * G, 0, st>>>(a);
-  else return cudaErrorInvalidValue;
+  if (a.nh % a.nkv != 0 || G > 8 || a.ksplit <= 0 || a.ksplit % kTileKV != 0)
+    return cudaErrorInvalidValue;
+  const int nsplit = (a.n_ctx + a.ksplit - 1) / a.ksplit;
+  const dim3 grid((rows + kTileQ - 1) / kTileQ, a.nkv, nsplit);
+  if (a.hd == 64) {
+    static bool set = false;
+    if (!set) {
+      cudaError_t e = cudaFuncSetAttribute(
+          attn_split_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize, Tile<64>::BYTES);
+      if (e != cudaSuccess) return e;
+      set = true;
+    }
+    attn_split_kernel<64><<<grid, 32 * G, Tile<64>::BYTES, st>>>(a);
+  } else if (a.hd == 128) {
+    static bool set = false;
+    if (!set) {
+      cudaError_t e = cudaFuncSetAttribute(
+          attn_split_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize, Tile<128>::BYTES);
+      if (e != cudaSuccess) return e;
+      set = true;
+    }
+    attn_split_kernel<128><<<grid, 32 * G, Tile<128>::BYTES, st>>>(a);
+  } else {
+    return cudaErrorInvalidValue;
+  }
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  if (a.nh > kMaxHeads || (a.n_ctx + a.ksplit - 1) / a.ksplit > kMaxSplitsSmem)
+    return cudaErrorInvalidValue;
+  return out.q8 ? combine_dispatch<true>(a, out, rows, st) : combine_dispatch<false>(a, out, rows, st);
+}
+
+cudaError_t kv_shadow_launch(const float* k, const float* v, int64_t count, __half* const* planes,
+                             cudaStream_t st) {
+  int64_t g = (count + 255) / 256;
+  if (g > 4096) g = 4096;
+  if (g < 1) g = 1;
+  kv_shadow_kernel<<<(unsigned)g, 256, 0, st>>>(k, v, count, planes[0], planes[1], planes[2],
+                                                planes[3]);
   return cudaGetLastError();
 }
 

@@ -83,7 +83,7 @@ __device__ __forceinline__ float silu_mul(float g, float u) {
   return __fmul_rn(__fdiv_rn(g, __fadd_rn(1.0f, expf(-g))), u);
 }
 
-template <int BN>
+template <int BN, int EPI>
 __global__ void __launch_bounds__(kThreads, 1)
     gemm_q8_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                    const __grid_constant__ CUtensorMap tmSA,
@@ -249,19 +249,21 @@ __global__ void __launch_bounds__(kThreads, 1)
               tmem_base + ((uint32_t)(quad * 32) << 16) + (uint32_t)(slot * BN + half * C::CPW);
           const int b = 2 * s + blk;
 #pragma unroll
-          for (int c = 0; c < C::CPW; c += 32) {
-            uint32_t r[32];
-            tmem_ld32(taddr + c, r);
+          for (int c = 0; c < C::CPW; c += 64) {
+            // both 32-column loads in flight before one wait
+            uint32_t r[64];
+            tmem_ld32(taddr + c, *reinterpret_cast<uint32_t(*)[32]>(&r[0]));
+            tmem_ld32(taddr + c + 32, *reinterpret_cast<uint32_t(*)[32]>(&r[32]));
             tmem_wait_ld();
-            if (c + 32 >= C::CPW) {
+            if (c + 64 >= C::CPW) {
               // slot fully read: hand it back to the MMA issuer
               tc_fence_before();
               __syncwarp();
               if (lane == 0) mbar_arrive(&tempty[slot]);
             }
-            if (p.epi == kEpiDots && m < p.M && b < p.nb) {
+            if (EPI == kEpiDots && m < p.M && b < p.nb) {
 #pragma unroll
-              for (int j = 0; j < 32; ++j) {
+              for (int j = 0; j < 64; ++j) {
                 const int n = ncol0 + c + j;
                 if (n < p.N)
                   p.dots[((int64_t)m * p.N + n) * p.nb + b] = __float2int_rn(__uint_as_float(r[j]));
@@ -269,11 +271,15 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             const float2 da2 = make_float2(da, da);
 #pragma unroll
-            for (int j = 0; j < 32; j += 2) {
-              const float2 w2 = *reinterpret_cast<const float2*>(dw + c + j);
-              const float2 sc = __fmul2_rn(da2, w2);
-              const float2 v = make_float2(__uint_as_float(r[j]), __uint_as_float(r[j + 1]));
-              acc[(c + j) / 2] = __ffma2_rn(v, sc, acc[(c + j) / 2]);
+            for (int j = 0; j < 64; j += 4) {
+              const float4 w4 = *reinterpret_cast<const float4*>(dw + c + j);
+              const float2 s0 = __fmul2_rn(da2, make_float2(w4.x, w4.y));
+              const float2 s1 = __fmul2_rn(da2, make_float2(w4.z, w4.w));
+              acc[(c + j) / 2] = __ffma2_rn(
+                  make_float2(__uint_as_float(r[j]), __uint_as_float(r[j + 1])), s0, acc[(c + j) / 2]);
+              acc[(c + j) / 2 + 1] = __ffma2_rn(
+                  make_float2(__uint_as_float(r[j + 2]), __uint_as_float(r[j + 3])), s1,
+                  acc[(c + j) / 2 + 1]);
             }
           }
           ++sit;
@@ -287,7 +293,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
       // ---------------------------------------------------------- store
       if (m < p.M) {
-        if (p.epi == kEpiSwiGLU) {
+        if (EPI == kEpiSwiGLU) {
           // columns come in groups of 64: 32 gate then 32 up rows of W
 #pragma unroll
           for (int g0 = 0; g0 < C::CPW; g0 += 64) {
@@ -367,12 +373,12 @@ int make_map(CUtensorMap* map, const void* base, CUtensorMapDataType dt, uint64_
   return r == CUDA_SUCCESS ? 0 : -2;
 }
 
-template <int BN>
+template <int BN, int EPI>
 cudaError_t launch_bn(const GemmLaunch& g, const GemmMaps& maps, int num_sms, cudaStream_t st) {
   using C = Cfg<BN>;
   static bool attr_set = false;
   if (!attr_set) {
-    cudaError_t e = cudaFuncSetAttribute(gemm_q8_kernel<BN>,
+    cudaError_t e = cudaFuncSetAttribute(gemm_q8_kernel<BN, EPI>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
     if (e != cudaSuccess) return e;
     attr_set = true;
@@ -400,7 +406,7 @@ cudaError_t launch_bn(const GemmLaunch& g, const GemmMaps& maps, int num_sms, cu
   a.err = g.err;
   const int total = a.m_tiles * a.n_tiles * a.splits;
   const int grid = std::max(1, std::min(total, num_sms));
-  gemm_q8_kernel<BN><<<grid, kThreads, C::SMEM, st>>>(maps.a, maps.b, maps.sa, maps.sb, a);
+  gemm_q8_kernel<BN, EPI><<<grid, kThreads, C::SMEM, st>>>(maps.a, maps.b, maps.sa, maps.sb, a);
   return cudaGetLastError();
 }
 
@@ -411,7 +417,7 @@ GemmPlan gemm_plan(int64_t M, int64_t N, int nb, int num_sms, bool allow_split) 
   const int64_t mt = (M + kBM - 1) / kBM;
   const int stages = (nb + 1) / 2;
   // wide N: 256-column tiles when they still fill the machine
-  p.bn = (mt * ((N + 255) / 256) >= num_sms) ? 256 : 128;
+  p.bn = 128;
   const int64_t tiles = mt * ((N + p.bn - 1) / p.bn);
   p.splits = 1;
   if (allow_split && tiles < num_sms) {
@@ -439,9 +445,13 @@ int gemm_make_maps(const GemmOperand& A, const GemmOperand& B, int bn, GemmMaps*
 
 cudaError_t gemm_launch(const GemmLaunch& g, const GemmMaps& maps, int num_sms,
                         cudaStream_t stream) {
-  if (g.A.nb != g.B.nb) return cudaErrorInvalidValue;
-  if (g.plan.bn == 256) return launch_bn<256>(g, maps, num_sms, stream);
-  return launch_bn<128>(g, maps, num_sms, stream);
+  if (g.A.nb != g.B.nb || g.plan.bn != 128) return cudaErrorInvalidValue;
+  switch (g.epi) {
+    case kEpiF32: return launch_bn<128, kEpiF32>(g, maps, num_sms, stream);
+    case kEpiSwiGLU: return launch_bn<128, kEpiSwiGLU>(g, maps, num_sms, stream);
+    case kEpiDots: return launch_bn<128, kEpiDots>(g, maps, num_sms, stream);
+    default: return cudaErrorInvalidValue;
+  }
 }
 
 }  // namespace minfer

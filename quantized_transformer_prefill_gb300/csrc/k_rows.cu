@@ -17,8 +17,6 @@ namespace minfer {
 
 namespace {
 
-constexpr int kRowThreads = 128;
-constexpr int kMaxPerThread = 32;  // rows up to 4096 elements
 
 // ---------------------------------------------------------------- error-free sums
 // Knuth's TwoSum and the fma-based TwoProduct: the pair (hi, lo) carries the
@@ -39,34 +37,50 @@ __device__ __forceinline__ void ff_add(float& hi, float& lo, float bhi, float bl
 }
 
 // ---------------------------------------------------------------- row quant
-// One CTA (128 threads) per row.  Thread i holds elements i + 128 k; in step
-// k, warp w holds block 4k + w, lane = element within the block.
-template <bool kGemvOut>
+// One CTA of 256 threads per row; thread i holds elements i + 256 k (k < PER,
+// all loads issued before any arithmetic).  In step k, warp w holds block
+// 8 k + w, so a block's amax is a 5-step shuffle max.  The sum of squares is
+// a float-float (hi, lo) pair reduced over the warp, then over the 8 warps.
+constexpr int kRowThreads = 256;
+
+template <bool kGemvOut, int PER>
 __global__ void __launch_bounds__(kRowThreads) row_quant_kernel(const RowQuantArgs a) {
   __shared__ float red_hi[kRowThreads / 32], red_lo[kRowThreads / 32];
   __shared__ float s_scale;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int64_t r = blockIdx.x;
   const int64_t hr = a.row_offset + r;
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int64_t n = a.n;
-  const int per = (int)((n + kRowThreads - 1) / kRowThreads);
+  const int nb = (int)((n + 31) / 32);
   float* hrow = a.h + hr * n;
 
-  float x[kMaxPerThread];
+  float x[PER];
 #pragma unroll
-  for (int i = 0; i < kMaxPerThread; ++i) {
-    x[i] = 0.f;
-    if (i < per) {
+  for (int i = 0; i < PER; ++i) {
+    const int64_t k = tid + (int64_t)kRowThreads * i;
+    x[i] = k < n ? hrow[k] : 0.f;
+  }
+  if (a.nsplit > 0) {
+    float o[PER];
+#pragma unroll
+    for (int i = 0; i < PER; ++i) {
+      const int64_t k = tid + (int64_t)kRowThreads * i;
+      o[i] = k < n ? a.partials[hr * n + k] : 0.f;
+    }
+    for (int s = 1; s < a.nsplit; ++s) {
+      const float* ps = a.partials + s * a.split_stride + hr * n;
+#pragma unroll
+      for (int i = 0; i < PER; ++i) {
+        const int64_t k = tid + (int64_t)kRowThreads * i;
+        if (k < n) o[i] = __fadd_rn(o[i], ps[k]);
+      }
+    }
+#pragma unroll
+    for (int i = 0; i < PER; ++i) {
       const int64_t k = tid + (int64_t)kRowThreads * i;
       if (k < n) {
-        float v = hrow[k];
-        if (a.nsplit > 0) {
-          float o = a.partials[hr * n + k];
-          for (int s = 1; s < a.nsplit; ++s) o = __fadd_rn(o, a.partials[s * a.split_stride + hr * n + k]);
-          v = __fadd_rn(v, o);
-          hrow[k] = v;
-        }
-        x[i] = v;
+        x[i] = __fadd_rn(x[i], o[i]);
+        hrow[k] = x[i];
       }
     }
   }
@@ -75,12 +89,9 @@ __global__ void __launch_bounds__(kRowThreads) row_quant_kernel(const RowQuantAr
   if (a.norm_w) {
     float hi = 0.f, lo = 0.f;
 #pragma unroll
-    for (int i = 0; i < kMaxPerThread; ++i) {
-      if (i < per) {
-        const float p = __fmul_rn(x[i], x[i]);
-        const float e = fmaf(x[i], x[i], -p);
-        ff_add(hi, lo, p, e);
-      }
+    for (int i = 0; i < PER; ++i) {
+      const float p = __fmul_rn(x[i], x[i]);
+      ff_add(hi, lo, p, fmaf(x[i], x[i], -p));
     }
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) {
@@ -88,7 +99,10 @@ __global__ void __launch_bounds__(kRowThreads) row_quant_kernel(const RowQuantAr
       const float blo = __shfl_xor_sync(0xffffffffu, lo, o);
       ff_add(hi, lo, bhi, blo);
     }
-    if (lane == 0) { red_hi[warp] = hi; red_lo[warp] = lo; }
+    if (lane == 0) {
+      red_hi[warp] = hi;
+      red_lo[warp] = lo;
+    }
     __syncthreads();
     if (tid == 0) {
       float h2 = red_hi[0], l2 = red_lo[0];
@@ -100,32 +114,41 @@ __global__ void __launch_bounds__(kRowThreads) row_quant_kernel(const RowQuantAr
     scale = s_scale;
   }
 
-  const int nb = (int)((n + 31) / 32);
 #pragma unroll
-  for (int i = 0; i < kMaxPerThread; ++i) {
-    if (i < per) {
-      const int64_t k = tid + (int64_t)kRowThreads * i;
-      const int b = 4 * i + warp;
-      float y = x[i];
-      if (a.norm_w) y = (k < n) ? __fmul_rn(__fmul_rn(y, scale), a.norm_w[k]) : 0.f;
-      const float amax = warp_max(fabsf(y));
-      if (b < nb) {
-        const float d = __fdiv_rn(amax, 127.0f);
-        const float code = q8_code(y, q8_inv(d));
-        const __half d16 = __float2half_rn(d);
-        if (kGemvOut) {
-          a.q8[r * (int64_t)nb * 32 + k] = (int8_t)code;
-          if (lane == 0) {
-            a.s8[r * nb + b] = __half2float(d16);
-            if (a.s8_bits) a.s8_bits[r * nb + b] = __half_as_ushort(d16);
-          }
-        } else {
-          a.q16[r * a.ldq + k] = __float2half_rn(code);
-          if (lane == 0) a.s16[(int64_t)b * a.ldqs + r] = __half2float(d16);
-        }
+  for (int i = 0; i < PER; ++i) {
+    const int64_t k = tid + (int64_t)kRowThreads * i;
+    const int b = 8 * i + warp;
+    if (b >= nb) continue;  // warp-uniform
+    float y = x[i];
+    if (a.norm_w) y = (k < n) ? __fmul_rn(__fmul_rn(y, scale), a.norm_w[k]) : 0.f;
+    const float amax = warp_max(fabsf(y));
+    const float d = __fdiv_rn(amax, 127.0f);
+    const float code = q8_code(y, q8_inv(d));
+    const __half d16 = __float2half_rn(d);
+    if (kGemvOut) {
+      a.q8[r * (int64_t)nb * 32 + k] = (int8_t)code;
+      if (lane == 0) {
+        a.s8[r * nb + b] = __half2float(d16);
+        if (a.s8_bits) a.s8_bits[r * nb + b] = __half_as_ushort(d16);
       }
+    } else {
+      a.q16[r * a.ldq + k] = __float2half_rn(code);
+      if (lane == 0) a.s16[(int64_t)b * a.ldqs + r] = __half2float(d16);
     }
   }
+}
+
+template <bool kGemvOut>
+cudaError_t row_quant_dispatch(const RowQuantArgs& a, cudaStream_t st) {
+  const int per = (int)((a.n + kRowThreads - 1) / kRowThreads);
+  const unsigned grid = (unsigned)a.rows;
+  if (per <= 1) row_quant_kernel<kGemvOut, 1><<<grid, kRowThreads, 0, st>>>(a);
+  else if (per <= 2) row_quant_kernel<kGemvOut, 2><<<grid, kRowThreads, 0, st>>>(a);
+  else if (per <= 4) row_quant_kernel<kGemvOut, 4><<<grid, kRowThreads, 0, st>>>(a);
+  else if (per <= 8) row_quant_kernel<kGemvOut, 8><<<grid, kRowThreads, 0, st>>>(a);
+  else if (per <= 16) row_quant_kernel<kGemvOut, 16><<<grid, kRowThreads, 0, st>>>(a);
+  else return cudaErrorInvalidValue;
+  return cudaGetLastError();
 }
 
 // ---------------------------------------------------------------- embedding
@@ -174,40 +197,60 @@ __global__ void rope_store_kernel(const RopeStoreArgs a) {
   const int p_in = a.pos[t];
   // an out-of-range position is reported by validation; it only selects a
   // table row here (clamped) and never a region row
-  const bool write_kv = ((a.status == nullptr) || (*a.status == 0)) && p_in >= 0 && p_in < a.n_ctx;
+  const bool write_kv =
+      ((a.status == nullptr) || (*a.status == 0)) && p_in >= 0 && p_in < a.n_ctx;
   const int p = (p_in >= 0 && p_in < a.n_ctx) ? p_in : 0;
-  const int half = a.hd / 2;
+  const int half = a.hd >> 1;
+  const int hshift = half == 64 ? 6 : 5;  // head_dim is 64 or 128
   const int W = (a.nh + 2 * a.nkv) * a.hd;
   const int64_t row = (int64_t)t * W;
   const int npairs = (a.nh + a.nkv) * half;
+  const int kw = a.nkv * a.hd;
   const float* cs = a.cos_t + (int64_t)p * half;
   const float* sn = a.sin_t + (int64_t)p * half;
-  auto load = [&](int e) -> float {
-    float o = a.partials[row + e];
-    for (int s = 1; s < a.nsplit; ++s) o = __fadd_rn(o, a.partials[s * a.split_stride + row + e]);
-    return a.bias ? __fadd_rn(o, a.bias[e]) : o;
-  };
-  for (int pi = threadIdx.x; pi < npairs; pi += blockDim.x) {
-    const int head = pi / half, i = pi % half;
-    const int e0 = head * a.hd + i;
-    const float x0 = load(e0), x1 = load(e0 + half);
-    const float c = cs[i], s = sn[i];
-    const float v0 = __fsub_rn(__fmul_rn(x0, c), __fmul_rn(x1, s));
-    const float v1 = __fadd_rn(__fmul_rn(x0, s), __fmul_rn(x1, c));
-    if (head < a.nh) {
-      a.q_out[(int64_t)t * a.nh * a.hd + e0] = v0;
-      a.q_out[(int64_t)t * a.nh * a.hd + e0 + half] = v1;
+  for (int pi = threadIdx.x; pi < npairs + kw; pi += blockDim.x) {
+    if (pi < npairs) {
+      const int head = pi >> hshift, i = pi & (half - 1);
+      const int e0 = head * a.hd + i;
+      float x0 = a.partials[row + e0], x1 = a.partials[row + e0 + half];
+      for (int s = 1; s < a.nsplit; ++s) {
+        const float* ps = a.partials + s * a.split_stride + row;
+        x0 = __fadd_rn(x0, ps[e0]);
+        x1 = __fadd_rn(x1, ps[e0 + half]);
+      }
+      if (a.bias) {
+        x0 = __fadd_rn(x0, a.bias[e0]);
+        x1 = __fadd_rn(x1, a.bias[e0 + half]);
+      }
+      const float c = cs[i], sv = sn[i];
+      const float v0 = __fsub_rn(__fmul_rn(x0, c), __fmul_rn(x1, sv));
+      const float v1 = __fadd_rn(__fmul_rn(x0, sv), __fmul_rn(x1, c));
+      if (head < a.nh) {
+        a.q_out[(int64_t)t * a.nh * a.hd + e0] = v0;
+        a.q_out[(int64_t)t * a.nh * a.hd + e0 + half] = v1;
+      } else if (write_kv) {
+        const int ke = (head - a.nh) * a.hd + i;
+        const int64_t o0 = (int64_t)p * kw + ke;
+        a.kreg[o0] = v0;
+        a.kreg[o0 + half] = v1;
+        const __half h0 = __float2half_rn(v0), h1 = __float2half_rn(v1);
+        a.shadow[0][o0] = h0;
+        a.shadow[0][o0 + half] = h1;
+        a.shadow[1][o0] = __float2half_rn(__fsub_rn(v0, __half2float(h0)));
+        a.shadow[1][o0 + half] = __float2half_rn(__fsub_rn(v1, __half2float(h1)));
+      }
     } else if (write_kv) {
-      const int64_t kw = (int64_t)a.nkv * a.hd;
-      const int ke = (head - a.nh) * a.hd + i;
-      a.kreg[(int64_t)p * kw + ke] = v0;
-      a.kreg[(int64_t)p * kw + ke + half] = v1;
+      const int e = pi - npairs;
+      const int col = (a.nh + a.nkv) * a.hd + e;
+      float v = a.partials[row + col];
+      for (int s = 1; s < a.nsplit; ++s) v = __fadd_rn(v, a.partials[s * a.split_stride + row + col]);
+      if (a.bias) v = __fadd_rn(v, a.bias[col]);
+      const int64_t o0 = (int64_t)p * kw + e;
+      a.vreg[o0] = v;
+      const __half vh = __float2half_rn(v);
+      a.shadow[2][o0] = vh;
+      a.shadow[3][o0] = __float2half_rn(__fsub_rn(v, __half2float(vh)));
     }
-  }
-  if (write_kv) {
-    const int kw = a.nkv * a.hd;
-    const int v0e = (a.nh + a.nkv) * a.hd;
-    for (int e = threadIdx.x; e < kw; e += blockDim.x) a.vreg[(int64_t)p * kw + e] = load(v0e + e);
   }
 }
 
@@ -357,10 +400,7 @@ int grid_for(int64_t work, int threads) {
 
 cudaError_t row_quant_launch(const RowQuantArgs& a, cudaStream_t st) {
   if (a.rows <= 0) return cudaSuccess;
-  if (a.n > (int64_t)kRowThreads * kMaxPerThread) return cudaErrorInvalidValue;
-  if (a.q8) row_quant_kernel<true><<<(unsigned)a.rows, kRowThreads, 0, st>>>(a);
-  else row_quant_kernel<false><<<(unsigned)a.rows, kRowThreads, 0, st>>>(a);
-  return cudaGetLastError();
+  return a.q8 ? row_quant_dispatch<true>(a, st) : row_quant_dispatch<false>(a, st);
 }
 
 cudaError_t embed_launch(const int8_t* q, const float* s, int64_t kpad, int nb, const int32_t* ids,
@@ -377,7 +417,7 @@ cudaError_t validate_launch(const int32_t* ids, const int32_t* pos, int nt, int 
 
 cudaError_t rope_store_launch(const RopeStoreArgs& a, cudaStream_t st) {
   if (a.nt <= 0) return cudaSuccess;
-  rope_store_kernel<<<a.nt, 128, 0, st>>>(a);
+  rope_store_kernel<<<a.nt, 256, 0, st>>>(a);
   return cudaGetLastError();
 }
 

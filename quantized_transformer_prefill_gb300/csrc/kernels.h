@@ -116,22 +116,44 @@ struct RopeStoreArgs {
   float* q_out = nullptr;  // [nt][nh*hd]
   float* kreg = nullptr;   // [n_ctx][nkv*hd]
   float* vreg = nullptr;
+  __half* shadow[4] = {nullptr, nullptr, nullptr, nullptr};  // fp16 hi/lo copies of K, V
   const int* status = nullptr;  // skip all writes to the regions when *status != 0
 };
 cudaError_t rope_store_launch(const RopeStoreArgs& a, cudaStream_t stream);
 
-// Causal GQA attention of query rows [r0, r1).
+// Causal GQA attention of query rows [r0, r1) over the fp16 hi/lo shadow
+// planes of a layer's K/V regions, split along the keys (ksplit keys per
+// split, a multiple of 32), then merged, normalized and quantized.
 struct AttnArgs {
   const float* q = nullptr;  // [nt][nh*hd]
   const int32_t* pos = nullptr;
   int r0 = 0, r1 = 0;
-  const float* k = nullptr;  // [n_ctx][nkv*hd]
-  const float* v = nullptr;
+  const __half* shadow[4] = {nullptr, nullptr, nullptr, nullptr};  // K hi, K lo, V hi, V lo [n_ctx][nkv*hd]
   int nh = 0, nkv = 0, hd = 0;
-  int n_ctx = 0;       // positions are clamped into [0, n_ctx) before any region read
-  float* o = nullptr;  // [nt][nh*hd]
+  int n_ctx = 0;        // positions are clamped into [0, n_ctx) before any region read
+  int ksplit = 0;
+  float* part_o = nullptr;   // scratch [n_ctx/ksplit][r1-r0][nh][hd]
+  float* part_ml = nullptr;  // scratch [n_ctx/ksplit][r1-r0][nh][2]
 };
-cudaError_t attention_launch(const AttnArgs& a, cudaStream_t stream);
+// Where the attention output goes: Q8_0 codes in the GEMM layout (q16 [rows][ldq]
+// fp16 + s16 [nb][ldqs]) or the GEMV layout (q8 [rows][nb*32] + s8 [rows][nb]);
+// output row index = query row - row_base.  f32 (optional): [nt][nh*hd].
+struct AttnOut {
+  __half* q16 = nullptr;
+  int64_t ldq = 0;
+  float* s16 = nullptr;
+  int64_t ldqs = 0;
+  int8_t* q8 = nullptr;
+  float* s8 = nullptr;
+  int64_t row_base = 0;
+  float* f32 = nullptr;
+};
+// Number of key splits and the split length for rows query rows.
+int attention_splits(int rows, int nkv, int n_ctx, int num_sms, int* ksplit);
+cudaError_t attention_launch(const AttnArgs& a, const AttnOut& out, cudaStream_t stream);
+// f32 K/V values -> fp16 hi/lo planes (planes[0..3] = K hi, K lo, V hi, V lo).
+cudaError_t kv_shadow_launch(const float* k, const float* v, int64_t count, __half* const* planes,
+                             cudaStream_t stream);
 
 // One-row quantized GEMV: y[n] = sum_b dw[n][b] * da[b] * dot_b (+ resid[n]).
 // W int8 [N][kpad] + f32 scales [N][nb]; x int8 [kpad] + f32 scales [nb].

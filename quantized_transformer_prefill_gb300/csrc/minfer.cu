@@ -161,11 +161,15 @@ struct Workspace {
   float* t_s = nullptr;      // [max nb]
   float* gu = nullptr;       // [2F]
   float* logits = nullptr;   // [V]
+  float* att_o = nullptr;    // attention split scratch [splits][nt][q]
+  float* att_ml = nullptr;   // [splits][nt][nh][2]
+  size_t att_o_cap = 0, att_ml_cap = 0;
   int ntp = 0;
   void release() {
     dfree(ids); dfree(pos); dfree(h); dfree(xa); dfree(xa_s); dfree(xf); dfree(xf_s);
     dfree(part); dfree(qrot); dfree(att); dfree(h_last); dfree(t_q); dfree(t_s); dfree(gu);
-    dfree(logits);
+    dfree(logits); dfree(att_o); dfree(att_ml);
+    att_o_cap = att_ml_cap = 0;
     max_nt = 0;
   }
 };
@@ -186,11 +190,13 @@ struct minfer_kv {
   minfer_model* m = nullptr;
   int n_ctx = 0;
   float* regions = nullptr;  // [L][2][n_ctx][kvw]
+  __half* shadow = nullptr;  // [L][4][n_ctx][kvw]: fp16 hi/lo of K and V, read by attention
   float* cos_t = nullptr;    // [n_ctx][hd/2]
   float* sin_t = nullptr;
   uint32_t* seen = nullptr;  // n_ctx bits (duplicate-position check)
   float* k(int l) const;
   float* v(int l) const;
+  __half* plane(int l, int i) const;
 };
 
 struct minfer_model {
@@ -239,6 +245,7 @@ struct minfer_model {
   float* dump_host = nullptr;
   int dump_max_nt = 0;
   int last_device_status = 0;
+  bool debug_f32 = false;  // also write the f32 attention output (debug reads)
 };
 
 float* minfer_kv::k(int l) const {
@@ -246,6 +253,9 @@ float* minfer_kv::k(int l) const {
 }
 float* minfer_kv::v(int l) const {
   return regions + ((int64_t)l * 2 + 1) * n_ctx * m->kvw;
+}
+__half* minfer_kv::plane(int l, int i) const {
+  return shadow + ((int64_t)l * 4 + i) * n_ctx * m->kvw;
 }
 
 namespace {
@@ -642,6 +652,7 @@ int enqueue_forward(minfer_model* m, minfer_kv* kv, const int32_t* ids, const in
       r.q_out = w.qrot;
       r.kreg = kv->k(l);
       r.vreg = kv->v(l);
+      for (int i = 0; i < 4; ++i) r.shadow[i] = kv->plane(l, i);
       r.status = m->d_status;
       LAUNCH(kKRope, rope_store_launch(r, st));
     }
@@ -650,26 +661,28 @@ int enqueue_forward(minfer_model* m, minfer_kv* kv, const int32_t* ids, const in
     at.pos = pos;
     at.r0 = last ? nt - 1 : 0;
     at.r1 = nt;
-    at.k = kv->k(l);
-    at.v = kv->v(l);
+    for (int i = 0; i < 4; ++i) at.shadow[i] = kv->plane(l, i);
     at.nh = hp.n_head;
     at.nkv = hp.n_head_kv;
     at.hd = hp.head_dim;
     at.n_ctx = kv->n_ctx;
-    at.o = w.att;
-    LAUNCH(kKAttn, attention_launch(at, st));
+    attention_splits(at.r1 - at.r0, at.nkv, at.n_ctx, m->num_sms, &at.ksplit);
+    at.part_o = w.att_o;
+    at.part_ml = w.att_ml;
+    AttnOut ao;
+    ao.f32 = m->debug_f32 ? w.att : nullptr;
     if (!last) {
-      {
-        RowQuantArgs r;
-        r.h = w.att;
-        r.rows = nt;
-        r.n = m->q;
-        r.q16 = w.xa;
-        r.ldq = (int64_t)m->nbq * 32;
-        r.s16 = w.xa_s;
-        r.ldqs = ntp;
-        LAUNCH(kKRowQuant, row_quant_launch(r, st));
-      }
+      ao.q16 = w.xa;
+      ao.ldq = (int64_t)m->nbq * 32;
+      ao.s16 = w.xa_s;
+      ao.ldqs = ntp;
+    } else {
+      ao.q8 = w.t_q;
+      ao.s8 = w.t_s;
+      ao.row_base = nt - 1;
+    }
+    LAUNCH(kKAttn, attention_launch(at, ao, st));
+    if (!last) {
       if ((rc = gemm_call(m, L, kKGemmO, xo, Ly.wo, nt, kEpiF32, true, w.part, m->H, nullptr, 0,
                           nullptr, 0, &ns)))
         return rc;
@@ -715,16 +728,6 @@ int enqueue_forward(minfer_model* m, minfer_kv* kv, const int32_t* ids, const in
     } else {
       // last row only: o-projection, FFN, final norm, lm_head as GEMVs
       const int64_t last_row = nt - 1;
-      {
-        RowQuantArgs r;
-        r.h = w.att;
-        r.row_offset = last_row;
-        r.rows = 1;
-        r.n = m->q;
-        r.q8 = w.t_q;
-        r.s8 = w.t_s;
-        LAUNCH(kKRowQuant, row_quant_launch(r, st));
-      }
       {
         GemvArgs g;
         g.wq = Ly.wo_v.q;
@@ -807,10 +810,36 @@ int enqueue_forward(minfer_model* m, minfer_kv* kv, const int32_t* ids, const in
 }
 
 // Run (record or replay) the forward on stream st.
+int ensure_attn_scratch(minfer_model* m, int nt, int n_ctx) {
+  Workspace& w = m->ws;
+  int ks = 0;
+  const int ns = attention_splits(nt, m->hp.n_head_kv, n_ctx, m->num_sms, &ks);
+  const size_t need_o = (size_t)ns * nt * m->q;
+  const size_t need_ml = (size_t)ns * nt * m->hp.n_head * 2;
+  if (need_o <= w.att_o_cap && need_ml <= w.att_ml_cap) return MINFER_OK;
+  if (m->gexec) {
+    cudaGraphExecDestroy(m->gexec);
+    m->gexec = nullptr;
+  }
+  if (m->graph) {
+    cudaGraphDestroy(m->graph);
+    m->graph = nullptr;
+  }
+  dfree(w.att_o);
+  dfree(w.att_ml);
+  w.att_o_cap = w.att_ml_cap = 0;
+  int rc;
+  if ((rc = dalloc(&w.att_o, need_o)) || (rc = dalloc(&w.att_ml, need_ml))) return rc;
+  w.att_o_cap = need_o;
+  w.att_ml_cap = need_ml;
+  return MINFER_OK;
+}
+
 int run_forward(minfer_model* m, minfer_kv* kv, const int32_t* ids, const int32_t* pos, int nt,
                 float* logits, cudaStream_t st) {
   int rc = ensure_workspace(m, nt);
   if (rc) return rc;
+  if ((rc = ensure_attn_scratch(m, nt, kv->n_ctx))) return rc;
   const bool dumps = m->dump_host != nullptr && nt <= m->dump_max_nt;
   if (dumps) {
     // dumps copy to host memory mid-sequence: run eagerly
@@ -990,6 +1019,7 @@ int minfer_kv_create(minfer_model* m, int n_ctx, minfer_kv** out) {
   std::vector<float> c, s;
   rope_tables(kv->n_ctx, m->hp.head_dim, m->hp.rope_theta, c, s);
   if ((rc = dalloc(&kv->regions, (size_t)m->hp.n_layer * 2 * kv->n_ctx * m->kvw)) ||
+      (rc = dalloc(&kv->shadow, (size_t)m->hp.n_layer * 4 * kv->n_ctx * m->kvw)) ||
       (rc = dalloc(&kv->cos_t, c.size())) || (rc = dalloc(&kv->sin_t, s.size())) ||
       (rc = dalloc(&kv->seen, (size_t)(kv->n_ctx + 31) / 32))) {
     minfer_kv_free(kv);
@@ -1017,6 +1047,7 @@ void minfer_kv_free(minfer_kv* kv) {
     kv->m->gkey = minfer_model::GraphKey();
   }
   dfree(kv->regions);
+  dfree(kv->shadow);
   dfree(kv->cos_t);
   dfree(kv->sin_t);
   dfree(kv->seen);
@@ -1040,6 +1071,13 @@ int minfer_kv_write(minfer_kv* kv, int layer, int which, int row0, int nrows, co
   float* dst = (which ? kv->v(layer) : kv->k(layer)) + (int64_t)row0 * kv->m->kvw;
   CK(cudaDeviceSynchronize());
   CK(cudaMemcpy(dst, in, (size_t)nrows * kv->m->kvw * 4, cudaMemcpyHostToDevice));
+  // keep the fp16 hi/lo copies the attention reads in step with the regions
+  const int64_t off = (int64_t)row0 * kv->m->kvw;
+  __half* planes[4];
+  for (int i = 0; i < 4; ++i) planes[i] = kv->plane(layer, i) + off;
+  CK(kv_shadow_launch(kv->k(layer) + off, kv->v(layer) + off, (int64_t)nrows * kv->m->kvw, planes,
+                      0));
+  CK(cudaDeviceSynchronize());
   return MINFER_OK;
 }
 
@@ -1094,6 +1132,7 @@ int minfer_set_dump(minfer_model* m, float* host_hidden, int max_tokens) {
   if (!m || (host_hidden && max_tokens <= 0)) return MINFER_ERR_ARG;
   m->dump_host = host_hidden;
   m->dump_max_nt = host_hidden ? max_tokens : 0;
+  m->debug_f32 = host_hidden != nullptr;
   return MINFER_OK;
 }
 
@@ -1287,22 +1326,57 @@ int minfer_op_attention(const float* d_q, const int32_t* d_pos, int nt, const fl
                         const float* d_v, int n_ctx, int n_head, int n_head_kv, int head_dim,
                         float* d_o) {
   if (!d_q || !d_pos || !d_k || !d_v || !d_o || nt <= 0 || n_ctx <= 0 || n_head_kv <= 0 ||
-      n_head % n_head_kv != 0)
+      n_head % n_head_kv != 0 || head_dim % 32 != 0)
     return MINFER_ERR_ARG;
+  int num_sms = 148, dev = 0;
+  CK(cudaGetDevice(&dev));
+  CK(cudaDeviceGetAttribute(&num_sms, cudaDevAttrMultiProcessorCount, dev));
+  const int64_t kvw = (int64_t)n_head_kv * head_dim;
+  const int64_t q = (int64_t)n_head * head_dim;
   AttnArgs a;
   a.q = d_q;
   a.pos = d_pos;
   a.r0 = 0;
   a.r1 = nt;
-  a.k = d_k;
-  a.v = d_v;
   a.nh = n_head;
   a.nkv = n_head_kv;
   a.hd = head_dim;
   a.n_ctx = n_ctx;
-  a.o = d_o;
-  CK(attention_launch(a, 0));
-  CK(cudaDeviceSynchronize());
+  const int ns = attention_splits(nt, n_head_kv, n_ctx, num_sms, &a.ksplit);
+  __half* sh = nullptr;
+  float *po = nullptr, *pml = nullptr, *s16 = nullptr;
+  __half* q16 = nullptr;
+  int rc = dalloc(&sh, (size_t)4 * n_ctx * kvw);
+  if (!rc) rc = dalloc(&po, (size_t)ns * nt * q);
+  if (!rc) rc = dalloc(&pml, (size_t)ns * nt * n_head * 2);
+  if (!rc) rc = dalloc(&q16, (size_t)nt * q);
+  if (!rc) rc = dalloc(&s16, (size_t)(q / 32) * nt);
+  cudaError_t e = cudaSuccess;
+  if (!rc) {
+    __half* planes[4];
+    for (int i = 0; i < 4; ++i) {
+      planes[i] = sh + (int64_t)i * n_ctx * kvw;
+      a.shadow[i] = planes[i];
+    }
+    a.part_o = po;
+    a.part_ml = pml;
+    AttnOut out;
+    out.q16 = q16;
+    out.ldq = q;
+    out.s16 = s16;
+    out.ldqs = nt;
+    out.f32 = d_o;
+    e = kv_shadow_launch(d_k, d_v, (int64_t)n_ctx * kvw, planes, 0);
+    if (e == cudaSuccess) e = attention_launch(a, out, 0);
+    if (e == cudaSuccess) e = cudaDeviceSynchronize();
+  }
+  dfree(sh);
+  dfree(po);
+  dfree(pml);
+  dfree(q16);
+  dfree(s16);
+  if (rc) return rc;
+  CK(e);
   return MINFER_OK;
 }
 
@@ -1333,10 +1407,16 @@ int minfer_op_rope_store(const float* d_qkv, const float* d_bias, const int32_t*
   a.q_out = d_q_out;
   a.kreg = d_k;
   a.vreg = d_v;
+  __half* sh = nullptr;
+  const int64_t kvw = (int64_t)n_head_kv * head_dim;
+  if (!rc) rc = dalloc(&sh, (size_t)4 * n_ctx * kvw);
+  if (!rc)
+    for (int i = 0; i < 4; ++i) a.shadow[i] = sh + (int64_t)i * n_ctx * kvw;
   if (!rc && e == cudaSuccess) e = rope_store_launch(a, 0);
   if (!rc && e == cudaSuccess) e = cudaDeviceSynchronize();
   dfree(dc);
   dfree(ds);
+  dfree(sh);
   if (rc) return rc;
   CK(e);
   return MINFER_OK;
