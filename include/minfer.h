@@ -47,6 +47,7 @@ extern "C" {
 #define MINFER_ERR_OOM (-7)            /* device allocation failed */
 #define MINFER_ERR_DEVICE (-8)         /* a kernel gave up a bounded wait (status word set) */
 #define MINFER_ERR_STATE (-9)          /* call order violated (e.g. prefill before finalize) */
+#define MINFER_ERR_TOO_LARGE (-10)     /* the problem does not fit a fixed-size scratch area */
 
 /* ---------------------------------------------------------------- tensors */
 #define MINFER_F32 0  /* float32 values */
@@ -217,6 +218,20 @@ int minfer_op_attention(const float* d_q, const int32_t* d_pos, int nt, const fl
 int minfer_op_rope_store(const float* d_qkv, const float* d_bias, const int32_t* d_pos, int nt,
                          int n_head, int n_head_kv, int head_dim, float theta, int n_ctx,
                          float* d_q_out, float* d_k, float* d_v);
+
+/* Same product as minfer_op_gemm (same kernels, same split plan) without any
+ * device allocation: for callers that cannot call cudaMalloc (their own
+ * allocator owns nearly all device memory, or they must not trigger the
+ * device-wide synchronization of cudaFree).  The operand planes and split-K
+ * partials live in a 32 MiB __device__ array inside the library, which every
+ * GPU that loads the library holds until exit; a problem whose scratch does
+ * not fit returns MINFER_ERR_TOO_LARGE before any device work.  The first call
+ * on each device looks up the array's device address (do it before any stream
+ * capture).  All calls share the array: calls whose work overlaps on the GPU
+ * race.  Synchronous.  The pages have no counterpart of this entry point. */
+int minfer_op_gemm_noalloc(const int8_t* d_xq, const uint16_t* d_xd, int64_t M,
+                           const int8_t* d_wq, const uint16_t* d_wd, int64_t N, int64_t K,
+                           float* d_y);
 
 /* ---------------------------------------------------------------- misc */
 const char* minfer_strerror(int code);

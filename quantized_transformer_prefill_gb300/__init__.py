@@ -23,7 +23,7 @@ MINFER_Q8_0 = 8
 
 ERR_NAMES = {0: "OK", -1: "ERR_ARG", -2: "ERR_POS_OOB", -3: "ERR_TOKEN_OOB",
              -4: "ERR_MISSING_TENSOR", -5: "ERR_SHAPE", -6: "ERR_CUDA", -7: "ERR_OOM",
-             -8: "ERR_DEVICE", -9: "ERR_STATE"}
+             -8: "ERR_DEVICE", -9: "ERR_STATE", -10: "ERR_TOO_LARGE"}
 
 # every entry point declared in include/minfer.h: name -> (argtypes, restype)
 _P, _I, _I64, _F = ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.c_float
@@ -65,6 +65,7 @@ SIGNATURES = {
     "minfer_op_quantize": ([_P, _I64, _I64, _P, _P], _I),
     "minfer_op_rmsnorm_quantize": ([_P, _P, _I64, _I64, _F, _P, _P], _I),
     "minfer_op_gemm": ([_P, _P, _I64, _P, _P, _I64, _I64, _P, _P], _I),
+    "minfer_op_gemm_noalloc": ([_P, _P, _I64, _P, _P, _I64, _I64, _P], _I),
     "minfer_op_gemm_swiglu": ([_P, _P, _I64, _P, _P, _P, _P, _I64, _I64, _P, _P], _I),
     "minfer_op_attention": ([_P, _P, _I, _P, _P, _I, _I, _I, _I, _P], _I),
     "minfer_op_rope_store": ([_P, _P, _P, _I, _I, _I, _I, _F, _I, _P, _P, _P], _I),
@@ -280,6 +281,16 @@ def op_gemm(xq, xd, wq, wd, K: int, dots: bool = False):
     check(lib().minfer_op_gemm(_ptr(xq), _ptr(xd), M, _ptr(wq), _ptr(wd), N, K, _ptr(y), _ptr(dd)),
           "op_gemm")
     return (y, dd) if dots else y
+
+
+def op_gemm_noalloc(xq, xd, wq, wd, K: int):
+    """minfer_op_gemm without device allocation (fixed 32 MiB scratch in the library)."""
+    import torch
+    M, N = xq.shape[0], wq.shape[0]
+    y = torch.zeros((M, N), dtype=torch.float32, device=xq.device)
+    check(lib().minfer_op_gemm_noalloc(_ptr(xq), _ptr(xd), M, _ptr(wq), _ptr(wd), N, K, _ptr(y)),
+          "op_gemm_noalloc")
+    return y
 
 
 def op_gemm_swiglu(xq, xd, gq, gd, uq, ud, F: int, K: int):

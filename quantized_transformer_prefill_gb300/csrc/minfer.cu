@@ -1451,6 +1451,7 @@ const char* minfer_strerror(int code) {
     case MINFER_ERR_OOM: return "device out of memory";
     case MINFER_ERR_DEVICE: return "device-side wait timed out";
     case MINFER_ERR_STATE: return "call order or device violated";
+    case MINFER_ERR_TOO_LARGE: return "problem larger than the fixed scratch area";
     default: return "unknown error";
   }
 }
