@@ -87,6 +87,8 @@ __global__ void __launch_bounds__(256) attn_split_kernel(const AttnArgs a) {
   using T = Tile<HD>;
   extern __shared__ __align__(16) __half smem_h[];
   __shared__ int s_maxp;
+  pdl_trigger();
+  pdl_wait();
 
   const int G = a.nh / a.nkv;
   const int tile = (int)gridDim.x - 1 - (int)blockIdx.x;  // longest rows first
@@ -297,6 +299,8 @@ constexpr int kMaxHeads = 64;
 template <bool kGemvOut, int PER>
 __global__ void __launch_bounds__(kCombThreads) attn_combine_kernel(const AttnArgs a, const AttnOut out) {
   __shared__ float s_w[kMaxHeads][kMaxSplitsSmem];
+  pdl_trigger();
+  pdl_wait();
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int r = a.r0 + (int)blockIdx.x;
   const int nrows = a.r1 - a.r0;
@@ -358,11 +362,10 @@ __global__ void __launch_bounds__(kCombThreads) attn_combine_kernel(const AttnAr
 template <bool kGemvOut>
 cudaError_t combine_dispatch(const AttnArgs& a, const AttnOut& out, int rows, cudaStream_t st) {
   const int per = (a.nh * a.hd + kCombThreads - 1) / kCombThreads;
-  if (per <= 4) attn_combine_kernel<kGemvOut, 4><<<rows, kCombThreads, 0, st>>>(a, out);
-  else if (per <= 8) attn_combine_kernel<kGemvOut, 8><<<rows, kCombThreads, 0, st>>>(a, out);
-  else if (per <= 16) attn_combine_kernel<kGemvOut, 16><<<rows, kCombThreads, 0, st>>>(a, out);
-  else return cudaErrorInvalidValue;
-  return cudaGetLastError();
+  if (per <= 4) return launch_pdl(attn_combine_kernel<kGemvOut, 4>, rows, kCombThreads, 0, st, a, out);
+  if (per <= 8) return launch_pdl(attn_combine_kernel<kGemvOut, 8>, rows, kCombThreads, 0, st, a, out);
+  if (per <= 16) return launch_pdl(attn_combine_kernel<kGemvOut, 16>, rows, kCombThreads, 0, st, a, out);
+  return cudaErrorInvalidValue;
 }
 
 // K/V rows of one layer -> fp16 hi/lo shadow planes (count f32 values each).
@@ -410,7 +413,8 @@ cudaError_t attention_launch(const AttnArgs& a, const AttnOut& out, cudaStream_t
       if (e != cudaSuccess) return e;
       set = true;
     }
-    attn_split_kernel<64><<<grid, 32 * G, Tile<64>::BYTES, st>>>(a);
+    cudaError_t e = launch_pdl(attn_split_kernel<64>, grid, 32 * G, Tile<64>::BYTES, st, a);
+    if (e != cudaSuccess) return e;
   } else if (a.hd == 128) {
     static bool set = false;
     if (!set) {
@@ -419,7 +423,8 @@ cudaError_t attention_launch(const AttnArgs& a, const AttnOut& out, cudaStream_t
       if (e != cudaSuccess) return e;
       set = true;
     }
-    attn_split_kernel<128><<<grid, 32 * G, Tile<128>::BYTES, st>>>(a);
+    cudaError_t e = launch_pdl(attn_split_kernel<128>, grid, 32 * G, Tile<128>::BYTES, st, a);
+    if (e != cudaSuccess) return e;
   } else {
     return cudaErrorInvalidValue;
   }

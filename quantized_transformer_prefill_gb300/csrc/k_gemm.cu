@@ -16,15 +16,18 @@
 // dequantize-first scheme would round the operands.
 //
 // Warp roles (320 threads, one CTA per SM, persistent over output tiles):
-//   warp 0     TMA producer: A/B code tiles (128-byte swizzle) and the two
-//              blocks' scale rows per 64-wide K stage
+//   warp 0     TMA producer: A/B code tiles (128-byte swizzle) per 64-wide K
+//              stage, and the two blocks' scale rows into a separate ring
 //   warp 1     TMEM allocator and MMA issuer (one thread)
 //   warps 2-9  epilogue: warp w reads TMEM lane quadrant w % 4 (32 rows of
 //              the 128-row tile); warps 2-5 take the left half of the N
-//              tile, warps 6-9 the right half
-// Rings: STAGES smem stages (full/empty mbarriers; a stage is free once the
-// MMAs that read it completed and all epilogue warps read its scales) and
-// NSLOT TMEM slots of BN columns (tfull/tempty).  Every wait is bounded; on
+//              tile, warps 6-9 the right half; finished f32 rows leave
+//              through a per-warp shared-memory transpose so every store
+//              writes 128 contiguous bytes
+// Rings: STAGES A/B stages, free as soon as the MMAs that read them
+// completed (TMA latency is ~1.6k cycles, so refills must not wait for the
+// epilogue); SSTAGES scale stages, freed by the epilogue; NSLOT TMEM slots
+// of BN columns (tfull/tempty).  Every wait is bounded; on
 // timeout the kernel records a status code, drains its own TMA loads and
 // MMAs, frees TMEM and returns.
 #include <algorithm>
@@ -45,23 +48,28 @@ constexpr int kThreads = 64 + 32 * kEpiWarps;
 
 template <int BN>
 struct Cfg {
-  static constexpr int STAGES = BN == 256 ? 4 : 6;
+  static constexpr int STAGES = 5;
+  static constexpr int SSTAGES = 8;
   static constexpr int NSLOT = 512 / BN;
   static constexpr int CPW = BN / 2;  // columns per epilogue thread
   static constexpr int A_BYTES = kBM * kBK * 2;
   static constexpr int B_BYTES = BN * kBK * 2;
   static constexpr int SA_BYTES = 2 * kBM * 4;
   static constexpr int SB_BYTES = 2 * BN * 4;
-  static constexpr uint32_t STAGE_TX = A_BYTES + B_BYTES + SA_BYTES + SB_BYTES;
+  static constexpr uint32_t STAGE_TX = A_BYTES + B_BYTES;
+  static constexpr uint32_t SCALE_TX = SA_BYTES + SB_BYTES;
   static constexpr int OFF_A = 0;
   static constexpr int OFF_B = OFF_A + STAGES * A_BYTES;
   static constexpr int OFF_SA = OFF_B + STAGES * B_BYTES;
-  static constexpr int OFF_SB = OFF_SA + STAGES * SA_BYTES;
-  static constexpr int OFF_BAR = OFF_SB + STAGES * SB_BYTES;
-  static constexpr int NBAR = 2 * STAGES + 2 * NSLOT;
+  static constexpr int OFF_SB = OFF_SA + SSTAGES * SA_BYTES;
+  static constexpr int T_FLOATS = 32 * 33;  // per-warp transpose tile
+  static constexpr int OFF_T = OFF_SB + SSTAGES * SB_BYTES;
+  static constexpr int OFF_BAR = OFF_T + kEpiWarps * T_FLOATS * 4;
+  static constexpr int NBAR = 2 * STAGES + 2 * SSTAGES + 2 * NSLOT;
   static constexpr int OFF_TMEM = OFF_BAR + NBAR * 8;
   static constexpr int SMEM = OFF_TMEM + 16 + 1024;  // + slack to align the base to 1024
   static_assert(OFF_B % 1024 == 0 && OFF_SA % 1024 == 0, "swizzled tiles need 1024-B alignment");
+  static_assert(SMEM <= 227 * 1024, "shared memory budget");
 };
 
 struct Args {
@@ -98,7 +106,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   float* sSB = reinterpret_cast<float*>(smem + C::OFF_SB);
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + C::OFF_BAR);
   uint64_t* empty = full + C::STAGES;
-  uint64_t* tfull = empty + C::STAGES;
+  uint64_t* sfull = empty + C::STAGES;
+  uint64_t* sempty = sfull + C::SSTAGES;
+  uint64_t* tfull = sempty + C::SSTAGES;
   uint64_t* tempty = tfull + C::NSLOT;
   uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(smem + C::OFF_TMEM);
 
@@ -108,7 +118,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (threadIdx.x == 0) {
     for (int s = 0; s < C::STAGES; ++s) {
       mbar_init(&full[s], 1);
-      mbar_init(&empty[s], 1 + kEpiWarps);
+      mbar_init(&empty[s], 1);
+    }
+    for (int s = 0; s < C::SSTAGES; ++s) {
+      mbar_init(&sfull[s], 1);
+      mbar_init(&sempty[s], kEpiWarps);
     }
     for (int k = 0; k < C::NSLOT; ++k) {
       mbar_init(&tfull[k], 1);
@@ -128,13 +142,16 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem_base = *tmem_holder;
+  // set-up above overlaps the previous kernel; global memory only after it
+  pdl_trigger();
+  pdl_wait();
 
   const int total = p.m_tiles * p.n_tiles * p.splits;
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer
     if (lane == 0) {
-      int it = 0;
+      int it = 0, n_ab = 0, n_s = 0;  // stages issued; A/B loads and scale loads in flight
       bool ok = true;
       for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
         const int mt = t % p.m_tiles;
@@ -145,19 +162,31 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int s1 = min(p.n_stages, s0 + p.stages_per_split);
         for (int s = s0; s < s1; ++s, ++it) {
           const int st = it % C::STAGES;
-          const uint32_t ph = ((it / C::STAGES) & 1) ^ 1;
-          if (!mbar_wait(&empty[st], ph, p.err, kDevTimeoutTmaEmpty)) { ok = false; break; }
+          if (!mbar_wait(&empty[st], ((it / C::STAGES) & 1) ^ 1, p.err, kDevTimeoutTmaEmpty)) {
+            ok = false;
+            break;
+          }
           mbar_arrive_expect_tx(&full[st], C::STAGE_TX);
           tma_load_2d(sA + st * C::A_BYTES, &tmA, &full[st], s * kBK, mt * kBM);
           tma_load_2d(sB + st * C::B_BYTES, &tmB, &full[st], s * kBK, ntile * BN);
-          tma_load_2d(sSA + st * (C::SA_BYTES / 4), &tmSA, &full[st], mt * kBM, 2 * s);
-          tma_load_2d(sSB + st * (C::SB_BYTES / 4), &tmSB, &full[st], ntile * BN, 2 * s);
+          n_ab = it + 1;
+          const int ss = it % C::SSTAGES;
+          if (!mbar_wait(&sempty[ss], ((it / C::SSTAGES) & 1) ^ 1, p.err, kDevTimeoutTmaEmpty)) {
+            ok = false;
+            break;
+          }
+          mbar_arrive_expect_tx(&sfull[ss], C::SCALE_TX);
+          tma_load_2d(sSA + ss * (C::SA_BYTES / 4), &tmSA, &sfull[ss], mt * kBM, 2 * s);
+          tma_load_2d(sSB + ss * (C::SB_BYTES / 4), &tmSB, &sfull[ss], ntile * BN, 2 * s);
+          n_s = it + 1;
         }
       }
       if (!ok) {
         // drain the loads that may still be in flight before the CTA exits
-        for (int j = max(0, it - C::STAGES); j < it; ++j)
+        for (int j = max(0, n_ab - C::STAGES); j < n_ab; ++j)
           mbar_wait(&full[j % C::STAGES], (j / C::STAGES) & 1, p.err, kDevTimeoutDrain);
+        for (int j = max(0, n_s - C::SSTAGES); j < n_s; ++j)
+          mbar_wait(&sfull[j % C::SSTAGES], (j / C::SSTAGES) & 1, p.err, kDevTimeoutDrain);
       }
     }
   } else if (warp == 1) {
@@ -213,6 +242,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int quad = warp & 3;
     const int half = ew >> 2;
     const int row = quad * 32 + lane;
+    float* sT = reinterpret_cast<float*>(smem + C::OFF_T) + ew * C::T_FLOATS;
     int it = 0, sit = 0;
     bool ok = true;
     for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
@@ -230,8 +260,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int j = 0; j < C::CPW / 2; ++j) acc[j] = make_float2(0.f, 0.f);
 
       for (int s = s0; s < s1 && ok; ++s, ++it) {
-        const int st = it % C::STAGES;
-        if (!mbar_wait(&full[st], (it / C::STAGES) & 1, p.err, kDevTimeoutEpilogue)) {
+        const int ss = it % C::SSTAGES;
+        if (!mbar_wait(&sfull[ss], (it / C::SSTAGES) & 1, p.err, kDevTimeoutEpilogue)) {
           ok = false;
           break;
         }
@@ -243,8 +273,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             break;
           }
           tc_fence_after();
-          const float da = sSA[st * 2 * kBM + blk * kBM + row];
-          const float* dw = sSB + st * 2 * BN + blk * BN + half * C::CPW;
+          const float da = sSA[ss * 2 * kBM + blk * kBM + row];
+          const float* dw = sSB + ss * 2 * BN + blk * BN + half * C::CPW;
           const uint32_t taddr =
               tmem_base + ((uint32_t)(quad * 32) << 16) + (uint32_t)(slot * BN + half * C::CPW);
           const int b = 2 * s + blk;
@@ -273,12 +303,12 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
             for (int j = 0; j < 64; j += 4) {
               const float4 w4 = *reinterpret_cast<const float4*>(dw + c + j);
-              const float2 s0 = __fmul2_rn(da2, make_float2(w4.x, w4.y));
-              const float2 s1 = __fmul2_rn(da2, make_float2(w4.z, w4.w));
+              const float2 s0v = __fmul2_rn(da2, make_float2(w4.x, w4.y));
+              const float2 s1v = __fmul2_rn(da2, make_float2(w4.z, w4.w));
               acc[(c + j) / 2] = __ffma2_rn(
-                  make_float2(__uint_as_float(r[j]), __uint_as_float(r[j + 1])), s0, acc[(c + j) / 2]);
+                  make_float2(__uint_as_float(r[j]), __uint_as_float(r[j + 1])), s0v, acc[(c + j) / 2]);
               acc[(c + j) / 2 + 1] = __ffma2_rn(
-                  make_float2(__uint_as_float(r[j + 2]), __uint_as_float(r[j + 3])), s1,
+                  make_float2(__uint_as_float(r[j + 2]), __uint_as_float(r[j + 3])), s1v,
                   acc[(c + j) / 2 + 1]);
             }
           }
@@ -287,13 +317,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (!ok) break;
         // this stage's scales are consumed
         __syncwarp();
-        if (lane == 0) mbar_arrive(&empty[st]);
+        if (lane == 0) mbar_arrive(&sempty[ss]);
       }
       if (!ok) break;
 
       // ---------------------------------------------------------- store
-      if (m < p.M) {
-        if (EPI == kEpiSwiGLU) {
+      if (EPI == kEpiSwiGLU) {
+        if (m < p.M) {
           // columns come in groups of 64: 32 gate then 32 up rows of W
 #pragma unroll
           for (int g0 = 0; g0 < C::CPW; g0 += 64) {
@@ -320,18 +350,29 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             p.qs_out[(j0 / 32) * p.ldqs + m] = __half2float(__float2half_rn(d));
           }
-        } else {
-          float* dst = p.out + (int64_t)sp * p.split_stride + (int64_t)m * p.ldo + ncol0;
-          if (ncol0 + C::CPW <= p.N && (p.ldo & 3) == 0) {
+        }
+      } else {
+        // 32 x 32 sub-tiles through shared memory: each store instruction
+        // writes one row's 32 consecutive columns (128 bytes)
+        const int mrow0 = mt * kBM + quad * 32;
+        float* base = p.out + (int64_t)sp * p.split_stride;
 #pragma unroll
-            for (int j = 0; j < C::CPW; j += 4)
-              *reinterpret_cast<float4*>(dst + j) =
-                  make_float4(acc[j / 2].x, acc[j / 2].y, acc[j / 2 + 1].x, acc[j / 2 + 1].y);
-          } else {
+        for (int c = 0; c < C::CPW; c += 32) {
 #pragma unroll
-            for (int j = 0; j < C::CPW; ++j)
-              if (ncol0 + j < p.N) dst[j] = (j & 1) ? acc[j / 2].y : acc[j / 2].x;
+          for (int j = 0; j < 32; j += 2) {
+            sT[lane * 33 + j] = acc[(c + j) / 2].x;
+            sT[lane * 33 + j + 1] = acc[(c + j) / 2].y;
           }
+          __syncwarp();
+          const int n = ncol0 + c + lane;
+          if (n < p.N) {
+#pragma unroll 4
+            for (int rr = 0; rr < 32; ++rr) {
+              const int mm = mrow0 + rr;
+              if (mm < p.M) base[(int64_t)mm * p.ldo + n] = sT[rr * 33 + lane];
+            }
+          }
+          __syncwarp();
         }
       }
     }
@@ -406,8 +447,8 @@ cudaError_t launch_bn(const GemmLaunch& g, const GemmMaps& maps, int num_sms, cu
   a.err = g.err;
   const int total = a.m_tiles * a.n_tiles * a.splits;
   const int grid = std::max(1, std::min(total, num_sms));
-  gemm_q8_kernel<BN, EPI><<<grid, kThreads, C::SMEM, st>>>(maps.a, maps.b, maps.sa, maps.sb, a);
-  return cudaGetLastError();
+  return launch_pdl(gemm_q8_kernel<BN, EPI>, grid, kThreads, C::SMEM, st, maps.a, maps.b, maps.sa,
+                    maps.sb, a);
 }
 
 }  // namespace

@@ -45,6 +45,8 @@ constexpr int kRowThreads = 256;
 
 template <bool kGemvOut, int PER>
 __global__ void __launch_bounds__(kRowThreads) row_quant_kernel(const RowQuantArgs a) {
+  pdl_trigger();
+  pdl_wait();
   __shared__ float red_hi[kRowThreads / 32], red_lo[kRowThreads / 32];
   __shared__ float s_scale;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -142,19 +144,20 @@ template <bool kGemvOut>
 cudaError_t row_quant_dispatch(const RowQuantArgs& a, cudaStream_t st) {
   const int per = (int)((a.n + kRowThreads - 1) / kRowThreads);
   const unsigned grid = (unsigned)a.rows;
-  if (per <= 1) row_quant_kernel<kGemvOut, 1><<<grid, kRowThreads, 0, st>>>(a);
-  else if (per <= 2) row_quant_kernel<kGemvOut, 2><<<grid, kRowThreads, 0, st>>>(a);
-  else if (per <= 4) row_quant_kernel<kGemvOut, 4><<<grid, kRowThreads, 0, st>>>(a);
-  else if (per <= 8) row_quant_kernel<kGemvOut, 8><<<grid, kRowThreads, 0, st>>>(a);
-  else if (per <= 16) row_quant_kernel<kGemvOut, 16><<<grid, kRowThreads, 0, st>>>(a);
-  else return cudaErrorInvalidValue;
-  return cudaGetLastError();
+  if (per <= 1) return launch_pdl(row_quant_kernel<kGemvOut, 1>, grid, kRowThreads, 0, st, a);
+  if (per <= 2) return launch_pdl(row_quant_kernel<kGemvOut, 2>, grid, kRowThreads, 0, st, a);
+  if (per <= 4) return launch_pdl(row_quant_kernel<kGemvOut, 4>, grid, kRowThreads, 0, st, a);
+  if (per <= 8) return launch_pdl(row_quant_kernel<kGemvOut, 8>, grid, kRowThreads, 0, st, a);
+  if (per <= 16) return launch_pdl(row_quant_kernel<kGemvOut, 16>, grid, kRowThreads, 0, st, a);
+  return cudaErrorInvalidValue;
 }
 
 // ---------------------------------------------------------------- embedding
 __global__ void embed_kernel(const int8_t* __restrict__ q, const float* __restrict__ s,
                              int64_t kpad, int nb, const int32_t* __restrict__ ids, int64_t H,
                              float* __restrict__ h, int n_vocab) {
+  pdl_trigger();
+  pdl_wait();
   const int t = blockIdx.x;
   int id = ids[t];
   id = id < 0 ? 0 : (id >= n_vocab ? n_vocab - 1 : id);  // invalid ids are reported by validation
@@ -167,6 +170,8 @@ __global__ void embed_kernel(const int8_t* __restrict__ q, const float* __restri
 // ---------------------------------------------------------------- validation
 __global__ void validate_kernel(const int32_t* __restrict__ ids, const int32_t* __restrict__ pos,
                                 int nt, int n_vocab, int n_ctx, uint32_t* seen, int* status) {
+  pdl_trigger();
+  pdl_wait();
   __shared__ int code;
   if (threadIdx.x == 0) code = 0;
   const int words = (n_ctx + 31) / 32;
@@ -193,6 +198,8 @@ __global__ void validate_kernel(const int32_t* __restrict__ ids, const int32_t* 
 // rotation angle's input and names the K/V row written).  The products and
 // the differences are separate IEEE roundings, as written.
 __global__ void rope_store_kernel(const RopeStoreArgs a) {
+  pdl_trigger();
+  pdl_wait();
   const int t = blockIdx.x;
   const int p_in = a.pos[t];
   // an out-of-range position is reported by validation; it only selects a
@@ -259,6 +266,8 @@ __global__ void rope_store_kernel(const RopeStoreArgs a) {
 // (half of a Q8_0 block); dp4a gives the integer partial, the lane pair adds
 // up the block's exact int32 dot, the even lane scales it by dw * da.
 __global__ void gemv_kernel(const GemvArgs a) {
+  pdl_trigger();
+  pdl_wait();
   const int lane = threadIdx.x & 31;
   const int64_t n = (int64_t)blockIdx.x * (blockDim.x / 32) + (threadIdx.x >> 5);
   if (n >= a.N) return;
@@ -292,6 +301,8 @@ __global__ void gemv_kernel(const GemvArgs a) {
 
 __global__ void swiglu_quant_row_kernel(const float* __restrict__ gu, int64_t F, int8_t* q,
                                         float* s) {
+  pdl_trigger();
+  pdl_wait();
   const int lane = threadIdx.x & 31;
   const int64_t nb = (F + 31) / 32;
   for (int64_t b = threadIdx.x >> 5; b < nb; b += blockDim.x >> 5) {
@@ -405,32 +416,27 @@ cudaError_t row_quant_launch(const RowQuantArgs& a, cudaStream_t st) {
 
 cudaError_t embed_launch(const int8_t* q, const float* s, int64_t kpad, int nb, const int32_t* ids,
                          int nt, int64_t H, int n_vocab, float* h, cudaStream_t st) {
-  embed_kernel<<<nt, 128, 0, st>>>(q, s, kpad, nb, ids, H, h, n_vocab);
-  return cudaGetLastError();
+  return launch_pdl(embed_kernel, nt, 128, 0, st, q, s, kpad, nb, ids, H, h, n_vocab);
 }
 
 cudaError_t validate_launch(const int32_t* ids, const int32_t* pos, int nt, int n_vocab, int n_ctx,
                             uint32_t* seen, int* status, cudaStream_t st) {
-  validate_kernel<<<1, 1024, 0, st>>>(ids, pos, nt, n_vocab, n_ctx, seen, status);
-  return cudaGetLastError();
+  return launch_pdl(validate_kernel, 1, 1024, 0, st, ids, pos, nt, n_vocab, n_ctx, seen, status);
 }
 
 cudaError_t rope_store_launch(const RopeStoreArgs& a, cudaStream_t st) {
   if (a.nt <= 0) return cudaSuccess;
-  rope_store_kernel<<<a.nt, 256, 0, st>>>(a);
-  return cudaGetLastError();
+  return launch_pdl(rope_store_kernel, a.nt, 256, 0, st, a);
 }
 
 cudaError_t gemv_launch(const GemvArgs& a, cudaStream_t st) {
   const int warps = 8;
-  gemv_kernel<<<(unsigned)((a.N + warps - 1) / warps), 32 * warps, 0, st>>>(a);
-  return cudaGetLastError();
+  return launch_pdl(gemv_kernel, (unsigned)((a.N + warps - 1) / warps), 32 * warps, 0, st, a);
 }
 
 cudaError_t swiglu_quant_row_launch(const float* gu, int64_t F, int8_t* q, float* s,
                                     cudaStream_t st) {
-  swiglu_quant_row_kernel<<<1, 1024, 0, st>>>(gu, F, q, s);
-  return cudaGetLastError();
+  return launch_pdl(swiglu_quant_row_kernel, 1, 1024, 0, st, gu, F, q, s);
 }
 
 cudaError_t quantize_rows_launch(const float* x, int64_t rows, int64_t n, int8_t* q,
