@@ -169,6 +169,28 @@ int minfer_set_dump(minfer_model* m, float* host_hidden, int max_tokens);
  * host buffer size; MINFER_ERR_ARG for an unknown name or a short buffer. */
 int minfer_debug_read(minfer_model* m, const char* buffer, void* host, int64_t bytes);
 
+/* Capture the intermediates of layer `layer` (0 <= layer < n_layer; -1 turns
+ * it off) during the next prefill calls, which then run without the graph.
+ * minfer_debug_read then also serves, for the last captured call (nt rows,
+ * ntp = ceil(nt/128)*128, kx = ceil(n_embd/32)*32), the buffers below; the
+ * last layer, which carries only the final token past its K/V projections,
+ * captures h_in, x_codes, x_scales and qkv alone:
+ *   "h_in", "h_mid", "h_out"  f32 [nt][n_embd]: residual stream entering the
+ *                             layer, after the attention residual, leaving it
+ *   "x_codes", "f_codes"      fp16 [nt][kx]: Q8_0 codes of attn_norm(h_in) and
+ *                             ffn_norm(h_mid); "x_scales", "f_scales" f32
+ *                             [kx/32][ntp] (block-major)
+ *   "qkv"                     f32 [nt][(n_head + 2 n_head_kv) head_dim]: Q|K|V
+ *                             projections before bias and RoPE
+ *   "qrot"                    f32 [nt][n_head*head_dim]: rotated Q
+ *   "att_codes", "att_scales" Q8_0 of the attention output (fp16 [nt][q],
+ *                             f32 [q/32][ntp]); "att" its f32 values [nt][q]
+ *   "s_codes", "s_scales"     Q8_0 of the SwiGLU output (fp16 [nt][ceil(n_ff/32)*32],
+ *                             f32 [ceil(n_ff/32)][ntp])
+ * Returns MINFER_ERR_ARG for a layer out of range; a failed capture
+ * allocation fails the prefill call with MINFER_ERR_CUDA. */
+int minfer_debug_layer(minfer_model* m, int layer);
+
 /* Per-kernel device time of the prefill calls since the last reset, measured
  * with CUDA events around each launch: kernel class k in [0, n) gets its
  * name, its launch count and its total milliseconds.  enable = 1 turns the

@@ -59,6 +59,7 @@ SIGNATURES = {
     "minfer_sync_status": ([_P, _P], _I),
     "minfer_set_dump": ([_P, _P, _I], _I),
     "minfer_debug_read": ([_P, ctypes.c_char_p, _P, _I64], _I),
+    "minfer_debug_layer": ([_P, _I], _I),
     "minfer_profile_enable": ([_P, _I], _I),
     "minfer_profile_read": ([_P, _I, ctypes.POINTER(ctypes.c_char_p), ctypes.POINTER(_I64),
                              ctypes.POINTER(ctypes.c_double)], _I),
@@ -173,6 +174,10 @@ class Model:
         check(lib().minfer_debug_read(self.ptr, name.encode(), out.ctypes.data, out.nbytes),
               f"debug_read {name}")
         return out
+
+    def debug_layer(self, layer: int):
+        """Capture layer `layer`'s intermediates on the next prefill (-1: off)."""
+        check(lib().minfer_debug_layer(self.ptr, layer), "debug_layer")
 
     def profile_enable(self, on: bool = True):
         check(lib().minfer_profile_enable(self.ptr, int(on)), "profile_enable")

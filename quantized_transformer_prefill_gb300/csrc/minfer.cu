@@ -246,6 +246,11 @@ struct minfer_model {
   int dump_max_nt = 0;
   int last_device_status = 0;
   bool debug_f32 = false;  // also write the f32 attention output (debug reads)
+  // stage capture of one layer (debug): copies of that layer's intermediates
+  int dbg_layer = -1;
+  int dbg_nt = 0;
+  bool dump_on = false;  // this call copies hidden states to dump_host
+  std::map<std::string, std::pair<void*, size_t>> dbg;  // name -> (device buffer, bytes)
 };
 
 float* minfer_kv::k(int l) const {
@@ -380,6 +385,9 @@ int model_alloc(minfer_model* m) {
 }
 
 void model_release(minfer_model* m) {
+  for (auto& kv : m->dbg)
+    if (kv.second.first) cudaFree(kv.second.first);
+  m->dbg.clear();
   if (m->gexec) cudaGraphExecDestroy(m->gexec);
   if (m->graph) cudaGraphDestroy(m->graph);
   for (auto e : m->ev) cudaEventDestroy(e);
@@ -582,8 +590,39 @@ int gemm_call(minfer_model* m, Launcher& L, int cls, const GemmOperand& A, const
   return MINFER_OK;
 }
 
+// Copy `bytes` from src into the named stage-capture buffer (debug only).
+int dbg_capture(minfer_model* m, cudaStream_t st, const char* name, const void* src, size_t bytes) {
+  auto& e = m->dbg[name];
+  if (e.second < bytes) {
+    if (e.first) cudaFree(e.first);
+    e.first = nullptr;
+    e.second = 0;
+    CK(cudaMalloc(&e.first, bytes));
+    e.second = bytes;
+  }
+  CK(cudaMemcpyAsync(e.first, src, bytes, cudaMemcpyDeviceToDevice, st));
+  return MINFER_OK;
+}
+
+// Capture a block-major scale plane [nb][ld] as [nb][ntp_call] (debug only).
+int dbg_capture_scales(minfer_model* m, cudaStream_t st, const char* name, const float* src,
+                       int nb, int64_t ld, int64_t ntp_call) {
+  auto& e = m->dbg[name];
+  const size_t bytes = (size_t)nb * ntp_call * 4;
+  if (e.second < bytes) {
+    if (e.first) cudaFree(e.first);
+    e.first = nullptr;
+    e.second = 0;
+    CK(cudaMalloc(&e.first, bytes));
+    e.second = bytes;
+  }
+  CK(cudaMemcpy2DAsync(e.first, ntp_call * 4, src, ld * 4, ntp_call * 4, nb,
+                       cudaMemcpyDeviceToDevice, st));
+  return MINFER_OK;
+}
+
 void dump_hidden(minfer_model* m, cudaStream_t st, int slot, const float* src, int rows) {
-  if (!m->dump_host) return;
+  if (!m->dump_on) return;
   float* dst = m->dump_host + (int64_t)slot * m->dump_max_nt * m->H;
   cudaMemcpyAsync(dst, src, (size_t)rows * m->H * 4, cudaMemcpyDeviceToHost, st);
 }
@@ -628,10 +667,25 @@ int enqueue_forward(minfer_model* m, minfer_kv* kv, const int32_t* ids, const in
     r.ldqs = ntp;
     LAUNCH(kKRowQuant, row_quant_launch(r, st));
   }
+  const int64_t kx = (int64_t)m->nbH * 32;
+  const int64_t ntp_call = ((int64_t)nt + 127) / 128 * 128;  // captured scale planes' width
   for (int l = 0; l < hp.n_layer; ++l) {
     Layer& Ly = m->layers[l];
     const bool last = l == hp.n_layer - 1;
+    // the last layer keeps all rows only through its K/V projections
+    const bool cap = dumps && l == m->dbg_layer;
+    const bool cap_all = cap && !last;
     int ns = 1, rc;
+    if (cap) {
+      for (auto& e : m->dbg)  // drop the previous call's captures
+        if (e.second.first) cudaFree(e.second.first);
+      m->dbg.clear();
+      m->dbg_nt = nt;
+      if ((rc = dbg_capture(m, st, "h_in", w.h, (size_t)nt * m->H * 4)) ||
+          (rc = dbg_capture(m, st, "x_codes", w.xa, (size_t)nt * kx * 2)) ||
+          (rc = dbg_capture_scales(m, st, "x_scales", w.xa_s, m->nbH, ntp, ntp_call)))
+        return rc;
+    }
     if ((rc = gemm_call(m, L, kKGemmQKV, xa, Ly.wqkv, nt, kEpiF32, true, w.part, m->qkvN, nullptr,
                         0, nullptr, 0, &ns)))
       return rc;
@@ -656,6 +710,18 @@ int enqueue_forward(minfer_model* m, minfer_kv* kv, const int32_t* ids, const in
       r.status = m->d_status;
       LAUNCH(kKRope, rope_store_launch(r, st));
     }
+    if (cap) {
+      auto& e = m->dbg["qkv"];
+      const size_t bytes = (size_t)nt * m->qkvN * 4;
+      if (e.second < bytes) {
+        if (e.first) cudaFree(e.first);
+        CK(cudaMalloc(&e.first, bytes));
+        e.second = bytes;
+      }
+      CK(sum_splits_launch(w.part, ns, w.part_stride, (int64_t)nt * m->qkvN,
+                           static_cast<float*>(e.first), st));
+      if (cap_all && (rc = dbg_capture(m, st, "qrot", w.qrot, (size_t)nt * m->q * 4))) return rc;
+    }
     AttnArgs at;
     at.q = w.qrot;
     at.pos = pos;
@@ -670,7 +736,7 @@ int enqueue_forward(minfer_model* m, minfer_kv* kv, const int32_t* ids, const in
     at.part_o = w.att_o;
     at.part_ml = w.att_ml;
     AttnOut ao;
-    ao.f32 = m->debug_f32 ? w.att : nullptr;
+    ao.f32 = (m->debug_f32 || cap_all) ? w.att : nullptr;
     if (!last) {
       ao.q16 = w.xa;
       ao.ldq = (int64_t)m->nbq * 32;
@@ -682,6 +748,12 @@ int enqueue_forward(minfer_model* m, minfer_kv* kv, const int32_t* ids, const in
       ao.row_base = nt - 1;
     }
     LAUNCH(kKAttn, attention_launch(at, ao, st));
+    if (cap_all) {
+      if ((rc = dbg_capture(m, st, "att_codes", w.xa, (size_t)nt * m->nbq * 32 * 2)) ||
+          (rc = dbg_capture_scales(m, st, "att_scales", w.xa_s, m->nbq, ntp, ntp_call)) ||
+          (rc = dbg_capture(m, st, "att", w.att, (size_t)nt * m->q * 4)))
+        return rc;
+    }
     if (!last) {
       if ((rc = gemm_call(m, L, kKGemmO, xo, Ly.wo, nt, kEpiF32, true, w.part, m->H, nullptr, 0,
                           nullptr, 0, &ns)))
@@ -702,9 +774,20 @@ int enqueue_forward(minfer_model* m, minfer_kv* kv, const int32_t* ids, const in
         r.ldqs = ntp;
         LAUNCH(kKRowQuant, row_quant_launch(r, st));
       }
+      if (cap) {
+        if ((rc = dbg_capture(m, st, "h_mid", w.h, (size_t)nt * m->H * 4)) ||
+            (rc = dbg_capture(m, st, "f_codes", w.xa, (size_t)nt * kx * 2)) ||
+            (rc = dbg_capture_scales(m, st, "f_scales", w.xa_s, m->nbH, ntp, ntp_call)))
+          return rc;
+      }
       if ((rc = gemm_call(m, L, kKGemmGU, xa, Ly.wgu, nt, kEpiSwiGLU, false, nullptr, 0, w.xf,
                           m->Fp, w.xf_s, ntp, nullptr)))
         return rc;
+      if (cap) {
+        if ((rc = dbg_capture(m, st, "s_codes", w.xf, (size_t)nt * m->Fp * 2)) ||
+            (rc = dbg_capture_scales(m, st, "s_scales", w.xf_s, m->nbF, ntp, ntp_call)))
+          return rc;
+      }
       if ((rc = gemm_call(m, L, kKGemmDown, xf, Ly.wd, nt, kEpiF32, true, w.part, m->H, nullptr, 0,
                           nullptr, 0, &ns)))
         return rc;
@@ -725,6 +808,7 @@ int enqueue_forward(minfer_model* m, minfer_kv* kv, const int32_t* ids, const in
         LAUNCH(kKRowQuant, row_quant_launch(r, st));
       }
       if (dumps) dump_hidden(m, st, l + 1, w.h, nt);
+      if (cap && (rc = dbg_capture(m, st, "h_out", w.h, (size_t)nt * m->H * 4))) return rc;
     } else {
       // last row only: o-projection, FFN, final norm, lm_head as GEMVs
       const int64_t last_row = nt - 1;
@@ -840,7 +924,8 @@ int run_forward(minfer_model* m, minfer_kv* kv, const int32_t* ids, const int32_
   int rc = ensure_workspace(m, nt);
   if (rc) return rc;
   if ((rc = ensure_attn_scratch(m, nt, kv->n_ctx))) return rc;
-  const bool dumps = m->dump_host != nullptr && nt <= m->dump_max_nt;
+  m->dump_on = m->dump_host != nullptr && nt <= m->dump_max_nt;
+  const bool dumps = m->dump_on || m->dbg_layer >= 0;
   if (dumps) {
     // dumps copy to host memory mid-sequence: run eagerly
     m->ev_used = 0;
@@ -1422,8 +1507,24 @@ int minfer_op_rope_store(const float* d_qkv, const float* d_bias, const int32_t*
   return MINFER_OK;
 }
 
+int minfer_debug_layer(minfer_model* m, int layer) {
+  if (!m || layer < -1 || layer >= m->hp.n_layer) return MINFER_ERR_ARG;
+  m->dbg_layer = layer;
+  return MINFER_OK;
+}
+
 int minfer_debug_read(minfer_model* m, const char* buffer, void* host, int64_t bytes) {
-  if (!m || !buffer || !host || m->ws.max_nt == 0) return MINFER_ERR_ARG;
+  if (!m || !buffer || !host) return MINFER_ERR_ARG;
+  {
+    auto it = m->dbg.find(buffer);
+    if (it != m->dbg.end() && it->second.first) {
+      if (bytes < (int64_t)it->second.second) return MINFER_ERR_ARG;
+      CK(cudaDeviceSynchronize());
+      CK(cudaMemcpy(host, it->second.first, it->second.second, cudaMemcpyDeviceToHost));
+      return MINFER_OK;
+    }
+  }
+  if (m->ws.max_nt == 0) return MINFER_ERR_ARG;
   const Workspace& w = m->ws;
   const std::string b(buffer);
   const void* src = nullptr;

@@ -46,3 +46,62 @@ def check_logits(got, want, atol=2e-2, rtol_l2=1e-3):
     if top2[1] - top2[0] > err:
         assert int(np.argmax(got)) == int(np.argmax(want)), "argmax differs"
     return err, rl2
+
+
+U = 2.0 ** -24  # f32 unit roundoff
+
+
+def check_q8_sum(oracle_mod, got, aq, ad, wq, wd, K, base=None):
+    """got = base + (Q8_0 matmul) within the f32 bound of summing the nb block
+    terms S_b * d_a * d_w (and the residual add); the bound uses
+    sum_b sum_i |qa_i||qw_i| d_a d_w, an upper bound of sum_b |term_b|."""
+    want = oracle_mod.matmul_q8(aq, ad, wq, wd, K)
+    tol = q8_sum_bound(oracle_mod, aq, ad, wq, wd, K)
+    if base is not None:
+        want = (want.astype(np.float64) + base).astype(np.float32)
+        tol = tol + 4 * U * np.abs(base)
+    tol = tol + 4 * U * np.abs(want)
+    err = np.abs(got.astype(np.float64) - want)
+    bad = err > tol
+    assert not bad.any(), (f"{bad.sum()} of {bad.size} outside the f32 bound; worst "
+                           f"{(err / np.maximum(tol, 1e-30)).max():.2f}x")
+    return want
+
+
+def q8_sum_bound(oracle_mod, aq, ad, wq, wd, K):
+    """The f32 rounding bound of a Q8_0 matmul's block sums (see check_q8_sum)."""
+    bound = oracle_mod.matmul_q8(np.abs(aq.astype(np.int16)).astype(np.int8), ad,
+                                 np.abs(wq.astype(np.int16)).astype(np.int8), wd, K)
+    return (aq.shape[1] // 32 + 8) * U * bound.astype(np.float64)
+
+
+def check_q8_requant(oracle_mod, codes, scales, ref, slack):
+    """Q8_0 of a value the GPU computed in f32 (codes/scales) against the
+    oracle's value ref (Q8_0 block: d = amax/127 kept as fp16, codes round(x/d)).
+    The dequantized GPU value lies within the Q8_0 error of ref (half a step
+    plus 127 times the fp16 rounding of d) plus the f32 error `slack`; a code
+    that differs from the oracle's own quantization differs by one step and
+    only where ref lies within `slack` of a rounding boundary."""
+    rows, n = ref.shape
+    oq, od = oracle_mod.q8_quantize(ref)
+    deq = oracle_mod.q8_dequantize(codes, scales, n).astype(np.float64)
+    step = np.abs(oracle_mod.q8_dequantize(np.ones_like(codes), scales, n).astype(np.float64))
+    assert np.all(np.abs(deq - ref) <= (0.5 + 128 * 2.0 ** -11) * step * (1 + 1e-3) + slack)
+    diff = np.abs(codes[:, :n].astype(np.int32) - oq[:, :n].astype(np.int32))
+    same_scale = np.repeat(scales == od, 32, axis=1)[:, :n]
+    assert diff[same_scale].max(initial=0) <= 1
+    nb = (n + 31) // 32
+    padded = np.zeros((rows, nb * 32))
+    padded[:, :n] = ref
+    amax = np.abs(padded.reshape(rows, nb, 32)).max(axis=2, keepdims=True)
+    d32 = np.maximum(amax, 1e-30) / 127.0
+    t = (padded.reshape(rows, nb, 32) / d32).reshape(rows, nb * 32)[:, :n]
+    dist = np.abs(t - np.floor(t) - 0.5)
+    sl = np.zeros((rows, nb * 32))
+    sl[:, :n] = slack
+    tol_t = (sl.reshape(rows, nb, 32).max(axis=2, keepdims=True) / d32)
+    tol_t = np.broadcast_to(tol_t, (rows, nb, 32)).reshape(rows, nb * 32)[:, :n] + 1e-4 * np.abs(t)
+    flips = (diff > 0) & same_scale
+    assert np.all(dist[flips] <= tol_t[flips] + 1e-3), "code flip away from a rounding boundary"
+    assert flips.mean() <= 2e-3, flips.mean()
+    assert (scales != od).mean() <= 2e-3
