@@ -13,11 +13,16 @@
 namespace minfer {
 
 // ------------------------------------------------------------------ limits
-// Every spin on an mbarrier gives up after this many polls.  A poll is one
-// try_wait, which itself may sleep for a short, hardware-chosen time, so the
-// limit is far beyond any legitimate wait (milliseconds) yet ends a wait that
-// can never complete within a few seconds.
-constexpr uint32_t kMaxPolls = 1u << 22;
+// Every wait on an mbarrier is bounded twice: by elapsed time (kWaitLimitNs of
+// the global nanosecond timer, far beyond any legitimate wait, which lasts
+// microseconds) and, as a backstop, by a count of polls.  A poll is one
+// try_wait carrying a suspend-time hint: the waiting warp sleeps until the
+// phase completes (or the hint runs out) instead of spinning, so a waiting
+// producer or MMA thread leaves the issue slots of its sub-partition to the
+// epilogue warps that share it.
+constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s
+constexpr uint32_t kMaxPolls = 1u << 24;
+constexpr uint32_t kSuspendHintNs = 1000000u;  // at most 1 ms per poll
 
 // Device-side status codes written into the per-model status word.
 enum : int {
@@ -60,19 +65,29 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
   uint32_t ok;
   asm volatile(
       "{\n\t.reg .pred p;\n\t"
-      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
       "selp.u32 %0, 1, 0, p;\n\t}"
       : "=r"(ok)
-      : "r"(smem_u32(bar)), "r"(parity)
+      : "r"(smem_u32(bar)), "r"(parity), "r"(kSuspendHintNs)
       : "memory");
   return ok != 0;
 }
 
+__device__ __forceinline__ uint64_t global_ns() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %globaltimer;" : "=l"(t));
+  return t;
+}
+
 // Wait until the phase with the given parity has completed.  Returns false
-// (and records `code` in *err) when the poll limit runs out.
+// (and records `code` in *err) when the time or poll limit runs out.
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, int* err, int code) {
-  for (uint32_t i = 0; i < kMaxPolls; ++i)
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = global_ns();
+  for (uint32_t i = 0; i < kMaxPolls; ++i) {
     if (mbar_try_wait(bar, parity)) return true;
+    if (global_ns() - t0 > kWaitLimitNs) break;
+  }
   set_error(err, code);
   return false;
 }
