@@ -18,10 +18,16 @@
 // reduced across the four lanes of a row with warp shuffles.
 //
 // Short prompts have too few (rows, KV head) tiles to fill the GPU, so the
-// key range is split (the split-KV scheme of the pages' CUDA backend): each
-// split writes its unnormalized output and (max, sum) to scratch, and the
-// combine kernel merges the splits, normalizes, and quantizes each 32-block
-// of the output row to Q8_0 for the o-projection.
+// key range of each tile is split (the split-KV scheme of the pages' CUDA
+// backend) across the CTAs of one thread-block cluster: each CTA covers a
+// contiguous share of the keys 0..max position of its rows, leaves its
+// unnormalized output and (max, sum) in its own shared memory, and after a
+// cluster barrier every CTA merges a share of the (row, head, 32-block)
+// units by reading its peers' partials through distributed shared memory,
+// normalizes, and quantizes each 32-block of the output row to Q8_0 for the
+// o-projection.  No partials go through global memory and no second kernel
+// runs; without a split the cluster is one CTA.
+#include <algorithm>
 #include <cstdint>
 
 #include "common.cuh"
@@ -31,8 +37,8 @@ namespace minfer {
 
 namespace {
 
-constexpr int kMaxSplitsSmem = 64;  // key splits one combine CTA can merge
-constexpr int kTileQ = 16;   // query rows per CTA
+constexpr int kMaxSplits = 8;  // CTAs per cluster (portable cluster size)
+constexpr int kTileQ = 16;     // query rows per CTA
 constexpr int kTileKV = 32;  // keys per shared-memory tile
 
 __device__ __forceinline__ void mma16816(float (&d)[4], const uint32_t (&a)[4], uint32_t b0,
@@ -65,6 +71,32 @@ __device__ __forceinline__ void cp_async_wait() {
   asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
 }
 
+__device__ __forceinline__ uint32_t cluster_rank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+__device__ __forceinline__ void cluster_sync_all() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::
+                   : "memory");
+}
+// Shared-memory address of the same variable in CTA `rank` of the cluster.
+__device__ __forceinline__ uint32_t peer_addr(uint32_t saddr, uint32_t rank) {
+  uint32_t r;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(saddr), "r"(rank));
+  return r;
+}
+__device__ __forceinline__ float ld_peer(uint32_t addr) {
+  float v;
+  asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(addr) : "memory");
+  return v;
+}
+__device__ __forceinline__ float2 ld_peer2(uint32_t addr) {
+  float2 v;
+  asm volatile("ld.shared::cluster.v2.f32 {%0, %1}, [%2];" : "=f"(v.x), "=f"(v.y) : "r"(addr) : "memory");
+  return v;
+}
+
 // f32 pair -> (hi, lo) fp16x2 words with x = hi + lo to ~22 bits.
 __device__ __forceinline__ void split2(float x0, float x1, uint32_t& hi, uint32_t& lo) {
   const __half h0 = __float2half_rn(x0), h1 = __float2half_rn(x1);
@@ -80,10 +112,14 @@ struct Tile {
   static constexpr int PLANE = kTileKV * RS;   // halves per plane
   static constexpr int STAGE = 4 * PLANE;      // Kh, Kl, Vh, Vl
   static constexpr int BYTES = 2 * STAGE * 2;  // two stages, 2 B per half
+  // after the key loop the same bytes hold the CTA's partial result:
+  // o [16 rows][G heads][HD] and (max, sum) [16][G][2], f32
+  static constexpr int PART_BYTES = (kTileQ * 8 * HD + kTileQ * 8 * 2) * 4;  // G <= 8
+  static_assert(PART_BYTES <= BYTES, "partials must fit the staging buffers");
 };
 
-template <int HD>
-__global__ void __launch_bounds__(256) attn_split_kernel(const AttnArgs a) {
+template <int HD, bool kGemvOut>
+__global__ void __launch_bounds__(256) attn_kernel(const AttnArgs a, const AttnOut out) {
   using T = Tile<HD>;
   extern __shared__ __align__(16) __half smem_h[];
   __shared__ int s_maxp;
@@ -91,9 +127,10 @@ __global__ void __launch_bounds__(256) attn_split_kernel(const AttnArgs a) {
   pdl_wait();
 
   const int G = a.nh / a.nkv;
+  const int ns = (int)gridDim.z;  // key splits = CTAs of this cluster
   const int tile = (int)gridDim.x - 1 - (int)blockIdx.x;  // longest rows first
   const int g = blockIdx.y;
-  const int split = blockIdx.z;
+  const int split = (int)cluster_rank();
   const int rbase = a.r0 + tile * kTileQ;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int h = g * G + warp;
@@ -110,11 +147,13 @@ __global__ void __launch_bounds__(256) attn_split_kernel(const AttnArgs a) {
   __syncthreads();
   if (threadIdx.x < kTileQ) atomicMax(&s_maxp, clamp_pos(rbase + threadIdx.x));
   __syncthreads();
-  const int maxp = s_maxp;
-  const int kbeg = split * a.ksplit;
-  if (kbeg > maxp) return;  // uniform across the CTA
-  const int kend = min(maxp + 1, kbeg + a.ksplit);
-  const int ntile = (kend - kbeg + kTileKV - 1) / kTileKV;
+  // this split's share of the keys 0..max position of the tile's rows
+  const int nkeys = s_maxp + 1;
+  int share = (nkeys + ns - 1) / ns;
+  share = (share + kTileKV - 1) / kTileKV * kTileKV;
+  const int kbeg = split * share;
+  const int kend = min(nkeys, kbeg + share);
+  const int ntile = kend > kbeg ? (kend - kbeg + kTileKV - 1) / kTileKV : 0;
 
   const int ra = rbase + qr, rb = rbase + qr + 8;
   const int pa = clamp_pos(ra), pb = clamp_pos(rb);
@@ -139,7 +178,7 @@ __global__ void __launch_bounds__(256) attn_split_kernel(const AttnArgs a) {
     }
     cp_async_commit();
   };
-  load_tile(0, 0);
+  if (ntile > 0) load_tile(0, 0);
 
   // Q fragments (A operand, row-major 16 x HD), split into fp16 hi/lo
   uint32_t qh[HD / 16][4], ql[HD / 16][4];
@@ -270,102 +309,148 @@ __global__ void __launch_bounds__(256) attn_split_kernel(const AttnArgs a) {
   l_a += __shfl_xor_sync(0xffffffffu, l_a, 2);
   l_b += __shfl_xor_sync(0xffffffffu, l_b, 1);
   l_b += __shfl_xor_sync(0xffffffffu, l_b, 2);
-  // partial: unnormalized o, running max (log2 units) and sum per row
-  const int nrows = a.r1 - a.r0;
-  if (ra < a.r1) {
-    const int64_t base = ((int64_t)split * nrows + (ra - a.r0)) * a.nh + h;
-    float* dst = a.part_o + base * HD + qc;
-#pragma unroll
-    for (int nd = 0; nd < HD / 8; ++nd)
-      *reinterpret_cast<float2*>(dst + nd * 8) = make_float2(o[nd][0], o[nd][1]);
-    if ((lane & 3) == 0) *reinterpret_cast<float2*>(a.part_ml + base * 2) = make_float2(m_a, l_a);
-  }
-  if (rb < a.r1) {
-    const int64_t base = ((int64_t)split * nrows + (rb - a.r0)) * a.nh + h;
-    float* dst = a.part_o + base * HD + qc;
-#pragma unroll
-    for (int nd = 0; nd < HD / 8; ++nd)
-      *reinterpret_cast<float2*>(dst + nd * 8) = make_float2(o[nd][2], o[nd][3]);
-    if ((lane & 3) == 0) *reinterpret_cast<float2*>(a.part_ml + base * 2) = make_float2(m_b, l_b);
-  }
-}
 
-// One CTA of 256 threads per query row: per-head split weights
-// w_s = 2^(m_s - M) / L in shared memory, then every thread merges its
-// elements over the splits, and each warp quantizes its 32-block.
-constexpr int kCombThreads = 256;
-constexpr int kMaxHeads = 64;
-
-template <bool kGemvOut, int PER>
-__global__ void __launch_bounds__(kCombThreads) attn_combine_kernel(const AttnArgs a, const AttnOut out) {
-  __shared__ float s_w[kMaxHeads][kMaxSplitsSmem];
-  pdl_trigger();
-  pdl_wait();
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int r = a.r0 + (int)blockIdx.x;
-  const int nrows = a.r1 - a.r0;
-  int p = a.pos[r];
-  p = p < 0 ? 0 : (p >= a.n_ctx ? a.n_ctx - 1 : p);
-  const int nsplit = min(p / a.ksplit + 1, kMaxSplitsSmem);
-  const int hd = a.hd;
-  const int q = a.nh * hd;
+  const int nblk = HD / 32;
+  const int q = a.nh * HD;
   const int nb = q / 32;
-  if (tid < a.nh) {
-    const int h = tid;
-    float M = -INFINITY;
-    for (int s = 0; s < nsplit; ++s)
-      M = fmaxf(M, a.part_ml[(((int64_t)s * nrows + (r - a.r0)) * a.nh + h) * 2]);
-    float L = 0.f;
-    for (int s = 0; s < nsplit; ++s) {
-      const int64_t base = ((int64_t)s * nrows + (r - a.r0)) * a.nh + h;
-      const float m = a.part_ml[base * 2];
-      const float w = (m == -INFINITY) ? 0.f : exp2f(m - M);
-      s_w[h][s] = w;
-      L = fmaf(a.part_ml[base * 2 + 1], w, L);
-    }
-    const float inv = L > 0.f ? __fdiv_rn(1.0f, L) : 0.f;
-    for (int s = 0; s < nsplit; ++s) s_w[h][s] = __fmul_rn(s_w[h][s], inv);
-  }
-  __syncthreads();
-  float y[PER];
+  const int r_a = rbase + qr, r_b = rbase + qr + 8;
+  // Normalized values of this thread's 8 + 8 elements of 32-block bq (rows
+  // r_a, r_b; dims bq*32 + i*8 + qc + {0,1}) -> f32 (debug), Q8_0 codes and
+  // the block scale.  The four lanes of a row hold the whole block.
+  auto emit = [&](int bq, const float (&va)[8], const float (&vb)[8]) {
+    float ma = 0.f, mb = 0.f;
 #pragma unroll
-  for (int i = 0; i < PER; ++i) y[i] = 0.f;
-  for (int s = 0; s < nsplit; ++s) {
-    const float* po = a.part_o + ((int64_t)s * nrows + (r - a.r0)) * q;
-#pragma unroll
-    for (int i = 0; i < PER; ++i) {
-      const int k = tid + kCombThreads * i;
-      if (k < q) y[i] = fmaf(po[k], s_w[k / hd][s], y[i]);
+    for (int i = 0; i < 8; ++i) {
+      ma = fmaxf(ma, fabsf(va[i]));
+      mb = fmaxf(mb, fabsf(vb[i]));
     }
-  }
-  const int64_t orow = r - out.row_base;
+    ma = fmaxf(ma, __shfl_xor_sync(0xffffffffu, ma, 1));
+    ma = fmaxf(ma, __shfl_xor_sync(0xffffffffu, ma, 2));
+    mb = fmaxf(mb, __shfl_xor_sync(0xffffffffu, mb, 1));
+    mb = fmaxf(mb, __shfl_xor_sync(0xffffffffu, mb, 2));
+    const int kb = h * HD + bq * 32;  // first element of the block in the output row
+    const int b = kb / 32;
 #pragma unroll
-  for (int i = 0; i < PER; ++i) {
-    const int k = tid + kCombThreads * i;
-    const int b = 8 * i + warp;
-    if (b >= nb) continue;  // warp-uniform
-    if (out.f32) out.f32[(int64_t)r * q + k] = y[i];
-    const float amax = warp_max(fabsf(y[i]));
-    const float dd = __fdiv_rn(amax, 127.0f);
-    const float code = q8_code(y[i], q8_inv(dd));
-    const __half d16 = __float2half_rn(dd);
-    if (kGemvOut) {
-      out.q8[orow * (int64_t)nb * 32 + k] = (int8_t)code;
-      if (lane == 0) out.s8[orow * nb + b] = __half2float(d16);
-    } else {
-      out.q16[orow * out.ldq + k] = __float2half_rn(code);
-      if (lane == 0) out.s16[(int64_t)b * out.ldqs + orow] = __half2float(d16);
+    for (int half = 0; half < 2; ++half) {
+      const int r = half ? r_b : r_a;
+      if (r >= a.r1) continue;
+      const float* v = half ? vb : va;
+      const float amax = half ? mb : ma;
+      const float dd = __fdiv_rn(amax, 127.0f);
+      const float id = q8_inv(dd);
+      const int64_t orow = r - out.row_base;
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const int k = kb + i * 8 + qc;
+        if (out.f32) *reinterpret_cast<float2*>(out.f32 + (int64_t)r * q + k) = make_float2(v[2 * i], v[2 * i + 1]);
+        const float c0 = q8_code(v[2 * i], id), c1 = q8_code(v[2 * i + 1], id);
+        if (kGemvOut) {
+          out.q8[orow * (int64_t)nb * 32 + k] = (int8_t)c0;
+          out.q8[orow * (int64_t)nb * 32 + k + 1] = (int8_t)c1;
+        } else {
+          *reinterpret_cast<__half2*>(out.q16 + orow * out.ldq + k) = __floats2half2_rn(c0, c1);
+        }
+      }
+      if ((lane & 3) == 0) {
+        const float d16 = __half2float(__float2half_rn(dd));
+        if (kGemvOut)
+          out.s8[orow * nb + b] = d16;
+        else
+          out.s16[(int64_t)b * out.ldqs + orow] = d16;
+      }
     }
-  }
-}
+  };
 
-template <bool kGemvOut>
-cudaError_t combine_dispatch(const AttnArgs& a, const AttnOut& out, int rows, cudaStream_t st) {
-  const int per = (a.nh * a.hd + kCombThreads - 1) / kCombThreads;
-  if (per <= 4) return launch_pdl(attn_combine_kernel<kGemvOut, 4>, rows, kCombThreads, 0, st, a, out);
-  if (per <= 8) return launch_pdl(attn_combine_kernel<kGemvOut, 8>, rows, kCombThreads, 0, st, a, out);
-  if (per <= 16) return launch_pdl(attn_combine_kernel<kGemvOut, 16>, rows, kCombThreads, 0, st, a, out);
-  return cudaErrorInvalidValue;
+  if (ns == 1) {
+    // the whole key range is here: normalize and quantize from registers
+    const float ia = l_a > 0.f ? __fdiv_rn(1.0f, l_a) : 0.f;
+    const float ib = l_b > 0.f ? __fdiv_rn(1.0f, l_b) : 0.f;
+#pragma unroll
+    for (int bq = 0; bq < nblk; ++bq) {
+      float va[8], vb[8];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        va[2 * i] = __fmul_rn(o[4 * bq + i][0], ia);
+        va[2 * i + 1] = __fmul_rn(o[4 * bq + i][1], ia);
+        vb[2 * i] = __fmul_rn(o[4 * bq + i][2], ib);
+        vb[2 * i + 1] = __fmul_rn(o[4 * bq + i][3], ib);
+      }
+      emit(bq, va, vb);
+    }
+    return;  // a cluster of one: nothing to wait for
+  }
+
+  // partial result into this CTA's shared memory (the staging buffers are
+  // free once every warp has left the key loop)
+  __syncthreads();
+  float* po = reinterpret_cast<float*>(smem_h);  // [16][G][HD]
+  float* pml = po + kTileQ * G * HD;             // [16][G][2]
+#pragma unroll
+  for (int nd = 0; nd < HD / 8; ++nd) {
+    *reinterpret_cast<float2*>(po + ((qr * G) + warp) * HD + nd * 8 + qc) =
+        make_float2(o[nd][0], o[nd][1]);
+    *reinterpret_cast<float2*>(po + (((qr + 8) * G) + warp) * HD + nd * 8 + qc) =
+        make_float2(o[nd][2], o[nd][3]);
+  }
+  if ((lane & 3) == 0) {
+    *reinterpret_cast<float2*>(pml + (qr * G + warp) * 2) = make_float2(m_a, l_a);
+    *reinterpret_cast<float2*>(pml + ((qr + 8) * G + warp) * 2) = make_float2(m_b, l_b);
+  }
+  cluster_sync_all();
+
+  // merge: the (head, 32-block) units are dealt round the CTAs of the
+  // cluster; the warp of that head merges its 16 rows from every CTA's
+  // partials (distributed shared memory) at its own fragment positions
+  const uint32_t po_s = smem_u32(po), pml_s = smem_u32(pml);
+  const uint32_t mla_off = (uint32_t)((qr * G + warp) * 2 * 4);
+  const uint32_t mlb_off = (uint32_t)(((qr + 8) * G + warp) * 2 * 4);
+  for (int bq = 0; bq < nblk; ++bq) {
+    if ((warp * nblk + bq) % ns != split) continue;  // warp-uniform
+    float2 mla[kMaxSplits], mlb[kMaxSplits];
+    float Ma = -INFINITY, Mb = -INFINITY;
+#pragma unroll
+    for (int sidx = 0; sidx < kMaxSplits; ++sidx) {
+      if (sidx < ns) {
+        mla[sidx] = ld_peer2(peer_addr(pml_s + mla_off, (uint32_t)sidx));
+        mlb[sidx] = ld_peer2(peer_addr(pml_s + mlb_off, (uint32_t)sidx));
+        Ma = fmaxf(Ma, mla[sidx].x);
+        Mb = fmaxf(Mb, mlb[sidx].x);
+      }
+    }
+    float va[8], vb[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) va[i] = vb[i] = 0.f;
+    float La = 0.f, Lb = 0.f;
+#pragma unroll
+    for (int sidx = 0; sidx < kMaxSplits; ++sidx) {
+      if (sidx < ns) {
+        const float wa = (mla[sidx].x == -INFINITY) ? 0.f : exp2f(mla[sidx].x - Ma);
+        const float wb = (mlb[sidx].x == -INFINITY) ? 0.f : exp2f(mlb[sidx].x - Mb);
+        La = fmaf(mla[sidx].y, wa, La);
+        Lb = fmaf(mlb[sidx].y, wb, Lb);
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const int dim = bq * 32 + i * 8 + qc;
+          const float2 xa = ld_peer2(peer_addr(po_s + (uint32_t)(((qr * G + warp) * HD + dim) * 4), (uint32_t)sidx));
+          const float2 xb = ld_peer2(peer_addr(po_s + (uint32_t)((((qr + 8) * G + warp) * HD + dim) * 4), (uint32_t)sidx));
+          va[2 * i] = fmaf(xa.x, wa, va[2 * i]);
+          va[2 * i + 1] = fmaf(xa.y, wa, va[2 * i + 1]);
+          vb[2 * i] = fmaf(xb.x, wb, vb[2 * i]);
+          vb[2 * i + 1] = fmaf(xb.y, wb, vb[2 * i + 1]);
+        }
+      }
+    }
+    const float ia = La > 0.f ? __fdiv_rn(1.0f, La) : 0.f;
+    const float ib = Lb > 0.f ? __fdiv_rn(1.0f, Lb) : 0.f;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      va[i] = __fmul_rn(va[i], ia);
+      vb[i] = __fmul_rn(vb[i], ib);
+    }
+    emit(bq, va, vb);
+  }
+  // peers may still be reading this CTA's partials
+  cluster_sync_all();
 }
 
 // K/V rows of one layer -> fp16 hi/lo shadow planes (count f32 values each).
@@ -384,55 +469,51 @@ __global__ void kv_shadow_kernel(const float* __restrict__ k, const float* __res
 
 }  // namespace
 
-int attention_splits(int rows, int nkv, int n_ctx, int num_sms, int* ksplit) {
-  const int tiles = (rows + kTileQ - 1) / kTileQ;
-  if (tiles * nkv >= num_sms) {
-    *ksplit = (n_ctx + kTileKV - 1) / kTileKV * kTileKV;
-    return 1;
+int attention_nsplit(int rows, int nkv, int num_sms) {
+  const int ctas = (rows + kTileQ - 1) / kTileQ * nkv;
+  if (ctas >= num_sms) return 1;
+  int ns = (2 * num_sms + ctas - 1) / std::max(ctas, 1);
+  return ns < 1 ? 1 : (ns > kMaxSplits ? kMaxSplits : ns);
+}
+
+template <int HD, bool kGemvOut>
+cudaError_t launch_attn(const AttnArgs& a, const AttnOut& out, int rows, cudaStream_t st) {
+  static bool set = false;
+  if (!set) {
+    cudaError_t e = cudaFuncSetAttribute(attn_kernel<HD, kGemvOut>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, Tile<HD>::BYTES);
+    if (e != cudaSuccess) return e;
+    set = true;
   }
-  // 128 keys per split, fewer (longer) splits for very long regions
-  int ks = (n_ctx + kMaxSplitsSmem - 1) / kMaxSplitsSmem;
-  ks = ks < 128 ? 128 : (ks + kTileKV - 1) / kTileKV * kTileKV;
-  *ksplit = ks;
-  return (n_ctx + ks - 1) / ks;
+  const int G = a.nh / a.nkv;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((rows + kTileQ - 1) / kTileQ, a.nkv, a.nsplit);
+  cfg.blockDim = dim3(32 * G);
+  cfg.dynamicSmemBytes = Tile<HD>::BYTES;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 1;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = a.nsplit;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 2;
+  return cudaLaunchKernelEx(&cfg, attn_kernel<HD, kGemvOut>, a, out);
 }
 
 cudaError_t attention_launch(const AttnArgs& a, const AttnOut& out, cudaStream_t st) {
   const int rows = a.r1 - a.r0;
   if (rows <= 0) return cudaSuccess;
   const int G = a.nh / a.nkv;
-  if (a.nh % a.nkv != 0 || G > 8 || a.ksplit <= 0 || a.ksplit % kTileKV != 0)
+  if (a.nh % a.nkv != 0 || G > 8 || a.nsplit < 1 || a.nsplit > kMaxSplits)
     return cudaErrorInvalidValue;
-  const int nsplit = (a.n_ctx + a.ksplit - 1) / a.ksplit;
-  const dim3 grid((rows + kTileQ - 1) / kTileQ, a.nkv, nsplit);
-  if (a.hd == 64) {
-    static bool set = false;
-    if (!set) {
-      cudaError_t e = cudaFuncSetAttribute(
-          attn_split_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize, Tile<64>::BYTES);
-      if (e != cudaSuccess) return e;
-      set = true;
-    }
-    cudaError_t e = launch_pdl(attn_split_kernel<64>, grid, 32 * G, Tile<64>::BYTES, st, a);
-    if (e != cudaSuccess) return e;
-  } else if (a.hd == 128) {
-    static bool set = false;
-    if (!set) {
-      cudaError_t e = cudaFuncSetAttribute(
-          attn_split_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize, Tile<128>::BYTES);
-      if (e != cudaSuccess) return e;
-      set = true;
-    }
-    cudaError_t e = launch_pdl(attn_split_kernel<128>, grid, 32 * G, Tile<128>::BYTES, st, a);
-    if (e != cudaSuccess) return e;
-  } else {
-    return cudaErrorInvalidValue;
-  }
-  cudaError_t e = cudaGetLastError();
-  if (e != cudaSuccess) return e;
-  if (a.nh > kMaxHeads || (a.n_ctx + a.ksplit - 1) / a.ksplit > kMaxSplitsSmem)
-    return cudaErrorInvalidValue;
-  return out.q8 ? combine_dispatch<true>(a, out, rows, st) : combine_dispatch<false>(a, out, rows, st);
+  const bool gemv = out.q8 != nullptr;
+  if (a.hd == 64) return gemv ? launch_attn<64, true>(a, out, rows, st) : launch_attn<64, false>(a, out, rows, st);
+  if (a.hd == 128)
+    return gemv ? launch_attn<128, true>(a, out, rows, st) : launch_attn<128, false>(a, out, rows, st);
+  return cudaErrorInvalidValue;
 }
 
 cudaError_t kv_shadow_launch(const float* k, const float* v, int64_t count, __half* const* planes,

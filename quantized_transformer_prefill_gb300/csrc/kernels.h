@@ -149,10 +149,8 @@ struct AttnArgs {
   int r0 = 0, r1 = 0;
   const __half* shadow[4] = {nullptr, nullptr, nullptr, nullptr};  // K hi, K lo, V hi, V lo [n_ctx][nkv*hd]
   int nh = 0, nkv = 0, hd = 0;
-  int n_ctx = 0;        // positions are clamped into [0, n_ctx) before any region read
-  int ksplit = 0;
-  float* part_o = nullptr;   // scratch [n_ctx/ksplit][r1-r0][nh][hd]
-  float* part_ml = nullptr;  // scratch [n_ctx/ksplit][r1-r0][nh][2]
+  int n_ctx = 0;   // positions are clamped into [0, n_ctx) before any region read
+  int nsplit = 1;  // key splits (CTAs per cluster), 1..8
 };
 // Where the attention output goes: Q8_0 codes in the GEMM layout (q16 [rows][ldq]
 // fp16 + s16 [nb][ldqs]) or the GEMV layout (q8 [rows][nb*32] + s8 [rows][nb]);
@@ -167,8 +165,8 @@ struct AttnOut {
   int64_t row_base = 0;
   float* f32 = nullptr;
 };
-// Number of key splits and the split length for rows query rows.
-int attention_splits(int rows, int nkv, int n_ctx, int num_sms, int* ksplit);
+// Key splits for `rows` query rows: enough CTAs to fill the GPU about twice.
+int attention_nsplit(int rows, int nkv, int num_sms);
 cudaError_t attention_launch(const AttnArgs& a, const AttnOut& out, cudaStream_t stream);
 // f32 K/V values -> fp16 hi/lo planes (planes[0..3] = K hi, K lo, V hi, V lo).
 cudaError_t kv_shadow_launch(const float* k, const float* v, int64_t count, __half* const* planes,

@@ -161,15 +161,11 @@ struct Workspace {
   float* t_s = nullptr;      // [max nb]
   float* gu = nullptr;       // [2F]
   float* logits = nullptr;   // [V]
-  float* att_o = nullptr;    // attention split scratch [splits][nt][q]
-  float* att_ml = nullptr;   // [splits][nt][nh][2]
-  size_t att_o_cap = 0, att_ml_cap = 0;
   int ntp = 0;
   void release() {
     dfree(ids); dfree(pos); dfree(h); dfree(xa); dfree(xa_s); dfree(xf); dfree(xf_s);
     dfree(part); dfree(qrot); dfree(att); dfree(h_last); dfree(t_q); dfree(t_s); dfree(gu);
-    dfree(logits); dfree(att_o); dfree(att_ml);
-    att_o_cap = att_ml_cap = 0;
+    dfree(logits);
     max_nt = 0;
   }
 };
@@ -732,9 +728,7 @@ int enqueue_forward(minfer_model* m, minfer_kv* kv, const int32_t* ids, const in
     at.nkv = hp.n_head_kv;
     at.hd = hp.head_dim;
     at.n_ctx = kv->n_ctx;
-    attention_splits(at.r1 - at.r0, at.nkv, at.n_ctx, m->num_sms, &at.ksplit);
-    at.part_o = w.att_o;
-    at.part_ml = w.att_ml;
+    at.nsplit = attention_nsplit(at.r1 - at.r0, at.nkv, m->num_sms);
     AttnOut ao;
     ao.f32 = (m->debug_f32 || cap_all) ? w.att : nullptr;
     if (!last) {
@@ -894,36 +888,10 @@ int enqueue_forward(minfer_model* m, minfer_kv* kv, const int32_t* ids, const in
 }
 
 // Run (record or replay) the forward on stream st.
-int ensure_attn_scratch(minfer_model* m, int nt, int n_ctx) {
-  Workspace& w = m->ws;
-  int ks = 0;
-  const int ns = attention_splits(nt, m->hp.n_head_kv, n_ctx, m->num_sms, &ks);
-  const size_t need_o = (size_t)ns * nt * m->q;
-  const size_t need_ml = (size_t)ns * nt * m->hp.n_head * 2;
-  if (need_o <= w.att_o_cap && need_ml <= w.att_ml_cap) return MINFER_OK;
-  if (m->gexec) {
-    cudaGraphExecDestroy(m->gexec);
-    m->gexec = nullptr;
-  }
-  if (m->graph) {
-    cudaGraphDestroy(m->graph);
-    m->graph = nullptr;
-  }
-  dfree(w.att_o);
-  dfree(w.att_ml);
-  w.att_o_cap = w.att_ml_cap = 0;
-  int rc;
-  if ((rc = dalloc(&w.att_o, need_o)) || (rc = dalloc(&w.att_ml, need_ml))) return rc;
-  w.att_o_cap = need_o;
-  w.att_ml_cap = need_ml;
-  return MINFER_OK;
-}
-
 int run_forward(minfer_model* m, minfer_kv* kv, const int32_t* ids, const int32_t* pos, int nt,
                 float* logits, cudaStream_t st) {
   int rc = ensure_workspace(m, nt);
   if (rc) return rc;
-  if ((rc = ensure_attn_scratch(m, nt, kv->n_ctx))) return rc;
   m->dump_on = m->dump_host != nullptr && nt <= m->dump_max_nt;
   const bool dumps = m->dump_on || m->dbg_layer >= 0;
   if (dumps) {
@@ -1427,13 +1395,11 @@ int minfer_op_attention(const float* d_q, const int32_t* d_pos, int nt, const fl
   a.nkv = n_head_kv;
   a.hd = head_dim;
   a.n_ctx = n_ctx;
-  const int ns = attention_splits(nt, n_head_kv, n_ctx, num_sms, &a.ksplit);
+  a.nsplit = attention_nsplit(nt, n_head_kv, num_sms);
   __half* sh = nullptr;
-  float *po = nullptr, *pml = nullptr, *s16 = nullptr;
+  float* s16 = nullptr;
   __half* q16 = nullptr;
   int rc = dalloc(&sh, (size_t)4 * n_ctx * kvw);
-  if (!rc) rc = dalloc(&po, (size_t)ns * nt * q);
-  if (!rc) rc = dalloc(&pml, (size_t)ns * nt * n_head * 2);
   if (!rc) rc = dalloc(&q16, (size_t)nt * q);
   if (!rc) rc = dalloc(&s16, (size_t)(q / 32) * nt);
   cudaError_t e = cudaSuccess;
@@ -1443,8 +1409,6 @@ int minfer_op_attention(const float* d_q, const int32_t* d_pos, int nt, const fl
       planes[i] = sh + (int64_t)i * n_ctx * kvw;
       a.shadow[i] = planes[i];
     }
-    a.part_o = po;
-    a.part_ml = pml;
     AttnOut out;
     out.q16 = q16;
     out.ldq = q;
@@ -1456,8 +1420,6 @@ int minfer_op_attention(const float* d_q, const int32_t* d_pos, int nt, const fl
     if (e == cudaSuccess) e = cudaDeviceSynchronize();
   }
   dfree(sh);
-  dfree(po);
-  dfree(pml);
   dfree(q16);
   dfree(s16);
   if (rc) return rc;
