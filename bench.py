@@ -118,6 +118,27 @@ def forward_macs(cfg, nt, p0=0):
     return mm, H * V, attn
 
 
+_PROFILE_OF = {"gemm_gate_up_swiglu": "gemm_gate_up", "attention": "attention",
+               "rmsnorm_quant": "row_quant"}
+
+
+def profiled_traffic(kernel: str, workload: str):
+    """DRAM bytes per launch (read + write) of `kernel` on `workload` from the
+    committed ncu summary under profiles/, or None when there is none."""
+    name = _PROFILE_OF.get(kernel)
+    if not name:
+        return None
+    path = os.path.join(ROOT, "profiles", f"{name}_{workload}.md")
+    try:
+        with open(path) as f:
+            for line in f:
+                if line.startswith("traffic_bytes_per_launch:"):
+                    return int(line.split(":")[1])
+    except OSError:
+        pass
+    return None
+
+
 def oracle_model(cfg):
     import oracle
     m = oracle.Model(cfg)
@@ -286,12 +307,13 @@ def ours(args, w, rank, world, dist):
         avg_ms = tot / n
         achieved = flops[dom] / (avg_ms / 1e3) / 1e12
         roof = {"kernel": dom, "bound": "tensor", "achieved": achieved, "peak": bf16,
-                "unit": "TFLOP/s", "frac": achieved / bf16, "traffic": None,
+                "unit": "TFLOP/s", "frac": achieved / bf16,
+                "traffic": profiled_traffic(dom, w.name),
                 "peak_source": f"{peak_src} bf16 burst (fp16 operands run at the bf16 rate)",
                 "per_launch_flops": flops[dom], "avg_launch_us": 1e3 * avg_ms}
     else:
         roof = {"kernel": dom, "bound": "hbm", "achieved": None, "peak": hbm, "unit": "GB/s",
-                "frac": None, "traffic": None}
+                "frac": None, "traffic": profiled_traffic(dom, w.name)}
     mm, lm, attn = forward_macs(cfg, nt, w.p0)
     # forward roofline: GEMM + attention flops at the tensor peak, lm_head and
     # the hidden-state traffic at HBM bandwidth
