@@ -38,7 +38,7 @@ class Hparams(ctypes.Structure):
                 ("n_head_kv", ctypes.c_int), ("head_dim", ctypes.c_int), ("n_ff", ctypes.c_int),
                 ("n_vocab", ctypes.c_int), ("max_seq_len", ctypes.c_int),
                 ("rope_theta", ctypes.c_float), ("rms_eps", ctypes.c_float),
-                ("tied_embeddings", ctypes.c_int)]
+                ("tied_embeddings", ctypes.c_int), ("qk_norm", ctypes.c_int)]
 
 
 def _lib_handle():
@@ -197,7 +197,8 @@ def argmax(x: np.ndarray) -> int:
 
 def hparams_of(cfg) -> Hparams:
     return Hparams(cfg.n_layer, cfg.n_embd, cfg.n_head, cfg.n_head_kv, cfg.head_dim, cfg.n_ff,
-                   cfg.n_vocab, cfg.max_seq_len, cfg.rope_theta, cfg.rms_eps, int(cfg.tied))
+                   cfg.n_vocab, cfg.max_seq_len, cfg.rope_theta, cfg.rms_eps, int(cfg.tied),
+                   int(getattr(cfg, "qk_norm", False)))
 
 
 class Model:

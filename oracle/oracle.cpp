@@ -29,6 +29,12 @@
  *      scores and softmax in double; KV rows never written read as zero.
  *   R6 SiLU(g) * u evaluated in double, rounded to f32.
  *   R7 argmax ties go to the lowest index.
+ *   R8 Qwen3 QK-norm ([P05] section 2.5 operation family "qk_norm (Qwen3)";
+ *      section 3.2 "FusedQkvNorm": the per-head Q/K RMSNorm sits between the
+ *      three matmuls and the two RoPEs): each head of Q and of K is RMS-
+ *      normalized over its head_dim values as in R3, with one weight vector
+ *      of head_dim entries per layer for Q and one for K, after the bias and
+ *      before RoPE.  Models with QK-norm carry no Q/K/V bias.
  *
  * Every floating-point statement below is evaluated exactly as written: the
  * file is compiled with -ffp-contract=off and without fast-math.
@@ -38,6 +44,8 @@
  *   block dots      -- brute-force integer sums
  *   matmul          -- dequantize-then-float64-GEMM closed form (numpy)
  *   rmsnorm         -- float64 closed form (numpy), scale invariance
+ *   qk-norm         -- per-head rmsnorm; in the model: logits invariant to a
+ *                      power-of-two scaling of Wq/Wk (and not without it)
  *   rope            -- norm preservation, R(a)R(b)=R(a+b), relative-position
  *                      property, a single-unit-vector closed form
  *   attention       -- brute-force masked softmax(QK^T/sqrt(d))V (numpy)
@@ -308,10 +316,11 @@ typedef struct {
   int n_layer, n_embd, n_head, n_head_kv, head_dim, n_ff, n_vocab, max_seq_len;
   float rope_theta, rms_eps;
   int tied_embeddings;
+  int qk_norm; /* reading R8 */
 } orc_hparams;
 
 struct OrcLayer {
-  std::vector<float> attn_norm, ffn_norm, bq, bk, bv;
+  std::vector<float> attn_norm, ffn_norm, bq, bk, bv, q_norm, k_norm;
   QMat wq, wk, wv, wo, wg, wu, wd;
 };
 
@@ -440,6 +449,8 @@ static int lookup(orc_model* m, const char* name, QMat** qm, std::vector<float>*
   if (k == "attn_q.bias") { *vec = &L.bq; *ne0 = q; *ne1 = 1; return 0; }
   if (k == "attn_k.bias") { *vec = &L.bk; *ne0 = kv; *ne1 = 1; return 0; }
   if (k == "attn_v.bias") { *vec = &L.bv; *ne0 = kv; *ne1 = 1; return 0; }
+  if (hp.qk_norm && k == "attn_q_norm.weight") { *vec = &L.q_norm; *ne0 = hp.head_dim; *ne1 = 1; return 0; }
+  if (hp.qk_norm && k == "attn_k_norm.weight") { *vec = &L.k_norm; *ne0 = hp.head_dim; *ne1 = 1; return 0; }
   if (k == "attn_q.weight") { *qm = &L.wq; *ne0 = H; *ne1 = q; return 0; }
   if (k == "attn_k.weight") { *qm = &L.wk; *ne0 = H; *ne1 = kv; return 0; }
   if (k == "attn_v.weight") { *qm = &L.wv; *ne0 = H; *ne1 = kv; return 0; }
@@ -484,11 +495,14 @@ int orc_model_get_q8(orc_model* m, const char* name, int8_t* q, uint16_t* d) {
 int orc_model_check(orc_model* m) {
   if (!m->tok_embd.present || m->out_norm.empty()) return -1;
   if (!m->hp.tied_embeddings && !m->output.present) return -1;
-  for (auto& L : m->layers)
-    if (L.attn_norm.empty() || L.ffn_norm.empty() || L.bq.empty() || L.bk.empty() ||
-        L.bv.empty() || !L.wq.present || !L.wk.present || !L.wv.present || !L.wo.present ||
-        !L.wg.present || !L.wu.present || !L.wd.present)
+  for (auto& L : m->layers) {
+    if (L.attn_norm.empty() || L.ffn_norm.empty() || !L.wq.present || !L.wk.present ||
+        !L.wv.present || !L.wo.present || !L.wg.present || !L.wu.present || !L.wd.present)
       return -1;
+    /* Qwen2: Q/K/V biases; Qwen3 (R8): the two QK-norm weights, biases optional */
+    if (!m->hp.qk_norm && (L.bq.empty() || L.bk.empty() || L.bv.empty())) return -1;
+    if (m->hp.qk_norm && (L.q_norm.empty() || L.k_norm.empty())) return -1;
+  }
   return 0;
 }
 
@@ -532,7 +546,9 @@ int orc_kv_write(orc_kv* kv, int layer, int which, int row0, int nrows, const fl
  *
  *   h = embed(ids)
  *   per layer: x = Q8_0(rmsnorm(h) * attn_norm)
- *              Q,K,V = x.W{q,k,v} + b; rope(Q), rope(K) at pos
+ *              Q,K,V = x.W{q,k,v} + b
+ *              (Qwen3, R8: Q, K = per-head rmsnorm(Q, K) * q_norm, k_norm)
+ *              rope(Q), rope(K) at pos
  *              K/V regions row pos[t] <- K[t], V[t]    (before attention)
  *              a = attention(Q, regions, pos)          (all rows)
  *              o = Q8_0(a).Wo
@@ -589,9 +605,25 @@ int orc_prefill(orc_model* m, orc_kv* kv, const int32_t* ids, const int32_t* pos
     orc_q8_quantize(xn.data(), rows, H, xq.data(), xd.data());
     /* Q, K, V with bias */
     Q.assign((int64_t)rows * q, 0); Kt.assign((int64_t)rows * kvw, 0); Vt.assign((int64_t)rows * kvw, 0);
-    matmul_q8(xq.data(), xd.data(), rows, L.wq, L.bq.data(), Q.data());
-    matmul_q8(xq.data(), xd.data(), rows, L.wk, L.bk.data(), Kt.data());
-    matmul_q8(xq.data(), xd.data(), rows, L.wv, L.bv.data(), Vt.data());
+    matmul_q8(xq.data(), xd.data(), rows, L.wq, L.bq.empty() ? nullptr : L.bq.data(), Q.data());
+    matmul_q8(xq.data(), xd.data(), rows, L.wk, L.bk.empty() ? nullptr : L.bk.data(), Kt.data());
+    matmul_q8(xq.data(), xd.data(), rows, L.wv, L.bv.empty() ? nullptr : L.bv.data(), Vt.data());
+    if (hp.qk_norm) {
+      /* reading R8: per-head RMSNorm of Q and K, after the bias, before RoPE */
+      std::vector<float> tmp(hd);
+      for (int t = 0; t < rows; ++t) {
+        for (int64_t hh = 0; hh < nh; ++hh) {
+          float* x = &Q[t * q + hh * hd];
+          rmsnorm_row(x, L.q_norm.data(), hd, hp.rms_eps, tmp.data());
+          std::memcpy(x, tmp.data(), sizeof(float) * hd);
+        }
+        for (int64_t hh = 0; hh < nkv; ++hh) {
+          float* x = &Kt[t * kvw + hh * hd];
+          rmsnorm_row(x, L.k_norm.data(), hd, hp.rms_eps, tmp.data());
+          std::memcpy(x, tmp.data(), sizeof(float) * hd);
+        }
+      }
+    }
     rope_apply(Q.data(), rows, (int)nh, (int)hd, pos, c.data(), s.data());
     rope_apply(Kt.data(), rows, (int)nkv, (int)hd, pos, c.data(), s.data());
     /* kvcache_store: position p writes row p ([P09] section 2.2) */

@@ -97,6 +97,8 @@ class ModelConfig:
     weight_std: float = 0.02
     bias_std: float = 0.02
     norm_std: float = 0.01
+    qk_norm: bool = False   # Qwen3: per-head RMSNorm of Q and K before RoPE
+    qkv_bias: bool = True   # Qwen2 carries Q/K/V biases, Qwen3 none
 
 
 @dataclass(frozen=True)
@@ -125,6 +127,12 @@ TINY = ModelConfig("tiny", 2, 256, 4, 2, 64, 688, 4096, tied=False, max_seq_len=
 QWEN2_0_5B = ModelConfig("qwen2-0.5b", 24, 896, 14, 2, 64, 4864, 151936, tied=True)
 QWEN2_1_5B = ModelConfig("qwen2-1.5b", 28, 1536, 12, 2, 128, 8960, 151936, tied=False)
 QWEN2_7B = ModelConfig("qwen2-7b", 28, 3584, 28, 4, 128, 18944, 152064, tied=False)
+# Qwen3 variant (per-head QK RMSNorm, no Q/K/V bias): a tiny model for strict
+# parity and the 0.6B shape (28 layers, H 1024, 16/8 heads of 128, FFN 3072)
+QWEN3_TINY = ModelConfig("qwen3-tiny", 2, 256, 4, 2, 64, 688, 4096, tied=True, max_seq_len=128,
+                         qk_norm=True, qkv_bias=False)
+QWEN3_0_6B = ModelConfig("qwen3-0.6b", 28, 1024, 16, 8, 128, 3072, 151936, tied=True,
+                         qk_norm=True, qkv_bias=False)
 
 WORKLOADS = {
     "tiny-32": Workload("tiny-32", TINY, 32, 0, 128),
@@ -133,13 +141,16 @@ WORKLOADS = {
     "qwen2-7b-4096": Workload("qwen2-7b-4096", QWEN2_7B, 4096, 0, 8192),
     "qwen2-1.5b-append-1024": Workload("qwen2-1.5b-append-1024", QWEN2_1_5B, 1024, 3072, 4096,
                                        prompt_seed=1, prefill_tokens=3072, prefill_seed=0),
+    "qwen3-tiny-32": Workload("qwen3-tiny-32", QWEN3_TINY, 32, 0, 128),
+    "qwen3-0.6b-512": Workload("qwen3-0.6b-512", QWEN3_0_6B, 512, 0, 4096),
 }
 
 # stream ids of the per-tensor generators
 _GLOBAL_STREAMS = {"token_embd.weight": 1, "output_norm.weight": 2, "output.weight": 3}
 _LAYER_KINDS = ["attn_norm.weight", "attn_q.weight", "attn_q.bias", "attn_k.weight", "attn_k.bias",
                 "attn_v.weight", "attn_v.bias", "attn_output.weight", "ffn_norm.weight",
-                "ffn_gate.weight", "ffn_up.weight", "ffn_down.weight"]
+                "ffn_gate.weight", "ffn_up.weight", "ffn_down.weight", "attn_q_norm.weight",
+                "attn_k_norm.weight"]
 
 
 @dataclass(frozen=True)
@@ -174,9 +185,16 @@ def tensor_specs(cfg: ModelConfig) -> list[TensorSpec]:
               "attn_k.bias": (kv, 1, 0.0, b), "attn_v.weight": (H, kv, 0.0, w),
               "attn_v.bias": (kv, 1, 0.0, b), "attn_output.weight": (q, H, 0.0, w),
               "ffn_norm.weight": (H, 1, 1.0, nrm), "ffn_gate.weight": (H, F, 0.0, w),
-              "ffn_up.weight": (H, F, 0.0, w), "ffn_down.weight": (F, H, 0.0, w)}
+              "ffn_up.weight": (H, F, 0.0, w), "ffn_down.weight": (F, H, 0.0, w),
+              "attn_q_norm.weight": (cfg.head_dim, 1, 1.0, nrm),
+              "attn_k_norm.weight": (cfg.head_dim, 1, 1.0, nrm)}
     for i in range(cfg.n_layer):
         for k, kind in enumerate(_LAYER_KINDS):
+            if kind.endswith(".bias") and not cfg.qkv_bias:
+                continue
+            if kind.endswith("_norm.weight") and kind.startswith("attn_") and kind != "attn_norm.weight" \
+                    and not cfg.qk_norm:
+                continue
             ne0, ne1, mean, std = shapes[kind]
             specs.append(TensorSpec(f"blk.{i}.{kind}", ne0, ne1, 16 + 16 * i + k, mean, std))
     return specs

@@ -268,11 +268,56 @@ def test_attention_brute_force_softmax(oracle_mod):
 
 # ---------------------------------------------------------------- whole model invariants
 
-@pytest.fixture(scope="module")
-def tiny(oracle_mod, synth_mod):
-    cfg = synth_mod.TINY
+@pytest.fixture(scope="module", params=["qwen2", "qwen3"])
+def tiny(request, oracle_mod, synth_mod):
+    """The tiny Qwen2-style model and its Qwen3 (QK-norm, no bias) variant:
+    every model invariant below holds for both."""
+    cfg = synth_mod.TINY if request.param == "qwen2" else synth_mod.QWEN3_TINY
     tensors = synth_mod.model_tensors(cfg)
     return cfg, tensors, oracle_mod.Model(cfg, tensors)
+
+
+def _q8_model(oracle_mod, synth_mod, cfg, scale_qk: float):
+    """cfg's model from Q8_0 blocks of its f32 tensors, with the Q and K
+    projection block scales multiplied by scale_qk (exact for a power of two)."""
+    m = oracle_mod.Model(cfg)
+    for spec in synth_mod.tensor_specs(cfg):
+        arr = synth_mod.tensor_data(spec)
+        if spec.is_matrix:
+            q, d = oracle_mod.q8_quantize(arr)
+            if spec.name.endswith(("attn_q.weight", "attn_k.weight")):
+                d = (d.view(np.float16) * np.float16(scale_qk)).view(np.uint16)
+            nb = q.shape[1] // 32
+            blocks = np.zeros((q.shape[0], nb, 34), np.uint8)
+            blocks[:, :, :2] = d.reshape(q.shape[0], nb, 1).view(np.uint8)
+            blocks[:, :, 2:] = q.reshape(q.shape[0], nb, 32).view(np.uint8)
+            m.set_q8_0(spec.name, blocks.reshape(-1), spec.ne0, spec.ne1)
+        else:
+            m.set_f32(spec.name, arr)
+    assert m.check()
+    return m
+
+
+def test_qk_norm_makes_attention_blind_to_the_qk_scale(oracle_mod, synth_mod):
+    """QK-norm ("05 · Graph build", section 2.5 operation family: qk_norm for
+    Qwen3; section 3.2, FusedQkvNorm: per-head Q/K RMSNorm before RoPE)
+    normalizes each head: doubling every Q and K block scale leaves the
+    logits bit-identical (with eps = 0 the doubling passes through the norm
+    exactly), while the same change without QK-norm sharpens every softmax."""
+    import dataclasses
+    ids = synth_mod.token_ids(5, 24, 4096)
+    pos = np.arange(24, dtype=np.int32)
+    out = {}
+    for qk in (True, False):
+        cfg = dataclasses.replace(synth_mod.QWEN3_TINY, rms_eps=0.0, qk_norm=qk, qkv_bias=not qk)
+        for scale in (1.0, 2.0):
+            m = _q8_model(oracle_mod, synth_mod, cfg, scale)
+            rc, lg, _ = m.prefill(m.kv(64), ids, pos)
+            assert rc == 0
+            out[qk, scale] = lg[0]
+    assert np.array_equal(out[True, 1.0], out[True, 2.0])
+    d = np.linalg.norm(out[False, 1.0] - out[False, 2.0]) / np.linalg.norm(out[False, 1.0])
+    assert d > 1e-2, d
 
 
 def test_model_causality(tiny, synth_mod):
