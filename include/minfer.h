@@ -67,6 +67,12 @@ typedef struct minfer_hparams {
   float rope_theta;  /* RoPE frequency base */
   float rms_eps;     /* RMSNorm epsilon */
   int tied_embeddings; /* 1: lm_head reuses token_embd.weight */
+  int qk_norm;       /* 1: Qwen3 -- each head of Q and K is RMS-normalized over head_dim
+                        (weights blk.{i}.attn_q_norm.weight / attn_k_norm.weight,
+                        head_dim entries each) after the bias and before RoPE
+                        ("05 · Graph build", section 2.5: qk_norm; section 3.2:
+                        FusedQkvNorm); the Q/K/V biases are then optional (zero
+                        when absent).  0: Qwen2, biases required. */
 } minfer_hparams;
 
 typedef struct minfer_tensor {
@@ -74,7 +80,8 @@ typedef struct minfer_tensor {
                        blk.{i}.{attn_norm.weight, attn_q.weight, attn_q.bias,
                        attn_k.weight, attn_k.bias, attn_v.weight, attn_v.bias,
                        attn_output.weight, ffn_norm.weight, ffn_gate.weight,
-                       ffn_up.weight, ffn_down.weight} */
+                       ffn_up.weight, ffn_down.weight}; with qk_norm also
+                       blk.{i}.{attn_q_norm.weight, attn_k_norm.weight} */
   int type;         /* MINFER_F32 (vectors and matrices) or MINFER_Q8_0 (matrices) */
   int64_t ne0, ne1; /* ne0 contiguous; ne1 = 1 for vectors */
   const void* data; /* host memory, borrowed during the call */
@@ -240,6 +247,16 @@ int minfer_op_attention(const float* d_q, const int32_t* d_pos, int nt, const fl
 int minfer_op_rope_store(const float* d_qkv, const float* d_bias, const int32_t* d_pos, int nt,
                          int n_head, int n_head_kv, int head_dim, float theta, int n_ctx,
                          float* d_q_out, float* d_k, float* d_v);
+
+/* The same with Qwen3 QK-norm between the bias and RoPE: each head of Q and
+ * K is RMS-normalized over its head_dim values (mean of squares, eps added,
+ * scale rounded to f32, then (x * scale) * w) with the weights d_qnorm /
+ * d_knorm [head_dim] ("05 · Graph build", section 3.2: FusedQkvNorm).
+ * d_bias may be NULL. */
+int minfer_op_qknorm_rope_store(const float* d_qkv, const float* d_bias, const float* d_qnorm,
+                                const float* d_knorm, float eps, const int32_t* d_pos, int nt,
+                                int n_head, int n_head_kv, int head_dim, float theta, int n_ctx,
+                                float* d_q_out, float* d_k, float* d_v);
 
 /* Same product as minfer_op_gemm (same kernels, same split plan) without any
  * device allocation: for callers that cannot call cudaMalloc (their own

@@ -34,7 +34,7 @@ class Hparams(ctypes.Structure):
                 ("n_head_kv", ctypes.c_int), ("head_dim", ctypes.c_int), ("n_ff", ctypes.c_int),
                 ("n_vocab", ctypes.c_int), ("max_seq_len", ctypes.c_int),
                 ("rope_theta", ctypes.c_float), ("rms_eps", ctypes.c_float),
-                ("tied_embeddings", ctypes.c_int)]
+                ("tied_embeddings", ctypes.c_int), ("qk_norm", ctypes.c_int)]
 
 
 class Tensor(ctypes.Structure):
@@ -70,6 +70,7 @@ SIGNATURES = {
     "minfer_op_gemm_swiglu": ([_P, _P, _I64, _P, _P, _P, _P, _I64, _I64, _P, _P], _I),
     "minfer_op_attention": ([_P, _P, _I, _P, _P, _I, _I, _I, _I, _P], _I),
     "minfer_op_rope_store": ([_P, _P, _P, _I, _I, _I, _I, _F, _I, _P, _P, _P], _I),
+    "minfer_op_qknorm_rope_store": ([_P, _P, _P, _P, _F, _P, _I, _I, _I, _I, _F, _I, _P, _P, _P], _I),
     "minfer_strerror": ([_I], ctypes.c_char_p),
     "minfer_device_status": ([_P], _I),
 }
@@ -106,7 +107,8 @@ def check(rc: int, what: str = "minfer"):
 
 def hparams_of(cfg) -> Hparams:
     return Hparams(cfg.n_layer, cfg.n_embd, cfg.n_head, cfg.n_head_kv, cfg.head_dim, cfg.n_ff,
-                   cfg.n_vocab, cfg.max_seq_len, cfg.rope_theta, cfg.rms_eps, int(cfg.tied))
+                   cfg.n_vocab, cfg.max_seq_len, cfg.rope_theta, cfg.rms_eps, int(cfg.tied),
+                   int(getattr(cfg, "qk_norm", False)))
 
 
 class Model:
@@ -315,6 +317,18 @@ def op_attention(q, pos, K, V, nh: int, nkv: int, hd: int):
     check(lib().minfer_op_attention(_ptr(q), _ptr(pos), q.shape[0], _ptr(K), _ptr(V), K.shape[0],
                                     nh, nkv, hd, _ptr(o)), "op_attention")
     return o
+
+
+def op_qknorm_rope_store(qkv, bias, qnorm, knorm, eps: float, pos, nh: int, nkv: int, hd: int,
+                         theta: float, K, V):
+    """RoPE/store with the Qwen3 per-head Q/K RMSNorm first (bias may be None)."""
+    import torch
+    nt = qkv.shape[0]
+    q_out = torch.zeros((nt, nh * hd), dtype=torch.float32, device=qkv.device)
+    check(lib().minfer_op_qknorm_rope_store(_ptr(qkv), _ptr(bias), _ptr(qnorm), _ptr(knorm), eps,
+                                            _ptr(pos), nt, nh, nkv, hd, theta, K.shape[0],
+                                            _ptr(q_out), _ptr(K), _ptr(V)), "op_qknorm_rope_store")
+    return q_out
 
 
 def op_rope_store(qkv, bias, pos, nh: int, nkv: int, hd: int, theta: float, K, V):

@@ -261,6 +261,86 @@ __global__ void rope_store_kernel(const RopeStoreArgs a) {
   }
 }
 
+// Qwen3: the same with the per-head QK RMSNorm between the bias and RoPE
+// ("05 · Graph build", section 3.2, FusedQkvNorm).  One CTA per token: the
+// Q and K sums go to shared memory, one warp per head takes the mean of
+// squares in double (the scale is rounded to f32 once, as in every RMSNorm
+// here), then the pairs are normalized, weighted and rotated.
+constexpr int kMaxQkHeads = 128;
+
+__global__ void rope_store_qknorm_kernel(const RopeStoreArgs a) {
+  extern __shared__ float xs[];  // [(nh + nkv) * hd]
+  __shared__ float rs[kMaxQkHeads];
+  pdl_trigger();
+  pdl_wait();
+  const int t = blockIdx.x;
+  const int p_in = a.pos[t];
+  const bool write_kv =
+      ((a.status == nullptr) || (*a.status == 0)) && p_in >= 0 && p_in < a.n_ctx;
+  const int p = (p_in >= 0 && p_in < a.n_ctx) ? p_in : 0;
+  const int half = a.hd >> 1;
+  const int hshift = half == 64 ? 6 : 5;  // head_dim is 64 or 128
+  const int nheads = a.nh + a.nkv;
+  const int nqk = nheads * a.hd;
+  const int W = nqk + a.nkv * a.hd;
+  const int64_t row = (int64_t)t * W;
+  const int kw = a.nkv * a.hd;
+  for (int e = threadIdx.x; e < W; e += blockDim.x) {
+    float v = a.partials[row + e];
+    for (int s = 1; s < a.nsplit; ++s) v = __fadd_rn(v, a.partials[s * a.split_stride + row + e]);
+    if (a.bias) v = __fadd_rn(v, a.bias[e]);
+    if (e < nqk) {
+      xs[e] = v;
+    } else if (write_kv) {
+      const int64_t o0 = (int64_t)p * kw + (e - nqk);
+      a.vreg[o0] = v;
+      const __half vh = __float2half_rn(v);
+      a.shadow[2][o0] = vh;
+      a.shadow[3][o0] = __float2half_rn(__fsub_rn(v, __half2float(vh)));
+    }
+  }
+  __syncthreads();
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, nwarps = blockDim.x >> 5;
+  for (int hh = warp; hh < nheads; hh += nwarps) {
+    double ss = 0.0;
+    for (int i = lane; i < a.hd; i += 32) {
+      const double x = (double)xs[hh * a.hd + i];
+      ss += x * x;
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
+    if (lane == 0) rs[hh] = (float)(1.0 / sqrt(ss / (double)a.hd + (double)a.eps));
+  }
+  __syncthreads();
+  const float* cs = a.cos_t + (int64_t)p * half;
+  const float* sn = a.sin_t + (int64_t)p * half;
+  for (int pi = threadIdx.x; pi < nheads * half; pi += blockDim.x) {
+    const int head = pi >> hshift, i = pi & (half - 1);
+    const int e0 = head * a.hd + i;
+    const float r = rs[head];
+    const float* w = head < a.nh ? a.q_norm : a.k_norm;
+    const float x0 = __fmul_rn(__fmul_rn(xs[e0], r), w[i]);
+    const float x1 = __fmul_rn(__fmul_rn(xs[e0 + half], r), w[i + half]);
+    const float c = cs[i], sv = sn[i];
+    const float v0 = __fsub_rn(__fmul_rn(x0, c), __fmul_rn(x1, sv));
+    const float v1 = __fadd_rn(__fmul_rn(x0, sv), __fmul_rn(x1, c));
+    if (head < a.nh) {
+      a.q_out[(int64_t)t * a.nh * a.hd + e0] = v0;
+      a.q_out[(int64_t)t * a.nh * a.hd + e0 + half] = v1;
+    } else if (write_kv) {
+      const int ke = (head - a.nh) * a.hd + i;
+      const int64_t o0 = (int64_t)p * kw + ke;
+      a.kreg[o0] = v0;
+      a.kreg[o0 + half] = v1;
+      const __half h0 = __float2half_rn(v0), h1 = __float2half_rn(v1);
+      a.shadow[0][o0] = h0;
+      a.shadow[0][o0 + half] = h1;
+      a.shadow[1][o0] = __float2half_rn(__fsub_rn(v0, __half2float(h0)));
+      a.shadow[1][o0 + half] = __float2half_rn(__fsub_rn(v1, __half2float(h1)));
+    }
+  }
+}
+
 // ---------------------------------------------------------------- one-row GEMV
 // One warp per output row.  Lane l reads 16 code bytes of each 512-byte chunk
 // (half of a Q8_0 block); dp4a gives the integer partial, the lane pair adds
@@ -426,6 +506,13 @@ cudaError_t validate_launch(const int32_t* ids, const int32_t* pos, int nt, int 
 
 cudaError_t rope_store_launch(const RopeStoreArgs& a, cudaStream_t st) {
   if (a.nt <= 0) return cudaSuccess;
+  if (a.q_norm || a.k_norm) {
+    const int nheads = a.nh + a.nkv;
+    if (!a.q_norm || !a.k_norm || nheads > kMaxQkHeads) return cudaErrorInvalidValue;
+    const size_t smem = (size_t)nheads * a.hd * sizeof(float);
+    if (smem > 48 * 1024) return cudaErrorInvalidValue;
+    return launch_pdl(rope_store_qknorm_kernel, a.nt, 256, smem, st, a);
+  }
   return launch_pdl(rope_store_kernel, a.nt, 256, 0, st, a);
 }
 

@@ -137,6 +137,10 @@ struct RopeStoreArgs {
   float* vreg = nullptr;
   __half* shadow[4] = {nullptr, nullptr, nullptr, nullptr};  // fp16 hi/lo copies of K, V
   const int* status = nullptr;  // skip all writes to the regions when *status != 0
+  // Qwen3 QK-norm (null: none): per-head RMSNorm weights [hd] of Q and of K
+  const float* q_norm = nullptr;
+  const float* k_norm = nullptr;
+  float eps = 0.f;
 };
 cudaError_t rope_store_launch(const RopeStoreArgs& a, cudaStream_t stream);
 

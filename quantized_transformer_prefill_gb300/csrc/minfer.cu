@@ -137,7 +137,8 @@ struct GemvW {
 struct Layer {
   float* attn_norm = nullptr;
   float* ffn_norm = nullptr;
-  float* bqkv = nullptr;
+  float* bqkv = nullptr;                              // zero when the model has no biases
+  float* q_norm = nullptr, *k_norm = nullptr;  // Qwen3 QK-norm weights [hd]
   GemmW wqkv, wo, wgu, wd;  // wo/wgu/wd unused on the last layer
   GemvW wo_v, wgu_v, wd_v;  // last layer only
 };
@@ -364,6 +365,9 @@ int model_alloc(minfer_model* m) {
     if ((rc = dalloc(&L.attn_norm, m->H)) || (rc = dalloc(&L.ffn_norm, m->H)) ||
         (rc = dalloc(&L.bqkv, m->qkvN)))
       return rc;
+    if (hp.qk_norm &&
+        ((rc = dalloc(&L.q_norm, hp.head_dim)) || (rc = dalloc(&L.k_norm, hp.head_dim))))
+      return rc;
     if ((rc = L.wqkv.alloc(m->qkvN, m->nbH))) return rc;
     if (!last) {
       if ((rc = L.wo.alloc(m->H, m->nbq)) || (rc = L.wgu.alloc(2 * m->Fp, m->nbH)) ||
@@ -391,7 +395,7 @@ void model_release(minfer_model* m) {
   m->output.release();
   dfree(m->out_norm);
   for (auto& L : m->layers) {
-    dfree(L.attn_norm); dfree(L.ffn_norm); dfree(L.bqkv);
+    dfree(L.attn_norm); dfree(L.ffn_norm); dfree(L.bqkv); dfree(L.q_norm); dfree(L.k_norm);
     L.wqkv.release(); L.wo.release(); L.wgu.release(); L.wd.release();
     L.wo_v.release(); L.wgu_v.release(); L.wd_v.release();
   }
@@ -434,6 +438,9 @@ int set_tensor(minfer_model* m, const minfer_tensor* t) {
     } else if (k == "ffn_norm.weight") {
       if (!vec_ok(m->H)) return MINFER_ERR_SHAPE;
       rc = upload_vec(m, L.ffn_norm, t);
+    } else if (hp.qk_norm && (k == "attn_q_norm.weight" || k == "attn_k_norm.weight")) {
+      if (!vec_ok(hp.head_dim)) return MINFER_ERR_SHAPE;
+      rc = upload_vec(m, k == "attn_q_norm.weight" ? L.q_norm : L.k_norm, t);
     } else if (k == "attn_q.bias" || k == "attn_k.bias" || k == "attn_v.bias") {
       const int64_t n = k == "attn_q.bias" ? m->q : m->kvw;
       const int64_t off = k == "attn_q.bias" ? 0 : (k == "attn_k.bias" ? m->q : m->q + m->kvw);
@@ -471,11 +478,20 @@ int set_tensor(minfer_model* m, const minfer_tensor* t) {
 std::vector<std::string> required_names(const minfer_hparams& hp) {
   std::vector<std::string> v = {"token_embd.weight", "output_norm.weight"};
   if (!hp.tied_embeddings) v.push_back("output.weight");
-  const char* kinds[] = {"attn_norm.weight", "attn_q.weight", "attn_q.bias", "attn_k.weight",
-                         "attn_k.bias", "attn_v.weight", "attn_v.bias", "attn_output.weight",
-                         "ffn_norm.weight", "ffn_gate.weight", "ffn_up.weight", "ffn_down.weight"};
-  for (int l = 0; l < hp.n_layer; ++l)
-    for (const char* k : kinds) v.push_back("blk." + std::to_string(l) + "." + k);
+  const char* kinds[] = {"attn_norm.weight", "attn_q.weight", "attn_k.weight", "attn_v.weight",
+                         "attn_output.weight", "ffn_norm.weight", "ffn_gate.weight",
+                         "ffn_up.weight", "ffn_down.weight"};
+  // Qwen2: Q/K/V biases; Qwen3: the QK-norm weights (biases optional)
+  const char* qwen2[] = {"attn_q.bias", "attn_k.bias", "attn_v.bias"};
+  const char* qwen3[] = {"attn_q_norm.weight", "attn_k_norm.weight"};
+  for (int l = 0; l < hp.n_layer; ++l) {
+    const std::string b = "blk." + std::to_string(l) + ".";
+    for (const char* k : kinds) v.push_back(b + k);
+    if (hp.qk_norm)
+      for (const char* k : qwen3) v.push_back(b + k);
+    else
+      for (const char* k : qwen2) v.push_back(b + k);
+  }
   return v;
 }
 
@@ -704,6 +720,11 @@ int enqueue_forward(minfer_model* m, minfer_kv* kv, const int32_t* ids, const in
       r.vreg = kv->v(l);
       for (int i = 0; i < 4; ++i) r.shadow[i] = kv->plane(l, i);
       r.status = m->d_status;
+      if (hp.qk_norm) {
+        r.q_norm = Ly.q_norm;
+        r.k_norm = Ly.k_norm;
+        r.eps = hp.rms_eps;
+      }
       LAUNCH(kKRope, rope_store_launch(r, st));
     }
     if (cap) {
@@ -1430,7 +1451,16 @@ int minfer_op_attention(const float* d_q, const int32_t* d_pos, int nt, const fl
 int minfer_op_rope_store(const float* d_qkv, const float* d_bias, const int32_t* d_pos, int nt,
                          int n_head, int n_head_kv, int head_dim, float theta, int n_ctx,
                          float* d_q_out, float* d_k, float* d_v) {
+  return minfer_op_qknorm_rope_store(d_qkv, d_bias, nullptr, nullptr, 0.f, d_pos, nt, n_head,
+                                     n_head_kv, head_dim, theta, n_ctx, d_q_out, d_k, d_v);
+}
+
+int minfer_op_qknorm_rope_store(const float* d_qkv, const float* d_bias, const float* d_qnorm,
+                                const float* d_knorm, float eps, const int32_t* d_pos, int nt,
+                                int n_head, int n_head_kv, int head_dim, float theta, int n_ctx,
+                                float* d_q_out, float* d_k, float* d_v) {
   if (!d_qkv || !d_pos || !d_q_out || !d_k || !d_v || nt <= 0 || n_ctx <= 0) return MINFER_ERR_ARG;
+  if ((d_qnorm == nullptr) != (d_knorm == nullptr)) return MINFER_ERR_ARG;
   std::vector<float> c, s;
   rope_tables(n_ctx, head_dim, theta, c, s);
   float *dc = nullptr, *ds = nullptr;
@@ -1454,6 +1484,9 @@ int minfer_op_rope_store(const float* d_qkv, const float* d_bias, const int32_t*
   a.q_out = d_q_out;
   a.kreg = d_k;
   a.vreg = d_v;
+  a.q_norm = d_qnorm;
+  a.k_norm = d_knorm;
+  a.eps = eps;
   __half* sh = nullptr;
   const int64_t kvw = (int64_t)n_head_kv * head_dim;
   if (!rc) rc = dalloc(&sh, (size_t)4 * n_ctx * kvw);

@@ -65,8 +65,11 @@ class LayerWeights:
         self.q8 = {}
         for kind in ("attn_norm.weight", "attn_q.weight", "attn_q.bias", "attn_k.weight",
                      "attn_k.bias", "attn_v.weight", "attn_v.bias", "attn_output.weight",
-                     "ffn_norm.weight", "ffn_gate.weight", "ffn_up.weight", "ffn_down.weight"):
-            spec = specs[f"blk.{layer}.{kind}"]
+                     "ffn_norm.weight", "ffn_gate.weight", "ffn_up.weight", "ffn_down.weight",
+                     "attn_q_norm.weight", "attn_k_norm.weight"):
+            spec = specs.get(f"blk.{layer}.{kind}")
+            if spec is None:  # a bias of a QK-norm model, or QK-norm of a plain one
+                continue
             arr = synth.tensor_data(spec)
             if spec.is_matrix:
                 self.q8[kind] = oracle_mod.q8_quantize(arr)
@@ -74,7 +77,25 @@ class LayerWeights:
                 self.f32[kind] = arr
         q, k, v = (self.q8[f"attn_{x}.weight"] for x in "qkv")
         self.q8["qkv"] = (np.concatenate([q[0], k[0], v[0]]), np.concatenate([q[1], k[1], v[1]]))
-        self.bias = np.concatenate([self.f32[f"attn_{x}.bias"] for x in "qkv"])
+        nq, nkv = cfg.n_head * cfg.head_dim, cfg.n_head_kv * cfg.head_dim
+        self.bias = (np.concatenate([self.f32[f"attn_{x}.bias"] for x in "qkv"]) if cfg.qkv_bias
+                     else np.zeros(nq + 2 * nkv, np.float32))
+        self.cfg = cfg
+
+    def qk_normed(self, oracle_mod, full):
+        """Q|K|V after the bias -> Q and K heads RMS-normalized (Qwen3), V as is."""
+        cfg = self.cfg
+        if not cfg.qk_norm:
+            return full
+        hd, nq, nkv = cfg.head_dim, cfg.n_head * cfg.head_dim, cfg.n_head_kv * cfg.head_dim
+        out = full.copy()
+        rows = full.shape[0]
+        out[:, :nq] = oracle_mod.rmsnorm(full[:, :nq].reshape(-1, hd), self.f32["attn_q_norm.weight"],
+                                         cfg.rms_eps).reshape(rows, nq)
+        out[:, nq:nq + nkv] = oracle_mod.rmsnorm(full[:, nq:nq + nkv].reshape(-1, hd),
+                                                 self.f32["attn_k_norm.weight"],
+                                                 cfg.rms_eps).reshape(rows, nkv)
+        return out
 
 
 def _sample_rows(nt, k, seed):
@@ -129,7 +150,7 @@ def _check_layer(oracle_mod, g, kv, cfg, layer, pos, rows):
 
     qkv = _f32(g, "qkv", nt, q + 2 * kvw)[rows]
     _check_sum(oracle_mod, qkv, xq, xd, *Wt.q8["qkv"], H)
-    full = (qkv + Wt.bias).astype(np.float32)
+    full = Wt.qk_normed(oracle_mod, (qkv + Wt.bias).astype(np.float32))
     cos_t, sin_t = oracle_mod.rope_table(int(pos.max()) + 1, hd, cfg.rope_theta)
     want_q = oracle_mod.rope(full[:, :q], p, nh, hd, cos_t, sin_t)
     want_k = oracle_mod.rope(full[:, q:q + kvw], p, nkv, hd, cos_t, sin_t)
@@ -195,7 +216,7 @@ def _check_last_layer(oracle_mod, g, kv, cfg, pos, rows, logits):
     assert np.array_equal(xd, od) and np.array_equal(xq, oq)
     qkv = _f32(g, "qkv", nt, q + 2 * kvw)[rows]
     _check_sum(oracle_mod, qkv, xq, xd, *Wt.q8["qkv"], H)
-    full = (qkv + Wt.bias).astype(np.float32)
+    full = Wt.qk_normed(oracle_mod, (qkv + Wt.bias).astype(np.float32))
     cos_t, sin_t = oracle_mod.rope_table(int(pos.max()) + 1, hd, cfg.rope_theta)
     want_k = oracle_mod.rope(full[:, q:q + kvw], p, nkv, hd, cos_t, sin_t)
     assert np.array_equal(_kv_rows(kv, L, 0, p), want_k)
@@ -267,3 +288,9 @@ def test_qwen2_1_5b_append_1024(qp, oracle_mod):
 
 def test_qwen2_7b_4096(qp, oracle_mod):
     _run(qp, oracle_mod, synth.WORKLOADS["qwen2-7b-4096"], 20, 32, 3)
+
+
+def test_qwen3_0_6b_512(qp, oracle_mod):
+    """The Qwen3 variant: per-head QK RMSNorm before RoPE, no Q/K/V bias,
+    16 query / 8 KV heads of 128."""
+    _run(qp, oracle_mod, synth.WORKLOADS["qwen3-0.6b-512"], 9, 40, 4)

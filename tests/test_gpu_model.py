@@ -60,6 +60,22 @@ def test_tiny_prefill_matches_oracle(tiny_pair):
             assert not np.any(a[w.n_tokens:])
 
 
+def test_qwen3_tiny_prefill_matches_oracle(qp, oracle_mod):
+    """The Qwen3 variant (per-head QK RMSNorm, no bias) at the strict bar."""
+    cfg = synth.QWEN3_TINY
+    g, o = gpu_model(cfg), oracle_model(cfg)
+    w = synth.WORKLOADS["qwen3-tiny-32"]
+    lg, lo, dump, ho, kv_g, kv_o = _run_both(cfg, g, o, w.ids(), w.positions(), w.n_ctx)
+    check_logits(lg, lo)
+    _check_hidden(cfg, dump, ho, w.n_tokens)
+    # layer 0's K/V come from the exact embedding; later layers' from a hidden
+    # state held to the 1e-3 bar
+    for layer in range(cfg.n_layer):
+        for which in (0, 1):
+            got = rel_l2(kv_g.read(layer, which), kv_o.read(layer, which))
+            assert got <= (1e-5 if layer == 0 else 1e-3), (layer, which, got)
+
+
 def test_written_slots_and_canaries(tiny_pair):
     cfg, g, o = tiny_pair
     kv = g.kv(64)

@@ -155,3 +155,27 @@ def test_rope_store_vs_oracle(qp, oracle_mod):
     want_v[pos] = full[:, (nh + nkv) * hd:]
     assert np.array_equal(Kh, want_k)
     assert np.array_equal(Vh, want_v)
+
+
+@pytest.mark.parametrize("nh,nkv,hd", [(4, 2, 64), (16, 8, 128)])
+def test_qknorm_rope_store_vs_oracle(qp, oracle_mod, nh, nkv, hd):
+    """Qwen3: per-head RMSNorm of Q and K between the bias and RoPE, bit-exact
+    against the oracle's rmsnorm and rope on the same sums."""
+    nt, n_ctx, theta, eps = 37, 80, 1.0e6, 1e-6
+    rng = np.random.default_rng(nh + hd)
+    W = (nh + 2 * nkv) * hd
+    qkv = (rng.normal(0, 1, (nt, W)) * np.exp(rng.uniform(-3, 3, (nt, 1)))).astype(np.float32)
+    qn = (1 + rng.normal(0, 0.01, hd)).astype(np.float32)
+    kn = (1 + rng.normal(0, 0.01, hd)).astype(np.float32)
+    pos = rng.permutation(n_ctx)[:nt].astype(np.int32)
+    Kd = _dev(np.zeros((n_ctx, nkv * hd), np.float32))
+    Vd = _dev(np.zeros((n_ctx, nkv * hd), np.float32))
+    q_out = qp.op_qknorm_rope_store(_dev(qkv), None, _dev(qn), _dev(kn), eps, _dev(pos), nh, nkv,
+                                    hd, theta, Kd, Vd)
+    c, s = oracle_mod.rope_table(n_ctx, hd, theta)
+    qh = oracle_mod.rmsnorm(qkv[:, :nh * hd].reshape(-1, hd), qn, eps).reshape(nt, nh * hd)
+    kh = oracle_mod.rmsnorm(qkv[:, nh * hd:(nh + nkv) * hd].reshape(-1, hd), kn, eps).reshape(nt, -1)
+    assert np.array_equal(q_out.cpu().numpy(), oracle_mod.rope(qh, pos, nh, hd, c, s))
+    Kh, Vh = Kd.cpu().numpy(), Vd.cpu().numpy()
+    assert np.array_equal(Kh[pos], oracle_mod.rope(kh, pos, nkv, hd, c, s))
+    assert np.array_equal(Vh[pos], qkv[:, (nh + nkv) * hd:])
