@@ -6,9 +6,10 @@
 //     o[t, h] = sum_{j <= pos[t]} softmax_j(q[t,h] . K[j, g] / sqrt(hd)) V[j, g],
 //     g = h / (n_head / n_head_kv)
 //
-// Design.  One CTA per (16 query rows, KV head g, key split): warp w serves
-// query head g * G + w, so the G heads that share a KV head share every K/V
-// tile in shared memory.  K/V tiles come from fp16 hi/lo shadow planes of the
+// Design.  One CTA per (16 * R query rows, KV head g, key split): warp w
+// serves 16 of the rows for query head g * G + (w % G), so the G heads that
+// share a KV head, and R row tiles (R = 8 / G when a group is small), share
+// every K/V tile in shared memory.  K/V tiles come from fp16 hi/lo shadow planes of the
 // f32 regions (written next to the regions by the RoPE/store kernel), staged
 // with double-buffered cp.async.  Scores and P.V run on the tensor cores
 // (mma.sync m16n8k16, fp16 operands, f32 accumulate) with every f32 operand
@@ -131,9 +132,15 @@ __global__ void __launch_bounds__(256) attn_kernel(const AttnArgs a, const AttnO
   const int tile = (int)gridDim.x - 1 - (int)blockIdx.x;  // longest rows first
   const int g = blockIdx.y;
   const int split = (int)cluster_rank();
-  const int rbase = a.r0 + tile * kTileQ;
+  // R row tiles of 16 per CTA when a KV group has few heads (R * G <= 8
+  // warps share every K/V tile); warp = (row tile tl, head hg of the group)
+  const int nw = (int)(blockDim.x >> 5);
+  const int R = nw / G;
+  const int rbase = a.r0 + tile * kTileQ * R;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int h = g * G + warp;
+  const int tl = warp / G, hg = warp - tl * G;
+  const int h = g * G + hg;
+  const int wbase = rbase + tl * kTileQ;  // this warp's 16 rows
   const int qr = lane >> 2, qc = (lane & 3) * 2;
   const int64_t qw = (int64_t)a.nh * HD;
   const int64_t kw = (int64_t)a.nkv * HD;
@@ -145,7 +152,7 @@ __global__ void __launch_bounds__(256) attn_kernel(const AttnArgs a, const AttnO
   };
   if (threadIdx.x == 0) s_maxp = -1;
   __syncthreads();
-  if (threadIdx.x < kTileQ) atomicMax(&s_maxp, clamp_pos(rbase + threadIdx.x));
+  if (threadIdx.x < kTileQ * R) atomicMax(&s_maxp, clamp_pos(rbase + threadIdx.x));
   __syncthreads();
   // this split's share of the keys 0..max position of the tile's rows
   const int nkeys = s_maxp + 1;
@@ -155,7 +162,7 @@ __global__ void __launch_bounds__(256) attn_kernel(const AttnArgs a, const AttnO
   const int kend = min(nkeys, kbeg + share);
   const int ntile = kend > kbeg ? (kend - kbeg + kTileKV - 1) / kTileKV : 0;
 
-  const int ra = rbase + qr, rb = rbase + qr + 8;
+  const int ra = wbase + qr, rb = wbase + qr + 8;
   const int pa = clamp_pos(ra), pb = clamp_pos(rb);
 
   // stage loader: 32 keys x HD of Kh, Kl, Vh, Vl in 16-byte chunks
@@ -313,7 +320,7 @@ __global__ void __launch_bounds__(256) attn_kernel(const AttnArgs a, const AttnO
   const int nblk = HD / 32;
   const int q = a.nh * HD;
   const int nb = q / 32;
-  const int r_a = rbase + qr, r_b = rbase + qr + 8;
+  const int r_a = wbase + qr, r_b = wbase + qr + 8;
   // Normalized values of this thread's 8 + 8 elements of 32-block bq (rows
   // r_a, r_b; dims bq*32 + i*8 + qc + {0,1}) -> f32 (debug), Q8_0 codes and
   // the block scale.  The four lanes of a row hold the whole block.
@@ -384,17 +391,17 @@ __global__ void __launch_bounds__(256) attn_kernel(const AttnArgs a, const AttnO
   // free once every warp has left the key loop)
   __syncthreads();
   float* po = reinterpret_cast<float*>(smem_h);  // [16][G][HD]
-  float* pml = po + kTileQ * G * HD;             // [16][G][2]
+  float* pml = po + kTileQ * nw * HD;            // [16][warps][2]
 #pragma unroll
   for (int nd = 0; nd < HD / 8; ++nd) {
-    *reinterpret_cast<float2*>(po + ((qr * G) + warp) * HD + nd * 8 + qc) =
+    *reinterpret_cast<float2*>(po + ((qr * nw) + warp) * HD + nd * 8 + qc) =
         make_float2(o[nd][0], o[nd][1]);
-    *reinterpret_cast<float2*>(po + (((qr + 8) * G) + warp) * HD + nd * 8 + qc) =
+    *reinterpret_cast<float2*>(po + (((qr + 8) * nw) + warp) * HD + nd * 8 + qc) =
         make_float2(o[nd][2], o[nd][3]);
   }
   if ((lane & 3) == 0) {
-    *reinterpret_cast<float2*>(pml + (qr * G + warp) * 2) = make_float2(m_a, l_a);
-    *reinterpret_cast<float2*>(pml + ((qr + 8) * G + warp) * 2) = make_float2(m_b, l_b);
+    *reinterpret_cast<float2*>(pml + (qr * nw + warp) * 2) = make_float2(m_a, l_a);
+    *reinterpret_cast<float2*>(pml + ((qr + 8) * nw + warp) * 2) = make_float2(m_b, l_b);
   }
   cluster_sync_all();
 
@@ -402,8 +409,8 @@ __global__ void __launch_bounds__(256) attn_kernel(const AttnArgs a, const AttnO
   // cluster; the warp of that head merges its 16 rows from every CTA's
   // partials (distributed shared memory) at its own fragment positions
   const uint32_t po_s = smem_u32(po), pml_s = smem_u32(pml);
-  const uint32_t mla_off = (uint32_t)((qr * G + warp) * 2 * 4);
-  const uint32_t mlb_off = (uint32_t)(((qr + 8) * G + warp) * 2 * 4);
+  const uint32_t mla_off = (uint32_t)((qr * nw + warp) * 2 * 4);
+  const uint32_t mlb_off = (uint32_t)(((qr + 8) * nw + warp) * 2 * 4);
   for (int bq = 0; bq < nblk; ++bq) {
     if ((warp * nblk + bq) % ns != split) continue;  // warp-uniform
     float2 mla[kMaxSplits], mlb[kMaxSplits];
@@ -431,8 +438,8 @@ __global__ void __launch_bounds__(256) attn_kernel(const AttnArgs a, const AttnO
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
           const int dim = bq * 32 + i * 8 + qc;
-          const float2 xa = ld_peer2(peer_addr(po_s + (uint32_t)(((qr * G + warp) * HD + dim) * 4), (uint32_t)sidx));
-          const float2 xb = ld_peer2(peer_addr(po_s + (uint32_t)((((qr + 8) * G + warp) * HD + dim) * 4), (uint32_t)sidx));
+          const float2 xa = ld_peer2(peer_addr(po_s + (uint32_t)(((qr * nw + warp) * HD + dim) * 4), (uint32_t)sidx));
+          const float2 xb = ld_peer2(peer_addr(po_s + (uint32_t)((((qr + 8) * nw + warp) * HD + dim) * 4), (uint32_t)sidx));
           va[2 * i] = fmaf(xa.x, wa, va[2 * i]);
           va[2 * i + 1] = fmaf(xa.y, wa, va[2 * i + 1]);
           vb[2 * i] = fmaf(xb.x, wb, vb[2 * i]);
@@ -469,8 +476,13 @@ __global__ void kv_shadow_kernel(const float* __restrict__ k, const float* __res
 
 }  // namespace
 
-int attention_nsplit(int rows, int nkv, int num_sms) {
-  const int ctas = (rows + kTileQ - 1) / kTileQ * nkv;
+// 16-row tiles per CTA: enough to give the CTA 8 warps when a KV group has
+// few query heads.
+int attn_row_tiles(int G) { return G >= 8 ? 1 : 8 / G; }
+
+int attention_nsplit(int rows, int nkv, int num_sms, int G) {
+  const int rtiles = attn_row_tiles(G);
+  const int ctas = (rows + kTileQ * rtiles - 1) / (kTileQ * rtiles) * nkv;
   if (ctas >= num_sms) return 1;
   int ns = (2 * num_sms + ctas - 1) / std::max(ctas, 1);
   return ns < 1 ? 1 : (ns > kMaxSplits ? kMaxSplits : ns);
@@ -487,8 +499,9 @@ cudaError_t launch_attn(const AttnArgs& a, const AttnOut& out, int rows, cudaStr
   }
   const int G = a.nh / a.nkv;
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3((rows + kTileQ - 1) / kTileQ, a.nkv, a.nsplit);
-  cfg.blockDim = dim3(32 * G);
+  const int R = attn_row_tiles(G);
+  cfg.gridDim = dim3((rows + kTileQ * R - 1) / (kTileQ * R), a.nkv, a.nsplit);
+  cfg.blockDim = dim3(32 * G * R);
   cfg.dynamicSmemBytes = Tile<HD>::BYTES;
   cfg.stream = st;
   cudaLaunchAttribute attr[2];

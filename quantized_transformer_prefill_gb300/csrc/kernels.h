@@ -170,7 +170,7 @@ struct AttnOut {
   float* f32 = nullptr;
 };
 // Key splits for `rows` query rows: enough CTAs to fill the GPU about twice.
-int attention_nsplit(int rows, int nkv, int num_sms);
+int attention_nsplit(int rows, int nkv, int num_sms, int G);
 cudaError_t attention_launch(const AttnArgs& a, const AttnOut& out, cudaStream_t stream);
 // f32 K/V values -> fp16 hi/lo planes (planes[0..3] = K hi, K lo, V hi, V lo).
 cudaError_t kv_shadow_launch(const float* k, const float* v, int64_t count, __half* const* planes,

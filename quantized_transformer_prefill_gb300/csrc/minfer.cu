@@ -749,7 +749,7 @@ int enqueue_forward(minfer_model* m, minfer_kv* kv, const int32_t* ids, const in
     at.nkv = hp.n_head_kv;
     at.hd = hp.head_dim;
     at.n_ctx = kv->n_ctx;
-    at.nsplit = attention_nsplit(at.r1 - at.r0, at.nkv, m->num_sms);
+    at.nsplit = attention_nsplit(at.r1 - at.r0, at.nkv, m->num_sms, at.nh / at.nkv);
     AttnOut ao;
     ao.f32 = (m->debug_f32 || cap_all) ? w.att : nullptr;
     if (!last) {
@@ -1416,7 +1416,7 @@ int minfer_op_attention(const float* d_q, const int32_t* d_pos, int nt, const fl
   a.nkv = n_head_kv;
   a.hd = head_dim;
   a.n_ctx = n_ctx;
-  a.nsplit = attention_nsplit(nt, n_head_kv, num_sms);
+  a.nsplit = attention_nsplit(nt, n_head_kv, num_sms, n_head / n_head_kv);
   __half* sh = nullptr;
   float* s16 = nullptr;
   __half* q16 = nullptr;
