@@ -194,6 +194,10 @@ int minfer_debug_read(minfer_model* m, const char* buffer, void* host, int64_t b
  *                             f32 [q/32][ntp]); "att" its f32 values [nt][q]
  *   "s_codes", "s_scales"     Q8_0 of the SwiGLU output (fp16 [nt][ceil(n_ff/32)*32],
  *                             f32 [ceil(n_ff/32)][ntp])
+ * A single-token call (one-row GEMV path) captures instead, one row each:
+ * "h_in", "h_mid", "h_out", "qkv", "qrot", "att" (f32) and the Q8_0 inputs
+ * of its GEMVs as int8 codes + f32 scales: "x_q8"/"x_s8" (attn_norm),
+ * "att_q8"/"att_s8", "f_q8"/"f_s8" (ffn_norm), "s_q8"/"s_s8" (SwiGLU).
  * Returns MINFER_ERR_ARG for a layer out of range; a failed capture
  * allocation fails the prefill call with MINFER_ERR_CUDA. */
 int minfer_debug_layer(minfer_model* m, int layer);

@@ -140,7 +140,9 @@ struct Layer {
   float* bqkv = nullptr;                              // zero when the model has no biases
   float* q_norm = nullptr, *k_norm = nullptr;  // Qwen3 QK-norm weights [hd]
   GemmW wqkv, wo, wgu, wd;  // wo/wgu/wd unused on the last layer
-  GemvW wo_v, wgu_v, wd_v;  // last layer only
+  // one-row (GEMV) layout of every matrix: the last layer's tail and
+  // single-token calls (decode-shaped prefill)
+  GemvW wqkv_v, wo_v, wgu_v, wd_v;
 };
 
 // Activation buffers for up to max_nt rows.
@@ -373,11 +375,10 @@ int model_alloc(minfer_model* m) {
       if ((rc = L.wo.alloc(m->H, m->nbq)) || (rc = L.wgu.alloc(2 * m->Fp, m->nbH)) ||
           (rc = L.wd.alloc(m->H, m->nbF)))
         return rc;
-    } else {
-      if ((rc = L.wo_v.alloc(m->H, m->nbq)) || (rc = L.wgu_v.alloc(2 * m->F, m->nbH)) ||
-          (rc = L.wd_v.alloc(m->H, m->nbF)))
-        return rc;
     }
+    if ((rc = L.wqkv_v.alloc(m->qkvN, m->nbH)) || (rc = L.wo_v.alloc(m->H, m->nbq)) ||
+        (rc = L.wgu_v.alloc(2 * m->F, m->nbH)) || (rc = L.wd_v.alloc(m->H, m->nbF)))
+      return rc;
   }
   if ((rc = dalloc(&m->d_status, 4))) return rc;
   CK(cudaMallocHost(&m->h_status, 4 * sizeof(int)));
@@ -397,7 +398,7 @@ void model_release(minfer_model* m) {
   for (auto& L : m->layers) {
     dfree(L.attn_norm); dfree(L.ffn_norm); dfree(L.bqkv); dfree(L.q_norm); dfree(L.k_norm);
     L.wqkv.release(); L.wo.release(); L.wgu.release(); L.wd.release();
-    L.wo_v.release(); L.wgu_v.release(); L.wd_v.release();
+    L.wqkv_v.release(); L.wo_v.release(); L.wgu_v.release(); L.wd_v.release();
   }
   m->ws.release();
   dfree(m->d_status);
@@ -450,21 +451,25 @@ int set_tensor(minfer_model* m, const minfer_tensor* t) {
       const int64_t n = k == "attn_q.weight" ? m->q : m->kvw;
       const int64_t off = k == "attn_q.weight" ? 0 : (k == "attn_k.weight" ? m->q : m->q + m->kvw);
       if (!mat_ok(m->H, n)) return MINFER_ERR_SHAPE;
-      if ((rc = stage_matrix(m, t)) || (rc = to_gemm(m, n, m->nbH, L.wqkv, off, 0, 0))) return rc;
+      if ((rc = stage_matrix(m, t)) || (rc = to_gemm(m, n, m->nbH, L.wqkv, off, 0, 0)) ||
+          (rc = to_gemv(m, n, m->nbH, L.wqkv_v, off)))
+        return rc;
     } else if (k == "attn_output.weight") {
       if (!mat_ok(m->q, m->H)) return MINFER_ERR_SHAPE;
       if ((rc = stage_matrix(m, t))) return rc;
-      rc = last ? to_gemv(m, m->H, m->nbq, L.wo_v, 0) : to_gemm(m, m->H, m->nbq, L.wo, 0, 0, 0);
+      if (!last && (rc = to_gemm(m, m->H, m->nbq, L.wo, 0, 0, 0))) return rc;
+      rc = to_gemv(m, m->H, m->nbq, L.wo_v, 0);
     } else if (k == "ffn_gate.weight" || k == "ffn_up.weight") {
       const int which = k == "ffn_gate.weight" ? 0 : 1;
       if (!mat_ok(m->H, m->F)) return MINFER_ERR_SHAPE;
       if ((rc = stage_matrix(m, t))) return rc;
-      rc = last ? to_gemv(m, m->F, m->nbH, L.wgu_v, which * m->F)
-                : to_gemm(m, m->F, m->nbH, L.wgu, 0, 1, which);
+      if (!last && (rc = to_gemm(m, m->F, m->nbH, L.wgu, 0, 1, which))) return rc;
+      rc = to_gemv(m, m->F, m->nbH, L.wgu_v, which * m->F);
     } else if (k == "ffn_down.weight") {
       if (!mat_ok(m->F, m->H)) return MINFER_ERR_SHAPE;
       if ((rc = stage_matrix(m, t))) return rc;
-      rc = last ? to_gemv(m, m->H, m->nbF, L.wd_v, 0) : to_gemm(m, m->H, m->nbF, L.wd, 0, 0, 0);
+      if (!last && (rc = to_gemm(m, m->H, m->nbF, L.wd, 0, 0, 0))) return rc;
+      rc = to_gemv(m, m->H, m->nbF, L.wd_v, 0);
     } else {
       return MINFER_ERR_SHAPE;
     }
@@ -639,9 +644,138 @@ void dump_hidden(minfer_model* m, cudaStream_t st, int slot, const float* src, i
   cudaMemcpyAsync(dst, src, (size_t)rows * m->H * 4, cudaMemcpyDeviceToHost, st);
 }
 
+// A single-token call (the decode shape, "09 · Prefill" section 2.3 with
+// n_tokens = 1): every projection is a one-row GEMV over the int8 layout,
+// which reads each weight byte once -- the work is bound by HBM, and the
+// tensor-core GEMM would pad the one row to 128.
+int enqueue_decode(minfer_model* m, minfer_kv* kv, const int32_t* ids, const int32_t* pos,
+                   float* logits, cudaStream_t st, bool prof, bool dumps) {
+  const auto& hp = m->hp;
+  Workspace& w = m->ws;
+  Launcher L{m, st, prof};
+  auto gemv = [&](int cls, const GemvW& W, int64_t N, int nb, float* y, const float* resid,
+                  const int* status) -> int {
+    GemvArgs g;
+    g.wq = W.q;
+    g.ws = W.s;
+    g.N = N;
+    g.nb = nb;
+    g.kpad = (int64_t)nb * 32;
+    g.xq = w.t_q;
+    g.xs = w.t_s;
+    g.y = y;
+    g.resid = resid;
+    g.status = status;
+    LAUNCH(cls, gemv_launch(g, st));
+    return MINFER_OK;
+  };
+  auto norm_quant = [&](const float* norm_w) -> int {
+    RowQuantArgs r;
+    r.h = w.h;
+    r.norm_w = norm_w;
+    r.eps = hp.rms_eps;
+    r.rows = 1;
+    r.n = m->H;
+    r.q8 = w.t_q;
+    r.s8 = w.t_s;
+    LAUNCH(kKRowQuant, row_quant_launch(r, st));
+    return MINFER_OK;
+  };
+  int rc;
+  // stage capture of one layer (debug): one-row layouts, int8 codes + f32 scales
+  auto cap_q8 = [&](const char* qname, const char* sname, int nb) -> int {
+    int r;
+    if ((r = dbg_capture(m, st, qname, w.t_q, (size_t)nb * 32)) ||
+        (r = dbg_capture(m, st, sname, w.t_s, (size_t)nb * 4)))
+      return r;
+    return MINFER_OK;
+  };
+  CK(cudaMemsetAsync(m->d_status + 1, 0, sizeof(int), st));
+  LAUNCH(kKValidate, validate_launch(ids, pos, 1, (int)m->V, kv->n_ctx, kv->seen, m->d_status, st));
+  LAUNCH(kKEmbed, embed_launch(m->tok_embd.q, m->tok_embd.s, (int64_t)m->nbH * 32, m->nbH, ids, 1,
+                               m->H, (int)m->V, w.h, st));
+  if (dumps) dump_hidden(m, st, 0, w.h, 1);
+  if ((rc = norm_quant(m->layers[0].attn_norm))) return rc;
+  for (int l = 0; l < hp.n_layer; ++l) {
+    Layer& Ly = m->layers[l];
+    const bool cap = l == m->dbg_layer;
+    if (cap) {
+      for (auto& e : m->dbg)
+        if (e.second.first) cudaFree(e.second.first);
+      m->dbg.clear();
+      m->dbg_nt = 1;
+      if ((rc = dbg_capture(m, st, "h_in", w.h, (size_t)m->H * 4)) ||
+          (rc = cap_q8("x_q8", "x_s8", m->nbH)))
+        return rc;
+    }
+    if ((rc = gemv(kKTailGemv, Ly.wqkv_v, m->qkvN, m->nbH, w.part, nullptr, nullptr))) return rc;
+    if (cap && (rc = dbg_capture(m, st, "qkv", w.part, (size_t)m->qkvN * 4))) return rc;
+    {
+      RopeStoreArgs r;
+      r.partials = w.part;
+      r.bias = Ly.bqkv;
+      r.pos = pos;
+      r.nt = 1;
+      r.nh = hp.n_head;
+      r.nkv = hp.n_head_kv;
+      r.hd = hp.head_dim;
+      r.n_ctx = kv->n_ctx;
+      r.cos_t = kv->cos_t;
+      r.sin_t = kv->sin_t;
+      r.q_out = w.qrot;
+      r.kreg = kv->k(l);
+      r.vreg = kv->v(l);
+      for (int i = 0; i < 4; ++i) r.shadow[i] = kv->plane(l, i);
+      r.status = m->d_status;
+      if (hp.qk_norm) {
+        r.q_norm = Ly.q_norm;
+        r.k_norm = Ly.k_norm;
+        r.eps = hp.rms_eps;
+      }
+      LAUNCH(kKRope, rope_store_launch(r, st));
+    }
+    {
+      AttnArgs at;
+      at.q = w.qrot;
+      at.pos = pos;
+      at.r0 = 0;
+      at.r1 = 1;
+      for (int i = 0; i < 4; ++i) at.shadow[i] = kv->plane(l, i);
+      at.nh = hp.n_head;
+      at.nkv = hp.n_head_kv;
+      at.hd = hp.head_dim;
+      at.n_ctx = kv->n_ctx;
+      at.nsplit = attention_nsplit(1, at.nkv, m->num_sms, at.nh / at.nkv);
+      AttnOut ao;
+      ao.f32 = (m->debug_f32 || cap) ? w.att : nullptr;
+      ao.q8 = w.t_q;
+      ao.s8 = w.t_s;
+      LAUNCH(kKAttn, attention_launch(at, ao, st));
+    }
+    if (cap && ((rc = dbg_capture(m, st, "qrot", w.qrot, (size_t)m->q * 4)) ||
+                (rc = dbg_capture(m, st, "att", w.att, (size_t)m->q * 4)) ||
+                (rc = cap_q8("att_q8", "att_s8", m->nbq))))
+      return rc;
+    if ((rc = gemv(kKTailGemv, Ly.wo_v, m->H, m->nbq, w.h, w.h, nullptr))) return rc;
+    if (cap && (rc = dbg_capture(m, st, "h_mid", w.h, (size_t)m->H * 4))) return rc;
+    if ((rc = norm_quant(Ly.ffn_norm))) return rc;
+    if (cap && (rc = cap_q8("f_q8", "f_s8", m->nbH))) return rc;
+    if ((rc = gemv(kKTailGemv, Ly.wgu_v, 2 * m->F, m->nbH, w.gu, nullptr, nullptr))) return rc;
+    LAUNCH(kKTailSwiglu, swiglu_quant_row_launch(w.gu, m->F, w.t_q, w.t_s, st));
+    if (cap && (rc = cap_q8("s_q8", "s_s8", m->nbF))) return rc;
+    if ((rc = gemv(kKTailGemv, Ly.wd_v, m->H, m->nbF, w.h, w.h, nullptr))) return rc;
+    if (cap && (rc = dbg_capture(m, st, "h_out", w.h, (size_t)m->H * 4))) return rc;
+    if (dumps) dump_hidden(m, st, l + 1, w.h, 1);
+    if ((rc = norm_quant(l + 1 < hp.n_layer ? m->layers[l + 1].attn_norm : m->out_norm))) return rc;
+  }
+  const GemvW& out = hp.tied_embeddings ? m->tok_embd : m->output;
+  return gemv(kKLmHead, out, m->V, m->nbH, logits, nullptr, m->d_status);
+}
+
 // Enqueue one forward.  ids/pos/logits are device pointers.
 int enqueue_forward(minfer_model* m, minfer_kv* kv, const int32_t* ids, const int32_t* pos, int nt,
                     float* logits, cudaStream_t st, bool prof, bool dumps) {
+  if (nt == 1) return enqueue_decode(m, kv, ids, pos, logits, st, prof, dumps);
   const auto& hp = m->hp;
   Workspace& w = m->ws;
   Launcher L{m, st, prof};

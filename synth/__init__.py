@@ -141,6 +141,11 @@ WORKLOADS = {
     "qwen2-7b-4096": Workload("qwen2-7b-4096", QWEN2_7B, 4096, 0, 8192),
     "qwen2-1.5b-append-1024": Workload("qwen2-1.5b-append-1024", QWEN2_1_5B, 1024, 3072, 4096,
                                        prompt_seed=1, prefill_tokens=3072, prefill_seed=0),
+    # decode-shaped calls: one token after a 512-token turn already in the cache
+    "qwen2-0.5b-decode-1": Workload("qwen2-0.5b-decode-1", QWEN2_0_5B, 1, 512, 4096,
+                                    prompt_seed=2, prefill_tokens=512, prefill_seed=0),
+    "qwen2-7b-decode-1": Workload("qwen2-7b-decode-1", QWEN2_7B, 1, 512, 8192,
+                                  prompt_seed=2, prefill_tokens=512, prefill_seed=0),
     "qwen3-tiny-32": Workload("qwen3-tiny-32", QWEN3_TINY, 32, 0, 128),
     "qwen3-0.6b-512": Workload("qwen3-0.6b-512", QWEN3_0_6B, 512, 0, 4096),
 }
