@@ -106,16 +106,18 @@ def gemm_flops(cfg, nt):
             "gemm_gate_up_swiglu": 2.0 * nt * H * 2 * F, "gemm_down": 2.0 * nt * F * H}
 
 
-def forward_macs(cfg, nt, p0=0):
-    """Matmul, lm_head and causal-attention MACs of one forward (last-row tail)."""
+def forward_macs(cfg, nt, p0=0, n_out=1):
+    """Matmul, lm_head and causal-attention MACs of one forward whose last
+    layer carries the n_out tail rows past its K/V projections."""
     H, q = cfg.n_embd, cfg.n_head * cfg.head_dim
     kv = cfg.n_head_kv * cfg.head_dim
     F, L, V = cfg.n_ff, cfg.n_layer, cfg.n_vocab
     per_tok = H * (q + 2 * kv) + q * H + 3 * H * F
-    mm = (L - 1) * nt * per_tok + nt * H * (q + 2 * kv) + (q * H + 3 * H * F)
+    mm = (L - 1) * nt * per_tok + nt * H * (q + 2 * kv) + n_out * (q * H + 3 * H * F)
     keys = sum(p0 + t + 1 for t in range(nt))
-    attn = (L - 1) * keys * 2 * q + (p0 + nt) * 2 * q
-    return mm, H * V, attn
+    tail_keys = sum(p0 + t + 1 for t in range(nt - n_out, nt))
+    attn = (L - 1) * keys * 2 * q + tail_keys * 2 * q
+    return mm, n_out * H * V, attn
 
 
 _PROFILE_OF = {"gemm_gate_up_swiglu": "gemm_gate_up", "attention": "attention",
@@ -218,12 +220,14 @@ def ours(args, w, rank, world, dist):
     nt = w.n_tokens
     d_ids = torch.from_numpy(ids).cuda()
     d_pos = torch.from_numpy(pos).cuda()
-    d_logits = torch.empty(cfg.n_vocab, dtype=torch.float32, device="cuda")
+    n_out = w.n_out
+    d_logits = torch.empty((n_out, cfg.n_vocab), dtype=torch.float32, device="cuda")
     stream = torch.cuda.Stream()
     sp = stream.cuda_stream
 
     def step():
-        rc = model.prefill_device(kv, d_ids.data_ptr(), d_pos.data_ptr(), nt, d_logits.data_ptr(), sp)
+        rc = model.prefill_device_n(kv, d_ids.data_ptr(), d_pos.data_ptr(), nt, n_out,
+                                    d_logits.data_ptr(), sp)
         if rc != 0:
             raise RuntimeError(f"prefill_device rc={rc}")
 
@@ -275,13 +279,13 @@ def ours(args, w, rank, world, dist):
     # ---- end-to-end through the host-buffer call (H2D inputs, D2H logits inside)
     h_ids = torch.from_numpy(ids).pin_memory().numpy()
     h_pos = torch.from_numpy(pos).pin_memory().numpy()
-    h_logits = torch.empty(cfg.n_vocab, dtype=torch.float32).pin_memory().numpy()
+    h_logits = torch.empty((n_out, cfg.n_vocab), dtype=torch.float32).pin_memory().numpy()
     for _ in range(3):
-        model.prefill(kv, h_ids, h_pos, h_logits)
+        model.prefill_n(kv, h_ids, h_pos, n_out, h_logits)
     barrier()
     t0 = time.perf_counter()
     for _ in range(args.steps):
-        model.prefill(kv, h_ids, h_pos, h_logits)
+        model.prefill_n(kv, h_ids, h_pos, n_out, h_logits)
     e2e_s = time.perf_counter() - t0
     if dist is not None:
         t = torch.tensor([e2e_s], device="cuda")
@@ -314,17 +318,19 @@ def ours(args, w, rank, world, dist):
     else:
         roof = {"kernel": dom, "bound": "hbm", "achieved": None, "peak": hbm, "unit": "GB/s",
                 "frac": None, "traffic": profiled_traffic(dom, w.name)}
-    mm, lm, attn = forward_macs(cfg, nt, w.p0)
+    mm, lm, attn = forward_macs(cfg, nt, w.p0, n_out)
     # forward roofline: GEMM + attention flops at the tensor peak, lm_head and
     # the hidden-state traffic at HBM bandwidth
+    # lm_head: its weights read once (Q8_0 bytes) or its flops, whichever is longer
+    lm_bytes = cfg.n_vocab * cfg.n_embd * 34 / 32
     t_star = (2 * mm / (bf16 * 1e12) + 2 * attn / (bf16 * 1e12)
-              + (lm * 34 / 32) / (hbm * 1e9))
+              + max(lm_bytes / (hbm * 1e9), 2 * lm / (bf16 * 1e12)))
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": max(3, args.warmup), "ms_per_step": ms_per_step, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "q8_0 (fp16-held int8 codes, f32 acc)",
         "data": "synthetic (seeded N(0,0.02) weights, uniform ids)",
-        "config": {"workload": w.name, "n_tokens": nt,
+        "config": {"workload": w.name, "n_tokens": nt, "n_out": n_out,
                    "positions": f"{w.p0}..{w.p0 + nt - 1}", "n_ctx": w.n_ctx,
                    "layers": cfg.n_layer, "hidden": cfg.n_embd, "vocab": cfg.n_vocab,
                    "l2": "weights (>= 0.9 GB) larger than L2 stream through it every step",
@@ -336,7 +342,7 @@ def ours(args, w, rank, world, dist):
         "kernels_last_step": {k: {"launches": n, "ms": t} for k, (n, t) in prof.items() if n},
         "gpu_launches": int(launches_per_step * args.steps),
         "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": 2 * nt * 4,
-                "d2h_bytes_per_step": cfg.n_vocab * 4},
+                "d2h_bytes_per_step": n_out * cfg.n_vocab * 4},
         "clocks": clk.summary(),
     }
     if not args.no_cpu_baseline and world >= 1 and rank == 0:

@@ -153,6 +153,20 @@ int minfer_prefill_device(minfer_model* m, const int32_t* d_token_ids,
                           const int32_t* d_positions, int n_tokens, minfer_kv* kv,
                           float* d_logits, void* stream);
 
+/* Several logits rows ("09 · Prefill", section 2.4: n_out; "05 · Graph
+ * build", section 2.8: the last layer keeps the tail n_out rows): the logits
+ * of the last n_out tokens, in token order, into logits_out [n_out][n_vocab]
+ * (host) or d_logits (device).  1 <= n_out <= n_tokens, else MINFER_ERR_ARG.
+ * n_out = 1 is minfer_prefill / minfer_prefill_device.  With n_out > 1 the
+ * last layer carries its tail rows on the tensor cores and the lm_head runs
+ * as one GEMM; its tensor-core copy of the lm_head weights is built on the
+ * first such call. */
+int minfer_prefill_n(minfer_model* m, const int32_t* token_ids, const int32_t* positions,
+                     int n_tokens, minfer_kv* kv, int n_out, float* logits_out);
+int minfer_prefill_device_n(minfer_model* m, const int32_t* d_token_ids,
+                            const int32_t* d_positions, int n_tokens, minfer_kv* kv, int n_out,
+                            float* d_logits, void* stream);
+
 /* Wait for the work enqueued by minfer_prefill_device on `stream` and return
  * its status (MINFER_OK, MINFER_ERR_POS_OOB, MINFER_ERR_TOKEN_OOB,
  * MINFER_ERR_ARG or MINFER_ERR_DEVICE). */

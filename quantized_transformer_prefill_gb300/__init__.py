@@ -56,6 +56,8 @@ SIGNATURES = {
     "minfer_kv_write": ([_P, _I, _I, _I, _I, _P], _I),
     "minfer_prefill": ([_P, _P, _P, _I, _P, _P], _I),
     "minfer_prefill_device": ([_P, _P, _P, _I, _P, _P, _P], _I),
+    "minfer_prefill_n": ([_P, _P, _P, _I, _P, _I, _P], _I),
+    "minfer_prefill_device_n": ([_P, _P, _P, _I, _P, _I, _P, _P], _I),
     "minfer_sync_status": ([_P, _P], _I),
     "minfer_set_dump": ([_P, _P, _I], _I),
     "minfer_debug_read": ([_P, ctypes.c_char_p, _P, _I64], _I),
@@ -145,6 +147,23 @@ class Model:
                                   out.ctypes.data)
         check(rc, "prefill")
         return out
+
+    def prefill_n(self, kv: "KV", ids: np.ndarray, pos: np.ndarray, n_out: int,
+                  out: np.ndarray | None = None):
+        """Host-buffer prefill returning the logits of the last n_out tokens
+        (float32 [n_out][V], token order)."""
+        ids = np.ascontiguousarray(ids, dtype=np.int32)
+        pos = np.ascontiguousarray(pos, dtype=np.int32)
+        if out is None:
+            out = np.empty((n_out, self.n_vocab), np.float32)
+        check(lib().minfer_prefill_n(self.ptr, ids.ctypes.data, pos.ctypes.data, ids.size, kv.ptr,
+                                     n_out, out.ctypes.data), "prefill_n")
+        return out
+
+    def prefill_device_n(self, kv: "KV", d_ids: int, d_pos: int, nt: int, n_out: int,
+                         d_logits: int, stream: int | None = None) -> int:
+        return lib().minfer_prefill_device_n(self.ptr, d_ids, d_pos, nt, kv.ptr, n_out, d_logits,
+                                             stream)
 
     def prefill_rc(self, kv: "KV", ids, pos, out=None) -> int:
         ids = np.ascontiguousarray(ids, dtype=np.int32)

@@ -8,6 +8,7 @@
 // fp16 scale): d = amax / 127 (f32), codes = round-half-away(x * (1/d))
 // clamped to +-127, stored scale = fp16(d) round-to-nearest-even.  One warp
 // owns one block, one lane one element, so amax is a 5-step shuffle max.
+#include <algorithm>
 #include <cstdint>
 
 #include "common.cuh"
@@ -446,6 +447,32 @@ __global__ void repack_gemm_kernel(const RepackArgs a) {
   }
 }
 
+// One-row (GEMV) layout -> tensor-core layout: int8 codes [rows][kpad] and f32
+// scales [rows][nb] -> fp16 codes [rows][kpad] and block-major scales
+// [nb][rows_pad] (the lm_head when several rows need logits).
+__global__ void gemv_to_gemm_kernel(const int8_t* __restrict__ q, const float* __restrict__ s,
+                                    int64_t rows, int nb, __half* codes, float* scales,
+                                    int64_t rows_pad) {
+  const int64_t kpad = (int64_t)nb * 32;
+  for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < rows * kpad;
+       i += (int64_t)gridDim.x * blockDim.x) {
+    const int64_t r = i / kpad, k = i % kpad;
+    codes[i] = __float2half_rn((float)q[i]);
+    if ((k & 31) == 0) scales[(k / 32) * rows_pad + r] = s[r * nb + k / 32];
+  }
+}
+
+// dst = src when the call's status is clean (a rejected call writes no logit).
+__global__ void copy_if_ok_kernel(const float* __restrict__ src, float* dst, int64_t n,
+                                  const int* status) {
+  pdl_trigger();
+  pdl_wait();
+  if (*status != 0) return;
+  for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n;
+       i += (int64_t)gridDim.x * blockDim.x)
+    dst[i] = src[i];
+}
+
 __global__ void repack_gemv_kernel(const int8_t* __restrict__ q, const uint16_t* __restrict__ dbits,
                                    int64_t rows, int nb, int8_t* dst_q, float* dst_s) {
   const int64_t kpad = (int64_t)nb * 32;
@@ -519,6 +546,19 @@ cudaError_t rope_store_launch(const RopeStoreArgs& a, cudaStream_t st) {
 cudaError_t gemv_launch(const GemvArgs& a, cudaStream_t st) {
   const int warps = 8;
   return launch_pdl(gemv_kernel, (unsigned)((a.N + warps - 1) / warps), 32 * warps, 0, st, a);
+}
+
+cudaError_t gemv_to_gemm_launch(const int8_t* q, const float* sc, int64_t rows, int nb,
+                                __half* codes, float* scales, int64_t rows_pad, cudaStream_t st) {
+  gemv_to_gemm_kernel<<<grid_for(rows * nb * 32, 256), 256, 0, st>>>(q, sc, rows, nb, codes, scales,
+                                                                    rows_pad);
+  return cudaGetLastError();
+}
+
+cudaError_t copy_if_ok_launch(const float* src, float* dst, int64_t n, const int* status,
+                              cudaStream_t st) {
+  return launch_pdl(copy_if_ok_kernel, (unsigned)std::min<int64_t>((n + 255) / 256, 4096), 256, 0,
+                    st, src, dst, n, status);
 }
 
 cudaError_t swiglu_quant_row_launch(const float* gu, int64_t F, int8_t* q, float* s,

@@ -194,6 +194,12 @@ cudaError_t gemv_launch(const GemvArgs& a, cudaStream_t stream);
 
 // s = silu(g) * u for one row of F outputs (g = y[0:F], u = y[F:2F]) -> Q8_0
 // int8 codes [nbF*32] + f32 scales [nbF].
+// int8 [rows][nb*32] + f32 [rows][nb] (GEMV layout) -> fp16 codes + block-major scales.
+cudaError_t gemv_to_gemm_launch(const int8_t* q, const float* sc, int64_t rows, int nb,
+                                __half* codes, float* scales, int64_t rows_pad, cudaStream_t stream);
+// dst[0:n] = src[0:n] unless *status != 0.
+cudaError_t copy_if_ok_launch(const float* src, float* dst, int64_t n, const int* status,
+                              cudaStream_t stream);
 cudaError_t swiglu_quant_row_launch(const float* gu, int64_t F, int8_t* q, float* s,
                                     cudaStream_t stream);
 

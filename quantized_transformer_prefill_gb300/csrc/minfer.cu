@@ -139,7 +139,7 @@ struct Layer {
   float* ffn_norm = nullptr;
   float* bqkv = nullptr;                              // zero when the model has no biases
   float* q_norm = nullptr, *k_norm = nullptr;  // Qwen3 QK-norm weights [hd]
-  GemmW wqkv, wo, wgu, wd;  // wo/wgu/wd unused on the last layer
+  GemmW wqkv, wo, wgu, wd;  // the last layer's o/FFN serve calls that want several logits rows
   // one-row (GEMV) layout of every matrix: the last layer's tail and
   // single-token calls (decode-shaped prefill)
   GemvW wqkv_v, wo_v, wgu_v, wd_v;
@@ -163,12 +163,15 @@ struct Workspace {
   int8_t* t_q = nullptr;     // [max kpad] one-row codes
   float* t_s = nullptr;      // [max nb]
   float* gu = nullptr;       // [2F]
-  float* logits = nullptr;   // [V]
+  float* logits = nullptr;   // [logits_rows][V]
+  int logits_rows = 0;
+  float* lm_out = nullptr;   // [logits_rows][V]: lm_head GEMM output before the status-gated copy
   int ntp = 0;
   void release() {
     dfree(ids); dfree(pos); dfree(h); dfree(xa); dfree(xa_s); dfree(xf); dfree(xf_s);
     dfree(part); dfree(qrot); dfree(att); dfree(h_last); dfree(t_q); dfree(t_s); dfree(gu);
-    dfree(logits);
+    dfree(logits); dfree(lm_out);
+    logits_rows = 0;
     max_nt = 0;
   }
 };
@@ -206,6 +209,7 @@ struct minfer_model {
   int nbH = 0, nbq = 0, nbF = 0;
   cudaStream_t stream = nullptr;
   GemvW tok_embd, output;
+  GemmW lm_gemm;  // the lm_head in the tensor-core layout, built on the first n_out > 1 call
   float* out_norm = nullptr;
   std::vector<Layer> layers;
   std::map<std::string, bool> have;
@@ -221,13 +225,13 @@ struct minfer_model {
   size_t stage_q_bytes = 0;
   // graph cache
   struct GraphKey {
-    int nt = 0;
+    int nt = 0, n_out = 1;
     const minfer_kv* kv = nullptr;
     const void *ids = nullptr, *pos = nullptr, *logits = nullptr;
     bool profile = false;
     bool operator==(const GraphKey& o) const {
-      return nt == o.nt && kv == o.kv && ids == o.ids && pos == o.pos && logits == o.logits &&
-             profile == o.profile;
+      return nt == o.nt && n_out == o.n_out && kv == o.kv && ids == o.ids && pos == o.pos &&
+             logits == o.logits && profile == o.profile;
     }
   };
   GraphKey gkey;
@@ -370,12 +374,9 @@ int model_alloc(minfer_model* m) {
     if (hp.qk_norm &&
         ((rc = dalloc(&L.q_norm, hp.head_dim)) || (rc = dalloc(&L.k_norm, hp.head_dim))))
       return rc;
-    if ((rc = L.wqkv.alloc(m->qkvN, m->nbH))) return rc;
-    if (!last) {
-      if ((rc = L.wo.alloc(m->H, m->nbq)) || (rc = L.wgu.alloc(2 * m->Fp, m->nbH)) ||
-          (rc = L.wd.alloc(m->H, m->nbF)))
-        return rc;
-    }
+    if ((rc = L.wqkv.alloc(m->qkvN, m->nbH)) || (rc = L.wo.alloc(m->H, m->nbq)) ||
+        (rc = L.wgu.alloc(2 * m->Fp, m->nbH)) || (rc = L.wd.alloc(m->H, m->nbF)))
+      return rc;
     if ((rc = L.wqkv_v.alloc(m->qkvN, m->nbH)) || (rc = L.wo_v.alloc(m->H, m->nbq)) ||
         (rc = L.wgu_v.alloc(2 * m->F, m->nbH)) || (rc = L.wd_v.alloc(m->H, m->nbF)))
       return rc;
@@ -386,6 +387,7 @@ int model_alloc(minfer_model* m) {
 }
 
 void model_release(minfer_model* m) {
+  m->lm_gemm.release();
   for (auto& kv : m->dbg)
     if (kv.second.first) cudaFree(kv.second.first);
   m->dbg.clear();
@@ -457,18 +459,18 @@ int set_tensor(minfer_model* m, const minfer_tensor* t) {
     } else if (k == "attn_output.weight") {
       if (!mat_ok(m->q, m->H)) return MINFER_ERR_SHAPE;
       if ((rc = stage_matrix(m, t))) return rc;
-      if (!last && (rc = to_gemm(m, m->H, m->nbq, L.wo, 0, 0, 0))) return rc;
+      if ((rc = to_gemm(m, m->H, m->nbq, L.wo, 0, 0, 0))) return rc;
       rc = to_gemv(m, m->H, m->nbq, L.wo_v, 0);
     } else if (k == "ffn_gate.weight" || k == "ffn_up.weight") {
       const int which = k == "ffn_gate.weight" ? 0 : 1;
       if (!mat_ok(m->H, m->F)) return MINFER_ERR_SHAPE;
       if ((rc = stage_matrix(m, t))) return rc;
-      if (!last && (rc = to_gemm(m, m->F, m->nbH, L.wgu, 0, 1, which))) return rc;
+      if ((rc = to_gemm(m, m->F, m->nbH, L.wgu, 0, 1, which))) return rc;
       rc = to_gemv(m, m->F, m->nbH, L.wgu_v, which * m->F);
     } else if (k == "ffn_down.weight") {
       if (!mat_ok(m->F, m->H)) return MINFER_ERR_SHAPE;
       if ((rc = stage_matrix(m, t))) return rc;
-      if (!last && (rc = to_gemm(m, m->H, m->nbF, L.wd, 0, 0, 0))) return rc;
+      if ((rc = to_gemm(m, m->H, m->nbF, L.wd, 0, 0, 0))) return rc;
       rc = to_gemv(m, m->H, m->nbF, L.wd_v, 0);
     } else {
       return MINFER_ERR_SHAPE;
@@ -528,6 +530,7 @@ int ensure_workspace(minfer_model* m, int nt) {
       (rc = dalloc(&w.t_s, std::max(nbx, m->nbF))) || (rc = dalloc(&w.gu, 2 * m->F)) ||
       (rc = dalloc(&w.logits, m->V)))
     return rc;
+  w.logits_rows = 1;
   w.part_stride = (int64_t)nt * pw;
   w.ntp = (int)ntp;
   w.max_nt = nt;
@@ -774,7 +777,7 @@ int enqueue_decode(minfer_model* m, minfer_kv* kv, const int32_t* ids, const int
 
 // Enqueue one forward.  ids/pos/logits are device pointers.
 int enqueue_forward(minfer_model* m, minfer_kv* kv, const int32_t* ids, const int32_t* pos, int nt,
-                    float* logits, cudaStream_t st, bool prof, bool dumps) {
+                    int n_out, float* logits, cudaStream_t st, bool prof, bool dumps) {
   if (nt == 1) return enqueue_decode(m, kv, ids, pos, logits, st, prof, dumps);
   const auto& hp = m->hp;
   Workspace& w = m->ws;
@@ -818,9 +821,14 @@ int enqueue_forward(minfer_model* m, minfer_kv* kv, const int32_t* ids, const in
   for (int l = 0; l < hp.n_layer; ++l) {
     Layer& Ly = m->layers[l];
     const bool last = l == hp.n_layer - 1;
-    // the last layer keeps all rows only through its K/V projections
+    // the last layer keeps all rows only through its K/V projections; after
+    // that it carries the n_out tail rows: one row on the GEMV path, several
+    // on the tensor-core path
+    const bool tail1 = last && n_out == 1;
+    const int r0 = last ? nt - n_out : 0;  // first row carried past attention
+    const int mrows = nt - r0;
     const bool cap = dumps && l == m->dbg_layer;
-    const bool cap_all = cap && !last;
+    const bool cap_all = cap && !tail1;  // the tail rows: rows r0..nt-1 of the call
     int ns = 1, rc;
     if (cap) {
       for (auto& e : m->dbg)  // drop the previous call's captures
@@ -876,7 +884,7 @@ int enqueue_forward(minfer_model* m, minfer_kv* kv, const int32_t* ids, const in
     AttnArgs at;
     at.q = w.qrot;
     at.pos = pos;
-    at.r0 = last ? nt - 1 : 0;
+    at.r0 = r0;
     at.r1 = nt;
     for (int i = 0; i < 4; ++i) at.shadow[i] = kv->plane(l, i);
     at.nh = hp.n_head;
@@ -886,11 +894,12 @@ int enqueue_forward(minfer_model* m, minfer_kv* kv, const int32_t* ids, const in
     at.nsplit = attention_nsplit(at.r1 - at.r0, at.nkv, m->num_sms, at.nh / at.nkv);
     AttnOut ao;
     ao.f32 = (m->debug_f32 || cap_all) ? w.att : nullptr;
-    if (!last) {
+    if (!tail1) {
       ao.q16 = w.xa;
       ao.ldq = (int64_t)m->nbq * 32;
       ao.s16 = w.xa_s;
       ao.ldqs = ntp;
+      ao.row_base = r0;
     } else {
       ao.q8 = w.t_q;
       ao.s8 = w.t_s;
@@ -903,19 +912,22 @@ int enqueue_forward(minfer_model* m, minfer_kv* kv, const int32_t* ids, const in
           (rc = dbg_capture(m, st, "att", w.att, (size_t)nt * m->q * 4)))
         return rc;
     }
-    if (!last) {
-      if ((rc = gemm_call(m, L, kKGemmO, xo, Ly.wo, nt, kEpiF32, true, w.part, m->H, nullptr, 0,
-                          nullptr, 0, &ns)))
+    if (!tail1) {
+      float* hr = w.h + (int64_t)r0 * m->H;  // the rows carried on
+      GemmOperand xo_r = xo, xa_r = xa, xf_r = xf;
+      xo_r.rows = xa_r.rows = xf_r.rows = mrows;
+      if ((rc = gemm_call(m, L, kKGemmO, xo_r, Ly.wo, mrows, kEpiF32, true, w.part, m->H, nullptr,
+                          0, nullptr, 0, &ns)))
         return rc;
       {
         RowQuantArgs r;
-        r.h = w.h;
+        r.h = hr;
         r.partials = w.part;
         r.nsplit = ns;
         r.split_stride = w.part_stride;
         r.norm_w = Ly.ffn_norm;
         r.eps = hp.rms_eps;
-        r.rows = nt;
+        r.rows = mrows;
         r.n = m->H;
         r.q16 = w.xa;
         r.ldq = (int64_t)m->nbH * 32;
@@ -929,7 +941,7 @@ int enqueue_forward(minfer_model* m, minfer_kv* kv, const int32_t* ids, const in
             (rc = dbg_capture_scales(m, st, "f_scales", w.xa_s, m->nbH, ntp, ntp_call)))
           return rc;
       }
-      if ((rc = gemm_call(m, L, kKGemmGU, xa, Ly.wgu, nt, kEpiSwiGLU, false, nullptr, 0, w.xf,
+      if ((rc = gemm_call(m, L, kKGemmGU, xa_r, Ly.wgu, mrows, kEpiSwiGLU, false, nullptr, 0, w.xf,
                           m->Fp, w.xf_s, ntp, nullptr)))
         return rc;
       if (cap) {
@@ -937,18 +949,18 @@ int enqueue_forward(minfer_model* m, minfer_kv* kv, const int32_t* ids, const in
             (rc = dbg_capture_scales(m, st, "s_scales", w.xf_s, m->nbF, ntp, ntp_call)))
           return rc;
       }
-      if ((rc = gemm_call(m, L, kKGemmDown, xf, Ly.wd, nt, kEpiF32, true, w.part, m->H, nullptr, 0,
-                          nullptr, 0, &ns)))
+      if ((rc = gemm_call(m, L, kKGemmDown, xf_r, Ly.wd, mrows, kEpiF32, true, w.part, m->H,
+                          nullptr, 0, nullptr, 0, &ns)))
         return rc;
       {
         RowQuantArgs r;
-        r.h = w.h;
+        r.h = hr;
         r.partials = w.part;
         r.nsplit = ns;
         r.split_stride = w.part_stride;
-        r.norm_w = m->layers[l + 1].attn_norm;
+        r.norm_w = last ? m->out_norm : m->layers[l + 1].attn_norm;
         r.eps = hp.rms_eps;
-        r.rows = nt;
+        r.rows = mrows;
         r.n = m->H;
         r.q16 = w.xa;
         r.ldq = (int64_t)m->nbH * 32;
@@ -956,8 +968,16 @@ int enqueue_forward(minfer_model* m, minfer_kv* kv, const int32_t* ids, const in
         r.ldqs = ntp;
         LAUNCH(kKRowQuant, row_quant_launch(r, st));
       }
-      if (dumps) dump_hidden(m, st, l + 1, w.h, nt);
+      if (dumps) dump_hidden(m, st, l + 1, hr, mrows);
       if (cap && (rc = dbg_capture(m, st, "h_out", w.h, (size_t)nt * m->H * 4))) return rc;
+      if (last) {
+        // lm_head over the n_out rows on the tensor cores, then one
+        // status-gated copy into the caller's buffer
+        if ((rc = gemm_call(m, L, kKLmHead, xa_r, m->lm_gemm, mrows, kEpiF32, false, w.lm_out,
+                            m->V, nullptr, 0, nullptr, 0, nullptr)))
+          return rc;
+        LAUNCH(kKLmHead, copy_if_ok_launch(w.lm_out, logits, (int64_t)mrows * m->V, m->d_status, st));
+      }
     } else {
       // last row only: o-projection, FFN, final norm, lm_head as GEMVs
       const int64_t last_row = nt - 1;
@@ -1043,20 +1063,53 @@ int enqueue_forward(minfer_model* m, minfer_kv* kv, const int32_t* ids, const in
 }
 
 // Run (record or replay) the forward on stream st.
+// The lm_head in the tensor-core layout, and the workspace for n_out logits
+// rows (both only when a call asks for more than one row).
+int ensure_logits(minfer_model* m, int n_out) {
+  Workspace& w = m->ws;
+  if (n_out <= 1) return MINFER_OK;
+  int rc;
+  if (!m->lm_gemm.codes) {
+    const GemvW& src = m->hp.tied_embeddings ? m->tok_embd : m->output;
+    if ((rc = m->lm_gemm.alloc(m->V, m->nbH))) return rc;
+    CK(gemv_to_gemm_launch(src.q, src.s, m->V, m->nbH, m->lm_gemm.codes, m->lm_gemm.scales,
+                           m->lm_gemm.rows_pad, m->stream));
+    CK(cudaStreamSynchronize(m->stream));
+  }
+  if (n_out <= w.logits_rows) return MINFER_OK;
+  if (m->gexec) {
+    cudaGraphExecDestroy(m->gexec);
+    m->gexec = nullptr;
+  }
+  if (m->graph) {
+    cudaGraphDestroy(m->graph);
+    m->graph = nullptr;
+  }
+  dfree(w.logits);
+  dfree(w.lm_out);
+  w.logits_rows = 0;
+  if ((rc = dalloc(&w.logits, (size_t)n_out * m->V)) || (rc = dalloc(&w.lm_out, (size_t)n_out * m->V)))
+    return rc;
+  w.logits_rows = n_out;
+  return MINFER_OK;
+}
+
 int run_forward(minfer_model* m, minfer_kv* kv, const int32_t* ids, const int32_t* pos, int nt,
-                float* logits, cudaStream_t st) {
+                int n_out, float* logits, cudaStream_t st) {
   int rc = ensure_workspace(m, nt);
   if (rc) return rc;
+  if ((rc = ensure_logits(m, n_out))) return rc;
   m->dump_on = m->dump_host != nullptr && nt <= m->dump_max_nt;
   const bool dumps = m->dump_on || m->dbg_layer >= 0;
   if (dumps) {
     // dumps copy to host memory mid-sequence: run eagerly
     m->ev_used = 0;
-    rc = enqueue_forward(m, kv, ids, pos, nt, logits, st, m->profile, true);
+    rc = enqueue_forward(m, kv, ids, pos, nt, n_out, logits, st, m->profile, true);
     return rc;
   }
   minfer_model::GraphKey key;
   key.nt = nt;
+  key.n_out = n_out;
   key.kv = kv;
   key.ids = ids;
   key.pos = pos;
@@ -1073,7 +1126,7 @@ int run_forward(minfer_model* m, minfer_kv* kv, const int32_t* ids, const int32_
     }
     m->ev_used = 0;
     CK(cudaStreamBeginCapture(st, cudaStreamCaptureModeThreadLocal));
-    rc = enqueue_forward(m, kv, ids, pos, nt, logits, st, m->profile, false);
+    rc = enqueue_forward(m, kv, ids, pos, nt, n_out, logits, st, m->profile, false);
     cudaGraph_t g = nullptr;
     cudaError_t e = cudaStreamEndCapture(st, &g);
     if (rc) {
@@ -1291,7 +1344,13 @@ int minfer_kv_write(minfer_kv* kv, int layer, int which, int row0, int nrows, co
 
 int minfer_prefill(minfer_model* m, const int32_t* token_ids, const int32_t* positions,
                    int n_tokens, minfer_kv* kv, float* logits_out) {
-  if (!m || !token_ids || !positions || !kv || !logits_out || n_tokens <= 0 || kv->m != m)
+  return minfer_prefill_n(m, token_ids, positions, n_tokens, kv, 1, logits_out);
+}
+
+int minfer_prefill_n(minfer_model* m, const int32_t* token_ids, const int32_t* positions,
+                     int n_tokens, minfer_kv* kv, int n_out, float* logits_out) {
+  if (!m || !token_ids || !positions || !kv || !logits_out || n_tokens <= 0 || kv->m != m ||
+      n_out < 1 || n_out > n_tokens)
     return MINFER_ERR_ARG;
   if (!m->finalized) return MINFER_ERR_STATE;
   int rc = check_device(m);
@@ -1313,21 +1372,30 @@ int minfer_prefill(minfer_model* m, const int32_t* token_ids, const int32_t* pos
   cudaStream_t st = m->stream;
   CK(cudaMemcpyAsync(m->ws.ids, token_ids, (size_t)n_tokens * 4, cudaMemcpyHostToDevice, st));
   CK(cudaMemcpyAsync(m->ws.pos, positions, (size_t)n_tokens * 4, cudaMemcpyHostToDevice, st));
-  if ((rc = run_forward(m, kv, m->ws.ids, m->ws.pos, n_tokens, m->ws.logits, st))) return rc;
-  CK(cudaMemcpyAsync(logits_out, m->ws.logits, (size_t)m->V * 4, cudaMemcpyDeviceToHost, st));
+  if ((rc = ensure_logits(m, n_out))) return rc;
+  if ((rc = run_forward(m, kv, m->ws.ids, m->ws.pos, n_tokens, n_out, m->ws.logits, st))) return rc;
+  CK(cudaMemcpyAsync(logits_out, m->ws.logits, (size_t)n_out * m->V * 4, cudaMemcpyDeviceToHost,
+                     st));
   return finish_status(m, st);
 }
 
 int minfer_prefill_device(minfer_model* m, const int32_t* d_token_ids, const int32_t* d_positions,
                           int n_tokens, minfer_kv* kv, float* d_logits, void* stream) {
-  if (!m || !d_token_ids || !d_positions || !kv || !d_logits || n_tokens <= 0 || kv->m != m)
+  return minfer_prefill_device_n(m, d_token_ids, d_positions, n_tokens, kv, 1, d_logits, stream);
+}
+
+int minfer_prefill_device_n(minfer_model* m, const int32_t* d_token_ids,
+                            const int32_t* d_positions, int n_tokens, minfer_kv* kv, int n_out,
+                            float* d_logits, void* stream) {
+  if (!m || !d_token_ids || !d_positions || !kv || !d_logits || n_tokens <= 0 || kv->m != m ||
+      n_out < 1 || n_out > n_tokens)
     return MINFER_ERR_ARG;
   if (!m->finalized) return MINFER_ERR_STATE;
   int rc = check_device(m);
   if (rc) return rc;
   std::lock_guard<std::mutex> lk(g_mu);
   cudaStream_t st = stream ? static_cast<cudaStream_t>(stream) : m->stream;
-  return run_forward(m, kv, d_token_ids, d_positions, n_tokens, d_logits, st);
+  return run_forward(m, kv, d_token_ids, d_positions, n_tokens, n_out, d_logits, st);
 }
 
 int minfer_sync_status(minfer_model* m, void* stream) {

@@ -112,6 +112,7 @@ class Workload:
     prompt_seed: int = 0
     prefill_tokens: int = 0      # tokens pre-filled (untimed) at positions 0..prefill_tokens-1
     prefill_seed: int = 0
+    n_out: int = 1               # logits rows returned (the last n_out tokens)
 
     def positions(self) -> np.ndarray:
         return np.arange(self.p0, self.p0 + self.n_tokens, dtype=np.int32)
@@ -146,6 +147,9 @@ WORKLOADS = {
                                     prompt_seed=2, prefill_tokens=512, prefill_seed=0),
     "qwen2-7b-decode-1": Workload("qwen2-7b-decode-1", QWEN2_7B, 1, 512, 8192,
                                   prompt_seed=2, prefill_tokens=512, prefill_seed=0),
+    # every prompt token's logits (n_out = n_tokens)
+    "qwen2-0.5b-512-all-logits": Workload("qwen2-0.5b-512-all-logits", QWEN2_0_5B, 512, 0, 4096,
+                                          n_out=512),
     "qwen3-tiny-32": Workload("qwen3-tiny-32", QWEN3_TINY, 32, 0, 128),
     "qwen3-0.6b-512": Workload("qwen3-0.6b-512", QWEN3_0_6B, 512, 0, 4096),
 }

@@ -131,8 +131,10 @@ def _kv_rows(kv, layer, which, rows_pos):
     return np.stack([kv.read(layer, which, int(p), 1)[0] for p in rows_pos])
 
 
-def _check_layer(oracle_mod, g, kv, cfg, layer, pos, rows):
-    """Teacher-forced check of one middle layer on rows `rows`."""
+def _check_layer(oracle_mod, g, kv, cfg, layer, pos, rows, tail0=0):
+    """Teacher-forced check of one layer on rows `rows`.  tail0 > 0: the last
+    layer of a call that keeps the rows tail0.. past attention (their
+    attention, FFN and SwiGLU captures start at row 0)."""
     nt = len(pos)
     ntp = (nt + 127) // 128 * 128
     H, hd, nh, nkv = cfg.n_embd, cfg.head_dim, cfg.n_head, cfg.n_head_kv
@@ -166,16 +168,16 @@ def _check_layer(oracle_mod, g, kv, cfg, layer, pos, rows):
     att = _f32(g, "att", nt, q)[rows]
     err = np.abs(att - att_ref).max()
     assert err <= 2e-5 * max(1.0, np.abs(att_ref).max()), err
-    aq = _codes(g, "att_codes", nt, nbq * 32)[rows]
-    ad = _scales(g, "att_scales", nbq, ntp, rows)
+    aq = _codes(g, "att_codes", nt, nbq * 32)[rows - tail0]
+    ad = _scales(g, "att_scales", nbq, ntp, rows - tail0)
     gq, gd = oracle_mod.q8_quantize(att)
     assert np.array_equal(ad, gd) and np.array_equal(aq, gq), "attention Q8_0 differs"
 
     h_mid = _f32(g, "h_mid", nt, H)[rows]
     _check_sum(oracle_mod, h_mid, aq, ad, *Wt.q8["attn_output.weight"], q, base=h_in)
 
-    fq = _codes(g, "f_codes", nt, nbH * 32)[rows]
-    fd = _scales(g, "f_scales", nbH, ntp, rows)
+    fq = _codes(g, "f_codes", nt, nbH * 32)[rows - tail0]
+    fd = _scales(g, "f_scales", nbH, ntp, rows - tail0)
     oq, od = oracle_mod.q8_quantize(oracle_mod.rmsnorm(h_mid, Wt.f32["ffn_norm.weight"],
                                                        cfg.rms_eps))
     assert np.array_equal(fd, od) and np.array_equal(fq, oq), "ffn_norm Q8_0 differs"
@@ -183,8 +185,8 @@ def _check_layer(oracle_mod, g, kv, cfg, layer, pos, rows):
     gate = oracle_mod.matmul_q8(fq, fd, *Wt.q8["ffn_gate.weight"], H).astype(np.float64)
     up = oracle_mod.matmul_q8(fq, fd, *Wt.q8["ffn_up.weight"], H).astype(np.float64)
     s_ref = oracle_mod.swiglu(gate, up)
-    sq = _codes(g, "s_codes", nt, nbF * 32)[rows]
-    sd = _scales(g, "s_scales", nbF, ntp, rows)
+    sq = _codes(g, "s_codes", nt, nbF * 32)[rows - tail0]
+    sd = _scales(g, "s_scales", nbF, ntp, rows - tail0)
     # the GPU's gate/up are f32 block sums (error dg, du within their bounds);
     # silu' <= 1.1 and |silu(g)| <= |g| + 0.28 carry them into s = silu(g) u,
     # plus the f32 rounding of silu and of the product
@@ -194,6 +196,7 @@ def _check_layer(oracle_mod, g, kv, cfg, layer, pos, rows):
 
     h_out = _f32(g, "h_out", nt, H)[rows]
     _check_sum(oracle_mod, h_out, sq, sd, *Wt.q8["ffn_down.weight"], cfg.n_ff, base=h_mid)
+    return h_out
 
 
 def _check_last_layer(oracle_mod, g, kv, cfg, pos, rows, logits):

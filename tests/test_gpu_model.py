@@ -212,6 +212,67 @@ def test_decode_steps_match_oracle(qp, oracle_mod, which):
         g.debug_layer(-1)
 
 
+@pytest.mark.parametrize("which", ["qwen2", "qwen3"])
+def test_several_logits_rows_match_oracle(qp, oracle_mod, which):
+    """n_out > 1 ("09 · Prefill", section 2.4; "05 · Graph build", section
+    2.8): the logits of the last n_out tokens in token order.  The last layer
+    then carries n_out rows on the tensor cores; it is checked teacher-forced
+    stage by stage on those rows (a Q8_0 decision of one row on a rounding
+    boundary would otherwise dominate), and every logits row against the
+    oracle's final norm and lm_head of the GPU's last hidden state."""
+    from test_gpu_fullsize import LayerWeights, _check_layer
+    cfg = synth.TINY if which == "qwen2" else synth.QWEN3_TINY
+    g = gpu_model(cfg)
+    w = synth.WORKLOADS["tiny-32"]
+    ids, pos = w.ids(), w.positions()
+    L = cfg.n_layer - 1
+    Wt = LayerWeights(oracle_mod, cfg, L)
+    specs = {sp.name: sp for sp in synth.tensor_specs(cfg)}
+    head = specs["token_embd.weight" if cfg.tied else "output.weight"]
+    wq, wd = oracle_mod.q8_quantize(synth.tensor_data(head))
+    out_norm = synth.tensor_data(specs["output_norm.weight"])
+    try:
+        for n_out in (2, 9, 32):
+            kv = g.kv(w.n_ctx)
+            g.debug_layer(L)
+            lg = g.prefill_n(kv, ids, pos, n_out)
+            assert lg.shape == (n_out, cfg.n_vocab)
+            tail = np.arange(w.n_tokens - n_out, w.n_tokens)
+            h_out = _check_layer(oracle_mod, g, kv, cfg, L, pos, tail, tail0=w.n_tokens - n_out)
+            yq, yd = oracle_mod.q8_quantize(oracle_mod.rmsnorm(h_out, out_norm, cfg.rms_eps))
+            want = oracle_mod.matmul_q8(yq, yd, wq, wd, cfg.n_embd)
+            for r in range(n_out):
+                check_logits(lg[r], want[r])
+    finally:
+        g.debug_layer(-1)
+
+
+def test_several_logits_rows_device_path(qp, tiny_pair):
+    """The device-buffer n_out call replays as a graph, and a rejected call
+    (a position out of range, found on the device) writes no logits row."""
+    cfg, g, o = tiny_pair
+    w = synth.WORKLOADS["tiny-32"]
+    ids, pos = w.ids(), w.positions()
+    ref = g.prefill_n(g.kv(w.n_ctx), ids, pos, 5)
+    d_ids = torch.from_numpy(ids).cuda()
+    d_pos = torch.from_numpy(pos).cuda()
+    d_lg = torch.zeros((5, cfg.n_vocab), dtype=torch.float32, device="cuda")
+    s = torch.cuda.Stream()
+    kv = g.kv(w.n_ctx)
+    for _ in range(2):
+        assert g.prefill_device_n(kv, d_ids.data_ptr(), d_pos.data_ptr(), len(ids), 5,
+                                  d_lg.data_ptr(), s.cuda_stream) == 0
+    assert g.sync_status(s.cuda_stream) == 0
+    assert np.array_equal(d_lg.cpu().numpy(), ref)
+    bad = torch.from_numpy(np.where(pos == 3, 900, pos).astype(np.int32)).cuda()
+    d_lg.fill_(7.0)
+    assert g.prefill_device_n(g.kv(w.n_ctx), d_ids.data_ptr(), bad.data_ptr(), len(ids), 5,
+                              d_lg.data_ptr(), s.cuda_stream) == 0
+    assert g.sync_status(s.cuda_stream) == -2
+    assert torch.all(d_lg == 7.0)
+    assert qp.lib().minfer_prefill_n(g.ptr, None, None, 4, kv.ptr, 5, None) == -1
+
+
 def test_device_path_graph_replay(qp, tiny_pair):
     cfg, g, o = tiny_pair
     w = synth.WORKLOADS["tiny-32"]
