@@ -10,7 +10,7 @@ import subprocess
 HERE = os.path.dirname(os.path.abspath(__file__))
 CSRC = os.path.join(HERE, "csrc")
 LIB_PATH = os.path.join(HERE, "libminfer.so")
-SOURCES = ["minfer.cu", "k_gemm.cu", "k_rows.cu", "k_attn.cu", "noalloc.cu"]
+SOURCES = ["minfer.cu", "k_gemm.cu", "k_rows.cu", "k_attn.cu", "k_attn_tc.cu", "noalloc.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "-Xcompiler", "-O2"]
 

@@ -462,15 +462,20 @@ __global__ void __launch_bounds__(256) attn_kernel(const AttnArgs a, const AttnO
 
 // K/V rows of one layer -> fp16 hi/lo shadow planes (count f32 values each).
 __global__ void kv_shadow_kernel(const float* __restrict__ k, const float* __restrict__ v,
-                                 int64_t count, __half* kh, __half* kl, __half* vh, __half* vl) {
+                                 int64_t count, __half* kh, __half* kl, __half* vh, __half* vl,
+                                 __half* vth, __half* vtl, int64_t vt_ld, int row0, int kvw) {
   for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < count;
        i += (int64_t)gridDim.x * blockDim.x) {
     const float x = k[i], y = v[i];
     const __half xh = __float2half_rn(x), yh = __float2half_rn(y);
+    const __half yl = __float2half_rn(__fsub_rn(y, __half2float(yh)));
     kh[i] = xh;
     kl[i] = __float2half_rn(__fsub_rn(x, __half2float(xh)));
     vh[i] = yh;
-    vl[i] = __float2half_rn(__fsub_rn(y, __half2float(yh)));
+    vl[i] = yl;
+    const int64_t row = row0 + i / kvw, e = i % kvw;
+    vth[e * vt_ld + row] = yh;
+    vtl[e * vt_ld + row] = yl;
   }
 }
 
@@ -530,12 +535,13 @@ cudaError_t attention_launch(const AttnArgs& a, const AttnOut& out, cudaStream_t
 }
 
 cudaError_t kv_shadow_launch(const float* k, const float* v, int64_t count, __half* const* planes,
+                             __half* const* vt, int64_t vt_ld, int row0, int kvw,
                              cudaStream_t st) {
   int64_t g = (count + 255) / 256;
   if (g > 4096) g = 4096;
   if (g < 1) g = 1;
   kv_shadow_kernel<<<(unsigned)g, 256, 0, st>>>(k, v, count, planes[0], planes[1], planes[2],
-                                                planes[3]);
+                                                planes[3], vt[0], vt[1], vt_ld, row0, kvw);
   return cudaGetLastError();
 }
 

@@ -1,0 +1,617 @@
+// k_attn_tc.cu -- causal GQA attention on the 5th-generation tensor cores
+// (tcgen05.mma with TMEM accumulators, TMA-fed), for prompts of 64 rows and
+// more; short calls (the last-row tail, single tokens) keep k_attn.cu.
+//
+// What it computes ("09 · Prefill: the first forward", section 2.2: token t
+// attends to positions 0..=pos[t]; "05 · Graph build", section 2.5: GQA,
+// scale 1/sqrt(head_dim)):
+//     o[t, h] = sum_{j <= pos[t]} softmax_j(q[t,h] . K[j, g] / sqrt(hd)) V[j, g],
+//     g = h / (n_head / n_head_kv)
+//
+// Design.  One CTA per (128 query rows, query head, key split).  Every f32
+// operand is split into fp16 hi + lo and the three significant products are
+// accumulated (about 22 significant bits, the precision the Q8_0 output
+// needs), as in the k_attn.cu kernel:
+//   S  = Qh.Kh^T + Qh.Kl^T + Ql.Kh^T        M = 128 rows, N = 64 keys, K = hd
+//   Ot = Ph.Vh + Ph.Vl + Pl.Vh              M = 128 rows, N = hd, K = 64 keys
+// warp 0 streams K (hi/lo, from the fp16 shadow planes) and V^T (hi/lo, from
+// the transposed planes) tiles with TMA into two-stage rings; warp 1 issues
+// the MMAs from one thread into TMEM (two S buffers and one O tile); warps
+// 2-5 own one query row per thread: they write Q's hi/lo into shared memory,
+// read each S row from TMEM, apply the causal mask and the online softmax
+// (log2 units, running max and sum in registers), write P's hi/lo into
+// shared memory for the P.V MMA, and fold each O tile into an f32 row held
+// in registers.  S of tile j+1 is computed while tile j's softmax runs.
+// With few row tiles the key range is split over the CTAs of a cluster,
+// merged through distributed shared memory as in k_attn.cu.  The output row
+// is normalized and each 32-block quantized to Q8_0 by its own thread.
+// Every wait is bounded; on timeout the kernel records a status code,
+// drains its own TMA loads and MMAs, frees TMEM and returns.
+#include <algorithm>
+#include <cstdint>
+
+#include "common.cuh"
+#include "kernels.h"
+
+namespace minfer {
+
+namespace {
+
+constexpr int kTcRows = 128;    // query rows per CTA (MMA M)
+constexpr int kTcKeys = 64;     // keys per tile (N of the S MMA, K of the P.V MMA)
+constexpr int kTcThreads = 192;  // TMA warp, MMA warp, four softmax warps
+constexpr int kTcMaxSplits = 8;  // CTAs per cluster (portable cluster size)
+
+enum : int { kDevTimeoutAttn = 6 };
+
+template <int HD>
+struct TcCfg {
+  static constexpr int QSUB = kTcRows * 128;   // bytes of one 64-wide swizzled Q sub-tile
+  static constexpr int KSUB = kTcKeys * 128;   // one 64-wide K sub-tile
+  static constexpr int Q_BYTES = kTcRows * HD * 2;
+  static constexpr int K_BYTES = kTcKeys * HD * 2;
+  static constexpr int V_BYTES = HD * kTcKeys * 2;  // V^T tile [hd][64 keys]
+  static constexpr int P_BYTES = kTcRows * kTcKeys * 2;
+  static constexpr int STAGES = 2;
+  static constexpr int OFF_QH = 0;
+  static constexpr int OFF_QL = OFF_QH + Q_BYTES;
+  static constexpr int OFF_K = OFF_QL + Q_BYTES;            // stage s: hi, lo
+  static constexpr int OFF_V = OFF_K + STAGES * 2 * K_BYTES;  // stage s: hi, lo
+  static constexpr int OFF_P = OFF_V + STAGES * 2 * V_BYTES;  // hi, lo
+  static constexpr int OFF_BAR = OFF_P + 2 * P_BYTES;
+  static constexpr int NBAR = 4 * STAGES + 4 + 4 + 2;
+  static constexpr int OFF_TMEM = OFF_BAR + NBAR * 8;
+  static constexpr int SMEM = OFF_TMEM + 16 + 1024;
+  // the split-merge partials reuse the K/V rings: o [128 rows][hd], then
+  // (max, sum) [128 rows][2]
+  static constexpr int PART_ML = kTcRows * HD;  // float offset of the (max, sum) pairs
+  static_assert(kTcRows * (HD + 2) * 4 <= OFF_P - OFF_K, "partials fit the K/V rings");
+  static_assert(OFF_K % 1024 == 0 && OFF_V % 1024 == 0 && OFF_P % 1024 == 0, "1024-B alignment");
+  static_assert(SMEM <= 227 * 1024, "shared memory budget");
+  // TMEM columns: S buffers at 0 and 64, the O tile at 128
+  static constexpr uint32_t TCOLS = 256;
+};
+
+struct TcArgs {
+  const float* q;  // [nt][nh*hd]
+  const int32_t* pos;
+  int r0, r1, nh, nkv, n_ctx;
+  int* err;
+};
+
+// Byte offset of element (row, k) in a K-major, 128-byte-swizzled tile whose
+// rows are 64 fp16 wide (chunk of 8 halves XOR row % 8, as TMA writes it).
+__device__ __forceinline__ uint32_t sw128_off(int row, int k) {
+  return (uint32_t)(row * 128 + (((k >> 3) ^ (row & 7)) << 4) + ((k & 7) << 1));
+}
+
+__device__ __forceinline__ uint32_t cluster_rank_tc() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+__device__ __forceinline__ void cluster_sync_tc() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::
+                   : "memory");
+}
+__device__ __forceinline__ uint32_t peer_addr_tc(uint32_t saddr, uint32_t rank) {
+  uint32_t r;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(saddr), "r"(rank));
+  return r;
+}
+__device__ __forceinline__ float ld_peer_tc(uint32_t addr) {
+  float v;
+  asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(addr) : "memory");
+  return v;
+}
+
+__device__ __forceinline__ uint32_t pack_half2(__half a, __half b) {
+  return (uint32_t)__half_as_ushort(a) | ((uint32_t)__half_as_ushort(b) << 16);
+}
+
+template <int HD, bool kGemvOut>
+__global__ void __launch_bounds__(kTcThreads, 1)
+    attn_tc_kernel(const __grid_constant__ CUtensorMap tmKh, const __grid_constant__ CUtensorMap tmKl,
+                   const __grid_constant__ CUtensorMap tmVh, const __grid_constant__ CUtensorMap tmVl,
+                   const TcArgs a, const AttnOut out) {
+  using C = TcCfg<HD>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~uintptr_t(1023));
+  uint64_t* kfull = reinterpret_cast<uint64_t*>(smem + C::OFF_BAR);
+  uint64_t* kempty = kfull + C::STAGES;
+  uint64_t* vfull = kempty + C::STAGES;
+  uint64_t* vempty = vfull + C::STAGES;
+  uint64_t* sready = vempty + C::STAGES;  // [2]
+  uint64_t* sfree = sready + 2;           // [2]
+  uint64_t* pready = sfree + 2;
+  uint64_t* ofree = pready + 1;
+  uint64_t* oready = ofree + 1;
+  uint64_t* qready = oready + 1;
+  uint64_t* mdone = qready + 1;  // all MMAs of the CTA completed (before TMEM is freed)
+  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(smem + C::OFF_TMEM);
+  __shared__ int s_maxp;
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int G = a.nh / a.nkv;
+  const int ns = (int)gridDim.z;
+  const int split = (int)cluster_rank_tc();
+  const int tile = (int)gridDim.x - 1 - (int)blockIdx.x;  // longest rows first
+  const int h = blockIdx.y;
+  const int g = h / G;
+  const int rbase = a.r0 + tile * kTcRows;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < C::STAGES; ++s) {
+      mbar_init(&kfull[s], 1);
+      mbar_init(&kempty[s], 1);
+      mbar_init(&vfull[s], 1);
+      mbar_init(&vempty[s], 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&sready[b], 1);
+      mbar_init(&sfree[b], 4);
+    }
+    mbar_init(pready, 4);
+    mbar_init(ofree, 4);
+    mbar_init(oready, 1);
+    mbar_init(qready, 4);
+    mbar_init(mdone, 1);
+    fence_barrier_init();
+    tma_prefetch_desc(&tmKh);
+    tma_prefetch_desc(&tmKl);
+    tma_prefetch_desc(&tmVh);
+    tma_prefetch_desc(&tmVl);
+    s_maxp = -1;
+  }
+  if (warp == 1) {
+    tmem_alloc(tmem_holder, C::TCOLS);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_holder;
+  pdl_trigger();
+  pdl_wait();
+
+  auto clamp_pos = [&](int r) -> int {
+    if (r >= a.r1) return -1;
+    const int p = a.pos[r];
+    return p < 0 ? -1 : (p >= a.n_ctx ? a.n_ctx - 1 : p);
+  };
+  if (threadIdx.x < kTcRows) atomicMax(&s_maxp, clamp_pos(rbase + threadIdx.x));
+  __syncthreads();
+  const int nkeys = s_maxp + 1;
+  int share = (nkeys + ns - 1) / ns;
+  share = (share + kTcKeys - 1) / kTcKeys * kTcKeys;
+  const int kbeg = split * share;
+  const int kend = min(nkeys, kbeg + share);
+  const int ntile = kend > kbeg ? (kend - kbeg + kTcKeys - 1) / kTcKeys : 0;
+
+  uint8_t* sQh = smem + C::OFF_QH;
+  uint8_t* sQl = smem + C::OFF_QL;
+  uint8_t* sP = smem + C::OFF_P;
+
+  if (warp == 0) {
+    // ---------------------------------------------------------- TMA producer
+    if (lane == 0 && ntile > 0) {
+      bool ok = true;
+      int issued = 0;
+      for (int j = 0; j < ntile && ok; ++j) {
+        const int st = j % C::STAGES;
+        const uint32_t par = ((j / C::STAGES) & 1) ^ 1;
+        const int key0 = kbeg + j * kTcKeys;
+        if (!mbar_wait(&kempty[st], par, a.err, kDevTimeoutAttn)) {
+          ok = false;
+          break;
+        }
+        mbar_arrive_expect_tx(&kfull[st], 2 * C::K_BYTES);
+        uint8_t* kh = smem + C::OFF_K + st * 2 * C::K_BYTES;
+#pragma unroll
+        for (int sub = 0; sub < HD / 64; ++sub) {
+          tma_load_2d(kh + sub * C::KSUB, &tmKh, &kfull[st], g * HD + sub * 64, key0);
+          tma_load_2d(kh + C::K_BYTES + sub * C::KSUB, &tmKl, &kfull[st], g * HD + sub * 64, key0);
+        }
+        if (!mbar_wait(&vempty[st], par, a.err, kDevTimeoutAttn)) {
+          ok = false;
+          break;
+        }
+        mbar_arrive_expect_tx(&vfull[st], 2 * C::V_BYTES);
+        uint8_t* vh = smem + C::OFF_V + st * 2 * C::V_BYTES;
+        tma_load_2d(vh, &tmVh, &vfull[st], key0, g * HD);
+        tma_load_2d(vh + C::V_BYTES, &tmVl, &vfull[st], key0, g * HD);
+        issued = j + 1;
+      }
+      if (!ok) {
+        for (int j = max(0, issued - C::STAGES); j < issued; ++j) {
+          mbar_wait(&kfull[j % C::STAGES], (j / C::STAGES) & 1, a.err, kDevTimeoutAttn);
+          mbar_wait(&vfull[j % C::STAGES], (j / C::STAGES) & 1, a.err, kDevTimeoutAttn);
+        }
+      }
+    }
+  } else if (warp == 1) {
+    // ---------------------------------------------------------- MMA issuer
+    if (lane == 0 && ntile > 0) {
+      constexpr uint32_t idS = idesc_f16_f32(kTcRows, kTcKeys);
+      constexpr uint32_t idO = idesc_f16_f32(kTcRows, HD);
+      const uint32_t qh = smem_u32(sQh), ql = smem_u32(sQl);
+      const uint32_t ph = smem_u32(sP), pl = smem_u32(sP + C::P_BYTES);
+      const uint32_t tO = tmem_base + 128;
+      bool ok = mbar_wait(qready, 0, a.err, kDevTimeoutAttn);
+      bool committed = false;
+      auto issue_s = [&](int j) -> bool {
+        const int st = j % C::STAGES, b = j & 1;
+        if (!mbar_wait(&kfull[st], (j / C::STAGES) & 1, a.err, kDevTimeoutAttn)) return false;
+        if (!mbar_wait(&sfree[b], ((j >> 1) & 1) ^ 1, a.err, kDevTimeoutAttn)) return false;
+        tc_fence_after();
+        const uint32_t kh = smem_u32(smem + C::OFF_K + st * 2 * C::K_BYTES);
+        const uint32_t kl = kh + C::K_BYTES;
+        const uint32_t d = tmem_base + (uint32_t)(b * kTcKeys);
+#pragma unroll
+        for (int c = 0; c < 3; ++c) {
+          const uint32_t A = c == 2 ? ql : qh;
+          const uint32_t B = c == 1 ? kl : kh;
+#pragma unroll
+          for (int k = 0; k < HD / 16; ++k) {
+            const uint32_t off = (uint32_t)((k & 3) * 32);
+            tc_mma_f16(d, smem_desc_sw128(A + (k >> 2) * C::QSUB + off),
+                       smem_desc_sw128(B + (k >> 2) * C::KSUB + off), idS,
+                       (c == 0 && k == 0) ? 0u : 1u);
+          }
+        }
+        tc_commit(&sready[b]);
+        tc_commit(&kempty[st]);
+        committed = true;
+        return true;
+      };
+      auto issue_pv = [&](int j) -> bool {
+        const int st = j % C::STAGES;
+        if (!mbar_wait(pready, j & 1, a.err, kDevTimeoutAttn)) return false;
+        if (!mbar_wait(ofree, (j & 1) ^ 1, a.err, kDevTimeoutAttn)) return false;
+        if (!mbar_wait(&vfull[st], (j / C::STAGES) & 1, a.err, kDevTimeoutAttn)) return false;
+        tc_fence_after();
+        const uint32_t vh = smem_u32(smem + C::OFF_V + st * 2 * C::V_BYTES);
+        const uint32_t vl = vh + C::V_BYTES;
+#pragma unroll
+        for (int c = 0; c < 3; ++c) {
+          const uint32_t A = c == 2 ? pl : ph;
+          const uint32_t B = c == 1 ? vl : vh;
+#pragma unroll
+          for (int k = 0; k < kTcKeys / 16; ++k) {
+            const uint32_t off = (uint32_t)(k * 32);
+            tc_mma_f16(tO, smem_desc_sw128(A + off), smem_desc_sw128(B + off), idO,
+                       (c == 0 && k == 0) ? 0u : 1u);
+          }
+        }
+        tc_commit(oready);
+        tc_commit(&vempty[st]);
+        return true;
+      };
+      if (ok) ok = issue_s(0);
+      for (int j = 0; j < ntile && ok; ++j) {
+        if (j + 1 < ntile) ok = issue_s(j + 1);
+        if (ok) ok = issue_pv(j);
+      }
+      // every MMA issued must have landed before TMEM is released
+      if (committed) {
+        tc_commit(mdone);
+        mbar_wait(mdone, 0, a.err, kDevTimeoutAttn);
+      }
+    }
+  } else {
+    // ---------------------------------------------------------- softmax rows
+    const int quad = warp & 3;                // TMEM lane quadrant
+    const int rl = quad * 32 + lane;          // row within the tile
+    const int r = rbase + rl;
+    const int pr = clamp_pos(r);
+    const int q = a.nh * HD;
+    const uint32_t lanebase = (uint32_t)(quad * 32) << 16;
+    // Q row -> fp16 hi/lo, swizzled like a TMA tile
+    {
+      const float* src = a.q + (int64_t)(r < a.r1 ? r : a.r0) * q + (int64_t)h * HD;
+#pragma unroll 4
+      for (int c8 = 0; c8 < HD / 8; ++c8) {
+        float x[8];
+        if (r < a.r1) {
+          const float4 u = *reinterpret_cast<const float4*>(src + c8 * 8);
+          const float4 v = *reinterpret_cast<const float4*>(src + c8 * 8 + 4);
+          x[0] = u.x; x[1] = u.y; x[2] = u.z; x[3] = u.w;
+          x[4] = v.x; x[5] = v.y; x[6] = v.z; x[7] = v.w;
+        } else {
+#pragma unroll
+          for (int i = 0; i < 8; ++i) x[i] = 0.f;
+        }
+        uint32_t hi[4], lo[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const __half h0 = __float2half_rn(x[2 * i]), h1 = __float2half_rn(x[2 * i + 1]);
+          hi[i] = pack_half2(h0, h1);
+          lo[i] = pack_half2(__float2half_rn(__fsub_rn(x[2 * i], __half2float(h0))),
+                             __float2half_rn(__fsub_rn(x[2 * i + 1], __half2float(h1))));
+        }
+        const int d0 = c8 * 8;
+        const uint32_t off = (uint32_t)((d0 >> 6) * C::QSUB) + sw128_off(rl, d0 & 63);
+        *reinterpret_cast<uint4*>(sQh + off) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
+        *reinterpret_cast<uint4*>(sQl + off) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
+      }
+      fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(qready);
+    }
+
+    float o[HD];
+#pragma unroll
+    for (int d = 0; d < HD; ++d) o[d] = 0.f;
+    float m = -INFINITY, l = 0.f;
+    // scores in log2 units: s2 = (q.k) / sqrt(hd) * log2(e)
+    const float sc = __fmul_rn(__fdiv_rn(1.0f, __fsqrt_rn((float)HD)), 1.4426950408889634f);
+    bool ok = true;
+    for (int j = 0; j < ntile && ok; ++j) {
+      const int b = j & 1;
+      if (!mbar_wait(&sready[b], (j >> 1) & 1, a.err, kDevTimeoutAttn)) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      uint32_t sr[kTcKeys];
+      tmem_ld32(tmem_base + lanebase + (uint32_t)(b * kTcKeys),
+                *reinterpret_cast<uint32_t(*)[32]>(&sr[0]));
+      tmem_ld32(tmem_base + lanebase + (uint32_t)(b * kTcKeys + 32),
+                *reinterpret_cast<uint32_t(*)[32]>(&sr[32]));
+      tmem_wait_ld();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&sfree[b]);
+      const int key0 = kbeg + j * kTcKeys;
+      float mx = -INFINITY;
+#pragma unroll
+      for (int c = 0; c < kTcKeys; ++c) {
+        const float s2 = (key0 + c <= pr) ? __fmul_rn(__uint_as_float(sr[c]), sc) : -INFINITY;
+        sr[c] = __float_as_uint(s2);
+        mx = fmaxf(mx, s2);
+      }
+      const float mn = fmaxf(m, mx);
+      const float alpha = (mn == -INFINITY) ? 1.f : exp2f(m - mn);
+      m = mn;
+      l *= alpha;
+      // P row -> fp16 hi/lo tiles (the P buffer is free: the previous P.V completed)
+#pragma unroll
+      for (int c8 = 0; c8 < kTcKeys / 8; ++c8) {
+        uint32_t hi[4], lo[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const float s0 = __uint_as_float(sr[c8 * 8 + 2 * i]);
+          const float s1 = __uint_as_float(sr[c8 * 8 + 2 * i + 1]);
+          const float p0 = (s0 == -INFINITY) ? 0.f : exp2f(s0 - m);
+          const float p1 = (s1 == -INFINITY) ? 0.f : exp2f(s1 - m);
+          l += p0 + p1;
+          const __half h0 = __float2half_rn(p0), h1 = __float2half_rn(p1);
+          hi[i] = pack_half2(h0, h1);
+          lo[i] = pack_half2(__float2half_rn(__fsub_rn(p0, __half2float(h0))),
+                             __float2half_rn(__fsub_rn(p1, __half2float(h1))));
+        }
+        const uint32_t off = sw128_off(rl, c8 * 8);
+        *reinterpret_cast<uint4*>(sP + off) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
+        *reinterpret_cast<uint4*>(sP + C::P_BYTES + off) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
+      }
+      fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(pready);
+      if (!mbar_wait(oready, j & 1, a.err, kDevTimeoutAttn)) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+#pragma unroll
+      for (int d0 = 0; d0 < HD; d0 += 32) {
+        uint32_t ot[32];
+        tmem_ld32(tmem_base + lanebase + 128u + (uint32_t)d0, ot);
+        tmem_wait_ld();
+#pragma unroll
+        for (int i = 0; i < 32; ++i) o[d0 + i] = fmaf(o[d0 + i], alpha, __uint_as_float(ot[i]));
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(ofree);
+    }
+
+    // ------------------------------------------------------- merge + output
+    const int nb = q / 32;
+    auto emit = [&](const float* v, float inv) {
+      if (r >= a.r1) return;
+      const int64_t orow = r - out.row_base;
+#pragma unroll
+      for (int bq = 0; bq < HD / 32; ++bq) {
+        float y[32];
+        float amax = 0.f;
+#pragma unroll
+        for (int i = 0; i < 32; ++i) {
+          y[i] = __fmul_rn(v[bq * 32 + i], inv);
+          amax = fmaxf(amax, fabsf(y[i]));
+        }
+        const int k0 = h * HD + bq * 32;
+        const int blk = k0 / 32;
+        if (out.f32)
+#pragma unroll
+          for (int i = 0; i < 32; ++i) out.f32[(int64_t)r * q + k0 + i] = y[i];
+        const float dd = __fdiv_rn(amax, 127.0f);
+        const float id = q8_inv(dd);
+        const float d16 = __half2float(__float2half_rn(dd));
+        if (kGemvOut) {
+#pragma unroll
+          for (int i = 0; i < 32; ++i) out.q8[orow * (int64_t)nb * 32 + k0 + i] = (int8_t)q8_code(y[i], id);
+          out.s8[orow * nb + blk] = d16;
+        } else {
+#pragma unroll
+          for (int i = 0; i < 32; i += 2)
+            *reinterpret_cast<__half2*>(out.q16 + orow * out.ldq + k0 + i) =
+                __floats2half2_rn(q8_code(y[i], id), q8_code(y[i + 1], id));
+          out.s16[(int64_t)blk * out.ldqs + orow] = d16;
+        }
+      }
+    };
+    if (ns == 1) {
+      if (ok) emit(o, l > 0.f ? __fdiv_rn(1.0f, l) : 0.f);
+    } else {
+      // partials into this CTA's K/V rings (idle now), merged after the cluster barrier
+      float* po = reinterpret_cast<float*>(smem + C::OFF_K);
+#pragma unroll
+      for (int d = 0; d < HD; d += 4)
+        *reinterpret_cast<float4*>(po + rl * HD + d) = make_float4(o[d], o[d + 1], o[d + 2], o[d + 3]);
+      *reinterpret_cast<float2*>(po + C::PART_ML + rl * 2) = make_float2(m, l);
+    }
+  }
+
+  if (ns > 1) {
+    __syncthreads();
+    cluster_sync_tc();
+    // merge: CTA `split` takes rows rl = split, split + ns, ...; one warp per
+    // row, each lane VPL consecutive dims (a 32-block spans 32 / VPL lanes)
+    constexpr int VPL = HD / 32;
+    constexpr int LPB = 32 / VPL;  // lanes per 32-block
+    const uint32_t po_s = smem_u32(smem + C::OFF_K);
+    const int q = a.nh * HD;
+    const int nb = q / 32;
+    for (int rl = split + warp * ns; rl < kTcRows; rl += ns * (kTcThreads / 32)) {
+      const int r = rbase + rl;
+      if (r >= a.r1) continue;  // warp-uniform
+      float ms = -INFINITY, ls = 0.f;
+      if (lane < ns) {
+        const uint32_t ml = peer_addr_tc(po_s + (uint32_t)((C::PART_ML + rl * 2) * 4), (uint32_t)lane);
+        ms = ld_peer_tc(ml);
+        ls = ld_peer_tc(ml + 4);
+      }
+      float M = ms;
+#pragma unroll
+      for (int o2 = 16; o2 > 0; o2 >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o2));
+      const float wl = (lane < ns && ms != -INFINITY) ? exp2f(ms - M) : 0.f;
+      float L = wl * ls;
+#pragma unroll
+      for (int o2 = 16; o2 > 0; o2 >>= 1) L += __shfl_xor_sync(0xffffffffu, L, o2);
+      float y[VPL];
+#pragma unroll
+      for (int i = 0; i < VPL; ++i) y[i] = 0.f;
+      for (int sdx = 0; sdx < ns; ++sdx) {
+        const float w = __shfl_sync(0xffffffffu, wl, sdx);
+        const uint32_t pa =
+            peer_addr_tc(po_s + (uint32_t)((rl * HD + lane * VPL) * 4), (uint32_t)sdx);
+#pragma unroll
+        for (int i = 0; i < VPL; ++i) y[i] = fmaf(ld_peer_tc(pa + 4u * i), w, y[i]);
+      }
+      const float inv = L > 0.f ? __fdiv_rn(1.0f, L) : 0.f;
+      float amax = 0.f;
+#pragma unroll
+      for (int i = 0; i < VPL; ++i) {
+        y[i] = __fmul_rn(y[i], inv);
+        amax = fmaxf(amax, fabsf(y[i]));
+      }
+#pragma unroll
+      for (int o2 = 1; o2 < LPB; o2 <<= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o2));
+      const int k0 = h * HD + lane * VPL;  // first element of this lane in the output row
+      const int blk = k0 / 32;
+      if (out.f32)
+#pragma unroll
+        for (int i = 0; i < VPL; ++i) out.f32[(int64_t)r * q + k0 + i] = y[i];
+      const float dd = __fdiv_rn(amax, 127.0f);
+      const float id = q8_inv(dd);
+      const float d16 = __half2float(__float2half_rn(dd));
+      const int64_t orow = r - out.row_base;
+      if (kGemvOut) {
+#pragma unroll
+        for (int i = 0; i < VPL; ++i) out.q8[orow * (int64_t)nb * 32 + k0 + i] = (int8_t)q8_code(y[i], id);
+        if ((lane % LPB) == 0) out.s8[orow * nb + blk] = d16;
+      } else {
+#pragma unroll
+        for (int i = 0; i < VPL; i += 2)
+          *reinterpret_cast<__half2*>(out.q16 + orow * out.ldq + k0 + i) =
+              __floats2half2_rn(q8_code(y[i], id), q8_code(y[i + 1], id));
+        if ((lane % LPB) == 0) out.s16[(int64_t)blk * out.ldqs + orow] = d16;
+      }
+    }
+    cluster_sync_tc();  // peers may still be reading this CTA's partials
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == 1) tmem_dealloc(tmem_base, C::TCOLS);
+}
+
+}  // namespace
+
+bool attention_tc_supported(const AttnArgs& a) {
+  return (a.hd == 64 || a.hd == 128) && a.r1 - a.r0 >= 64 && a.vt[0] && a.vt[1] &&
+         a.vt_ld % 64 == 0 && ((int64_t)a.nkv * a.hd) % 8 == 0;
+}
+
+bool attention_tc_preferred(int rows, int nh, int num_sms) {
+  // short prompts: too few (128-row tile, head) CTAs to fill the GPU; the
+  // mma.sync kernel's 16-row tiles spread them better
+  return 2 * ((rows + kTcRows - 1) / kTcRows) * nh >= num_sms;
+}
+
+int attention_tc_nsplit(int rows, int nh, int num_sms) {
+  const int ctas = (rows + kTcRows - 1) / kTcRows * nh;
+  if (2 * ctas >= num_sms) return 1;
+  const int ns = (num_sms + ctas - 1) / std::max(ctas, 1);
+  return ns < 1 ? 1 : (ns > kTcMaxSplits ? kTcMaxSplits : ns);
+}
+
+template <int HD, bool kGemvOut>
+cudaError_t launch_tc(const AttnArgs& a, const AttnOut& out, int ns, int* err, cudaStream_t st) {
+  using C = TcCfg<HD>;
+  static bool set = false;
+  if (!set) {
+    cudaError_t e = cudaFuncSetAttribute(attn_tc_kernel<HD, kGemvOut>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
+    if (e != cudaSuccess) return e;
+    set = true;
+  }
+  const int64_t kvw = (int64_t)a.nkv * HD;
+  CUtensorMap mk[2], mv[2];
+  for (int i = 0; i < 2; ++i) {
+    if (tensor_map_2d(&mk[i], a.shadow[i], false, (uint64_t)kvw, (uint64_t)a.n_ctx,
+                      (uint64_t)kvw * 2, 64, kTcKeys, true) ||
+        tensor_map_2d(&mv[i], a.vt[i], false, (uint64_t)a.vt_ld, (uint64_t)kvw,
+                      (uint64_t)a.vt_ld * 2, kTcKeys, HD, true))
+      return cudaErrorInvalidValue;
+  }
+  TcArgs t;
+  t.q = a.q;
+  t.pos = a.pos;
+  t.r0 = a.r0;
+  t.r1 = a.r1;
+  t.nh = a.nh;
+  t.nkv = a.nkv;
+  t.n_ctx = a.n_ctx;
+  t.err = err;
+  const int rows = a.r1 - a.r0;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((rows + kTcRows - 1) / kTcRows, a.nh, ns);
+  cfg.blockDim = dim3(kTcThreads);
+  cfg.dynamicSmemBytes = C::SMEM;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 1;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = ns;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 2;
+  return cudaLaunchKernelEx(&cfg, attn_tc_kernel<HD, kGemvOut>, mk[0], mk[1], mv[0], mv[1], t, out);
+}
+
+cudaError_t attention_tc_launch(const AttnArgs& a, const AttnOut& out, int num_sms, int* err,
+                                cudaStream_t st) {
+  if (!attention_tc_supported(a) || a.nh % a.nkv != 0) return cudaErrorInvalidValue;
+  const int ns = attention_tc_nsplit(a.r1 - a.r0, a.nh, num_sms);
+  const bool gemv = out.q8 != nullptr;
+  if (a.hd == 64)
+    return gemv ? launch_tc<64, true>(a, out, ns, err, st) : launch_tc<64, false>(a, out, ns, err, st);
+  return gemv ? launch_tc<128, true>(a, out, ns, err, st) : launch_tc<128, false>(a, out, ns, err, st);
+}
+
+}  // namespace minfer

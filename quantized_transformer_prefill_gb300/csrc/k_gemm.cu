@@ -453,6 +453,13 @@ cudaError_t launch_bn(const GemmLaunch& g, const GemmMaps& maps, int num_sms, cu
 
 }  // namespace
 
+int tensor_map_2d(CUtensorMap* map, const void* base, bool f32, uint64_t inner, uint64_t outer,
+                  uint64_t row_bytes, uint32_t box_inner, uint32_t box_outer, bool swizzle128) {
+  return make_map(map, base, f32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16,
+                  inner, outer, row_bytes, box_inner, box_outer,
+                  swizzle128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE);
+}
+
 GemmPlan gemm_plan(int64_t M, int64_t N, int nb, int num_sms, bool allow_split) {
   GemmPlan p;
   const int64_t mt = (M + kBM - 1) / kBM;

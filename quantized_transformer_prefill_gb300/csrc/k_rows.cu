@@ -43,6 +43,7 @@ __device__ __forceinline__ void ff_add(float& hi, float& lo, float bhi, float bl
 // 8 k + w, so a block's amax is a 5-step shuffle max.  The sum of squares is
 // a float-float (hi, lo) pair reduced over the warp, then over the 8 warps.
 constexpr int kRowThreads = 256;
+constexpr int kMaxPartialSplits = 8;  // split-K partials a row kernel sums (GEMM split cap)
 
 template <bool kGemvOut, int PER>
 __global__ void __launch_bounds__(kRowThreads) row_quant_kernel(const RowQuantArgs a) {
@@ -70,12 +71,33 @@ __global__ void __launch_bounds__(kRowThreads) row_quant_kernel(const RowQuantAr
       const int64_t k = tid + (int64_t)kRowThreads * i;
       o[i] = k < n ? a.partials[hr * n + k] : 0.f;
     }
-    for (int s = 1; s < a.nsplit; ++s) {
-      const float* ps = a.partials + s * a.split_stride + hr * n;
+    if constexpr (PER <= 4) {
+      // short rows: every split's loads in flight at once, summed in split order
+      float ps[kMaxPartialSplits - 1][PER];
 #pragma unroll
-      for (int i = 0; i < PER; ++i) {
-        const int64_t k = tid + (int64_t)kRowThreads * i;
-        if (k < n) o[i] = __fadd_rn(o[i], ps[k]);
+      for (int s = 1; s < kMaxPartialSplits; ++s) {
+#pragma unroll
+        for (int i = 0; i < PER; ++i) {
+          const int64_t k = tid + (int64_t)kRowThreads * i;
+          ps[s - 1][i] =
+              (s < a.nsplit && k < n) ? a.partials[s * a.split_stride + hr * n + k] : 0.f;
+        }
+      }
+#pragma unroll
+      for (int s = 1; s < kMaxPartialSplits; ++s) {
+        if (s < a.nsplit) {
+#pragma unroll
+          for (int i = 0; i < PER; ++i) o[i] = __fadd_rn(o[i], ps[s - 1][i]);
+        }
+      }
+    } else {
+      for (int s = 1; s < a.nsplit; ++s) {
+        const float* ps = a.partials + s * a.split_stride + hr * n;
+#pragma unroll
+        for (int i = 0; i < PER; ++i) {
+          const int64_t k = tid + (int64_t)kRowThreads * i;
+          if (k < n) o[i] = __fadd_rn(o[i], ps[k]);
+        }
       }
     }
 #pragma unroll
@@ -256,8 +278,11 @@ __global__ void rope_store_kernel(const RopeStoreArgs a) {
       const int64_t o0 = (int64_t)p * kw + e;
       a.vreg[o0] = v;
       const __half vh = __float2half_rn(v);
+      const __half vl = __float2half_rn(__fsub_rn(v, __half2float(vh)));
       a.shadow[2][o0] = vh;
-      a.shadow[3][o0] = __float2half_rn(__fsub_rn(v, __half2float(vh)));
+      a.shadow[3][o0] = vl;
+      a.vt[0][e * a.vt_ld + p] = vh;
+      a.vt[1][e * a.vt_ld + p] = vl;
     }
   }
 }
@@ -296,8 +321,11 @@ __global__ void rope_store_qknorm_kernel(const RopeStoreArgs a) {
       const int64_t o0 = (int64_t)p * kw + (e - nqk);
       a.vreg[o0] = v;
       const __half vh = __float2half_rn(v);
+      const __half vl = __float2half_rn(__fsub_rn(v, __half2float(vh)));
       a.shadow[2][o0] = vh;
-      a.shadow[3][o0] = __float2half_rn(__fsub_rn(v, __half2float(vh)));
+      a.shadow[3][o0] = vl;
+      a.vt[0][(e - nqk) * a.vt_ld + p] = vh;
+      a.vt[1][(e - nqk) * a.vt_ld + p] = vl;
     }
   }
   __syncthreads();

@@ -85,6 +85,10 @@ struct GemmMaps {
   CUtensorMap a, b, sa, sb;
 };
 int gemm_make_maps(const GemmOperand& A, const GemmOperand& B, int bn, GemmMaps* maps);
+// A 2-D TMA map over a row-major [outer][inner] array of fp16 (or f32), box
+// [box_outer][box_inner], 128-byte swizzle or none.  0 on success.
+int tensor_map_2d(CUtensorMap* map, const void* base, bool f32, uint64_t inner, uint64_t outer,
+                  uint64_t row_bytes, uint32_t box_inner, uint32_t box_outer, bool swizzle128);
 cudaError_t gemm_launch(const GemmLaunch& g, const GemmMaps& maps, int num_sms,
                         cudaStream_t stream);
 
@@ -136,6 +140,8 @@ struct RopeStoreArgs {
   float* kreg = nullptr;   // [n_ctx][nkv*hd]
   float* vreg = nullptr;
   __half* shadow[4] = {nullptr, nullptr, nullptr, nullptr};  // fp16 hi/lo copies of K, V
+  __half* vt[2] = {nullptr, nullptr};  // fp16 hi/lo of V transposed: [nkv*hd][vt_ld] (key-major)
+  int64_t vt_ld = 0;
   const int* status = nullptr;  // skip all writes to the regions when *status != 0
   // Qwen3 QK-norm (null: none): per-head RMSNorm weights [hd] of Q and of K
   const float* q_norm = nullptr;
@@ -152,6 +158,8 @@ struct AttnArgs {
   const int32_t* pos = nullptr;
   int r0 = 0, r1 = 0;
   const __half* shadow[4] = {nullptr, nullptr, nullptr, nullptr};  // K hi, K lo, V hi, V lo [n_ctx][nkv*hd]
+  const __half* vt[2] = {nullptr, nullptr};  // V hi, V lo transposed [nkv*hd][vt_ld]
+  int64_t vt_ld = 0;                         // >= n_ctx, a multiple of 64
   int nh = 0, nkv = 0, hd = 0;
   int n_ctx = 0;   // positions are clamped into [0, n_ctx) before any region read
   int nsplit = 1;  // key splits (CTAs per cluster), 1..8
@@ -169,11 +177,23 @@ struct AttnOut {
   int64_t row_base = 0;
   float* f32 = nullptr;
 };
+// The tensor-core attention (k_attn_tc.cu) for calls of 64 rows and more with
+// head_dim 64 or 128: one CTA per (128 rows, query head, key split); err is the
+// device status word of timed-out waits.
+bool attention_tc_supported(const AttnArgs& a);
+// Whether the forward picks it: its (128-row tile, head) CTAs fill at least
+// half of the SMs.
+bool attention_tc_preferred(int rows, int nh, int num_sms);
+cudaError_t attention_tc_launch(const AttnArgs& a, const AttnOut& out, int num_sms, int* err,
+                                cudaStream_t stream);
 // Key splits for `rows` query rows: enough CTAs to fill the GPU about twice.
 int attention_nsplit(int rows, int nkv, int num_sms, int G);
 cudaError_t attention_launch(const AttnArgs& a, const AttnOut& out, cudaStream_t stream);
-// f32 K/V values -> fp16 hi/lo planes (planes[0..3] = K hi, K lo, V hi, V lo).
+// f32 K/V rows row0.. (count = rows * kvw values) -> fp16 hi/lo planes
+// (planes[0..3] = K hi, K lo, V hi, V lo, pointing at row row0) and the
+// transposed V planes vt[0..1] [kvw][vt_ld] at columns row0...
 cudaError_t kv_shadow_launch(const float* k, const float* v, int64_t count, __half* const* planes,
+                             __half* const* vt, int64_t vt_ld, int row0, int kvw,
                              cudaStream_t stream);
 
 // One-row quantized GEMV: y[n] = sum_b dw[n][b] * da[b] * dot_b (+ resid[n]).

@@ -193,12 +193,16 @@ struct minfer_kv {
   int n_ctx = 0;
   float* regions = nullptr;  // [L][2][n_ctx][kvw]
   __half* shadow = nullptr;  // [L][4][n_ctx][kvw]: fp16 hi/lo of K and V, read by attention
+  __half* vt = nullptr;      // [L][2][kvw][vt_ld]: fp16 hi/lo of V transposed (key-major)
+  int64_t vt_ld = 0;         // n_ctx rounded up to 64
   float* cos_t = nullptr;    // [n_ctx][hd/2]
   float* sin_t = nullptr;
   uint32_t* seen = nullptr;  // n_ctx bits (duplicate-position check)
   float* k(int l) const;
   float* v(int l) const;
   __half* plane(int l, int i) const;
+  __half* vtp(int l, int i) const { return vt + ((int64_t)l * 2 + i) * m_kvw * vt_ld; }
+  int64_t m_kvw = 0;
 };
 
 struct minfer_model {
@@ -729,6 +733,9 @@ int enqueue_decode(minfer_model* m, minfer_kv* kv, const int32_t* ids, const int
       r.kreg = kv->k(l);
       r.vreg = kv->v(l);
       for (int i = 0; i < 4; ++i) r.shadow[i] = kv->plane(l, i);
+      r.vt[0] = kv->vtp(l, 0);
+      r.vt[1] = kv->vtp(l, 1);
+      r.vt_ld = kv->vt_ld;
       r.status = m->d_status;
       if (hp.qk_norm) {
         r.q_norm = Ly.q_norm;
@@ -744,6 +751,9 @@ int enqueue_decode(minfer_model* m, minfer_kv* kv, const int32_t* ids, const int
       at.r0 = 0;
       at.r1 = 1;
       for (int i = 0; i < 4; ++i) at.shadow[i] = kv->plane(l, i);
+    at.vt[0] = kv->vtp(l, 0);
+    at.vt[1] = kv->vtp(l, 1);
+    at.vt_ld = kv->vt_ld;
       at.nh = hp.n_head;
       at.nkv = hp.n_head_kv;
       at.hd = hp.head_dim;
@@ -861,6 +871,9 @@ int enqueue_forward(minfer_model* m, minfer_kv* kv, const int32_t* ids, const in
       r.kreg = kv->k(l);
       r.vreg = kv->v(l);
       for (int i = 0; i < 4; ++i) r.shadow[i] = kv->plane(l, i);
+      r.vt[0] = kv->vtp(l, 0);
+      r.vt[1] = kv->vtp(l, 1);
+      r.vt_ld = kv->vt_ld;
       r.status = m->d_status;
       if (hp.qk_norm) {
         r.q_norm = Ly.q_norm;
@@ -887,13 +900,16 @@ int enqueue_forward(minfer_model* m, minfer_kv* kv, const int32_t* ids, const in
     at.r0 = r0;
     at.r1 = nt;
     for (int i = 0; i < 4; ++i) at.shadow[i] = kv->plane(l, i);
+    at.vt[0] = kv->vtp(l, 0);
+    at.vt[1] = kv->vtp(l, 1);
+    at.vt_ld = kv->vt_ld;
     at.nh = hp.n_head;
     at.nkv = hp.n_head_kv;
     at.hd = hp.head_dim;
     at.n_ctx = kv->n_ctx;
     at.nsplit = attention_nsplit(at.r1 - at.r0, at.nkv, m->num_sms, at.nh / at.nkv);
     AttnOut ao;
-    ao.f32 = (m->debug_f32 || cap_all) ? w.att : nullptr;
+    ao.f32 = (m->debug_f32 || cap) ? w.att : nullptr;
     if (!tail1) {
       ao.q16 = w.xa;
       ao.ldq = (int64_t)m->nbq * 32;
@@ -905,7 +921,10 @@ int enqueue_forward(minfer_model* m, minfer_kv* kv, const int32_t* ids, const in
       ao.s8 = w.t_s;
       ao.row_base = nt - 1;
     }
-    LAUNCH(kKAttn, attention_launch(at, ao, st));
+    if (attention_tc_supported(at) && attention_tc_preferred(at.r1 - at.r0, at.nh, m->num_sms))
+      LAUNCH(kKAttn, attention_tc_launch(at, ao, m->num_sms, m->d_status + 1, st));
+    else
+      LAUNCH(kKAttn, attention_launch(at, ao, st));
     if (cap_all) {
       if ((rc = dbg_capture(m, st, "att_codes", w.xa, (size_t)nt * m->nbq * 32 * 2)) ||
           (rc = dbg_capture_scales(m, st, "att_scales", w.xa_s, m->nbq, ntp, ntp_call)) ||
@@ -981,6 +1000,14 @@ int enqueue_forward(minfer_model* m, minfer_kv* kv, const int32_t* ids, const in
     } else {
       // last row only: o-projection, FFN, final norm, lm_head as GEMVs
       const int64_t last_row = nt - 1;
+      // stage capture of the last row (debug): one-row layouts as in enqueue_decode
+      auto cap_row = [&](const char* name, const void* src, size_t bytes) -> int {
+        return cap ? dbg_capture(m, st, name, src, bytes) : MINFER_OK;
+      };
+      if ((rc = cap_row("att", w.att + last_row * m->q, (size_t)m->q * 4)) ||
+          (rc = cap_row("att_q8", w.t_q, (size_t)m->nbq * 32)) ||
+          (rc = cap_row("att_s8", w.t_s, (size_t)m->nbq * 4)))
+        return rc;
       {
         GemvArgs g;
         g.wq = Ly.wo_v.q;
@@ -994,6 +1021,7 @@ int enqueue_forward(minfer_model* m, minfer_kv* kv, const int32_t* ids, const in
         g.resid = w.h + last_row * m->H;
         LAUNCH(kKTailGemv, gemv_launch(g, st));
       }
+      if ((rc = cap_row("h_mid", w.h_last, (size_t)m->H * 4))) return rc;
       {
         RowQuantArgs r;
         r.h = w.h_last;
@@ -1005,6 +1033,9 @@ int enqueue_forward(minfer_model* m, minfer_kv* kv, const int32_t* ids, const in
         r.s8 = w.t_s;
         LAUNCH(kKRowQuant, row_quant_launch(r, st));
       }
+      if ((rc = cap_row("f_q8", w.t_q, (size_t)m->nbH * 32)) ||
+          (rc = cap_row("f_s8", w.t_s, (size_t)m->nbH * 4)))
+        return rc;
       {
         GemvArgs g;
         g.wq = Ly.wgu_v.q;
@@ -1018,6 +1049,9 @@ int enqueue_forward(minfer_model* m, minfer_kv* kv, const int32_t* ids, const in
         LAUNCH(kKTailGemv, gemv_launch(g, st));
       }
       LAUNCH(kKTailSwiglu, swiglu_quant_row_launch(w.gu, m->F, w.t_q, w.t_s, st));
+      if ((rc = cap_row("s_q8", w.t_q, (size_t)m->nbF * 32)) ||
+          (rc = cap_row("s_s8", w.t_s, (size_t)m->nbF * 4)))
+        return rc;
       {
         GemvArgs g;
         g.wq = Ly.wd_v.q;
@@ -1031,6 +1065,7 @@ int enqueue_forward(minfer_model* m, minfer_kv* kv, const int32_t* ids, const in
         g.resid = w.h_last;
         LAUNCH(kKTailGemv, gemv_launch(g, st));
       }
+      if ((rc = cap_row("h_out", w.h_last, (size_t)m->H * 4))) return rc;
       if (dumps) dump_hidden(m, st, l + 1, w.h_last, 1);
       {
         RowQuantArgs r;
@@ -1277,10 +1312,13 @@ int minfer_kv_create(minfer_model* m, int n_ctx, minfer_kv** out) {
   minfer_kv* kv = new minfer_kv();
   kv->m = m;
   kv->n_ctx = std::min(n_ctx, m->hp.max_seq_len);
+  kv->vt_ld = rup(kv->n_ctx, 64);
+  kv->m_kvw = m->kvw;
   std::vector<float> c, s;
   rope_tables(kv->n_ctx, m->hp.head_dim, m->hp.rope_theta, c, s);
   if ((rc = dalloc(&kv->regions, (size_t)m->hp.n_layer * 2 * kv->n_ctx * m->kvw)) ||
       (rc = dalloc(&kv->shadow, (size_t)m->hp.n_layer * 4 * kv->n_ctx * m->kvw)) ||
+      (rc = dalloc(&kv->vt, (size_t)m->hp.n_layer * 2 * m->kvw * kv->vt_ld)) ||
       (rc = dalloc(&kv->cos_t, c.size())) || (rc = dalloc(&kv->sin_t, s.size())) ||
       (rc = dalloc(&kv->seen, (size_t)(kv->n_ctx + 31) / 32))) {
     minfer_kv_free(kv);
@@ -1309,6 +1347,7 @@ void minfer_kv_free(minfer_kv* kv) {
   }
   dfree(kv->regions);
   dfree(kv->shadow);
+  dfree(kv->vt);
   dfree(kv->cos_t);
   dfree(kv->sin_t);
   dfree(kv->seen);
@@ -1336,8 +1375,9 @@ int minfer_kv_write(minfer_kv* kv, int layer, int which, int row0, int nrows, co
   const int64_t off = (int64_t)row0 * kv->m->kvw;
   __half* planes[4];
   for (int i = 0; i < 4; ++i) planes[i] = kv->plane(layer, i) + off;
+  __half* vt[2] = {kv->vtp(layer, 0), kv->vtp(layer, 1)};
   CK(kv_shadow_launch(kv->k(layer) + off, kv->v(layer) + off, (int64_t)nrows * kv->m->kvw, planes,
-                      0));
+                      vt, kv->vt_ld, row0, (int)kv->m->kvw, 0));
   CK(cudaDeviceSynchronize());
   return MINFER_OK;
 }
@@ -1622,7 +1662,10 @@ int minfer_op_attention(const float* d_q, const int32_t* d_pos, int nt, const fl
   __half* sh = nullptr;
   float* s16 = nullptr;
   __half* q16 = nullptr;
+  const int64_t vt_ld = rup(n_ctx, 64);
+  __half* vt = nullptr;
   int rc = dalloc(&sh, (size_t)4 * n_ctx * kvw);
+  if (!rc) rc = dalloc(&vt, (size_t)2 * kvw * vt_ld);
   if (!rc) rc = dalloc(&q16, (size_t)nt * q);
   if (!rc) rc = dalloc(&s16, (size_t)(q / 32) * nt);
   cudaError_t e = cudaSuccess;
@@ -1632,17 +1675,34 @@ int minfer_op_attention(const float* d_q, const int32_t* d_pos, int nt, const fl
       planes[i] = sh + (int64_t)i * n_ctx * kvw;
       a.shadow[i] = planes[i];
     }
+    __half* vtp[2] = {vt, vt + kvw * vt_ld};
+    a.vt[0] = vtp[0];
+    a.vt[1] = vtp[1];
+    a.vt_ld = vt_ld;
     AttnOut out;
     out.q16 = q16;
     out.ldq = q;
     out.s16 = s16;
     out.ldqs = nt;
     out.f32 = d_o;
-    e = kv_shadow_launch(d_k, d_v, (int64_t)n_ctx * kvw, planes, 0);
-    if (e == cudaSuccess) e = attention_launch(a, out, 0);
+    e = kv_shadow_launch(d_k, d_v, (int64_t)n_ctx * kvw, planes, vtp, vt_ld, 0, (int)kvw, 0);
+    int* err = nullptr;
+    if (dalloc(&err, 1) != MINFER_OK) e = cudaErrorMemoryAllocation;
+    if (e == cudaSuccess)
+      e = attention_tc_supported(a) ? attention_tc_launch(a, out, num_sms, err, 0)
+                                    : attention_launch(a, out, 0);
+    if (e == cudaSuccess) e = cudaDeviceSynchronize();
+    int herr = 0;
+    if (e == cudaSuccess) e = cudaMemcpy(&herr, err, sizeof(int), cudaMemcpyDeviceToHost);
+    dfree(err);
+    if (e == cudaSuccess && herr != 0) {
+      snprintf(g_last_error, sizeof g_last_error, "device wait timed out (code %d)", herr);
+      e = cudaErrorLaunchTimeout;
+    }
     if (e == cudaSuccess) e = cudaDeviceSynchronize();
   }
   dfree(sh);
+  dfree(vt);
   dfree(q16);
   dfree(s16);
   if (rc) return rc;
@@ -1691,14 +1751,22 @@ int minfer_op_qknorm_rope_store(const float* d_qkv, const float* d_bias, const f
   a.eps = eps;
   __half* sh = nullptr;
   const int64_t kvw = (int64_t)n_head_kv * head_dim;
+  const int64_t vt_ld = rup(n_ctx, 64);
+  __half* vt = nullptr;
   if (!rc) rc = dalloc(&sh, (size_t)4 * n_ctx * kvw);
-  if (!rc)
+  if (!rc) rc = dalloc(&vt, (size_t)2 * kvw * vt_ld);
+  if (!rc) {
     for (int i = 0; i < 4; ++i) a.shadow[i] = sh + (int64_t)i * n_ctx * kvw;
+    a.vt[0] = vt;
+    a.vt[1] = vt + kvw * vt_ld;
+    a.vt_ld = vt_ld;
+  }
   if (!rc && e == cudaSuccess) e = rope_store_launch(a, 0);
   if (!rc && e == cudaSuccess) e = cudaDeviceSynchronize();
   dfree(dc);
   dfree(ds);
   dfree(sh);
+  dfree(vt);
   if (rc) return rc;
   CK(e);
   return MINFER_OK;

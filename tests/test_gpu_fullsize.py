@@ -20,6 +20,7 @@ import pytest
 
 import synth
 from helpers import U, check_logits, q8_sum_bound
+from stagecheck import LayerWeights, check_row_layer
 from helpers import check_q8_requant as _check_quantized
 from helpers import check_q8_sum as _check_sum
 
@@ -54,48 +55,6 @@ def _release_models():
     for m in _MODELS.values():
         m.free()
     _MODELS.clear()
-
-
-class LayerWeights:
-    """One layer's tensors, quantized by the oracle as the model loader does."""
-
-    def __init__(self, oracle_mod, cfg, layer):
-        specs = {s.name: s for s in synth.tensor_specs(cfg)}
-        self.f32 = {}
-        self.q8 = {}
-        for kind in ("attn_norm.weight", "attn_q.weight", "attn_q.bias", "attn_k.weight",
-                     "attn_k.bias", "attn_v.weight", "attn_v.bias", "attn_output.weight",
-                     "ffn_norm.weight", "ffn_gate.weight", "ffn_up.weight", "ffn_down.weight",
-                     "attn_q_norm.weight", "attn_k_norm.weight"):
-            spec = specs.get(f"blk.{layer}.{kind}")
-            if spec is None:  # a bias of a QK-norm model, or QK-norm of a plain one
-                continue
-            arr = synth.tensor_data(spec)
-            if spec.is_matrix:
-                self.q8[kind] = oracle_mod.q8_quantize(arr)
-            else:
-                self.f32[kind] = arr
-        q, k, v = (self.q8[f"attn_{x}.weight"] for x in "qkv")
-        self.q8["qkv"] = (np.concatenate([q[0], k[0], v[0]]), np.concatenate([q[1], k[1], v[1]]))
-        nq, nkv = cfg.n_head * cfg.head_dim, cfg.n_head_kv * cfg.head_dim
-        self.bias = (np.concatenate([self.f32[f"attn_{x}.bias"] for x in "qkv"]) if cfg.qkv_bias
-                     else np.zeros(nq + 2 * nkv, np.float32))
-        self.cfg = cfg
-
-    def qk_normed(self, oracle_mod, full):
-        """Q|K|V after the bias -> Q and K heads RMS-normalized (Qwen3), V as is."""
-        cfg = self.cfg
-        if not cfg.qk_norm:
-            return full
-        hd, nq, nkv = cfg.head_dim, cfg.n_head * cfg.head_dim, cfg.n_head_kv * cfg.head_dim
-        out = full.copy()
-        rows = full.shape[0]
-        out[:, :nq] = oracle_mod.rmsnorm(full[:, :nq].reshape(-1, hd), self.f32["attn_q_norm.weight"],
-                                         cfg.rms_eps).reshape(rows, nq)
-        out[:, nq:nq + nkv] = oracle_mod.rmsnorm(full[:, nq:nq + nkv].reshape(-1, hd),
-                                                 self.f32["attn_k_norm.weight"],
-                                                 cfg.rms_eps).reshape(rows, nkv)
-        return out
 
 
 def _sample_rows(nt, k, seed):
@@ -201,7 +160,8 @@ def _check_layer(oracle_mod, g, kv, cfg, layer, pos, rows, tail0=0):
 
 def _check_last_layer(oracle_mod, g, kv, cfg, pos, rows, logits):
     """Teacher-forced last layer: x codes, Q|K|V and the K/V rows of sampled
-    rows, then the last token through attention, FFN, output norm and head."""
+    rows, then the last token stage by stage through attention, FFN, output
+    norm and head."""
     L = cfg.n_layer - 1
     nt = len(pos)
     ntp = (nt + 127) // 128 * 128
@@ -225,23 +185,14 @@ def _check_last_layer(oracle_mod, g, kv, cfg, pos, rows, logits):
     assert np.array_equal(_kv_rows(kv, L, 0, p), want_k)
     assert np.array_equal(_kv_rows(kv, L, 1, p), full[:, q + kvw:])
 
-    # the last token, from the GPU's input to the layer and its K/V cache
-    t = -1
-    pl = p[t:]
-    ql = oracle_mod.rope(full[t:, :q], pl, nh, hd, cos_t, sin_t)
-    nctx = int(pl[0]) + 1
-    att = oracle_mod.attention(ql, pl, kv.read(L, 0, 0, nctx), kv.read(L, 1, 0, nctx), nh, nkv, hd)
-    aq, ad = oracle_mod.q8_quantize(att)
-    h = (h_in[t:] + oracle_mod.matmul_q8(aq, ad, *Wt.q8["attn_output.weight"], q))
-    h = h.astype(np.float32)
-    fq, fd = oracle_mod.q8_quantize(oracle_mod.rmsnorm(h, Wt.f32["ffn_norm.weight"], cfg.rms_eps))
-    s = oracle_mod.swiglu(oracle_mod.matmul_q8(fq, fd, *Wt.q8["ffn_gate.weight"], H),
-                          oracle_mod.matmul_q8(fq, fd, *Wt.q8["ffn_up.weight"], H))
-    sq, sd = oracle_mod.q8_quantize(s)
-    h = (h + oracle_mod.matmul_q8(sq, sd, *Wt.q8["ffn_down.weight"], cfg.n_ff)).astype(np.float32)
+    # the last token, stage by stage from the GPU's own input to each stage,
+    # then the logits from the GPU's output row of the layer
+    t = nt - 1
+    h_last = check_row_layer(oracle_mod, g, kv, cfg, Wt, L, int(pos[t]), h_in=h_in[-1:],
+                             qkv=qkv[-1:], x_captured=False)
     specs = {sp.name: sp for sp in synth.tensor_specs(cfg)}
     yq, yd = oracle_mod.q8_quantize(
-        oracle_mod.rmsnorm(h, synth.tensor_data(specs["output_norm.weight"]), cfg.rms_eps))
+        oracle_mod.rmsnorm(h_last, synth.tensor_data(specs["output_norm.weight"]), cfg.rms_eps))
     head = specs["token_embd.weight" if cfg.tied else "output.weight"]
     wq, wd = oracle_mod.q8_quantize(synth.tensor_data(head))
     want = oracle_mod.matmul_q8(yq, yd, wq, wd, H)[0]

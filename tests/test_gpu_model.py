@@ -127,59 +127,6 @@ def test_chunked_and_appended_prefill(tiny_pair):
     check_logits(lgs, lo[0])
 
 
-def _check_decode_layer(oracle_mod, g, kv, cfg, Wt, layer, p):
-    """Teacher-forced check of one layer of a single-token call: every stage
-    recomputed by the oracle from the GPU's own input to that stage."""
-    from helpers import U, check_q8_requant, check_q8_sum, q8_sum_bound
-    H, hd, nh, nkv, F = cfg.n_embd, cfg.head_dim, cfg.n_head, cfg.n_head_kv, cfg.n_ff
-    q, kvw = nh * hd, nkv * hd
-    nbH, nbq, nbF = (H + 31) // 32, (q + 31) // 32, (F + 31) // 32
-    pos = np.array([p], np.int32)
-
-    def f32(name, n):
-        return g.debug_read(name, np.empty((1, n), np.float32))
-
-    def q8(name, nb):
-        codes = g.debug_read(name + "_q8", np.empty((1, nb * 32), np.int8))
-        sc = g.debug_read(name + "_s8", np.empty((1, nb), np.float32))
-        assert np.array_equal(sc.astype(np.float16).astype(np.float32), sc)
-        return codes, sc.astype(np.float16).view(np.uint16)
-
-    h_in = f32("h_in", H)
-    xq, xd = q8("x", nbH)
-    oq, od = oracle_mod.q8_quantize(oracle_mod.rmsnorm(h_in, Wt.f32["attn_norm.weight"], cfg.rms_eps))
-    assert np.array_equal(xq, oq) and np.array_equal(xd, od), "attn_norm Q8_0"
-    qkv = f32("qkv", q + 2 * kvw)
-    check_q8_sum(oracle_mod, qkv, xq, xd, *Wt.q8["qkv"], H)
-    full = Wt.qk_normed(oracle_mod, (qkv + Wt.bias).astype(np.float32))
-    c, s_ = oracle_mod.rope_table(p + 1, hd, cfg.rope_theta)
-    want_q = oracle_mod.rope(full[:, :q], pos, nh, hd, c, s_)
-    assert np.array_equal(f32("qrot", q), want_q), "rotated Q"
-    K, V = kv.read(layer, 0, 0, p + 1), kv.read(layer, 1, 0, p + 1)
-    assert np.array_equal(K[p:], oracle_mod.rope(full[:, q:q + kvw], pos, nkv, hd, c, s_)), "K row"
-    assert np.array_equal(V[p:], full[:, q + kvw:]), "V row"
-    att = f32("att", q)
-    ref = oracle_mod.attention(want_q, pos, K, V, nh, nkv, hd)
-    assert np.abs(att - ref).max() <= 2e-5 * max(1.0, np.abs(ref).max()), "attention"
-    aq, ad = q8("att", nbq)
-    gq, gd = oracle_mod.q8_quantize(att)
-    assert np.array_equal(aq, gq) and np.array_equal(ad, gd), "attention Q8_0"
-    h_mid = f32("h_mid", H)
-    check_q8_sum(oracle_mod, h_mid, aq, ad, *Wt.q8["attn_output.weight"], q, base=h_in)
-    fq, fd = q8("f", nbH)
-    oq, od = oracle_mod.q8_quantize(oracle_mod.rmsnorm(h_mid, Wt.f32["ffn_norm.weight"], cfg.rms_eps))
-    assert np.array_equal(fq, oq) and np.array_equal(fd, od), "ffn_norm Q8_0"
-    gate = oracle_mod.matmul_q8(fq, fd, *Wt.q8["ffn_gate.weight"], H).astype(np.float64)
-    up = oracle_mod.matmul_q8(fq, fd, *Wt.q8["ffn_up.weight"], H).astype(np.float64)
-    s_ref = oracle_mod.swiglu(gate, up)
-    dg, du = (q8_sum_bound(oracle_mod, fq, fd, *Wt.q8[f"ffn_{x}.weight"], H) for x in ("gate", "up"))
-    sq, sd = q8("s", nbF)
-    check_q8_requant(oracle_mod, sq, sd, s_ref,
-                     1.1 * np.abs(up) * dg + (np.abs(gate) + 0.28) * du + 16 * U * np.abs(s_ref))
-    check_q8_sum(oracle_mod, f32("h_out", H), sq, sd, *Wt.q8["ffn_down.weight"], F, base=h_mid)
-    return f32("h_out", H)
-
-
 @pytest.mark.parametrize("which", ["qwen2", "qwen3"])
 def test_decode_steps_match_oracle(qp, oracle_mod, which):
     """Single-token calls (the decode shape: one-row GEMVs on the int8 layout)
@@ -188,7 +135,7 @@ def test_decode_steps_match_oracle(qp, oracle_mod, which):
     no other rows to average over, so end to end it would mostly measure
     whether some Q8_0 decision sits on a rounding boundary), and the logits
     from the GPU's last hidden state."""
-    from test_gpu_fullsize import LayerWeights
+    from stagecheck import LayerWeights, check_row_layer
     cfg = synth.TINY if which == "qwen2" else synth.QWEN3_TINY
     g = gpu_model(cfg)
     Ws = [LayerWeights(oracle_mod, cfg, layer) for layer in range(cfg.n_layer)]
@@ -205,7 +152,7 @@ def test_decode_steps_match_oracle(qp, oracle_mod, which):
             for layer in range(cfg.n_layer):  # the same call again: it rewrites the same rows
                 g.debug_layer(layer)
                 lg = g.prefill(kv, ids[t:t + 1], pos[t:t + 1])
-                h_last = _check_decode_layer(oracle_mod, g, kv, cfg, Ws[layer], layer, t)
+                h_last = check_row_layer(oracle_mod, g, kv, cfg, Ws[layer], layer, t)
             yq, yd = oracle_mod.q8_quantize(oracle_mod.rmsnorm(h_last, out_norm, cfg.rms_eps))
             check_logits(lg, oracle_mod.matmul_q8(yq, yd, wq, wd, cfg.n_embd)[0])
     finally:
@@ -220,7 +167,8 @@ def test_several_logits_rows_match_oracle(qp, oracle_mod, which):
     stage by stage on those rows (a Q8_0 decision of one row on a rounding
     boundary would otherwise dominate), and every logits row against the
     oracle's final norm and lm_head of the GPU's last hidden state."""
-    from test_gpu_fullsize import LayerWeights, _check_layer
+    from stagecheck import LayerWeights
+    from test_gpu_fullsize import _check_layer
     cfg = synth.TINY if which == "qwen2" else synth.QWEN3_TINY
     g = gpu_model(cfg)
     w = synth.WORKLOADS["tiny-32"]

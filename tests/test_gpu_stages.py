@@ -119,7 +119,12 @@ def test_gemm_swiglu_quantize(qp, oracle_mod, M, F, K):
 
 @pytest.mark.parametrize("nh,nkv,hd,nt,n_ctx,p0", [(4, 2, 64, 37, 64, 0), (14, 2, 64, 100, 160, 0),
                                                     (12, 2, 128, 50, 200, 120),
-                                                    (28, 4, 128, 33, 64, 7)])
+                                                    (28, 4, 128, 33, 64, 7),
+                                                    # 64 rows and more: the tensor-core kernel
+                                                    (14, 2, 64, 300, 512, 0),
+                                                    (12, 2, 128, 257, 640, 200),
+                                                    (16, 8, 128, 129, 256, 7),
+                                                    (28, 4, 128, 640, 704, 0)])
 def test_attention_vs_oracle(qp, oracle_mod, nh, nkv, hd, nt, n_ctx, p0):
     rng = np.random.default_rng(nh * hd + nt)
     q = rng.normal(0, 1, (nt, nh * hd)).astype(np.float32)
