@@ -255,8 +255,8 @@ int minfer_op_gemm_swiglu(const int8_t* d_xq, const uint16_t* d_xd, int64_t M,
  * rows 0..=pos[t] with scale 1/sqrt(head_dim) ("09 · Prefill", section 2.2;
  * "05 · Graph build", section 2.5). o [nt][n_head*head_dim] f32.  Calls of
  * 64 rows and more run the tensor-core kernel, shorter ones the mma.sync
- * kernel (the prefill uses the tensor-core kernel only when its 128-row
- * CTAs fill half of the GPU), so the stage tests reach both. */
+ * kernel (the prefill uses the tensor-core kernel from 128 rows on), so the
+ * stage tests reach both. */
 int minfer_op_attention(const float* d_q, const int32_t* d_pos, int nt, const float* d_k,
                         const float* d_v, int n_ctx, int n_head, int n_head_kv, int head_dim,
                         float* d_o);

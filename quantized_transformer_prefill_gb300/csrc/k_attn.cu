@@ -233,20 +233,26 @@ __global__ void __launch_bounds__(256) attn_kernel(const AttnArgs a, const AttnO
     float s[4][4];
 #pragma unroll
     for (int nt = 0; nt < 4; ++nt) s[nt][0] = s[nt][1] = s[nt][2] = s[nt][3] = 0.f;
+    // the three products of one accumulator are issued four MMAs apart (one
+    // per key group), so consecutive mma.sync never wait on each other
 #pragma unroll
     for (int kk = 0; kk < HD / 16; ++kk) {
+      uint32_t bh[4][2], bl[4][2];
 #pragma unroll
       for (int nt = 0; nt < 4; ++nt) {
         const __half* kh = Kh + (nt * 8 + qr) * T::RS + kk * 16 + qc;
         const __half* kl = Kl + (nt * 8 + qr) * T::RS + kk * 16 + qc;
-        const uint32_t bh0 = *reinterpret_cast<const uint32_t*>(kh);
-        const uint32_t bh1 = *reinterpret_cast<const uint32_t*>(kh + 8);
-        const uint32_t bl0 = *reinterpret_cast<const uint32_t*>(kl);
-        const uint32_t bl1 = *reinterpret_cast<const uint32_t*>(kl + 8);
-        mma16816(s[nt], qh[kk], bh0, bh1);
-        mma16816(s[nt], qh[kk], bl0, bl1);
-        mma16816(s[nt], ql[kk], bh0, bh1);
+        bh[nt][0] = *reinterpret_cast<const uint32_t*>(kh);
+        bh[nt][1] = *reinterpret_cast<const uint32_t*>(kh + 8);
+        bl[nt][0] = *reinterpret_cast<const uint32_t*>(kl);
+        bl[nt][1] = *reinterpret_cast<const uint32_t*>(kl + 8);
       }
+#pragma unroll
+      for (int nt = 0; nt < 4; ++nt) mma16816(s[nt], qh[kk], bh[nt][0], bh[nt][1]);
+#pragma unroll
+      for (int nt = 0; nt < 4; ++nt) mma16816(s[nt], qh[kk], bl[nt][0], bl[nt][1]);
+#pragma unroll
+      for (int nt = 0; nt < 4; ++nt) mma16816(s[nt], ql[kk], bh[nt][0], bh[nt][1]);
     }
 
     // mask, online softmax
@@ -292,21 +298,25 @@ __global__ void __launch_bounds__(256) attn_kernel(const AttnArgs a, const AttnO
       split2(p2, p3, ph[ks][hi8 * 2 + 1], pl[ks][hi8 * 2 + 1]);
     }
     // O += P V: B fragments of V (keys x dims) by transposing ldmatrix
+    // four output tiles per group, their three products interleaved as above
 #pragma unroll
     for (int ks = 0; ks < 2; ++ks) {
 #pragma unroll
-      for (int nd = 0; nd < HD / 8; nd += 2) {
-        const uint32_t off =
-            2u * (uint32_t)((ks * 16 + (mi & 1) * 8 + mr) * T::RS + nd * 8 + (mi >> 1) * 8);
-        uint32_t h0, h1, h2, h3, l0, l1, l2, l3;
-        ldsm_x4_t(vh_base + off, h0, h1, h2, h3);
-        ldsm_x4_t(vl_base + off, l0, l1, l2, l3);
-        mma16816(o[nd], ph[ks], h0, h1);
-        mma16816(o[nd], ph[ks], l0, l1);
-        mma16816(o[nd], pl[ks], h0, h1);
-        mma16816(o[nd + 1], ph[ks], h2, h3);
-        mma16816(o[nd + 1], ph[ks], l2, l3);
-        mma16816(o[nd + 1], pl[ks], h2, h3);
+      for (int ng = 0; ng < HD / 8; ng += 4) {
+        uint32_t vh[8], vl[8];
+#pragma unroll
+        for (int p2 = 0; p2 < 2; ++p2) {
+          const uint32_t off = 2u * (uint32_t)((ks * 16 + (mi & 1) * 8 + mr) * T::RS +
+                                               (ng + 2 * p2) * 8 + (mi >> 1) * 8);
+          ldsm_x4_t(vh_base + off, vh[4 * p2], vh[4 * p2 + 1], vh[4 * p2 + 2], vh[4 * p2 + 3]);
+          ldsm_x4_t(vl_base + off, vl[4 * p2], vl[4 * p2 + 1], vl[4 * p2 + 2], vl[4 * p2 + 3]);
+        }
+#pragma unroll
+        for (int t = 0; t < 4; ++t) mma16816(o[ng + t], ph[ks], vh[2 * t], vh[2 * t + 1]);
+#pragma unroll
+        for (int t = 0; t < 4; ++t) mma16816(o[ng + t], ph[ks], vl[2 * t], vl[2 * t + 1]);
+#pragma unroll
+        for (int t = 0; t < 4; ++t) mma16816(o[ng + t], pl[ks], vh[2 * t], vh[2 * t + 1]);
       }
     }
     __syncthreads();  // the next prefetch overwrites this stage's buffer

@@ -15,13 +15,16 @@
 //   S  = Qh.Kh^T + Qh.Kl^T + Ql.Kh^T        M = 128 rows, N = 64 keys, K = hd
 //   Ot = Ph.Vh + Ph.Vl + Pl.Vh              M = 128 rows, N = hd, K = 64 keys
 // warp 0 streams K (hi/lo, from the fp16 shadow planes) and V^T (hi/lo, from
-// the transposed planes) tiles with TMA into two-stage rings; warp 1 issues
-// the MMAs from one thread into TMEM (two S buffers and one O tile); warps
-// 2-5 own one query row per thread: they write Q's hi/lo into shared memory,
-// read each S row from TMEM, apply the causal mask and the online softmax
-// (log2 units, running max and sum in registers), write P's hi/lo into
-// shared memory for the P.V MMA, and fold each O tile into an f32 row held
-// in registers.  S of tile j+1 is computed while tile j's softmax runs.
+// the transposed planes) tiles with TMA into two-stage rings; one thread of
+// warp 1 issues the S MMAs into two TMEM buffers, one thread of warp 6 the
+// P.V MMAs, which accumulate O in TMEM over all key tiles; warps 2-5 own one
+// query row per thread: they write Q's hi/lo into shared memory, read each S
+// row from TMEM, apply the causal mask and the online softmax (log2 units,
+// reference max and sum in registers), and write P's hi/lo into shared
+// memory for the P.V MMA.  The reference max moves only when a row's scores
+// rise more than 2^8 above it; O in TMEM is then rescaled in place before the
+// next P.V.  S of tile j+1 is computed while tile j's softmax runs, and P of
+// tile j+1 while P.V of tile j runs.
 // With few row tiles the key range is split over the CTAs of a cluster,
 // merged through distributed shared memory as in k_attn.cu.  The output row
 // is normalized and each 32-block quantized to Q8_0 by its own thread.
@@ -39,10 +42,17 @@ namespace {
 
 constexpr int kTcRows = 128;    // query rows per CTA (MMA M)
 constexpr int kTcKeys = 64;     // keys per tile (N of the S MMA, K of the P.V MMA)
-constexpr int kTcThreads = 192;  // TMA warp, MMA warp, four softmax warps
+constexpr int kTcThreads = 224;  // TMA warp, S issuer, four softmax warps, P.V issuer
+constexpr int kPvWarp = 6;
 constexpr int kTcMaxSplits = 8;  // CTAs per cluster (portable cluster size)
 
 enum : int { kDevTimeoutAttn = 6 };
+// Largest rise of a row's scores over its reference max (log2 units) that is
+// absorbed without rescaling O: P then stays below 2^8.
+constexpr float kLazyMax = 8.0f;
+// Key tiles accumulated by the tensor core into T before T is folded into R.
+constexpr int kFoldTiles = 4;
+constexpr uint32_t kTcolT = 128;  // TMEM column of T; R follows at kTcolT + hd
 
 template <int HD>
 struct TcCfg {
@@ -59,7 +69,7 @@ struct TcCfg {
   static constexpr int OFF_V = OFF_K + STAGES * 2 * K_BYTES;  // stage s: hi, lo
   static constexpr int OFF_P = OFF_V + STAGES * 2 * V_BYTES;  // hi, lo
   static constexpr int OFF_BAR = OFF_P + 2 * P_BYTES;
-  static constexpr int NBAR = 4 * STAGES + 4 + 4 + 2;
+  static constexpr int NBAR = 4 * STAGES + 4 + 3 + 3;
   static constexpr int OFF_TMEM = OFF_BAR + NBAR * 8;
   static constexpr int SMEM = OFF_TMEM + 16 + 1024;
   // the split-merge partials reuse the K/V rings: o [128 rows][hd], then
@@ -68,8 +78,9 @@ struct TcCfg {
   static_assert(kTcRows * (HD + 2) * 4 <= OFF_P - OFF_K, "partials fit the K/V rings");
   static_assert(OFF_K % 1024 == 0 && OFF_V % 1024 == 0 && OFF_P % 1024 == 0, "1024-B alignment");
   static_assert(SMEM <= 227 * 1024, "shared memory budget");
-  // TMEM columns: S buffers at 0 and 64, the O tile at 128
-  static constexpr uint32_t TCOLS = 256;
+  // TMEM columns: S buffers at 0 and 64, the accumulating O part T at 128,
+  // the folded part R after it
+  static constexpr uint32_t TCOLS = 128 + 2 * HD <= 256 ? 256 : 512;
 };
 
 struct TcArgs {
@@ -105,9 +116,24 @@ __device__ __forceinline__ float ld_peer_tc(uint32_t addr) {
   return v;
 }
 
-__device__ __forceinline__ uint32_t pack_half2(__half a, __half b) {
-  return (uint32_t)__half_as_ushort(a) | ((uint32_t)__half_as_ushort(b) << 16);
+// 32 lanes x 32 columns of 32-bit TMEM words from registers (thread i -> row
+// lane base + i), and the wait for this thread's TMEM stores.
+__device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&r)[32]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], "
+      "{%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,"
+      "%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32};" ::"r"(taddr),
+      "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]),
+      "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]),
+      "r"(r[15]), "r"(r[16]), "r"(r[17]), "r"(r[18]), "r"(r[19]), "r"(r[20]), "r"(r[21]),
+      "r"(r[22]), "r"(r[23]), "r"(r[24]), "r"(r[25]), "r"(r[26]), "r"(r[27]), "r"(r[28]),
+      "r"(r[29]), "r"(r[30]), "r"(r[31])
+      : "memory");
 }
+__device__ __forceinline__ void tmem_wait_st() {
+  asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+}
+
 
 template <int HD, bool kGemvOut>
 __global__ void __launch_bounds__(kTcThreads, 1)
@@ -115,6 +141,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                    const __grid_constant__ CUtensorMap tmVh, const __grid_constant__ CUtensorMap tmVl,
                    const TcArgs a, const AttnOut out) {
   using C = TcCfg<HD>;
+  constexpr uint32_t kTcolR = kTcolT + (uint32_t)HD;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~uintptr_t(1023));
@@ -125,10 +152,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   uint64_t* sready = vempty + C::STAGES;  // [2]
   uint64_t* sfree = sready + 2;           // [2]
   uint64_t* pready = sfree + 2;
-  uint64_t* ofree = pready + 1;
-  uint64_t* oready = ofree + 1;
+  uint64_t* oready = pready + 1;
   uint64_t* qready = oready + 1;
-  uint64_t* mdone = qready + 1;  // all MMAs of the CTA completed (before TMEM is freed)
+  uint64_t* mdone = qready + 1;  // [2] each issuer's MMAs completed (before TMEM is freed)
   uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(smem + C::OFF_TMEM);
   __shared__ int s_maxp;
 
@@ -153,10 +179,10 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       mbar_init(&sfree[b], 4);
     }
     mbar_init(pready, 4);
-    mbar_init(ofree, 4);
     mbar_init(oready, 1);
     mbar_init(qready, 4);
-    mbar_init(mdone, 1);
+    mbar_init(&mdone[0], 1);
+    mbar_init(&mdone[1], 1);
     fence_barrier_init();
     tma_prefetch_desc(&tmKh);
     tma_prefetch_desc(&tmKl);
@@ -230,15 +256,17 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         }
       }
     }
-  } else if (warp == 1) {
-    // ---------------------------------------------------------- MMA issuer
+  } else if (warp == 1 || warp == kPvWarp) {
+    // ---------------------------------------------------------- MMA issuers
+    // One thread issues about one MMA per 70 cycles whatever its N, so S =
+    // Q.K^T (warp 1) and O += P.V (warp 6) have an issuing thread each.
     if (lane == 0 && ntile > 0) {
       constexpr uint32_t idS = idesc_f16_f32(kTcRows, kTcKeys);
       constexpr uint32_t idO = idesc_f16_f32(kTcRows, HD);
       const uint32_t qh = smem_u32(sQh), ql = smem_u32(sQl);
       const uint32_t ph = smem_u32(sP), pl = smem_u32(sP + C::P_BYTES);
-      const uint32_t tO = tmem_base + 128;
-      bool ok = mbar_wait(qready, 0, a.err, kDevTimeoutAttn);
+      const uint32_t tO = tmem_base + kTcolT;
+      bool ok = true;
       bool committed = false;
       auto issue_s = [&](int j) -> bool {
         const int st = j % C::STAGES, b = j & 1;
@@ -268,7 +296,6 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       auto issue_pv = [&](int j) -> bool {
         const int st = j % C::STAGES;
         if (!mbar_wait(pready, j & 1, a.err, kDevTimeoutAttn)) return false;
-        if (!mbar_wait(ofree, (j & 1) ^ 1, a.err, kDevTimeoutAttn)) return false;
         if (!mbar_wait(&vfull[st], (j / C::STAGES) & 1, a.err, kDevTimeoutAttn)) return false;
         tc_fence_after();
         const uint32_t vh = smem_u32(smem + C::OFF_V + st * 2 * C::V_BYTES);
@@ -280,23 +307,28 @@ __global__ void __launch_bounds__(kTcThreads, 1)
 #pragma unroll
           for (int k = 0; k < kTcKeys / 16; ++k) {
             const uint32_t off = (uint32_t)(k * 32);
+            // T accumulates over the key tiles since the last fold (rescaled in
+            // place by the softmax warps); the first tile after a fold restarts it
             tc_mma_f16(tO, smem_desc_sw128(A + off), smem_desc_sw128(B + off), idO,
-                       (c == 0 && k == 0) ? 0u : 1u);
+                       (j % kFoldTiles == 0 && c == 0 && k == 0) ? 0u : 1u);
           }
         }
         tc_commit(oready);
         tc_commit(&vempty[st]);
+        committed = true;
         return true;
       };
-      if (ok) ok = issue_s(0);
-      for (int j = 0; j < ntile && ok; ++j) {
-        if (j + 1 < ntile) ok = issue_s(j + 1);
-        if (ok) ok = issue_pv(j);
+      if (warp == 1) {
+        ok = mbar_wait(qready, 0, a.err, kDevTimeoutAttn);
+        for (int j = 0; j < ntile && ok; ++j) ok = issue_s(j);
+      } else {
+        for (int j = 0; j < ntile && ok; ++j) ok = issue_pv(j);
       }
-      // every MMA issued must have landed before TMEM is released
+      // every MMA this thread issued must have landed before TMEM is released
       if (committed) {
-        tc_commit(mdone);
-        mbar_wait(mdone, 0, a.err, kDevTimeoutAttn);
+        uint64_t* md = &mdone[warp == 1 ? 0 : 1];
+        tc_commit(md);
+        mbar_wait(md, 0, a.err, kDevTimeoutAttn);
       }
     }
   } else {
@@ -325,10 +357,11 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         uint32_t hi[4], lo[4];
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
-          const __half h0 = __float2half_rn(x[2 * i]), h1 = __float2half_rn(x[2 * i + 1]);
-          hi[i] = pack_half2(h0, h1);
-          lo[i] = pack_half2(__float2half_rn(__fsub_rn(x[2 * i], __half2float(h0))),
-                             __float2half_rn(__fsub_rn(x[2 * i + 1], __half2float(h1))));
+          const __half2 hh = __floats2half2_rn(x[2 * i], x[2 * i + 1]);
+          const float2 hf = __half22float2(hh);
+          const __half2 lw = __floats2half2_rn(__fsub_rn(x[2 * i], hf.x), __fsub_rn(x[2 * i + 1], hf.y));
+          hi[i] = *reinterpret_cast<const uint32_t*>(&hh);
+          lo[i] = *reinterpret_cast<const uint32_t*>(&lw);
         }
         const int d0 = c8 * 8;
         const uint32_t off = (uint32_t)((d0 >> 6) * C::QSUB) + sw128_off(rl, d0 & 63);
@@ -340,10 +373,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       if (lane == 0) mbar_arrive(qready);
     }
 
-    float o[HD];
-#pragma unroll
-    for (int d = 0; d < HD; ++d) o[d] = 0.f;
-    float m = -INFINITY, l = 0.f;
+    float m = -INFINITY, l = 0.f;  // reference max (log2 units) and sum of P against it
     // scores in log2 units: s2 = (q.k) / sqrt(hd) * log2(e)
     const float sc = __fmul_rn(__fdiv_rn(1.0f, __fsqrt_rn((float)HD)), 1.4426950408889634f);
     bool ok = true;
@@ -363,57 +393,118 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&sfree[b]);
-      const int key0 = kbeg + j * kTcKeys;
-      float mx = -INFINITY;
+      const int nvalid = pr - (kbeg + j * kTcKeys);  // keys c <= nvalid are visible
+      float mx4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
 #pragma unroll
       for (int c = 0; c < kTcKeys; ++c) {
-        const float s2 = (key0 + c <= pr) ? __fmul_rn(__uint_as_float(sr[c]), sc) : -INFINITY;
+        const float s2 = (c <= nvalid) ? __fmul_rn(__uint_as_float(sr[c]), sc) : -INFINITY;
         sr[c] = __float_as_uint(s2);
-        mx = fmaxf(mx, s2);
+        mx4[c & 3] = fmaxf(mx4[c & 3], s2);
       }
-      const float mn = fmaxf(m, mx);
-      const float alpha = (mn == -INFINITY) ? 1.f : exp2f(m - mn);
-      m = mn;
-      l *= alpha;
-      // P row -> fp16 hi/lo tiles (the P buffer is free: the previous P.V completed)
+      const float mx = fmaxf(fmaxf(mx4[0], mx4[1]), fmaxf(mx4[2], mx4[3]));
+      // The reference max moves only when a score exceeds it by more than
+      // kLazyMax (P stays below 2^kLazyMax, well inside f32 and fp16); the O
+      // accumulated in TMEM and the sum l are then rescaled by alpha.
+      float alpha = 1.f;
+      bool resc = false;
+      if (mx > m + kLazyMax) {
+        if (m != -INFINITY) {
+          alpha = exp2f(m - mx);
+          resc = true;
+        }
+        m = mx;
+        l *= alpha;
+      }
+      // P row -> fp16 hi/lo words, held until the P buffer is free.  A row
+      // whose reference max is still -inf has only -inf scores: exp2(-inf) = 0.
+      const float mref = (m == -INFINITY) ? 0.f : m;
+      uint32_t hi[kTcKeys / 2], lo[kTcKeys / 2];
+      float l4[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+      for (int i = 0; i < kTcKeys / 2; ++i) {
+        const float p0 = exp2f(__fsub_rn(__uint_as_float(sr[2 * i]), mref));
+        const float p1 = exp2f(__fsub_rn(__uint_as_float(sr[2 * i + 1]), mref));
+        l4[i & 3] += __fadd_rn(p0, p1);
+        const __half2 h = __floats2half2_rn(p0, p1);
+        const float2 hf = __half22float2(h);
+        const __half2 lw = __floats2half2_rn(__fsub_rn(p0, hf.x), __fsub_rn(p1, hf.y));
+        hi[i] = *reinterpret_cast<const uint32_t*>(&h);
+        lo[i] = *reinterpret_cast<const uint32_t*>(&lw);
+      }
+      l += (l4[0] + l4[1]) + (l4[2] + l4[3]);
+      // the previous P.V has read the P buffer and finished writing O
+      if (j > 0) {
+        if (!mbar_wait(oready, (j - 1) & 1, a.err, kDevTimeoutAttn)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        // O = R + T: T is what the tensor core accumulated since the last fold,
+        // R (TMEM too) the sum of the folded parts.  Every kFoldTiles tiles T is
+        // added into R with round-to-nearest f32 adds, and the next P.V starts
+        // T afresh, so no long sum builds up inside the tensor core.
+        const bool fold = (j % kFoldTiles) == 0;
+        const bool has_r = j > kFoldTiles;  // an earlier fold wrote R
+        if (fold || __any_sync(0xffffffffu, resc)) {
+#pragma unroll
+          for (int d0 = 0; d0 < HD; d0 += 32) {
+            uint32_t t[32], rr[32];
+            tmem_ld32(tmem_base + lanebase + kTcolT + (uint32_t)d0, t);
+            if (has_r) tmem_ld32(tmem_base + lanebase + kTcolR + (uint32_t)d0, rr);
+            tmem_wait_ld();
+#pragma unroll
+            for (int i = 0; i < 32; ++i) {
+              const float rv = has_r ? __uint_as_float(rr[i]) : 0.f;
+              const float tv = __uint_as_float(t[i]);
+              if (fold) {
+                rr[i] = __float_as_uint(__fmul_rn(__fadd_rn(rv, tv), alpha));
+              } else {
+                // rows whose reference max moved: O *= alpha (alpha = 1 elsewhere)
+                rr[i] = __float_as_uint(__fmul_rn(rv, alpha));
+                t[i] = __float_as_uint(__fmul_rn(tv, alpha));
+              }
+            }
+            if (fold || has_r) tmem_st32(tmem_base + lanebase + kTcolR + (uint32_t)d0, rr);
+            if (!fold) tmem_st32(tmem_base + lanebase + kTcolT + (uint32_t)d0, t);
+          }
+          tmem_wait_st();
+        }
+      }
 #pragma unroll
       for (int c8 = 0; c8 < kTcKeys / 8; ++c8) {
-        uint32_t hi[4], lo[4];
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          const float s0 = __uint_as_float(sr[c8 * 8 + 2 * i]);
-          const float s1 = __uint_as_float(sr[c8 * 8 + 2 * i + 1]);
-          const float p0 = (s0 == -INFINITY) ? 0.f : exp2f(s0 - m);
-          const float p1 = (s1 == -INFINITY) ? 0.f : exp2f(s1 - m);
-          l += p0 + p1;
-          const __half h0 = __float2half_rn(p0), h1 = __float2half_rn(p1);
-          hi[i] = pack_half2(h0, h1);
-          lo[i] = pack_half2(__float2half_rn(__fsub_rn(p0, __half2float(h0))),
-                             __float2half_rn(__fsub_rn(p1, __half2float(h1))));
-        }
         const uint32_t off = sw128_off(rl, c8 * 8);
-        *reinterpret_cast<uint4*>(sP + off) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
-        *reinterpret_cast<uint4*>(sP + C::P_BYTES + off) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
+        *reinterpret_cast<uint4*>(sP + off) =
+            make_uint4(hi[4 * c8], hi[4 * c8 + 1], hi[4 * c8 + 2], hi[4 * c8 + 3]);
+        *reinterpret_cast<uint4*>(sP + C::P_BYTES + off) =
+            make_uint4(lo[4 * c8], lo[4 * c8 + 1], lo[4 * c8 + 2], lo[4 * c8 + 3]);
       }
       fence_proxy_async_smem();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(pready);
-      if (!mbar_wait(oready, j & 1, a.err, kDevTimeoutAttn)) {
-        ok = false;
-        break;
-      }
-      tc_fence_after();
-#pragma unroll
-      for (int d0 = 0; d0 < HD; d0 += 32) {
-        uint32_t ot[32];
-        tmem_ld32(tmem_base + lanebase + 128u + (uint32_t)d0, ot);
-        tmem_wait_ld();
-#pragma unroll
-        for (int i = 0; i < 32; ++i) o[d0 + i] = fmaf(o[d0 + i], alpha, __uint_as_float(ot[i]));
-      }
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(ofree);
+      if (lane == 0) mbar_arrive(pready);
+    }
+    // the last P.V completes the O tile
+    float o[HD];
+#pragma unroll
+    for (int d = 0; d < HD; ++d) o[d] = 0.f;
+    if (ok && ntile > 0) {
+      if (!mbar_wait(oready, (ntile - 1) & 1, a.err, kDevTimeoutAttn)) {
+        ok = false;
+      } else {
+        tc_fence_after();
+        const bool has_r = ntile - 1 >= kFoldTiles;  // some tile folded T into R
+#pragma unroll
+        for (int d0 = 0; d0 < HD; d0 += 32) {
+          uint32_t t[32], rr[32];
+          tmem_ld32(tmem_base + lanebase + kTcolT + (uint32_t)d0, t);
+          if (has_r) tmem_ld32(tmem_base + lanebase + kTcolR + (uint32_t)d0, rr);
+          tmem_wait_ld();
+#pragma unroll
+          for (int i = 0; i < 32; ++i)
+            o[d0 + i] = has_r ? __fadd_rn(__uint_as_float(rr[i]), __uint_as_float(t[i]))
+                              : __uint_as_float(t[i]);
+        }
+      }
     }
 
     // ------------------------------------------------------- merge + output
@@ -444,9 +535,18 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           out.s8[orow * nb + blk] = d16;
         } else {
 #pragma unroll
-          for (int i = 0; i < 32; i += 2)
-            *reinterpret_cast<__half2*>(out.q16 + orow * out.ldq + k0 + i) =
-                __floats2half2_rn(q8_code(y[i], id), q8_code(y[i + 1], id));
+          for (int i = 0; i < 32; i += 8) {
+            uint4 w;
+            __half2 c0 = __floats2half2_rn(q8_code(y[i], id), q8_code(y[i + 1], id));
+            __half2 c1 = __floats2half2_rn(q8_code(y[i + 2], id), q8_code(y[i + 3], id));
+            __half2 c2 = __floats2half2_rn(q8_code(y[i + 4], id), q8_code(y[i + 5], id));
+            __half2 c3 = __floats2half2_rn(q8_code(y[i + 6], id), q8_code(y[i + 7], id));
+            w.x = *reinterpret_cast<uint32_t*>(&c0);
+            w.y = *reinterpret_cast<uint32_t*>(&c1);
+            w.z = *reinterpret_cast<uint32_t*>(&c2);
+            w.w = *reinterpret_cast<uint32_t*>(&c3);
+            *reinterpret_cast<uint4*>(out.q16 + orow * out.ldq + k0 + i) = w;
+          }
           out.s16[(int64_t)blk * out.ldqs + orow] = d16;
         }
       }
@@ -476,11 +576,23 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     for (int rl = split + warp * ns; rl < kTcRows; rl += ns * (kTcThreads / 32)) {
       const int r = rbase + rl;
       if (r >= a.r1) continue;  // warp-uniform
+      // every remote load of the row in flight at once: (max, sum) of split
+      // `lane` and this lane's values of every split
       float ms = -INFINITY, ls = 0.f;
       if (lane < ns) {
         const uint32_t ml = peer_addr_tc(po_s + (uint32_t)((C::PART_ML + rl * 2) * 4), (uint32_t)lane);
         ms = ld_peer_tc(ml);
         ls = ld_peer_tc(ml + 4);
+      }
+      float xs[kTcMaxSplits][VPL];
+#pragma unroll
+      for (int sdx = 0; sdx < kTcMaxSplits; ++sdx) {
+        if (sdx < ns) {
+          const uint32_t pa =
+              peer_addr_tc(po_s + (uint32_t)((rl * HD + lane * VPL) * 4), (uint32_t)sdx);
+#pragma unroll
+          for (int i = 0; i < VPL; ++i) xs[sdx][i] = ld_peer_tc(pa + 4u * i);
+        }
       }
       float M = ms;
 #pragma unroll
@@ -492,12 +604,12 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       float y[VPL];
 #pragma unroll
       for (int i = 0; i < VPL; ++i) y[i] = 0.f;
-      for (int sdx = 0; sdx < ns; ++sdx) {
-        const float w = __shfl_sync(0xffffffffu, wl, sdx);
-        const uint32_t pa =
-            peer_addr_tc(po_s + (uint32_t)((rl * HD + lane * VPL) * 4), (uint32_t)sdx);
 #pragma unroll
-        for (int i = 0; i < VPL; ++i) y[i] = fmaf(ld_peer_tc(pa + 4u * i), w, y[i]);
+      for (int sdx = 0; sdx < kTcMaxSplits; ++sdx) {
+        const float w = __shfl_sync(0xffffffffu, wl, sdx);
+        if (sdx < ns)
+#pragma unroll
+          for (int i = 0; i < VPL; ++i) y[i] = fmaf(xs[sdx][i], w, y[i]);
       }
       const float inv = L > 0.f ? __fdiv_rn(1.0f, L) : 0.f;
       float amax = 0.f;
@@ -546,14 +658,17 @@ bool attention_tc_supported(const AttnArgs& a) {
 }
 
 bool attention_tc_preferred(int rows, int nh, int num_sms) {
-  // short prompts: too few (128-row tile, head) CTAs to fill the GPU; the
-  // mma.sync kernel's 16-row tiles spread them better
-  return 2 * ((rows + kTcRows - 1) / kTcRows) * nh >= num_sms;
+  // from one full 128-row tile on; shorter calls keep the mma.sync kernel's
+  // 16-row tiles
+  (void)nh;
+  (void)num_sms;
+  return rows >= kTcRows;
 }
 
 int attention_tc_nsplit(int rows, int nh, int num_sms) {
   const int ctas = (rows + kTcRows - 1) / kTcRows * nh;
-  if (2 * ctas >= num_sms) return 1;
+  // a key split pays for its merge only when the CTAs are very few
+  if (3 * ctas >= num_sms) return 1;
   const int ns = (num_sms + ctas - 1) / std::max(ctas, 1);
   return ns < 1 ? 1 : (ns > kTcMaxSplits ? kTcMaxSplits : ns);
 }

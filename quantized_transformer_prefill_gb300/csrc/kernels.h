@@ -181,8 +181,7 @@ struct AttnOut {
 // head_dim 64 or 128: one CTA per (128 rows, query head, key split); err is the
 // device status word of timed-out waits.
 bool attention_tc_supported(const AttnArgs& a);
-// Whether the forward picks it: its (128-row tile, head) CTAs fill at least
-// half of the SMs.
+// Whether the forward picks it: from one full 128-row tile on.
 bool attention_tc_preferred(int rows, int nh, int num_sms);
 cudaError_t attention_tc_launch(const AttnArgs& a, const AttnOut& out, int num_sms, int* err,
                                 cudaStream_t stream);
