@@ -20,10 +20,8 @@
 //              stage, and the two blocks' scale rows into a separate ring
 //   warp 1     TMEM allocator and MMA issuer (one thread)
 //   warps 2-9  epilogue: warp w reads TMEM lane quadrant w % 4 (32 rows of
-//              the 128-row tile); warps 2-5 take the left half of the N
-//              tile, warps 6-9 the right half; finished f32 rows leave
-//              through a per-warp shared-memory transpose so every store
-//              writes 128 contiguous bytes
+//              the 128-row tile) in the 16x256b fragment shape; warps 2-5
+//              take the left half of the N tile, warps 6-9 the right half
 // Rings: STAGES A/B stages, free as soon as the MMAs that read them
 // completed (TMA latency is ~1.6k cycles, so refills must not wait for the
 // epilogue); SSTAGES scale stages, freed by the epilogue; NSLOT TMEM slots
@@ -48,7 +46,7 @@ constexpr int kThreads = 64 + 32 * kEpiWarps;
 
 template <int BN>
 struct Cfg {
-  static constexpr int STAGES = 5;
+  static constexpr int STAGES = 6;
   static constexpr int SSTAGES = 8;
   static constexpr int NSLOT = 512 / BN;
   static constexpr int CPW = BN / 2;  // columns per epilogue thread
@@ -62,9 +60,7 @@ struct Cfg {
   static constexpr int OFF_B = OFF_A + STAGES * A_BYTES;
   static constexpr int OFF_SA = OFF_B + STAGES * B_BYTES;
   static constexpr int OFF_SB = OFF_SA + SSTAGES * SA_BYTES;
-  static constexpr int T_FLOATS = 32 * 33;  // per-warp transpose tile
-  static constexpr int OFF_T = OFF_SB + SSTAGES * SB_BYTES;
-  static constexpr int OFF_BAR = OFF_T + kEpiWarps * T_FLOATS * 4;
+  static constexpr int OFF_BAR = OFF_SB + SSTAGES * SB_BYTES;
   static constexpr int NBAR = 2 * STAGES + 2 * SSTAGES + 2 * NSLOT;
   static constexpr int OFF_TMEM = OFF_BAR + NBAR * 8;
   static constexpr int SMEM = OFF_TMEM + 16 + 1024;  // + slack to align the base to 1024
@@ -238,11 +234,16 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else {
     // ------------------------------------------------------------ epilogue
+    // Fragment layout (tcgen05.ld 16x256b): lane l of warp w holds rows
+    // quad*32 + {g, g+8, g+16, g+24} (g = l / 4) and the column pairs
+    // 8k + 2(l % 4) + {0, 1}, k < 8, of its 64-column half.  A thread then
+    // needs 8 column scales and 4 row scales per K block instead of the 64
+    // broadcast column scales of a row-per-thread layout, which keeps the
+    // epilogue's shared-memory loads off the port the MMAs read operands from.
     const int ew = warp - 2;
     const int quad = warp & 3;
     const int half = ew >> 2;
-    const int row = quad * 32 + lane;
-    float* sT = reinterpret_cast<float*>(smem + C::OFF_T) + ew * C::T_FLOATS;
+    const int g = lane >> 2, t4 = lane & 3;
     int it = 0, sit = 0;
     bool ok = true;
     for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
@@ -252,12 +253,14 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int sp = rest / p.n_tiles;
       const int s0 = sp * p.stages_per_split;
       const int s1 = min(p.n_stages, s0 + p.stages_per_split);
-      const int m = mt * kBM + row;
+      const int mrow0 = mt * kBM + quad * 32;
       const int ncol0 = ntile * BN + half * C::CPW;
 
-      float2 acc[C::CPW / 2];
+      float2 acc[4][8];
 #pragma unroll
-      for (int j = 0; j < C::CPW / 2; ++j) acc[j] = make_float2(0.f, 0.f);
+      for (int rr = 0; rr < 4; ++rr)
+#pragma unroll
+        for (int k = 0; k < 8; ++k) acc[rr][k] = make_float2(0.f, 0.f);
 
       for (int s = s0; s < s1 && ok; ++s, ++it) {
         const int ss = it % C::SSTAGES;
@@ -273,43 +276,46 @@ __global__ void __launch_bounds__(kThreads, 1)
             break;
           }
           tc_fence_after();
-          const float da = sSA[ss * 2 * kBM + blk * kBM + row];
-          const float* dw = sSB + ss * 2 * BN + blk * BN + half * C::CPW;
           const uint32_t taddr =
               tmem_base + ((uint32_t)(quad * 32) << 16) + (uint32_t)(slot * BN + half * C::CPW);
+          uint32_t ra[32], rb[32];  // rows g, g+8 and g+16, g+24
+          tmem_ld16x256(taddr, ra);
+          tmem_ld16x256(taddr + (16u << 16), rb);
+          tmem_wait_ld();
+          // slot read: hand it back to the MMA issuer
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&tempty[slot]);
           const int b = 2 * s + blk;
+          if (EPI == kEpiDots && b < p.nb) {
 #pragma unroll
-          for (int c = 0; c < C::CPW; c += 64) {
-            // both 32-column loads in flight before one wait
-            uint32_t r[64];
-            tmem_ld32(taddr + c, *reinterpret_cast<uint32_t(*)[32]>(&r[0]));
-            tmem_ld32(taddr + c + 32, *reinterpret_cast<uint32_t(*)[32]>(&r[32]));
-            tmem_wait_ld();
-            if (c + 64 >= C::CPW) {
-              // slot fully read: hand it back to the MMA issuer
-              tc_fence_before();
-              __syncwarp();
-              if (lane == 0) mbar_arrive(&tempty[slot]);
-            }
-            if (EPI == kEpiDots && m < p.M && b < p.nb) {
+            for (int rr = 0; rr < 4; ++rr) {
+              const int m = mrow0 + g + 8 * rr;
+              if (m >= p.M) continue;
 #pragma unroll
-              for (int j = 0; j < 64; ++j) {
-                const int n = ncol0 + c + j;
-                if (n < p.N)
-                  p.dots[((int64_t)m * p.N + n) * p.nb + b] = __float2int_rn(__uint_as_float(r[j]));
-              }
+              for (int k = 0; k < 8; ++k)
+#pragma unroll
+                for (int e = 0; e < 2; ++e) {
+                  const int n = ncol0 + 8 * k + 2 * t4 + e;
+                  const uint32_t v = rr < 2 ? ra[4 * k + 2 * rr + e] : rb[4 * k + 2 * (rr - 2) + e];
+                  if (n < p.N) p.dots[((int64_t)m * p.N + n) * p.nb + b] = __float2int_rn(__uint_as_float(v));
+                }
             }
+          }
+          const float* sa = sSA + ss * 2 * kBM + blk * kBM + quad * 32 + g;
+          const float* dw = sSB + ss * 2 * BN + blk * BN + half * C::CPW + 2 * t4;
+          float2 w[8];
+#pragma unroll
+          for (int k = 0; k < 8; ++k) w[k] = *reinterpret_cast<const float2*>(dw + 8 * k);
+#pragma unroll
+          for (int rr = 0; rr < 4; ++rr) {
+            const float da = sa[8 * rr];
             const float2 da2 = make_float2(da, da);
 #pragma unroll
-            for (int j = 0; j < 64; j += 4) {
-              const float4 w4 = *reinterpret_cast<const float4*>(dw + c + j);
-              const float2 s0v = __fmul2_rn(da2, make_float2(w4.x, w4.y));
-              const float2 s1v = __fmul2_rn(da2, make_float2(w4.z, w4.w));
-              acc[(c + j) / 2] = __ffma2_rn(
-                  make_float2(__uint_as_float(r[j]), __uint_as_float(r[j + 1])), s0v, acc[(c + j) / 2]);
-              acc[(c + j) / 2 + 1] = __ffma2_rn(
-                  make_float2(__uint_as_float(r[j + 2]), __uint_as_float(r[j + 3])), s1v,
-                  acc[(c + j) / 2 + 1]);
+            for (int k = 0; k < 8; ++k) {
+              const uint32_t* rv = rr < 2 ? &ra[4 * k + 2 * rr] : &rb[4 * k + 2 * (rr - 2)];
+              acc[rr][k] = __ffma2_rn(make_float2(__uint_as_float(rv[0]), __uint_as_float(rv[1])),
+                                      __fmul2_rn(da2, w[k]), acc[rr][k]);
             }
           }
           ++sit;
@@ -323,56 +329,55 @@ __global__ void __launch_bounds__(kThreads, 1)
 
       // ---------------------------------------------------------- store
       if (EPI == kEpiSwiGLU) {
-        if (m < p.M) {
-          // columns come in groups of 64: 32 gate then 32 up rows of W
+        // the warp's 64 columns hold 32 gate (k < 4) then 32 up (k >= 4) rows
+        // of W for the same 32 outputs j0..j0+31: one Q8_0 block per row,
+        // spread over the four lanes of a quad
+        const int64_t j0 = (int64_t)ncol0 / 2;
+        if (j0 < p.n_out_cols) {
 #pragma unroll
-          for (int g0 = 0; g0 < C::CPW; g0 += 64) {
-            const int64_t j0 = (int64_t)(ncol0 + g0) / 2;  // first SwiGLU output of the group
-            if (j0 >= p.n_out_cols) continue;
-            float sv[32];
+          for (int rr = 0; rr < 4; ++rr) {
+            const int m = mrow0 + g + 8 * rr;
+            float sv[8];
             float amax = 0.f;
 #pragma unroll
-            for (int i = 0; i < 32; ++i) {
-              const float gg = (i & 1) ? acc[(g0 + i) / 2].y : acc[(g0 + i) / 2].x;
-              const float uu = (i & 1) ? acc[(g0 + 32 + i) / 2].y : acc[(g0 + 32 + i) / 2].x;
-              sv[i] = silu_mul(gg, uu);
-              amax = fmaxf(amax, fabsf(sv[i]));
+            for (int k = 0; k < 4; ++k) {
+              sv[2 * k] = silu_mul(acc[rr][k].x, acc[rr][k + 4].x);
+              sv[2 * k + 1] = silu_mul(acc[rr][k].y, acc[rr][k + 4].y);
+              amax = fmaxf(amax, fmaxf(fabsf(sv[2 * k]), fabsf(sv[2 * k + 1])));
             }
+            amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
+            amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 2));
+            if (m >= p.M) continue;
             const float d = __fdiv_rn(amax, 127.0f);
             const float id = q8_inv(d);
-            __half* dst = p.q_out + (int64_t)m * p.ldq + j0;
+            __half* dst = p.q_out + (int64_t)m * p.ldq + j0 + 2 * t4;
 #pragma unroll
-            for (int i = 0; i < 32; i += 8) {
-              __align__(16) __half hq[8];
-#pragma unroll
-              for (int k = 0; k < 8; ++k) hq[k] = __float2half_rn(q8_code(sv[i + k], id));
-              *reinterpret_cast<uint4*>(dst + i) = *reinterpret_cast<const uint4*>(hq);
-            }
-            p.qs_out[(j0 / 32) * p.ldqs + m] = __half2float(__float2half_rn(d));
+            for (int k = 0; k < 4; ++k)
+              *reinterpret_cast<__half2*>(dst + 8 * k) =
+                  __floats2half2_rn(q8_code(sv[2 * k], id), q8_code(sv[2 * k + 1], id));
+            if (t4 == 0) p.qs_out[(j0 / 32) * p.ldqs + m] = __half2float(__float2half_rn(d));
           }
         }
       } else {
-        // 32 x 32 sub-tiles through shared memory: each store instruction
-        // writes one row's 32 consecutive columns (128 bytes)
-        const int mrow0 = mt * kBM + quad * 32;
+        // column pairs straight to the row-major output: the four lanes of a
+        // quad fill one 32-byte sector per row
         float* base = p.out + (int64_t)sp * p.split_stride;
+        const bool pairs = (p.ldo & 1) == 0;
 #pragma unroll
-        for (int c = 0; c < C::CPW; c += 32) {
+        for (int rr = 0; rr < 4; ++rr) {
+          const int m = mrow0 + g + 8 * rr;
+          if (m >= p.M) continue;
+          float* row = base + (int64_t)m * p.ldo;
 #pragma unroll
-          for (int j = 0; j < 32; j += 2) {
-            sT[lane * 33 + j] = acc[(c + j) / 2].x;
-            sT[lane * 33 + j + 1] = acc[(c + j) / 2].y;
-          }
-          __syncwarp();
-          const int n = ncol0 + c + lane;
-          if (n < p.N) {
-#pragma unroll 4
-            for (int rr = 0; rr < 32; ++rr) {
-              const int mm = mrow0 + rr;
-              if (mm < p.M) base[(int64_t)mm * p.ldo + n] = sT[rr * 33 + lane];
+          for (int k = 0; k < 8; ++k) {
+            const int n = ncol0 + 8 * k + 2 * t4;
+            if (pairs && n + 1 < p.N) {
+              *reinterpret_cast<float2*>(row + n) = acc[rr][k];
+            } else {
+              if (n < p.N) row[n] = acc[rr][k].x;
+              if (n + 1 < p.N) row[n + 1] = acc[rr][k].y;
             }
           }
-          __syncwarp();
         }
       }
     }
