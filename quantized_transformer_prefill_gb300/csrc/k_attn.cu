@@ -470,6 +470,17 @@ __global__ void __launch_bounds__(256) attn_kernel(const AttnArgs a, const AttnO
   cluster_sync_all();
 }
 
+__global__ void split_planes_kernel(const float* __restrict__ x, int64_t count, __half* hi,
+                                    __half* lo) {
+  for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < count;
+       i += (int64_t)gridDim.x * blockDim.x) {
+    const float v = x[i];
+    const __half h = __float2half_rn(v);
+    hi[i] = h;
+    lo[i] = __float2half_rn(__fsub_rn(v, __half2float(h)));
+  }
+}
+
 // K/V rows of one layer -> fp16 hi/lo shadow planes (count f32 values each).
 __global__ void kv_shadow_kernel(const float* __restrict__ k, const float* __restrict__ v,
                                  int64_t count, __half* kh, __half* kl, __half* vh, __half* vl,
@@ -542,6 +553,15 @@ cudaError_t attention_launch(const AttnArgs& a, const AttnOut& out, cudaStream_t
   if (a.hd == 128)
     return gemv ? launch_attn<128, true>(a, out, rows, st) : launch_attn<128, false>(a, out, rows, st);
   return cudaErrorInvalidValue;
+}
+
+cudaError_t split_planes_launch(const float* x, int64_t count, __half* hi, __half* lo,
+                                cudaStream_t st) {
+  int64_t g = (count + 255) / 256;
+  if (g > 4096) g = 4096;
+  if (g < 1) g = 1;
+  split_planes_kernel<<<(unsigned)g, 256, 0, st>>>(x, count, hi, lo);
+  return cudaGetLastError();
 }
 
 cudaError_t kv_shadow_launch(const float* k, const float* v, int64_t count, __half* const* planes,

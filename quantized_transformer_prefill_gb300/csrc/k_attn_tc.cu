@@ -17,9 +17,10 @@
 // warp 0 streams K (hi/lo, from the fp16 shadow planes) and V^T (hi/lo, from
 // the transposed planes) tiles with TMA into two-stage rings; one thread of
 // warp 1 issues the S MMAs into two TMEM buffers, one thread of warp 6 the
-// P.V MMAs, which accumulate O in TMEM over all key tiles; warps 2-5 own one
-// query row per thread: they write Q's hi/lo into shared memory, read each S
-// row from TMEM, apply the causal mask and the online softmax (log2 units,
+// P.V MMAs, which accumulate O in TMEM over all key tiles; warp 0 also loads
+// the Q tile from the fp16 hi/lo planes the RoPE kernel writes; warps 2-5 own
+// one query row per thread: they read each S row from TMEM, apply the causal
+// mask and the online softmax (log2 units,
 // reference max and sum in registers), and write P's hi/lo into shared
 // memory for the P.V MMA.  The reference max moves only when a row's scores
 // rise more than 2^8 above it; O in TMEM is then rescaled in place before the
@@ -139,6 +140,7 @@ template <int HD, bool kGemvOut>
 __global__ void __launch_bounds__(kTcThreads, 1)
     attn_tc_kernel(const __grid_constant__ CUtensorMap tmKh, const __grid_constant__ CUtensorMap tmKl,
                    const __grid_constant__ CUtensorMap tmVh, const __grid_constant__ CUtensorMap tmVl,
+                   const __grid_constant__ CUtensorMap tmQh, const __grid_constant__ CUtensorMap tmQl,
                    const TcArgs a, const AttnOut out) {
   using C = TcCfg<HD>;
   constexpr uint32_t kTcolR = kTcolT + (uint32_t)HD;
@@ -180,7 +182,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     }
     mbar_init(pready, 4);
     mbar_init(oready, 1);
-    mbar_init(qready, 4);
+    mbar_init(qready, 1);
     mbar_init(&mdone[0], 1);
     mbar_init(&mdone[1], 1);
     fence_barrier_init();
@@ -188,6 +190,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     tma_prefetch_desc(&tmKl);
     tma_prefetch_desc(&tmVh);
     tma_prefetch_desc(&tmVl);
+    tma_prefetch_desc(&tmQh);
+    tma_prefetch_desc(&tmQl);
     s_maxp = -1;
   }
   if (warp == 1) {
@@ -222,6 +226,13 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   if (warp == 0) {
     // ---------------------------------------------------------- TMA producer
     if (lane == 0 && ntile > 0) {
+      // the Q tile (hi, lo), rows past the call's last are filled with zeros
+      mbar_arrive_expect_tx(qready, 2 * C::Q_BYTES);
+#pragma unroll
+      for (int sub = 0; sub < HD / 64; ++sub) {
+        tma_load_2d(sQh + sub * C::QSUB, &tmQh, qready, h * HD + sub * 64, rbase);
+        tma_load_2d(sQl + sub * C::QSUB, &tmQl, qready, h * HD + sub * 64, rbase);
+      }
       bool ok = true;
       int issued = 0;
       for (int j = 0; j < ntile && ok; ++j) {
@@ -250,6 +261,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         issued = j + 1;
       }
       if (!ok) {
+        mbar_wait(qready, 0, a.err, kDevTimeoutAttn);
         for (int j = max(0, issued - C::STAGES); j < issued; ++j) {
           mbar_wait(&kfull[j % C::STAGES], (j / C::STAGES) & 1, a.err, kDevTimeoutAttn);
           mbar_wait(&vfull[j % C::STAGES], (j / C::STAGES) & 1, a.err, kDevTimeoutAttn);
@@ -339,39 +351,6 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     const int pr = clamp_pos(r);
     const int q = a.nh * HD;
     const uint32_t lanebase = (uint32_t)(quad * 32) << 16;
-    // Q row -> fp16 hi/lo, swizzled like a TMA tile
-    {
-      const float* src = a.q + (int64_t)(r < a.r1 ? r : a.r0) * q + (int64_t)h * HD;
-#pragma unroll 4
-      for (int c8 = 0; c8 < HD / 8; ++c8) {
-        float x[8];
-        if (r < a.r1) {
-          const float4 u = *reinterpret_cast<const float4*>(src + c8 * 8);
-          const float4 v = *reinterpret_cast<const float4*>(src + c8 * 8 + 4);
-          x[0] = u.x; x[1] = u.y; x[2] = u.z; x[3] = u.w;
-          x[4] = v.x; x[5] = v.y; x[6] = v.z; x[7] = v.w;
-        } else {
-#pragma unroll
-          for (int i = 0; i < 8; ++i) x[i] = 0.f;
-        }
-        uint32_t hi[4], lo[4];
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          const __half2 hh = __floats2half2_rn(x[2 * i], x[2 * i + 1]);
-          const float2 hf = __half22float2(hh);
-          const __half2 lw = __floats2half2_rn(__fsub_rn(x[2 * i], hf.x), __fsub_rn(x[2 * i + 1], hf.y));
-          hi[i] = *reinterpret_cast<const uint32_t*>(&hh);
-          lo[i] = *reinterpret_cast<const uint32_t*>(&lw);
-        }
-        const int d0 = c8 * 8;
-        const uint32_t off = (uint32_t)((d0 >> 6) * C::QSUB) + sw128_off(rl, d0 & 63);
-        *reinterpret_cast<uint4*>(sQh + off) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
-        *reinterpret_cast<uint4*>(sQl + off) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
-      }
-      fence_proxy_async_smem();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(qready);
-    }
 
     float m = -INFINITY, l = 0.f;  // reference max (log2 units) and sum of P against it
     // scores in log2 units: s2 = (q.k) / sqrt(hd) * log2(e)
@@ -653,8 +632,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
 }  // namespace
 
 bool attention_tc_supported(const AttnArgs& a) {
-  return (a.hd == 64 || a.hd == 128) && a.r1 - a.r0 >= 64 && a.vt[0] && a.vt[1] &&
-         a.vt_ld % 64 == 0 && ((int64_t)a.nkv * a.hd) % 8 == 0;
+  return (a.hd == 64 || a.hd == 128) && a.r1 - a.r0 >= 64 && a.vt[0] && a.vt[1] && a.qp[0] &&
+         a.qp[1] && a.vt_ld % 64 == 0 && ((int64_t)a.nkv * a.hd) % 8 == 0;
 }
 
 bool attention_tc_preferred(int rows, int nh, int num_sms) {
@@ -684,12 +663,15 @@ cudaError_t launch_tc(const AttnArgs& a, const AttnOut& out, int ns, int* err, c
     set = true;
   }
   const int64_t kvw = (int64_t)a.nkv * HD;
-  CUtensorMap mk[2], mv[2];
+  const int64_t qw = (int64_t)a.nh * HD;
+  CUtensorMap mk[2], mv[2], mq[2];
   for (int i = 0; i < 2; ++i) {
     if (tensor_map_2d(&mk[i], a.shadow[i], false, (uint64_t)kvw, (uint64_t)a.n_ctx,
                       (uint64_t)kvw * 2, 64, kTcKeys, true) ||
         tensor_map_2d(&mv[i], a.vt[i], false, (uint64_t)a.vt_ld, (uint64_t)kvw,
-                      (uint64_t)a.vt_ld * 2, kTcKeys, HD, true))
+                      (uint64_t)a.vt_ld * 2, kTcKeys, HD, true) ||
+        tensor_map_2d(&mq[i], a.qp[i], false, (uint64_t)qw, (uint64_t)a.r1, (uint64_t)qw * 2, 64,
+                      kTcRows, true))
       return cudaErrorInvalidValue;
   }
   TcArgs t;
@@ -716,7 +698,8 @@ cudaError_t launch_tc(const AttnArgs& a, const AttnOut& out, int ns, int* err, c
   attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 2;
-  return cudaLaunchKernelEx(&cfg, attn_tc_kernel<HD, kGemvOut>, mk[0], mk[1], mv[0], mv[1], t, out);
+  return cudaLaunchKernelEx(&cfg, attn_tc_kernel<HD, kGemvOut>, mk[0], mk[1], mv[0], mv[1], mq[0],
+                            mq[1], t, out);
 }
 
 cudaError_t attention_tc_launch(const AttnArgs& a, const AttnOut& out, int num_sms, int* err,

@@ -220,6 +220,21 @@ __global__ void validate_kernel(const int32_t* __restrict__ ids, const int32_t* 
 // cos/sin table ("09 · Prefill", section 2.2: the positions buffer is the
 // rotation angle's input and names the K/V row written).  The products and
 // the differences are separate IEEE roundings, as written.
+// A rotated Q pair (elements o and o + half of a row) to the f32 output and,
+// when present, the fp16 hi/lo planes the tensor-core attention loads by TMA.
+__device__ __forceinline__ void store_q(const RopeStoreArgs& a, int64_t o, float v0, float v1,
+                                        int half) {
+  a.q_out[o] = v0;
+  a.q_out[o + half] = v1;
+  if (a.q_planes[0]) {
+    const __half h0 = __float2half_rn(v0), h1 = __float2half_rn(v1);
+    a.q_planes[0][o] = h0;
+    a.q_planes[0][o + half] = h1;
+    a.q_planes[1][o] = __float2half_rn(__fsub_rn(v0, __half2float(h0)));
+    a.q_planes[1][o + half] = __float2half_rn(__fsub_rn(v1, __half2float(h1)));
+  }
+}
+
 __global__ void rope_store_kernel(const RopeStoreArgs a) {
   pdl_trigger();
   pdl_wait();
@@ -256,8 +271,7 @@ __global__ void rope_store_kernel(const RopeStoreArgs a) {
       const float v0 = __fsub_rn(__fmul_rn(x0, c), __fmul_rn(x1, sv));
       const float v1 = __fadd_rn(__fmul_rn(x0, sv), __fmul_rn(x1, c));
       if (head < a.nh) {
-        a.q_out[(int64_t)t * a.nh * a.hd + e0] = v0;
-        a.q_out[(int64_t)t * a.nh * a.hd + e0 + half] = v1;
+        store_q(a, (int64_t)t * a.nh * a.hd + e0, v0, v1, half);
       } else if (write_kv) {
         const int ke = (head - a.nh) * a.hd + i;
         const int64_t o0 = (int64_t)p * kw + ke;
@@ -354,8 +368,7 @@ __global__ void rope_store_qknorm_kernel(const RopeStoreArgs a) {
     const float v0 = __fsub_rn(__fmul_rn(x0, c), __fmul_rn(x1, sv));
     const float v1 = __fadd_rn(__fmul_rn(x0, sv), __fmul_rn(x1, c));
     if (head < a.nh) {
-      a.q_out[(int64_t)t * a.nh * a.hd + e0] = v0;
-      a.q_out[(int64_t)t * a.nh * a.hd + e0 + half] = v1;
+      store_q(a, (int64_t)t * a.nh * a.hd + e0, v0, v1, half);
     } else if (write_kv) {
       const int ke = (head - a.nh) * a.hd + i;
       const int64_t o0 = (int64_t)p * kw + ke;

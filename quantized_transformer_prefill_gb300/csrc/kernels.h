@@ -142,6 +142,7 @@ struct RopeStoreArgs {
   __half* shadow[4] = {nullptr, nullptr, nullptr, nullptr};  // fp16 hi/lo copies of K, V
   __half* vt[2] = {nullptr, nullptr};  // fp16 hi/lo of V transposed: [nkv*hd][vt_ld] (key-major)
   int64_t vt_ld = 0;
+  __half* q_planes[2] = {nullptr, nullptr};  // optional fp16 hi/lo of the rotated Q [nt][nh*hd]
   const int* status = nullptr;  // skip all writes to the regions when *status != 0
   // Qwen3 QK-norm (null: none): per-head RMSNorm weights [hd] of Q and of K
   const float* q_norm = nullptr;
@@ -160,6 +161,7 @@ struct AttnArgs {
   const __half* shadow[4] = {nullptr, nullptr, nullptr, nullptr};  // K hi, K lo, V hi, V lo [n_ctx][nkv*hd]
   const __half* vt[2] = {nullptr, nullptr};  // V hi, V lo transposed [nkv*hd][vt_ld]
   int64_t vt_ld = 0;                         // >= n_ctx, a multiple of 64
+  const __half* qp[2] = {nullptr, nullptr};  // Q hi, Q lo [r1][nh*hd] (tensor-core kernel)
   int nh = 0, nkv = 0, hd = 0;
   int n_ctx = 0;   // positions are clamped into [0, n_ctx) before any region read
   int nsplit = 1;  // key splits (CTAs per cluster), 1..8
@@ -191,6 +193,9 @@ cudaError_t attention_launch(const AttnArgs& a, const AttnOut& out, cudaStream_t
 // f32 K/V rows row0.. (count = rows * kvw values) -> fp16 hi/lo planes
 // (planes[0..3] = K hi, K lo, V hi, V lo, pointing at row row0) and the
 // transposed V planes vt[0..1] [kvw][vt_ld] at columns row0...
+// x [count] f32 -> fp16 hi = rn(x), lo = rn(x - hi).
+cudaError_t split_planes_launch(const float* x, int64_t count, __half* hi, __half* lo,
+                                cudaStream_t stream);
 cudaError_t kv_shadow_launch(const float* k, const float* v, int64_t count, __half* const* planes,
                              __half* const* vt, int64_t vt_ld, int row0, int kvw,
                              cudaStream_t stream);

@@ -158,6 +158,7 @@ struct Workspace {
   float* part = nullptr;     // [splits][nt][max(qkvN, H)]
   int64_t part_stride = 0;
   float* qrot = nullptr;     // [nt][q]
+  __half* qpl = nullptr;     // [2][nt][q] fp16 hi/lo of qrot (tensor-core attention)
   float* att = nullptr;      // [nt][q]
   float* h_last = nullptr;   // [H]
   int8_t* t_q = nullptr;     // [max kpad] one-row codes
@@ -169,7 +170,7 @@ struct Workspace {
   int ntp = 0;
   void release() {
     dfree(ids); dfree(pos); dfree(h); dfree(xa); dfree(xa_s); dfree(xf); dfree(xf_s);
-    dfree(part); dfree(qrot); dfree(att); dfree(h_last); dfree(t_q); dfree(t_s); dfree(gu);
+    dfree(part); dfree(qrot); dfree(qpl); dfree(att); dfree(h_last); dfree(t_q); dfree(t_s); dfree(gu);
     dfree(logits); dfree(lm_out);
     logits_rows = 0;
     max_nt = 0;
@@ -529,6 +530,7 @@ int ensure_workspace(minfer_model* m, int nt) {
       (rc = dalloc(&w.xa, ntp * kx)) || (rc = dalloc(&w.xa_s, (size_t)nbx * ntp)) ||
       (rc = dalloc(&w.xf, ntp * m->Fp)) || (rc = dalloc(&w.xf_s, (size_t)m->nbF * ntp)) ||
       (rc = dalloc(&w.part, (size_t)kMaxSplits * nt * pw)) || (rc = dalloc(&w.qrot, nt * m->q)) ||
+      (rc = dalloc(&w.qpl, 2 * nt * m->q)) ||
       (rc = dalloc(&w.att, nt * m->q)) || (rc = dalloc(&w.h_last, m->H)) ||
       (rc = dalloc(&w.t_q, std::max<int64_t>(kx, m->Fp))) ||
       (rc = dalloc(&w.t_s, std::max(nbx, m->nbF))) || (rc = dalloc(&w.gu, 2 * m->F)) ||
@@ -868,6 +870,8 @@ int enqueue_forward(minfer_model* m, minfer_kv* kv, const int32_t* ids, const in
       r.cos_t = kv->cos_t;
       r.sin_t = kv->sin_t;
       r.q_out = w.qrot;
+      r.q_planes[0] = w.qpl;
+      r.q_planes[1] = w.qpl + (int64_t)w.max_nt * m->q;
       r.kreg = kv->k(l);
       r.vreg = kv->v(l);
       for (int i = 0; i < 4; ++i) r.shadow[i] = kv->plane(l, i);
@@ -896,6 +900,8 @@ int enqueue_forward(minfer_model* m, minfer_kv* kv, const int32_t* ids, const in
     }
     AttnArgs at;
     at.q = w.qrot;
+    at.qp[0] = w.qpl;
+    at.qp[1] = w.qpl + (int64_t)w.max_nt * m->q;
     at.pos = pos;
     at.r0 = r0;
     at.r1 = nt;
@@ -1664,8 +1670,10 @@ int minfer_op_attention(const float* d_q, const int32_t* d_pos, int nt, const fl
   __half* q16 = nullptr;
   const int64_t vt_ld = rup(n_ctx, 64);
   __half* vt = nullptr;
+  __half* qpl = nullptr;
   int rc = dalloc(&sh, (size_t)4 * n_ctx * kvw);
   if (!rc) rc = dalloc(&vt, (size_t)2 * kvw * vt_ld);
+  if (!rc) rc = dalloc(&qpl, (size_t)2 * nt * q);
   if (!rc) rc = dalloc(&q16, (size_t)nt * q);
   if (!rc) rc = dalloc(&s16, (size_t)(q / 32) * nt);
   cudaError_t e = cudaSuccess;
@@ -1685,7 +1693,10 @@ int minfer_op_attention(const float* d_q, const int32_t* d_pos, int nt, const fl
     out.s16 = s16;
     out.ldqs = nt;
     out.f32 = d_o;
+    a.qp[0] = qpl;
+    a.qp[1] = qpl + (int64_t)nt * q;
     e = kv_shadow_launch(d_k, d_v, (int64_t)n_ctx * kvw, planes, vtp, vt_ld, 0, (int)kvw, 0);
+    if (e == cudaSuccess) e = split_planes_launch(d_q, (int64_t)nt * q, qpl, qpl + (int64_t)nt * q, 0);
     int* err = nullptr;
     if (dalloc(&err, 1) != MINFER_OK) e = cudaErrorMemoryAllocation;
     if (e == cudaSuccess)
@@ -1703,6 +1714,7 @@ int minfer_op_attention(const float* d_q, const int32_t* d_pos, int nt, const fl
   }
   dfree(sh);
   dfree(vt);
+  dfree(qpl);
   dfree(q16);
   dfree(s16);
   if (rc) return rc;
