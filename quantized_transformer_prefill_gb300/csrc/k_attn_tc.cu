@@ -43,8 +43,9 @@ namespace {
 
 constexpr int kTcRows = 128;    // query rows per CTA (MMA M)
 constexpr int kTcKeys = 64;     // keys per tile (N of the S MMA, K of the P.V MMA)
-constexpr int kTcThreads = 224;  // TMA warp, S issuer, four softmax warps, P.V issuer
-constexpr int kPvWarp = 6;
+constexpr int kTcThreads = 352;  // TMA warp, S issuer, eight softmax warps, P.V issuer
+constexpr int kPvWarp = 10;
+constexpr int kSmWarps = 8;  // two per TMEM lane quadrant: two threads per query row
 constexpr int kTcMaxSplits = 8;  // CTAs per cluster (portable cluster size)
 
 enum : int { kDevTimeoutAttn = 6 };
@@ -70,12 +71,15 @@ struct TcCfg {
   static constexpr int OFF_V = OFF_K + STAGES * 2 * K_BYTES;  // stage s: hi, lo
   static constexpr int OFF_P = OFF_V + STAGES * 2 * V_BYTES;  // hi, lo
   static constexpr int OFF_BAR = OFF_P + 2 * P_BYTES;
-  static constexpr int NBAR = 4 * STAGES + 4 + 3 + 3;
+  static constexpr int NBAR = 4 * STAGES + 4 + 3 + 4;
   static constexpr int OFF_TMEM = OFF_BAR + NBAR * 8;
   static constexpr int SMEM = OFF_TMEM + 16 + 1024;
   // the split-merge partials reuse the K/V rings: o [128 rows][hd], then
   // (max, sum) [128 rows][2]
   static constexpr int PART_ML = kTcRows * HD;  // float offset of the (max, sum) pairs
+  // the two threads of a row exchange their partial sums at the end of the V ring
+  static constexpr int OFF_LX = OFF_P - 2 * kTcRows * 4;
+  static_assert(OFF_K + kTcRows * (HD + 2) * 4 <= OFF_LX, "sum exchange clear of the partials");
   static_assert(kTcRows * (HD + 2) * 4 <= OFF_P - OFF_K, "partials fit the K/V rings");
   static_assert(OFF_K % 1024 == 0 && OFF_V % 1024 == 0 && OFF_P % 1024 == 0, "1024-B alignment");
   static_assert(SMEM <= 227 * 1024, "shared memory budget");
@@ -157,6 +161,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   uint64_t* oready = pready + 1;
   uint64_t* qready = oready + 1;
   uint64_t* mdone = qready + 1;  // [2] each issuer's MMAs completed (before TMEM is freed)
+  uint64_t* lsum = mdone + 2;    // the two halves of every row have published their sums
   uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(smem + C::OFF_TMEM);
   __shared__ int s_maxp;
 
@@ -178,9 +183,10 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(&sready[b], 1);
-      mbar_init(&sfree[b], 4);
+      mbar_init(&sfree[b], kSmWarps);
     }
-    mbar_init(pready, 4);
+    mbar_init(pready, kSmWarps);
+    mbar_init(lsum, kSmWarps);
     mbar_init(oready, 1);
     mbar_init(qready, 1);
     mbar_init(&mdone[0], 1);
@@ -345,14 +351,20 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     }
   } else {
     // ---------------------------------------------------------- softmax rows
+    // Two threads per row (warps w and w + 4 share a TMEM lane quadrant): both
+    // read the whole S row and take the same max; each exponentiates its half
+    // of the keys, owns half of O's columns and keeps its part of the sum.
     const int quad = warp & 3;                // TMEM lane quadrant
+    const int kh = (warp - 2) >> 2;           // key half of S, column half of O
     const int rl = quad * 32 + lane;          // row within the tile
     const int r = rbase + rl;
     const int pr = clamp_pos(r);
     const int q = a.nh * HD;
     const uint32_t lanebase = (uint32_t)(quad * 32) << 16;
 
-    float m = -INFINITY, l = 0.f;  // reference max (log2 units) and sum of P against it
+    constexpr int HO = HD / 2;     // O columns of this thread
+    const uint32_t ocol = (uint32_t)(kh * HO);
+    float m = -INFINITY, l = 0.f;  // reference max (log2 units) and this half's sum of P against it
     // scores in log2 units: s2 = (q.k) / sqrt(hd) * log2(e)
     const float sc = __fmul_rn(__fdiv_rn(1.0f, __fsqrt_rn((float)HD)), 1.4426950408889634f);
     bool ok = true;
@@ -394,15 +406,18 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         m = mx;
         l *= alpha;
       }
-      // P row -> fp16 hi/lo words, held until the P buffer is free.  A row
-      // whose reference max is still -inf has only -inf scores: exp2(-inf) = 0.
+      // this half's P -> fp16 hi/lo words, held until the P buffer is free.  A
+      // row whose reference max is still -inf has only -inf scores: exp2(-inf) = 0.
       const float mref = (m == -INFINITY) ? 0.f : m;
-      uint32_t hi[kTcKeys / 2], lo[kTcKeys / 2];
+      uint32_t hi[kTcKeys / 4], lo[kTcKeys / 4];
       float l4[4] = {0.f, 0.f, 0.f, 0.f};
+      uint32_t sh[kTcKeys / 2];  // this thread's key half (selected, not indexed, to stay in registers)
 #pragma unroll
-      for (int i = 0; i < kTcKeys / 2; ++i) {
-        const float p0 = exp2f(__fsub_rn(__uint_as_float(sr[2 * i]), mref));
-        const float p1 = exp2f(__fsub_rn(__uint_as_float(sr[2 * i + 1]), mref));
+      for (int i = 0; i < kTcKeys / 2; ++i) sh[i] = kh ? sr[kTcKeys / 2 + i] : sr[i];
+#pragma unroll
+      for (int i = 0; i < kTcKeys / 4; ++i) {
+        const float p0 = exp2f(__fsub_rn(__uint_as_float(sh[2 * i]), mref));
+        const float p1 = exp2f(__fsub_rn(__uint_as_float(sh[2 * i + 1]), mref));
         l4[i & 3] += __fadd_rn(p0, p1);
         const __half2 h = __floats2half2_rn(p0, p1);
         const float2 hf = __half22float2(h);
@@ -426,10 +441,10 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         const bool has_r = j > kFoldTiles;  // an earlier fold wrote R
         if (fold || __any_sync(0xffffffffu, resc)) {
 #pragma unroll
-          for (int d0 = 0; d0 < HD; d0 += 32) {
+          for (int d0 = 0; d0 < HO; d0 += 32) {
             uint32_t t[32], rr[32];
-            tmem_ld32(tmem_base + lanebase + kTcolT + (uint32_t)d0, t);
-            if (has_r) tmem_ld32(tmem_base + lanebase + kTcolR + (uint32_t)d0, rr);
+            tmem_ld32(tmem_base + lanebase + kTcolT + ocol + (uint32_t)d0, t);
+            if (has_r) tmem_ld32(tmem_base + lanebase + kTcolR + ocol + (uint32_t)d0, rr);
             tmem_wait_ld();
 #pragma unroll
             for (int i = 0; i < 32; ++i) {
@@ -443,15 +458,15 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 t[i] = __float_as_uint(__fmul_rn(tv, alpha));
               }
             }
-            if (fold || has_r) tmem_st32(tmem_base + lanebase + kTcolR + (uint32_t)d0, rr);
-            if (!fold) tmem_st32(tmem_base + lanebase + kTcolT + (uint32_t)d0, t);
+            if (fold || has_r) tmem_st32(tmem_base + lanebase + kTcolR + ocol + (uint32_t)d0, rr);
+            if (!fold) tmem_st32(tmem_base + lanebase + kTcolT + ocol + (uint32_t)d0, t);
           }
           tmem_wait_st();
         }
       }
 #pragma unroll
-      for (int c8 = 0; c8 < kTcKeys / 8; ++c8) {
-        const uint32_t off = sw128_off(rl, c8 * 8);
+      for (int c8 = 0; c8 < kTcKeys / 16; ++c8) {
+        const uint32_t off = sw128_off(rl, kh * (kTcKeys / 2) + c8 * 8);
         *reinterpret_cast<uint4*>(sP + off) =
             make_uint4(hi[4 * c8], hi[4 * c8 + 1], hi[4 * c8 + 2], hi[4 * c8 + 3]);
         *reinterpret_cast<uint4*>(sP + C::P_BYTES + off) =
@@ -463,9 +478,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       if (lane == 0) mbar_arrive(pready);
     }
     // the last P.V completes the O tile
-    float o[HD];
+    float o[HO];
 #pragma unroll
-    for (int d = 0; d < HD; ++d) o[d] = 0.f;
+    for (int d = 0; d < HO; ++d) o[d] = 0.f;
     if (ok && ntile > 0) {
       if (!mbar_wait(oready, (ntile - 1) & 1, a.err, kDevTimeoutAttn)) {
         ok = false;
@@ -473,10 +488,10 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         tc_fence_after();
         const bool has_r = ntile - 1 >= kFoldTiles;  // some tile folded T into R
 #pragma unroll
-        for (int d0 = 0; d0 < HD; d0 += 32) {
+        for (int d0 = 0; d0 < HO; d0 += 32) {
           uint32_t t[32], rr[32];
-          tmem_ld32(tmem_base + lanebase + kTcolT + (uint32_t)d0, t);
-          if (has_r) tmem_ld32(tmem_base + lanebase + kTcolR + (uint32_t)d0, rr);
+          tmem_ld32(tmem_base + lanebase + kTcolT + ocol + (uint32_t)d0, t);
+          if (has_r) tmem_ld32(tmem_base + lanebase + kTcolR + ocol + (uint32_t)d0, rr);
           tmem_wait_ld();
 #pragma unroll
           for (int i = 0; i < 32; ++i)
@@ -486,13 +501,26 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       }
     }
 
+    // the row's sum: this half's plus the other's (the K/V rings are idle
+    // once the last P.V has completed)
+    if (ntile > 0) {
+      float* lx = reinterpret_cast<float*>(smem + C::OFF_LX);
+      lx[kh * kTcRows + rl] = l;
+      __syncwarp();
+      if (lane == 0) mbar_arrive(lsum);
+      if (ok && mbar_wait(lsum, 0, a.err, kDevTimeoutAttn))
+        l = __fadd_rn(lx[rl], lx[kTcRows + rl]);  // same order on both threads
+      else
+        ok = false;
+    }
+
     // ------------------------------------------------------- merge + output
     const int nb = q / 32;
     auto emit = [&](const float* v, float inv) {
       if (r >= a.r1) return;
       const int64_t orow = r - out.row_base;
 #pragma unroll
-      for (int bq = 0; bq < HD / 32; ++bq) {
+      for (int bq = 0; bq < HO / 32; ++bq) {
         float y[32];
         float amax = 0.f;
 #pragma unroll
@@ -500,7 +528,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           y[i] = __fmul_rn(v[bq * 32 + i], inv);
           amax = fmaxf(amax, fabsf(y[i]));
         }
-        const int k0 = h * HD + bq * 32;
+        const int k0 = h * HD + (int)ocol + bq * 32;
         const int blk = k0 / 32;
         if (out.f32)
 #pragma unroll
@@ -536,9 +564,10 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       // partials into this CTA's K/V rings (idle now), merged after the cluster barrier
       float* po = reinterpret_cast<float*>(smem + C::OFF_K);
 #pragma unroll
-      for (int d = 0; d < HD; d += 4)
-        *reinterpret_cast<float4*>(po + rl * HD + d) = make_float4(o[d], o[d + 1], o[d + 2], o[d + 3]);
-      *reinterpret_cast<float2*>(po + C::PART_ML + rl * 2) = make_float2(m, l);
+      for (int d = 0; d < HO; d += 4)
+        *reinterpret_cast<float4*>(po + rl * HD + ocol + d) =
+            make_float4(o[d], o[d + 1], o[d + 2], o[d + 3]);
+      if (kh == 0) *reinterpret_cast<float2*>(po + C::PART_ML + rl * 2) = make_float2(m, l);
     }
   }
 
