@@ -474,8 +474,8 @@ GemmPlan gemm_plan(int64_t M, int64_t N, int nb, int num_sms, bool allow_split) 
   const int64_t tiles = mt * ((N + p.bn - 1) / p.bn);
   p.splits = 1;
   if (allow_split && tiles < num_sms) {
-    // split K so that every SM gets work, keeping >= 4 stages per split
-    int s = (int)std::min<int64_t>(num_sms / std::max<int64_t>(tiles, 1), stages / 4);
+    // split K so that every SM gets work, keeping >= 2 stages (4 blocks) per split
+    int s = (int)std::min<int64_t>(num_sms / std::max<int64_t>(tiles, 1), stages / 2);
     p.splits = std::max(1, s);
   }
   return p;
