@@ -139,6 +139,24 @@ def test_attention_vs_oracle(qp, oracle_mod, nh, nkv, hd, nt, n_ctx, p0):
     assert err <= 2e-5 * max(1.0, np.abs(ref).max()), err
 
 
+@pytest.mark.parametrize("nh,nkv,hd,nt", [(14, 2, 64, 384), (12, 2, 128, 300)])
+def test_attention_rising_scores_vs_oracle(qp, oracle_mod, nh, nkv, hd, nt):
+    """Keys that grow with their position push every row's running max up
+    tile after tile, so the tensor-core kernel's rescaling of the O it keeps
+    in TMEM (and of the sum) runs many times, next to its periodic folds."""
+    rng = np.random.default_rng(hd + nt)
+    n_ctx = nt
+    q = rng.normal(0, 1, (nt, nh * hd)).astype(np.float32)
+    grow = (1.0 + np.arange(n_ctx) / 32.0).astype(np.float32)[:, None]
+    K = (rng.normal(0, 1, (n_ctx, nkv * hd)) * grow).astype(np.float32)
+    V = rng.normal(0, 1, (n_ctx, nkv * hd)).astype(np.float32)
+    pos = np.arange(nt, dtype=np.int32)
+    o = qp.op_attention(_dev(q), _dev(pos), _dev(K), _dev(V), nh, nkv, hd).cpu().numpy()
+    ref = oracle_mod.attention(q, pos, K, V, nh, nkv, hd)
+    err = np.abs(o - ref).max()
+    assert err <= 2e-5 * max(1.0, np.abs(ref).max()), err
+
+
 def test_rope_store_vs_oracle(qp, oracle_mod):
     nh, nkv, hd, nt, n_ctx, theta = 14, 2, 64, 40, 96, 1.0e6
     rng = np.random.default_rng(11)
