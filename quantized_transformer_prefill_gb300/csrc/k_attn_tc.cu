@@ -89,7 +89,6 @@ struct TcCfg {
 };
 
 struct TcArgs {
-  const float* q;  // [nt][nh*hd]
   const int32_t* pos;
   int r0, r1, nh, nkv, n_ctx;
   int* err;
@@ -704,7 +703,6 @@ cudaError_t launch_tc(const AttnArgs& a, const AttnOut& out, int ns, int* err, c
       return cudaErrorInvalidValue;
   }
   TcArgs t;
-  t.q = a.q;
   t.pos = a.pos;
   t.r0 = a.r0;
   t.r1 = a.r1;
