@@ -1,6 +1,7 @@
 // k_attn_tc.cu -- causal GQA attention on the 5th-generation tensor cores
-// (tcgen05.mma with TMEM accumulators, TMA-fed), for prompts of 64 rows and
-// more; short calls (the last-row tail, single tokens) keep k_attn.cu.
+// (tcgen05.mma with TMEM accumulators, TMA-fed), for calls of 64 rows and
+// more (the forward uses it from 128 rows on); short calls (the last-row tail,
+// single tokens) keep k_attn.cu.
 //
 // What it computes ("09 · Prefill: the first forward", section 2.2: token t
 // attends to positions 0..=pos[t]; "05 · Graph build", section 2.5: GQA,
@@ -14,21 +15,23 @@
 // needs), as in the k_attn.cu kernel:
 //   S  = Qh.Kh^T + Qh.Kl^T + Ql.Kh^T        M = 128 rows, N = 64 keys, K = hd
 //   Ot = Ph.Vh + Ph.Vl + Pl.Vh              M = 128 rows, N = hd, K = 64 keys
-// warp 0 streams K (hi/lo, from the fp16 shadow planes) and V^T (hi/lo, from
-// the transposed planes) tiles with TMA into two-stage rings; one thread of
-// warp 1 issues the S MMAs into two TMEM buffers, one thread of warp 6 the
-// P.V MMAs, which accumulate O in TMEM over all key tiles; warp 0 also loads
-// the Q tile from the fp16 hi/lo planes the RoPE kernel writes; warps 2-5 own
-// one query row per thread: they read each S row from TMEM, apply the causal
-// mask and the online softmax (log2 units,
-// reference max and sum in registers), and write P's hi/lo into shared
-// memory for the P.V MMA.  The reference max moves only when a row's scores
-// rise more than 2^8 above it; O in TMEM is then rescaled in place before the
-// next P.V.  S of tile j+1 is computed while tile j's softmax runs, and P of
-// tile j+1 while P.V of tile j runs.
+// warp 0 loads the Q tile (hi/lo planes written by the RoPE kernel) and
+// streams K (hi/lo shadow planes) and V^T (hi/lo transposed planes) tiles
+// with TMA into two-stage rings; one thread of warp 1 issues the S MMAs into
+// two TMEM buffers, one thread of warp 10 the P.V MMAs, which accumulate O in
+// TMEM over the key tiles.  Warps 2-9 run the softmax, two threads per query
+// row (the two warps of a TMEM lane quadrant): both read the whole S row and
+// take the same max after the causal mask (log2 units), each exponentiates
+// half of the keys into P's hi/lo in shared memory for the P.V MMA, owns half
+// of O's columns and keeps its part of the row sum.  The reference max moves
+// only when a row's scores rise more than 2^8 above it; O in TMEM is then
+// rescaled in place before the next P.V, and every four tiles the tensor-core
+// sum is folded into a second TMEM part with round-to-nearest adds.  S of tile
+// j+1 is computed while tile j's softmax runs, and P of tile j+1 while P.V of
+// tile j runs.
 // With few row tiles the key range is split over the CTAs of a cluster,
 // merged through distributed shared memory as in k_attn.cu.  The output row
-// is normalized and each 32-block quantized to Q8_0 by its own thread.
+// is normalized and each 32-block quantized to Q8_0 by the thread owning it.
 // Every wait is bounded; on timeout the kernel records a status code,
 // drains its own TMA loads and MMAs, frees TMEM and returns.
 #include <algorithm>
