@@ -581,7 +581,11 @@ cudaError_t rope_store_launch(const RopeStoreArgs& a, cudaStream_t st) {
     if (smem > 48 * 1024) return cudaErrorInvalidValue;
     return launch_pdl(rope_store_qknorm_kernel, a.nt, 256, smem, st, a);
   }
-  return launch_pdl(rope_store_kernel, a.nt, 256, 0, st, a);
+  // one thread per (Q/K pair, V element) of the token where that fits a CTA:
+  // every thread's loads go out in one round instead of several
+  const int items = (a.nh + a.nkv) * (a.hd / 2) + a.nkv * a.hd;
+  const int threads = std::min(1024, std::max(128, (items + 31) / 32 * 32));
+  return launch_pdl(rope_store_kernel, a.nt, threads, 0, st, a);
 }
 
 cudaError_t gemv_launch(const GemvArgs& a, cudaStream_t st) {
