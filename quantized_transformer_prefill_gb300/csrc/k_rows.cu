@@ -579,7 +579,11 @@ cudaError_t rope_store_launch(const RopeStoreArgs& a, cudaStream_t st) {
     if (!a.q_norm || !a.k_norm || nheads > kMaxQkHeads) return cudaErrorInvalidValue;
     const size_t smem = (size_t)nheads * a.hd * sizeof(float);
     if (smem > 48 * 1024) return cudaErrorInvalidValue;
-    return launch_pdl(rope_store_qknorm_kernel, a.nt, 256, smem, st, a);
+    // up to one thread per element of the token's Q|K|V sums: the loads go
+    // out in few rounds and every head's norm gets its own warp
+    const int W = (a.nh + 2 * a.nkv) * a.hd;
+    const int threads = std::min(1024, std::max(128, (W + 31) / 32 * 32));
+    return launch_pdl(rope_store_qknorm_kernel, a.nt, threads, smem, st, a);
   }
   // one thread per (Q/K pair, V element) of the token where that fits a CTA:
   // every thread's loads go out in one round instead of several
