@@ -1,10 +1,18 @@
-"""Prefill throughput of the GB300 library on the Qwen2-0.5B-shaped workload.
+"""Prefill throughput of the GB300 library, Qwen2-family shapes.
 
 One step = one whole prefill forward (every layer, every prompt token, the
-last-row tail and lm_head) over a 512-token synthetic prompt at positions
-0..511 into n_ctx-4096 KV regions, through the C ABI.  Prints one JSON line.
+last-row tail and lm_head) through the C ABI.  The headline (`value`) is the
+Qwen2-0.5B-shaped 512-token prompt at positions 0..511 into n_ctx-4096 KV
+regions, timed over exactly --steps graph replays.  The `per_config` block
+then measures each of the five workloads (tiny 32 tokens; 0.5B/512;
+1.5B/2048; 7B/4096; the 1.5B 1024-token append after 3072 cached tokens)
+over at least one second of replays each (mean and standard deviation of the
+per-forward time), with the GEMM and attention fractions of the measured
+peaks, the whole-forward roofline time T*, and the CPU oracle's time on the
+host cores.  Prints one JSON line.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                  [--workload NAME] [--no-per-config] [--no-cpu-baseline]
 
 --impl reference times the CPU oracle (test infrastructure, plain C++) on the
 box's host cores on the same workload.  Multi-GPU runs are independent
@@ -13,6 +21,7 @@ replicas (one prompt and one model per GPU, no collective).
 from __future__ import annotations
 
 import argparse
+import dataclasses
 import json
 import os
 import statistics
@@ -29,8 +38,12 @@ import numpy as np
 import synth
 
 WORKLOAD = "qwen2-0.5b-512"
+# the five configurations the measurement covers, in their listed order
+CONFIGS = ["tiny-32", "qwen2-0.5b-512", "qwen2-1.5b-2048", "qwen2-7b-4096",
+           "qwen2-1.5b-append-1024"]
 METRIC = "prefill tokens/sec on 1 GB300"
 UNIT = "tokens/s"
+Q8_BYTES = 34.0 / 32.0  # one Q8_0 element: an int8 code plus 1/32 of an fp16 scale
 
 
 def _peaks():
@@ -40,6 +53,25 @@ def _peaks():
         return p["hbm_gbs"], p["bf16_tflops"], "measured"
     except Exception:
         return 6800.0, 1900.0, "fallback"
+
+
+def cpu_model() -> str:
+    """The host CPU's model name (lscpu, else /proc/cpuinfo)."""
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for line in out.splitlines():
+            if line.strip().startswith("Model name:"):
+                return line.split(":", 1)[1].strip()
+    except Exception:
+        pass
+    try:
+        with open("/proc/cpuinfo") as f:
+            for line in f:
+                if line.lower().startswith(("model name", "cpu model")):
+                    return line.split(":", 1)[1].strip()
+    except OSError:
+        pass
+    return "unknown"
 
 
 class ClockSampler:
@@ -97,6 +129,8 @@ class ClockSampler:
                 "reasons": sorted(reasons), "samples": len(sm)}
 
 
+# ---------------------------------------------------------------- work counts
+
 def gemm_flops(cfg, nt):
     """Algorithmic FLOPs per launch of each GEMM class (2 per MAC)."""
     H, q = cfg.n_embd, cfg.n_head * cfg.head_dim
@@ -120,8 +154,64 @@ def forward_macs(cfg, nt, p0=0, n_out=1):
     return mm, n_out * H * V, attn
 
 
+def attention_flops(cfg, nt, p0=0):
+    """Causal attention FLOPs of one full layer (Q.K^T and P.V, 2 per MAC)."""
+    q = cfg.n_head * cfg.head_dim
+    keys = sum(p0 + t + 1 for t in range(nt))
+    return 2.0 * 2 * keys * q
+
+
+def forward_roofline(cfg, nt, p0, n_out, hbm_gbs, tflops):
+    """Whole-forward roofline time T* (seconds) as the sum
+        sum over GEMMs of max(2 MAC / P, B / BW)
+      + sum over attentions of max(2 MAC / P, B / BW)
+      + sum over the memory-bound steps of B / BW
+    with algorithmic bytes: Q8_0 weights and activations at 34/32 bytes per
+    element, f32 residual stream, K/V rows and logits read or written once.
+    Returns (T*, parts) with parts the per-term seconds."""
+    H, q = cfg.n_embd, cfg.n_head * cfg.head_dim
+    kv = cfg.n_head_kv * cfg.head_dim
+    F, L, V = cfg.n_ff, cfg.n_layer, cfg.n_vocab
+    P = tflops * 1e12
+    BW = hbm_gbs * 1e9
+    parts = {"gemm": 0.0, "attention": 0.0, "memory": 0.0}
+
+    def gemm(M, N, K, out_bytes_per_elt):
+        flops = 2.0 * M * N * K
+        b = N * K * Q8_BYTES + M * K * Q8_BYTES + M * N * out_bytes_per_elt
+        parts["gemm"] += max(flops / P, b / BW)
+
+    def mem(b):
+        parts["memory"] += b / BW
+
+    mem(nt * H * 4 + nt * H * 1)                          # embedding rows (int8) -> h f32
+    for layer in range(L):
+        last = layer == L - 1
+        r = n_out if last else nt                         # rows past the K/V projections
+        mem(nt * H * 4 + nt * H * Q8_BYTES)               # attn_norm + Q8_0 (h read, codes out)
+        gemm(nt, q + 2 * kv, H, 4)                        # Q|K|V
+        mem(nt * (q + 2 * kv) * 4 + nt * (q + 2 * kv) * 4)  # RoPE + store: sums in, Q/K/V rows out
+        keys = sum(p0 + t + 1 for t in range(nt - r, nt))
+        kv_rows = p0 + nt                                 # every region row 0..max pos read once
+        a_flops = 2.0 * 2 * keys * q
+        a_bytes = r * q * 4 + kv_rows * 2 * kv * 4 + r * q * Q8_BYTES
+        parts["attention"] += max(a_flops / P, a_bytes / BW)
+        gemm(r, H, q, 4)                                  # Wo
+        mem(3 * r * H * 4 + r * H * Q8_BYTES)             # residual add + ffn_norm + Q8_0
+        gemm(r, 2 * F, H, 0.0)                            # gate/up (the SwiGLU output below)
+        mem(r * F * Q8_BYTES)                             # SwiGLU Q8_0 out
+        gemm(r, H, F, 4)                                  # down
+        mem(2 * r * H * 4)                                # residual add
+    mem(n_out * H * 4 + n_out * H * Q8_BYTES)             # final norm
+    lm_flops = 2.0 * n_out * H * V
+    lm_bytes = V * H * Q8_BYTES + n_out * V * 4
+    parts["gemm"] += max(lm_flops / P, lm_bytes / BW)     # lm_head on the n_out rows
+    return sum(parts.values()), parts
+
+
 _PROFILE_OF = {"gemm_gate_up_swiglu": "gemm_gate_up", "attention": "attention",
-               "rmsnorm_quant": "row_quant"}
+               "rmsnorm_quant": "row_quant", "gemm_qkv": "gemm_qkv", "gemm_down": "gemm_down",
+               "gemm_o": "gemm_o", "rope_kv_store": "rope_store", "lm_head_gemv": "lm_head_gemv"}
 
 
 def profiled_traffic(kernel: str, workload: str):
@@ -141,12 +231,52 @@ def profiled_traffic(kernel: str, workload: str):
     return None
 
 
+# ---------------------------------------------------------------- the oracle on the host
+
 def oracle_model(cfg):
     import oracle
     m = oracle.Model(cfg)
     for spec in synth.tensor_specs(cfg):
         m.set_f32(spec.name, synth.tensor_data(spec))
     return m
+
+
+def _oracle_forward_s(w, cfg):
+    """Seconds of one oracle forward of workload w on model cfg (the cached
+    turn of an append is pre-filled first, untimed)."""
+    m = oracle_model(cfg)
+    kv = m.kv(w.n_ctx)
+    if w.prefill_tokens:
+        rc, _, _ = m.prefill(kv, w.prefill_ids(), np.arange(w.prefill_tokens, dtype=np.int32))
+        assert rc == 0
+    t = time.perf_counter()
+    rc, _, _ = m.prefill(kv, w.ids(), w.positions())
+    dt = time.perf_counter() - t
+    assert rc == 0
+    return dt
+
+
+def oracle_time(w, full: bool):
+    """The oracle, as it stands, on the host cores for workload w.  full: one
+    whole forward.  Otherwise a bounded sample: the same prompt through 1- and
+    2-layer models of the same shape (the first layers of the same weights),
+    t(L) = t(1) + (L - 1) (t(2) - t(1)): every layer but the last costs the
+    same, and the 1-layer model holds the embedding, the last layer's tail and
+    the lm_head."""
+    import oracle
+    oracle.build()
+    cfg = w.model
+    if full:
+        s = _oracle_forward_s(w, cfg)
+        sample = f"one full forward of {w.name}"
+    else:
+        t1 = _oracle_forward_s(w, dataclasses.replace(cfg, n_layer=1))
+        t2 = _oracle_forward_s(w, dataclasses.replace(cfg, n_layer=2))
+        s = t1 + (cfg.n_layer - 1) * max(t2 - t1, 0.0)
+        sample = (f"1- and 2-layer models of the {w.name} shape on its prompt "
+                  f"({t1:.2f} s, {t2:.2f} s), extrapolated to {cfg.n_layer} layers")
+    return {"value": w.n_tokens / s, "unit": UNIT, "seconds_per_forward": s,
+            "cores": os.cpu_count(), "cpu": cpu_model(), "kind": "oracle", "sample": sample}
 
 
 def cpu_baseline(w, reps: int = 2):
@@ -165,7 +295,8 @@ def cpu_baseline(w, reps: int = 2):
         times.append(time.perf_counter() - t)
         assert rc == 0
     dt = min(times)
-    return {"value": w.n_tokens / dt, "unit": UNIT, "cores": os.cpu_count(), "kind": "oracle",
+    return {"value": w.n_tokens / dt, "unit": UNIT, "cores": os.cpu_count(), "cpu": cpu_model(),
+            "kind": "oracle",
             "sample": f"{reps} full {w.n_tokens}-token prefills of {w.name} (best taken)",
             "seconds_per_forward": dt}
 
@@ -192,14 +323,158 @@ def reference_arm(args, w, rank, world):
     line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * total / args.steps,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32/f64",
-            "data": "synthetic", "config": {"workload": w.name, "n_tokens": w.n_tokens,
-                                            "n_ctx": w.n_ctx, "positions": "0..511"},
+            "data": "synthetic",
+            "config": {"workload": w.name, "n_tokens": w.n_tokens, "n_out": w.n_out,
+                       "positions": f"{w.p0}..{w.p0 + w.n_tokens - 1}", "n_ctx": w.n_ctx,
+                       "layers": cfg.n_layer, "hidden": cfg.n_embd, "vocab": cfg.n_vocab},
             "cpu_baseline": {"value": value, "unit": UNIT, "kind": "oracle",
-                             "cores": os.cpu_count(),
+                             "cores": os.cpu_count(), "cpu": cpu_model(),
                              "sample": f"{args.steps} full prefills of {w.name}"},
             "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0,
                     "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
+
+
+# ---------------------------------------------------------------- the GPU arm
+
+def load_gpu_model(qp, cfg):
+    model = qp.Model(qp.hparams_of(cfg))
+    for spec in synth.tensor_specs(cfg):
+        model.set_tensor(spec.name, synth.tensor_data(spec), spec.ne0, spec.ne1, qp.MINFER_F32)
+    model.finalize()
+    return model
+
+
+class Prepared:
+    """One workload ready to replay: model, KV (the cached turn pre-filled),
+    device-resident inputs, a stream."""
+
+    def __init__(self, qp, model, w):
+        import torch
+        self.w = w
+        self.model = model
+        self.kv = model.kv(w.n_ctx)
+        if w.prefill_tokens:  # the cached turn an append attends over (untimed)
+            model.prefill(self.kv, w.prefill_ids(), np.arange(w.prefill_tokens, dtype=np.int32))
+        self.ids, self.pos = w.ids(), w.positions()
+        self.d_ids = torch.from_numpy(self.ids).cuda()
+        self.d_pos = torch.from_numpy(self.pos).cuda()
+        self.d_logits = torch.empty((w.n_out, w.model.n_vocab), dtype=torch.float32, device="cuda")
+        self.stream = torch.cuda.Stream()
+        self.qp = qp
+
+    def step(self):
+        rc = self.model.prefill_device_n(self.kv, self.d_ids.data_ptr(), self.d_pos.data_ptr(),
+                                         self.w.n_tokens, self.w.n_out, self.d_logits.data_ptr(),
+                                         self.stream.cuda_stream)
+        if rc != 0:
+            raise RuntimeError(f"prefill_device rc={rc}")
+
+    def check(self, what):
+        self.qp.check(self.model.sync_status(self.stream.cuda_stream), what)
+
+    def profile(self, reps: int):
+        """Per-kernel-class (launches, ms) of one forward (the last of `reps`
+        replays) with CUDA events around every launch."""
+        self.model.profile_enable(True)
+        for _ in range(2):
+            self.step()
+        self.check("profile warmup")
+        self.model.profile_enable(True)  # reset the totals
+        for _ in range(reps):
+            self.step()
+        self.check("profiled region")
+        prof = self.model.profile_read()
+        self.model.profile_enable(False)
+        return prof
+
+    def free(self):
+        self.kv.free()
+
+
+def time_replays(p: Prepared, min_seconds: float, min_reps: int):
+    """Replays bracketed one by one by CUDA events on the launching stream
+    until at least min_seconds of device time and min_reps replays: per
+    forward times in ms."""
+    import torch
+    evs = []
+    torch.cuda.synchronize()
+    t_end = time.perf_counter() + min_seconds
+    while True:
+        batch = []
+        for _ in range(10):
+            e0 = torch.cuda.Event(enable_timing=True)
+            e1 = torch.cuda.Event(enable_timing=True)
+            e0.record(p.stream)
+            p.step()
+            e1.record(p.stream)
+            batch.append((e0, e1))
+        evs.extend(batch)
+        batch[-1][1].synchronize()
+        if len(evs) >= min_reps and time.perf_counter() >= t_end:
+            break
+    torch.cuda.synchronize()
+    p.check("timed replays")
+    return [a.elapsed_time(b) for a, b in evs]
+
+
+def gemm_and_attention_stats(cfg, w, prof, tflops):
+    flops = gemm_flops(cfg, w.n_tokens)
+    out = {}
+    for k, f in flops.items():
+        n, tot = prof.get(k, (0, 0.0))
+        if n:
+            avg_ms = tot / n
+            out[k] = {"avg_us": 1e3 * avg_ms, "tflops": f / (avg_ms / 1e3) / 1e12,
+                      "frac_of_bf16_peak": f / (avg_ms / 1e3) / 1e12 / tflops}
+    n, tot = prof.get("attention", (0, 0.0))
+    attn = None
+    if n:
+        # the full-layer launches (the last layer's one-row launch is a tail)
+        full = n - 1 if w.n_out == 1 else n
+        f_all = attention_flops(cfg, w.n_tokens, w.p0) * full
+        attn = {"launches": n, "ms": tot, "tflops": f_all / (tot / 1e3) / 1e12,
+                "frac_of_bf16_peak": f_all / (tot / 1e3) / 1e12 / tflops}
+    return out, attn
+
+
+def measure_config(qp, model, w, hbm, bf16, min_seconds, with_oracle):
+    p = Prepared(qp, model, w)
+    for _ in range(3):
+        p.step()
+    p.check("warmup")
+    ms = time_replays(p, min_seconds, 10)
+    prof = p.profile(3)
+    p.free()
+    cfg = w.model
+    mean = statistics.fmean(ms)
+    sd = statistics.stdev(ms) if len(ms) > 1 else 0.0
+    tps = [w.n_tokens / (x / 1e3) for x in ms]
+    gemms, attn = gemm_and_attention_stats(cfg, w, prof, bf16)
+    t_star, parts = forward_roofline(cfg, w.n_tokens, w.p0, w.n_out, hbm, bf16)
+    prof_sum = sum(t for _, t in prof.values())
+    res = {
+        "n_tokens": w.n_tokens, "p0": w.p0, "n_ctx": w.n_ctx, "layers": cfg.n_layer,
+        "tokens_per_s": {"mean": w.n_tokens / (mean / 1e3), "stdev": statistics.stdev(tps)
+                         if len(tps) > 1 else 0.0, "reps": len(ms)},
+        "ms_per_forward": {"mean": mean, "stdev": sd, "min": min(ms), "max": max(ms),
+                           "total_s": sum(ms) / 1e3},
+        "gemm": gemms,
+        "attention": attn,
+        "forward_roofline": {"t_star_ms": 1e3 * t_star, "frac": 1e3 * t_star / mean,
+                             "parts_ms": {k: 1e3 * v for k, v in parts.items()}},
+        "per_kernel_ms": {k: {"launches": n, "ms": t} for k, (n, t) in prof.items() if n},
+        "per_kernel_note": (f"CUDA events around every launch (no launch overlap): they sum to "
+                            f"{prof_sum:.3f} ms per forward against {mean:.3f} ms replayed, so "
+                            f"per-kernel fractions are conservative"),
+    }
+    if with_oracle:
+        try:
+            res["oracle"] = oracle_time(w, full=w.model.n_layer * w.n_tokens <= 24 * 512)
+            res["speedup_vs_oracle"] = res["tokens_per_s"]["mean"] / res["oracle"]["value"]
+        except Exception as e:  # a failed baseline must not lose the GPU numbers
+            res["oracle"] = {"error": repr(e)}
+    return res
 
 
 def ours(args, w, rank, world, dist):
@@ -208,52 +483,33 @@ def ours(args, w, rank, world, dist):
 
     dev = int(os.environ.get("LOCAL_RANK", 0))
     torch.cuda.set_device(dev)
+    hbm, bf16, peak_src = _peaks()
     cfg = w.model
-    model = qp.Model(qp.hparams_of(cfg))
-    for spec in synth.tensor_specs(cfg):
-        model.set_tensor(spec.name, synth.tensor_data(spec), spec.ne0, spec.ne1, qp.MINFER_F32)
-    model.finalize()
-    kv = model.kv(w.n_ctx)
-    if w.prefill_tokens:  # the cached turn an append attends over (untimed)
-        model.prefill(kv, w.prefill_ids(), np.arange(w.prefill_tokens, dtype=np.int32))
-    ids, pos = w.ids(), w.positions()
-    nt = w.n_tokens
-    d_ids = torch.from_numpy(ids).cuda()
-    d_pos = torch.from_numpy(pos).cuda()
-    n_out = w.n_out
-    d_logits = torch.empty((n_out, cfg.n_vocab), dtype=torch.float32, device="cuda")
-    stream = torch.cuda.Stream()
-    sp = stream.cuda_stream
-
-    def step():
-        rc = model.prefill_device_n(kv, d_ids.data_ptr(), d_pos.data_ptr(), nt, n_out,
-                                    d_logits.data_ptr(), sp)
-        if rc != 0:
-            raise RuntimeError(f"prefill_device rc={rc}")
-
+    model = load_gpu_model(qp, cfg)
+    p = Prepared(qp, model, w)
+    nt, n_out = w.n_tokens, w.n_out
     for _ in range(max(3, args.warmup)):
-        step()
-    qp.check(model.sync_status(sp), "warmup")
+        p.step()
+    p.check("warmup")
 
     def barrier():
         if dist is not None:
             dist.barrier()
 
-    # ---- timed region: K graph replays, device-resident inputs
+    # ---- timed region: exactly K graph replays, device-resident inputs
     e0 = torch.cuda.Event(enable_timing=True)
     e1 = torch.cuda.Event(enable_timing=True)
     barrier()
     torch.cuda.synchronize()
     with ClockSampler(dev) as clk:
-        with torch.cuda.stream(stream):
-            e0.record(stream)
-            for _ in range(args.steps):
-                step()
-            e1.record(stream)
+        e0.record(p.stream)
+        for _ in range(args.steps):
+            p.step()
+        e1.record(p.stream)
         torch.cuda.synchronize()
         time.sleep(0.25)
     barrier()
-    qp.check(model.sync_status(sp), "timed region")
+    p.check("timed region")
     ms = e0.elapsed_time(e1)
     if dist is not None:
         t = torch.tensor([ms], device="cuda")
@@ -262,50 +518,35 @@ def ours(args, w, rank, world, dist):
     ms_per_step = ms / args.steps
     value = world * nt * args.steps / (ms / 1e3)
 
-    # ---- per-kernel times: same replays with CUDA events around every launch
-    model.profile_enable(True)
-    for _ in range(2):
-        step()
-    qp.check(model.sync_status(sp), "profile warmup")
-    model.profile_enable(True)  # reset the totals
-    torch.cuda.synchronize()
-    for _ in range(args.steps):
-        step()
-    qp.check(model.sync_status(sp), "profiled region")
-    prof = model.profile_read()  # the last replay's launches and times
-    model.profile_enable(False)
+    # ---- per-kernel times: replays with CUDA events around every launch
+    prof = p.profile(args.steps)
     launches_per_step = sum(n for n, _ in prof.values())
 
     # ---- end-to-end through the host-buffer call (H2D inputs, D2H logits inside)
-    h_ids = torch.from_numpy(ids).pin_memory().numpy()
-    h_pos = torch.from_numpy(pos).pin_memory().numpy()
+    h_ids = torch.from_numpy(p.ids).pin_memory().numpy()
+    h_pos = torch.from_numpy(p.pos).pin_memory().numpy()
     h_logits = torch.empty((n_out, cfg.n_vocab), dtype=torch.float32).pin_memory().numpy()
     for _ in range(3):
-        model.prefill_n(kv, h_ids, h_pos, n_out, h_logits)
+        model.prefill_n(p.kv, h_ids, h_pos, n_out, h_logits)
     barrier()
     t0 = time.perf_counter()
     for _ in range(args.steps):
-        model.prefill_n(kv, h_ids, h_pos, n_out, h_logits)
+        model.prefill_n(p.kv, h_ids, h_pos, n_out, h_logits)
     e2e_s = time.perf_counter() - t0
     if dist is not None:
         t = torch.tensor([e2e_s], device="cuda")
         dist.all_reduce(t, op=dist.ReduceOp.MAX)
         e2e_s = float(t.item())
     e2e_value = world * nt * args.steps / e2e_s
+    p.free()
 
     if rank != 0:
+        model.free()
         return
-    hbm, bf16, peak_src = _peaks()
+    gemm_stats, attn_stats = gemm_and_attention_stats(cfg, w, prof, bf16)
     flops = gemm_flops(cfg, nt)
     # dominant kernel by device time
     dom = max(prof.items(), key=lambda kv_: kv_[1][1])[0]
-    gemm_stats = {}
-    for k, f in flops.items():
-        n, tot = prof.get(k, (0, 0.0))
-        if n:
-            avg_ms = tot / n
-            gemm_stats[k] = {"avg_us": 1e3 * avg_ms, "tflops": f / (avg_ms / 1e3) / 1e12,
-                             "frac_of_bf16_peak": f / (avg_ms / 1e3) / 1e12 / bf16}
     if dom in flops:
         n, tot = prof[dom]
         avg_ms = tot / n
@@ -319,12 +560,7 @@ def ours(args, w, rank, world, dist):
         roof = {"kernel": dom, "bound": "hbm", "achieved": None, "peak": hbm, "unit": "GB/s",
                 "frac": None, "traffic": profiled_traffic(dom, w.name)}
     mm, lm, attn = forward_macs(cfg, nt, w.p0, n_out)
-    # forward roofline: GEMM + attention flops at the tensor peak, lm_head and
-    # the hidden-state traffic at HBM bandwidth
-    # lm_head: its weights read once (Q8_0 bytes) or its flops, whichever is longer
-    lm_bytes = cfg.n_vocab * cfg.n_embd * 34 / 32
-    t_star = (2 * mm / (bf16 * 1e12) + 2 * attn / (bf16 * 1e12)
-              + max(lm_bytes / (hbm * 1e9), 2 * lm / (bf16 * 1e12)))
+    t_star, parts = forward_roofline(cfg, nt, w.p0, n_out, hbm, bf16)
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": max(3, args.warmup), "ms_per_step": ms_per_step, "higher_is_better": True,
@@ -337,16 +573,36 @@ def ours(args, w, rank, world, dist):
                    "parallelism": f"replicas x{world}"},
         "roofline": roof,
         "gemm": gemm_stats,
+        "attention": attn_stats,
         "forward_roofline": {"t_star_ms": 1e3 * t_star, "frac": 1e3 * t_star / ms_per_step,
+                             "parts_ms": {k: 1e3 * v for k, v in parts.items()},
                              "matmul_macs": mm, "attn_macs": attn, "lm_head_macs": lm},
-        "kernels_last_step": {k: {"launches": n, "ms": t} for k, (n, t) in prof.items() if n},
+        "kernels_per_step": {k: {"launches": n, "ms": t} for k, (n, t) in prof.items() if n},
         "gpu_launches": int(launches_per_step * args.steps),
         "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": 2 * nt * 4,
                 "d2h_bytes_per_step": n_out * cfg.n_vocab * 4},
         "clocks": clk.summary(),
     }
-    if not args.no_cpu_baseline and world >= 1 and rank == 0:
+    if not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(w)
+    if not args.no_per_config and world == 1:
+        per = {}
+        with ClockSampler(dev) as clk2:
+            models = {cfg.name: model}
+            for name in CONFIGS:
+                wc = synth.WORKLOADS[name]
+                if wc.model.name not in models:
+                    for m_ in models.values():
+                        m_.free()
+                    models = {wc.model.name: load_gpu_model(qp, wc.model)}
+                per[name] = measure_config(qp, models[wc.model.name], wc, hbm, bf16, 1.0,
+                                           not args.no_cpu_baseline)
+            for m_ in models.values():
+                m_.free()
+        line["per_config"] = per
+        line["per_config_clocks"] = clk2.summary()
+    else:
+        model.free()
     print(json.dumps(line), flush=True)
 
 
@@ -358,6 +614,7 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default=WORKLOAD, choices=sorted(synth.WORKLOADS))
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-per-config", action="store_true")
     args = ap.parse_args()
     w = synth.WORKLOADS[args.workload]
     world = int(os.environ.get("WORLD_SIZE", 1))

@@ -35,6 +35,8 @@
  *      normalized over its head_dim values as in R3, with one weight vector
  *      of head_dim entries per layer for Q and one for K, after the bias and
  *      before RoPE.  Models with QK-norm carry no Q/K/V bias.
+ *   R9 Positions within one call are distinct; a repeated position is
+ *      rejected as a bad argument before anything is written.
  *
  * Every floating-point statement below is evaluated exactly as written: the
  * file is compiled with -ffp-contract=off and without fast-math.
@@ -50,6 +52,7 @@
  *                      property, a single-unit-vector closed form
  *   attention       -- brute-force masked softmax(QK^T/sqrt(d))V (numpy)
  *   swiglu          -- float64 closed form (numpy)
+ *   argmax          -- brute force over vectors with planted ties
  *   model prefill   -- invariants only: causality, one-shot == token by
  *                      token, n_out=1 == last row of n_out=nt, written-slot
  *                      set, zero-weight special case.  The composition itself
@@ -558,7 +561,7 @@ int orc_kv_write(orc_kv* kv, int layer, int which, int row0, int nrows, const fl
  *              s = Q8_0(silu(x.Wg) * (x.Wu));  h = h + s.Wd
  *   logits = Q8_0(rmsnorm(h) * output_norm) . W_out   (W_out = tok_embd if tied)
  *
- * Returns 0; -1 bad arguments; -2 a position outside [0, n_ctx) ([P09]
+ * Returns 0; -1 bad arguments (including a repeated position, R9); -2 a position outside [0, n_ctx) ([P09]
  * section 3.4: positions must stay below n_ctx); -3 a token id outside the
  * vocabulary; -4 missing tensors.  Errors are detected before anything is
  * written.
@@ -572,6 +575,15 @@ int orc_prefill(orc_model* m, orc_kv* kv, const int32_t* ids, const int32_t* pos
   if (!m || !kv || !ids || !pos || nt <= 0 || n_out <= 0 || n_out > nt || !logits) return -1;
   for (int t = 0; t < nt; ++t)
     if (pos[t] < 0 || pos[t] >= kv->n_ctx) return -2;
+  /* reading R9: one call writes each region row at most once ([P09] section
+     2.2 gives every token its own slot); a repeated position is a bad argument */
+  {
+    std::vector<char> seen(kv->n_ctx, 0);
+    for (int t = 0; t < nt; ++t) {
+      if (seen[pos[t]]) return -1;
+      seen[pos[t]] = 1;
+    }
+  }
   const orc_hparams& hp = m->hp;
   for (int t = 0; t < nt; ++t)
     if (ids[t] < 0 || ids[t] >= hp.n_vocab) return -3;

@@ -24,6 +24,10 @@ MINFER_Q8_0 = 8
 ERR_NAMES = {0: "OK", -1: "ERR_ARG", -2: "ERR_POS_OOB", -3: "ERR_TOKEN_OOB",
              -4: "ERR_MISSING_TENSOR", -5: "ERR_SHAPE", -6: "ERR_CUDA", -7: "ERR_OOM",
              -8: "ERR_DEVICE", -9: "ERR_STATE", -10: "ERR_TOO_LARGE"}
+# device status codes (minfer_device_status): the bounded wait that gave up
+DEV_NAMES = {0: "DEV_OK", 1: "DEV_TIMEOUT_TMA_EMPTY", 2: "DEV_TIMEOUT_MMA_FULL",
+             3: "DEV_TIMEOUT_MMA_SLOT", 4: "DEV_TIMEOUT_EPILOGUE", 5: "DEV_TIMEOUT_DRAIN",
+             6: "DEV_TIMEOUT_ATTN"}
 
 # every entry point declared in include/minfer.h: name -> (argtypes, restype)
 _P, _I, _I64, _F = ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.c_float
@@ -75,6 +79,7 @@ SIGNATURES = {
     "minfer_op_qknorm_rope_store": ([_P, _P, _P, _P, _F, _P, _I, _I, _I, _I, _F, _I, _P, _P, _P], _I),
     "minfer_strerror": ([_I], ctypes.c_char_p),
     "minfer_device_status": ([_P], _I),
+    "minfer_debug_fault": ([_P, _I, _I64], _I),
 }
 
 
@@ -200,6 +205,15 @@ class Model:
         """Capture layer `layer`'s intermediates on the next prefill (-1: off)."""
         check(lib().minfer_debug_layer(self.ptr, layer), "debug_layer")
 
+    def debug_fault(self, layer: int, wait_limit_ns: int = 0):
+        """Test hook: layer >= 0 makes that layer's Q|K|V GEMM withhold one
+        operand stage and every GEMM wait give up after wait_limit_ns;
+        -1 turns it off."""
+        check(lib().minfer_debug_fault(self.ptr, layer, wait_limit_ns), "debug_fault")
+
+    def device_status(self) -> int:
+        return lib().minfer_device_status(self.ptr)
+
     def profile_enable(self, on: bool = True):
         check(lib().minfer_profile_enable(self.ptr, int(on)), "profile_enable")
 
@@ -310,10 +324,14 @@ def op_gemm(xq, xd, wq, wd, K: int, dots: bool = False):
 
 
 def op_gemm_noalloc(xq, xd, wq, wd, K: int):
-    """minfer_op_gemm without device allocation (fixed 32 MiB scratch in the library)."""
+    """minfer_op_gemm without device allocation (fixed 32 MiB scratch in the
+    library).  The call runs on the library's own stream, so the operands
+    must be complete when it starts: the current stream is synchronized
+    first."""
     import torch
     M, N = xq.shape[0], wq.shape[0]
-    y = torch.zeros((M, N), dtype=torch.float32, device=xq.device)
+    y = torch.empty((M, N), dtype=torch.float32, device=xq.device)
+    torch.cuda.current_stream(xq.device).synchronize()
     check(lib().minfer_op_gemm_noalloc(_ptr(xq), _ptr(xd), M, _ptr(wq), _ptr(wd), N, K, _ptr(y)),
           "op_gemm_noalloc")
     return y

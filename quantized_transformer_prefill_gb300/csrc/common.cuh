@@ -24,14 +24,16 @@ constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s
 constexpr uint32_t kMaxPolls = 1u << 24;
 constexpr uint32_t kSuspendHintNs = 1000000u;  // at most 1 ms per poll
 
-// Device-side status codes written into the per-model status word.
+// Device-side status codes written into the per-model status word (the
+// MINFER_DEV_* codes of the C ABI).
 enum : int {
-  kDevOk = 0,
-  kDevTimeoutTmaEmpty = 1,
-  kDevTimeoutMmaFull = 2,
-  kDevTimeoutMmaSlot = 3,
-  kDevTimeoutEpilogue = 4,
-  kDevTimeoutDrain = 5,
+  kDevOk = MINFER_DEV_OK,
+  kDevTimeoutTmaEmpty = MINFER_DEV_TIMEOUT_TMA_EMPTY,
+  kDevTimeoutMmaFull = MINFER_DEV_TIMEOUT_MMA_FULL,
+  kDevTimeoutMmaSlot = MINFER_DEV_TIMEOUT_MMA_SLOT,
+  kDevTimeoutEpilogue = MINFER_DEV_TIMEOUT_EPILOGUE,
+  kDevTimeoutDrain = MINFER_DEV_TIMEOUT_DRAIN,
+  kDevTimeoutAttn = MINFER_DEV_TIMEOUT_ATTN,
 };
 
 __device__ __forceinline__ void set_error(int* err, int code) {
@@ -80,16 +82,35 @@ __device__ __forceinline__ uint64_t global_ns() {
 }
 
 // Wait until the phase with the given parity has completed.  Returns false
-// (and records `code` in *err) when the time or poll limit runs out.
-__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, int* err, int code) {
+// (and records `code` in *err) when the time limit (limit_ns of the global
+// timer; a test may shorten it) or the poll limit runs out.
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, int* err, int code,
+                                          uint64_t limit_ns = kWaitLimitNs) {
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = global_ns();
   for (uint32_t i = 0; i < kMaxPolls; ++i) {
     if (mbar_try_wait(bar, parity)) return true;
-    if (global_ns() - t0 > kWaitLimitNs) break;
+    if (global_ns() - t0 > limit_ns) break;
   }
   set_error(err, code);
   return false;
+}
+
+// mbar_wait by every lane of a warp, with one verdict for the whole warp (a
+// lane that saw the phase complete just after another gave up follows the
+// warp), so the .sync.aligned tcgen05 instructions that follow stay
+// convergent.
+__device__ __forceinline__ bool mbar_wait_warp(uint64_t* bar, uint32_t parity, int* err, int code,
+                                               uint64_t limit_ns = kWaitLimitNs) {
+  const bool ok = mbar_wait(bar, parity, err, code, limit_ns);
+  return __all_sync(0xffffffffu, ok);
+}
+
+// The model's status words: [0] input validation (a MINFER error code),
+// [1] the first bounded wait that gave up (a kDev code).  Kernels that write
+// the KV regions or the logits skip those writes unless both are clear.
+__device__ __forceinline__ bool status_clear(const int* status) {
+  return status == nullptr || (status[0] == 0 && status[1] == 0);
 }
 
 // ------------------------------------------------------------------ TMA
@@ -201,6 +222,16 @@ __device__ __forceinline__ void tmem_ld16x256x4(uint32_t taddr, uint32_t (&r)[16
 }
 __device__ __forceinline__ void tmem_wait_ld() {
   asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+}
+// The same wait, with the 32 destination registers of the load it completes
+// passed through it: every use of them depends on the wait, so the compiler
+// cannot schedule one before it (a plain wait orders memory, not registers).
+__device__ __forceinline__ void tmem_wait_ld_regs(uint32_t (&r)[32]) {
+  asm volatile("tcgen05.wait::ld.sync.aligned;"
+               : "+r"(r[0]),"+r"(r[1]),"+r"(r[2]),"+r"(r[3]),"+r"(r[4]),"+r"(r[5]),"+r"(r[6]),"+r"(r[7]),"+r"(r[8]),"+r"(r[9]),"+r"(r[10]),"+r"(r[11]),"+r"(r[12]),"+r"(r[13]),"+r"(r[14]),"+r"(r[15]),
+                 "+r"(r[16]),"+r"(r[17]),"+r"(r[18]),"+r"(r[19]),"+r"(r[20]),"+r"(r[21]),"+r"(r[22]),"+r"(r[23]),"+r"(r[24]),"+r"(r[25]),"+r"(r[26]),"+r"(r[27]),"+r"(r[28]),"+r"(r[29]),"+r"(r[30]),"+r"(r[31])
+               :
+               : "memory");
 }
 
 // Shared-memory matrix descriptor for a K-major operand tile stored with the

@@ -51,7 +51,6 @@ constexpr int kPvWarp = 10;
 constexpr int kSmWarps = 8;  // two per TMEM lane quadrant: two threads per query row
 constexpr int kTcMaxSplits = 8;  // CTAs per cluster (portable cluster size)
 
-enum : int { kDevTimeoutAttn = 6 };
 // Largest rise of a row's scores over its reference max (log2 units) that is
 // absorbed without rescaling O: P then stays below 2^8.
 constexpr float kLazyMax = 8.0f;

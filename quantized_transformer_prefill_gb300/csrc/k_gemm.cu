@@ -81,8 +81,13 @@ struct Args {
   int64_t n_out_cols;
   int32_t* dots;
   int* err;
+  uint64_t wait_ns;  // time limit of every bounded wait
+  int skip_stage;    // test hook: a stage CTA 0's producer withholds (-1: none)
 };
 
+// silu(g) * u = (g / (1 + e^-g)) * u in f32, one correctly rounded division
+// (a reciprocal and two products instead flip measurably more Q8_0 scales of
+// the result against the float64 value)
 __device__ __forceinline__ float silu_mul(float g, float u) {
   return __fmul_rn(__fdiv_rn(g, __fadd_rn(1.0f, expf(-g))), u);
 }
@@ -158,16 +163,19 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int s1 = min(p.n_stages, s0 + p.stages_per_split);
         for (int s = s0; s < s1; ++s, ++it) {
           const int st = it % C::STAGES;
-          if (!mbar_wait(&empty[st], ((it / C::STAGES) & 1) ^ 1, p.err, kDevTimeoutTmaEmpty)) {
+          if (!mbar_wait(&empty[st], ((it / C::STAGES) & 1) ^ 1, p.err, kDevTimeoutTmaEmpty, p.wait_ns)) {
             ok = false;
             break;
           }
+          // test hook: withhold this stage (no loads, no arrival), so the
+          // consumers' bounded waits on it run out
+          if (it == p.skip_stage && blockIdx.x == 0) continue;
           mbar_arrive_expect_tx(&full[st], C::STAGE_TX);
           tma_load_2d(sA + st * C::A_BYTES, &tmA, &full[st], s * kBK, mt * kBM);
           tma_load_2d(sB + st * C::B_BYTES, &tmB, &full[st], s * kBK, ntile * BN);
           n_ab = it + 1;
           const int ss = it % C::SSTAGES;
-          if (!mbar_wait(&sempty[ss], ((it / C::SSTAGES) & 1) ^ 1, p.err, kDevTimeoutTmaEmpty)) {
+          if (!mbar_wait(&sempty[ss], ((it / C::SSTAGES) & 1) ^ 1, p.err, kDevTimeoutTmaEmpty, p.wait_ns)) {
             ok = false;
             break;
           }
@@ -180,9 +188,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (!ok) {
         // drain the loads that may still be in flight before the CTA exits
         for (int j = max(0, n_ab - C::STAGES); j < n_ab; ++j)
-          mbar_wait(&full[j % C::STAGES], (j / C::STAGES) & 1, p.err, kDevTimeoutDrain);
+          mbar_wait(&full[j % C::STAGES], (j / C::STAGES) & 1, p.err, kDevTimeoutDrain, p.wait_ns);
         for (int j = max(0, n_s - C::SSTAGES); j < n_s; ++j)
-          mbar_wait(&sfull[j % C::SSTAGES], (j / C::SSTAGES) & 1, p.err, kDevTimeoutDrain);
+          mbar_wait(&sfull[j % C::SSTAGES], (j / C::SSTAGES) & 1, p.err, kDevTimeoutDrain, p.wait_ns);
       }
     }
   } else if (warp == 1) {
@@ -198,7 +206,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int s1 = min(p.n_stages, s0 + p.stages_per_split);
         for (int s = s0; s < s1 && ok; ++s, ++it) {
           const int st = it % C::STAGES;
-          if (!mbar_wait(&full[st], (it / C::STAGES) & 1, p.err, kDevTimeoutMmaFull)) {
+          if (!mbar_wait(&full[st], (it / C::STAGES) & 1, p.err, kDevTimeoutMmaFull, p.wait_ns)) {
             ok = false;
             break;
           }
@@ -208,7 +216,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
           for (int blk = 0; blk < 2; ++blk) {
             const int slot = sit % C::NSLOT;
-            if (!mbar_wait(&tempty[slot], ((sit / C::NSLOT) & 1) ^ 1, p.err, kDevTimeoutMmaSlot)) {
+            if (!mbar_wait(&tempty[slot], ((sit / C::NSLOT) & 1) ^ 1, p.err, kDevTimeoutMmaSlot, p.wait_ns)) {
               ok = false;
               break;
             }
@@ -229,7 +237,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       // every MMA issued must have landed before TMEM is released
       if (sit > 0) {
         const int j = sit - 1;
-        mbar_wait(&tfull[j % C::NSLOT], (j / C::NSLOT) & 1, p.err, kDevTimeoutDrain);
+        mbar_wait(&tfull[j % C::NSLOT], (j / C::NSLOT) & 1, p.err, kDevTimeoutDrain, p.wait_ns);
       }
     }
   } else {
@@ -264,14 +272,16 @@ __global__ void __launch_bounds__(kThreads, 1)
 
       for (int s = s0; s < s1 && ok; ++s, ++it) {
         const int ss = it % C::SSTAGES;
-        if (!mbar_wait(&sfull[ss], (it / C::SSTAGES) & 1, p.err, kDevTimeoutEpilogue)) {
+        if (!mbar_wait_warp(&sfull[ss], (it / C::SSTAGES) & 1, p.err, kDevTimeoutEpilogue,
+                            p.wait_ns)) {
           ok = false;
           break;
         }
 #pragma unroll 1
         for (int blk = 0; blk < 2; ++blk) {
           const int slot = sit % C::NSLOT;
-          if (!mbar_wait(&tfull[slot], (sit / C::NSLOT) & 1, p.err, kDevTimeoutEpilogue)) {
+          if (!mbar_wait_warp(&tfull[slot], (sit / C::NSLOT) & 1, p.err, kDevTimeoutEpilogue,
+                              p.wait_ns)) {
             ok = false;
             break;
           }
@@ -281,7 +291,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           uint32_t ra[32], rb[32];  // rows g, g+8 and g+16, g+24
           tmem_ld16x256(taddr, ra);
           tmem_ld16x256(taddr + (16u << 16), rb);
-          tmem_wait_ld();
+          tmem_wait_ld_regs(ra);
+          tmem_wait_ld_regs(rb);
           // slot read: hand it back to the MMA issuer
           tc_fence_before();
           __syncwarp();
@@ -298,7 +309,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 for (int e = 0; e < 2; ++e) {
                   const int n = ncol0 + 8 * k + 2 * t4 + e;
                   const uint32_t v = rr < 2 ? ra[4 * k + 2 * rr + e] : rb[4 * k + 2 * (rr - 2) + e];
-                  if (n < p.N) p.dots[((int64_t)m * p.N + n) * p.nb + b] = __float2int_rn(__uint_as_float(v));
+                  if (n < p.N)
+                    p.dots[((int64_t)m * p.N + n) * p.nb + b] = __float2int_rn(__uint_as_float(v));
                 }
             }
           }
@@ -348,6 +360,13 @@ __global__ void __launch_bounds__(kThreads, 1)
             amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
             amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 2));
             if (m >= p.M) continue;
+            if (p.out) {
+              // debug capture: the f32 SwiGLU values this epilogue quantizes
+              float* fo = p.out + (int64_t)m * p.ldo + j0 + 2 * t4;
+#pragma unroll
+              for (int k = 0; k < 4; ++k)
+                *reinterpret_cast<float2*>(fo + 8 * k) = make_float2(sv[2 * k], sv[2 * k + 1]);
+            }
             const float d = __fdiv_rn(amax, 127.0f);
             const float id = q8_inv(d);
             __half* dst = p.q_out + (int64_t)m * p.ldq + j0 + 2 * t4;
@@ -383,6 +402,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   }
 
+  if (warp >= 2) tmem_wait_ld();  // no TMEM load of this warp outlives the allocation
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
@@ -450,6 +470,8 @@ cudaError_t launch_bn(const GemmLaunch& g, const GemmMaps& maps, int num_sms, cu
   a.n_out_cols = g.n_out_cols;
   a.dots = g.dots;
   a.err = g.err;
+  a.wait_ns = g.wait_ns ? g.wait_ns : kWaitLimitNs;
+  a.skip_stage = g.skip_stage;
   const int total = a.m_tiles * a.n_tiles * a.splits;
   const int grid = std::max(1, std::min(total, num_sms));
   return launch_pdl(gemm_q8_kernel<BN, EPI>, grid, kThreads, C::SMEM, st, maps.a, maps.b, maps.sa,
@@ -469,7 +491,7 @@ GemmPlan gemm_plan(int64_t M, int64_t N, int nb, int num_sms, bool allow_split) 
   GemmPlan p;
   const int64_t mt = (M + kBM - 1) / kBM;
   const int stages = (nb + 1) / 2;
-  // wide N: 256-column tiles when they still fill the machine
+  // one tile width (128 columns) for every shape
   p.bn = 128;
   const int64_t tiles = mt * ((N + p.bn - 1) / p.bn);
   p.splits = 1;

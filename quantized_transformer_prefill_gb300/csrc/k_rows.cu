@@ -235,7 +235,7 @@ __device__ __forceinline__ void store_q(const RopeStoreArgs& a, int64_t o, float
   }
 }
 
-__global__ void rope_store_kernel(const RopeStoreArgs a) {
+__global__ void __launch_bounds__(1024) rope_store_kernel(const RopeStoreArgs a) {
   pdl_trigger();
   pdl_wait();
   const int t = blockIdx.x;
@@ -243,7 +243,7 @@ __global__ void rope_store_kernel(const RopeStoreArgs a) {
   // an out-of-range position is reported by validation; it only selects a
   // table row here (clamped) and never a region row
   const bool write_kv =
-      ((a.status == nullptr) || (*a.status == 0)) && p_in >= 0 && p_in < a.n_ctx;
+      status_clear(a.status) && p_in >= 0 && p_in < a.n_ctx;
   const int p = (p_in >= 0 && p_in < a.n_ctx) ? p_in : 0;
   const int half = a.hd >> 1;
   const int hshift = half == 64 ? 6 : 5;  // head_dim is 64 or 128
@@ -308,7 +308,7 @@ __global__ void rope_store_kernel(const RopeStoreArgs a) {
 // here), then the pairs are normalized, weighted and rotated.
 constexpr int kMaxQkHeads = 128;
 
-__global__ void rope_store_qknorm_kernel(const RopeStoreArgs a) {
+__global__ void __launch_bounds__(1024) rope_store_qknorm_kernel(const RopeStoreArgs a) {
   extern __shared__ float xs[];  // [(nh + nkv) * hd]
   __shared__ float rs[kMaxQkHeads];
   pdl_trigger();
@@ -316,7 +316,7 @@ __global__ void rope_store_qknorm_kernel(const RopeStoreArgs a) {
   const int t = blockIdx.x;
   const int p_in = a.pos[t];
   const bool write_kv =
-      ((a.status == nullptr) || (*a.status == 0)) && p_in >= 0 && p_in < a.n_ctx;
+      status_clear(a.status) && p_in >= 0 && p_in < a.n_ctx;
   const int p = (p_in >= 0 && p_in < a.n_ctx) ? p_in : 0;
   const int half = a.hd >> 1;
   const int hshift = half == 64 ? 6 : 5;  // head_dim is 64 or 128
@@ -384,40 +384,63 @@ __global__ void rope_store_qknorm_kernel(const RopeStoreArgs a) {
 }
 
 // ---------------------------------------------------------------- one-row GEMV
-// One warp per output row.  Lane l reads 16 code bytes of each 512-byte chunk
-// (half of a Q8_0 block); dp4a gives the integer partial, the lane pair adds
-// up the block's exact int32 dot, the even lane scales it by dw * da.
-__global__ void gemv_kernel(const GemvArgs a) {
+// y[n] = sum_b dw[n][b] * dx[b] * dot_b, one output row n at a time per warp
+// slot.  Lane l reads bytes 16 l .. 16 l + 15 of each 512-byte chunk of a
+// row's codes (half of a Q8_0 block, coalesced across the warp); dp4a gives
+// the integer partial and the lane pair (l, l ^ 1) adds up the block's exact
+// int32 dot, which the even lane scales by dw * dx.  A warp owns R rows and
+// issues every load of all of them before any arithmetic, so R times more
+// bytes are in flight per lane than with one row per warp: the kernel is
+// bound by HBM, and the number of bytes in flight sets how close it gets.
+constexpr int kGemvWarps = 8;
+
+template <int R>
+__global__ void __launch_bounds__(32 * kGemvWarps) gemv_kernel(const GemvArgs a) {
   pdl_trigger();
   pdl_wait();
   const int lane = threadIdx.x & 31;
-  const int64_t n = (int64_t)blockIdx.x * (blockDim.x / 32) + (threadIdx.x >> 5);
-  if (n >= a.N) return;
-  const int8_t* wr = a.wq + n * a.kpad;
-  const float* wsr = a.ws + n * a.nb;
-  float acc = 0.f;
+  const int64_t n0 = ((int64_t)blockIdx.x * kGemvWarps + (threadIdx.x >> 5)) * R;
+  if (n0 >= a.N) return;
+  float acc[R];
+#pragma unroll
+  for (int r = 0; r < R; ++r) acc[r] = 0.f;
   for (int64_t c = 0; c < a.kpad; c += 512) {
     const int64_t k = c + 16 * lane;
-    int isum = 0;
-    if (k < a.kpad) {
-      const int4 w = *reinterpret_cast<const int4*>(wr + k);
-      const int4 x = *reinterpret_cast<const int4*>(a.xq + k);
-      isum = __dp4a(w.x, x.x, isum);
-      isum = __dp4a(w.y, x.y, isum);
-      isum = __dp4a(w.z, x.z, isum);
-      isum = __dp4a(w.w, x.w, isum);
+    const bool in = k < a.kpad;
+    const int b = (int)(k >> 5);
+    int4 w[R];
+    float dw[R];
+#pragma unroll
+    for (int r = 0; r < R; ++r) {
+      const int64_t n = n0 + r;
+      const bool ok = in && n < a.N;
+      w[r] = ok ? __ldg(reinterpret_cast<const int4*>(a.wq + n * a.kpad + k)) : make_int4(0, 0, 0, 0);
+      dw[r] = ok ? __ldg(a.ws + n * a.nb + b) : 0.f;
     }
-    isum += __shfl_xor_sync(0xffffffffu, isum, 1);
-    if (!(lane & 1) && k < a.kpad) {
-      const int b = (int)(k / 32);
-      acc = fmaf((float)isum, __fmul_rn(wsr[b], a.xs[b]), acc);
+    const int4 x = in ? *reinterpret_cast<const int4*>(a.xq + k) : make_int4(0, 0, 0, 0);
+    const float dx = in ? a.xs[b] : 0.f;
+#pragma unroll
+    for (int r = 0; r < R; ++r) {
+      int isum = __dp4a(w[r].x, x.x, 0);
+      isum = __dp4a(w[r].y, x.y, isum);
+      isum = __dp4a(w[r].z, x.z, isum);
+      isum = __dp4a(w[r].w, x.w, isum);
+      isum += __shfl_xor_sync(0xffffffffu, isum, 1);
+      if (!(lane & 1)) acc[r] = fmaf((float)isum, __fmul_rn(dw[r], dx), acc[r]);
     }
   }
 #pragma unroll
-  for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
-  if (lane == 0) {
-    if (a.status && *a.status != 0) return;
-    a.y[n] = a.resid ? __fadd_rn(a.resid[n], acc) : acc;
+  for (int r = 0; r < R; ++r)
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) acc[r] += __shfl_xor_sync(0xffffffffu, acc[r], o);
+  if (lane < R && n0 + lane < a.N) {
+    if (!status_clear(a.status)) return;
+    float v = acc[0];
+#pragma unroll
+    for (int r = 1; r < R; ++r)
+      if (lane == r) v = acc[r];
+    const int64_t n = n0 + lane;
+    a.y[n] = a.resid ? __fadd_rn(a.resid[n], v) : v;
   }
 }
 
@@ -508,7 +531,7 @@ __global__ void copy_if_ok_kernel(const float* __restrict__ src, float* dst, int
                                   const int* status) {
   pdl_trigger();
   pdl_wait();
-  if (*status != 0) return;
+  if (!status_clear(status)) return;
   for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n;
        i += (int64_t)gridDim.x * blockDim.x)
     dst[i] = src[i];
@@ -593,8 +616,21 @@ cudaError_t rope_store_launch(const RopeStoreArgs& a, cudaStream_t st) {
 }
 
 cudaError_t gemv_launch(const GemvArgs& a, cudaStream_t st) {
-  const int warps = 8;
-  return launch_pdl(gemv_kernel, (unsigned)((a.N + warps - 1) / warps), 32 * warps, 0, st, a);
+  // the most rows per warp that still gives every SM two CTAs
+  const int64_t per_cta[4] = {8 * kGemvWarps, 4 * kGemvWarps, 2 * kGemvWarps, kGemvWarps};
+  int pick = 3;
+  for (int i = 0; i < 4; ++i)
+    if ((a.N + per_cta[i] - 1) / per_cta[i] >= 2 * a.num_sms) {
+      pick = i;
+      break;
+    }
+  const unsigned grid = (unsigned)((a.N + per_cta[pick] - 1) / per_cta[pick]);
+  switch (pick) {
+    case 0: return launch_pdl(gemv_kernel<8>, grid, 32 * kGemvWarps, 0, st, a);
+    case 1: return launch_pdl(gemv_kernel<4>, grid, 32 * kGemvWarps, 0, st, a);
+    case 2: return launch_pdl(gemv_kernel<2>, grid, 32 * kGemvWarps, 0, st, a);
+    default: return launch_pdl(gemv_kernel<1>, grid, 32 * kGemvWarps, 0, st, a);
+  }
 }
 
 cudaError_t gemv_to_gemm_launch(const int8_t* q, const float* sc, int64_t rows, int nb,

@@ -63,7 +63,8 @@ GemmPlan gemm_plan(int64_t M, int64_t N, int nb, int num_sms, bool allow_split);
 // y = A . B^T on the tensor cores.  A: activations (rows = M), B: weights
 // (rows = N).  Epilogue kEpiF32 writes split s to out + s * split_stride.
 // kEpiSwiGLU expects B rows interleaved in groups of 32 gate / 32 up rows and
-// writes codes [M][ldq] fp16 and scales [nbF][ldqs] f32.
+// writes codes [M][ldq] fp16 and scales [nbF][ldqs] f32; with `out` set it
+// also writes the f32 values it quantized to out [M][ldo] (debug capture).
 struct GemmLaunch {
   GemmOperand A, B;
   int64_t M = 0, N = 0;
@@ -78,6 +79,11 @@ struct GemmLaunch {
   int64_t n_out_cols = 0;  // kEpiSwiGLU: padded count of SwiGLU outputs
   int32_t* dots = nullptr;
   int* err = nullptr;
+  // test hook (off by default): the time limit of every bounded wait (0: the
+  // default) and one K stage that CTA 0's producer withholds (-1: none), so
+  // that the MMA issuer's wait on it runs out
+  uint64_t wait_ns = 0;
+  int skip_stage = -1;
 };
 
 // Tensor maps are built once per (buffer, shape) and cached by the caller.
@@ -143,7 +149,7 @@ struct RopeStoreArgs {
   __half* vt[2] = {nullptr, nullptr};  // fp16 hi/lo of V transposed: [nkv*hd][vt_ld] (key-major)
   int64_t vt_ld = 0;
   __half* q_planes[2] = {nullptr, nullptr};  // optional fp16 hi/lo of the rotated Q [nt][nh*hd]
-  const int* status = nullptr;  // skip all writes to the regions when *status != 0
+  const int* status = nullptr;  // the model's two status words: no region write unless both are 0
   // Qwen3 QK-norm (null: none): per-head RMSNorm weights [hd] of Q and of K
   const float* q_norm = nullptr;
   const float* k_norm = nullptr;
@@ -212,7 +218,8 @@ struct GemvArgs {
   const float* xs = nullptr;
   float* y = nullptr;
   const float* resid = nullptr;  // y = resid + W.x when set (may alias y)
-  const int* status = nullptr;   // skip writing y when *status != 0
+  const int* status = nullptr;   // the model's two status words: no write of y unless both are 0
+  int num_sms = 152;             // rows per warp are chosen to give every SM two CTAs
 };
 cudaError_t gemv_launch(const GemvArgs& a, cudaStream_t stream);
 
@@ -221,7 +228,7 @@ cudaError_t gemv_launch(const GemvArgs& a, cudaStream_t stream);
 // int8 [rows][nb*32] + f32 [rows][nb] (GEMV layout) -> fp16 codes + block-major scales.
 cudaError_t gemv_to_gemm_launch(const int8_t* q, const float* sc, int64_t rows, int nb,
                                 __half* codes, float* scales, int64_t rows_pad, cudaStream_t stream);
-// dst[0:n] = src[0:n] unless *status != 0.
+// dst[0:n] = src[0:n] when both status words are 0.
 cudaError_t copy_if_ok_launch(const float* src, float* dst, int64_t n, const int* status,
                               cudaStream_t stream);
 cudaError_t swiglu_quant_row_launch(const float* gu, int64_t F, int8_t* q, float* s,

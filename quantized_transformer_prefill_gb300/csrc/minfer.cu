@@ -253,6 +253,9 @@ struct minfer_model {
   float* dump_host = nullptr;
   int dump_max_nt = 0;
   int last_device_status = 0;
+  // test hook of the bounded-wait failure path (minfer_debug_fault)
+  int fault_layer = -1;
+  uint64_t fault_wait_ns = 0;
   bool debug_f32 = false;  // also write the f32 attention output (debug reads)
   // stage capture of one layer (debug): copies of that layer's intermediates
   int dbg_layer = -1;
@@ -583,7 +586,7 @@ struct Launcher {
 
 int gemm_call(minfer_model* m, Launcher& L, int cls, const GemmOperand& A, const GemmW& W,
               int64_t M, int epi, bool allow_split, float* out, int64_t ldo, __half* q_out,
-              int64_t ldq, float* qs_out, int64_t ldqs, int* nsplit_out) {
+              int64_t ldq, float* qs_out, int64_t ldqs, int* nsplit_out, bool fault = false) {
   GemmLaunch g;
   g.A = A;
   g.B = W.op();
@@ -601,6 +604,10 @@ int gemm_call(minfer_model* m, Launcher& L, int cls, const GemmOperand& A, const
   g.ldqs = ldqs;
   g.n_out_cols = m->Fp;
   g.err = m->d_status + 1;
+  if (m->fault_layer >= 0) {
+    g.wait_ns = m->fault_wait_ns;
+    if (fault) g.skip_stage = 0;
+  }
   GemmMaps maps;
   if (gemm_make_maps(g.A, g.B, g.plan.bn, &maps)) {
     snprintf(g_last_error, sizeof g_last_error, "cuTensorMapEncodeTiled failed");
@@ -665,6 +672,7 @@ int enqueue_decode(minfer_model* m, minfer_kv* kv, const int32_t* ids, const int
   auto gemv = [&](int cls, const GemvW& W, int64_t N, int nb, float* y, const float* resid,
                   const int* status) -> int {
     GemvArgs g;
+    g.num_sms = m->num_sms;
     g.wq = W.q;
     g.ws = W.s;
     g.N = N;
@@ -853,7 +861,7 @@ int enqueue_forward(minfer_model* m, minfer_kv* kv, const int32_t* ids, const in
         return rc;
     }
     if ((rc = gemm_call(m, L, kKGemmQKV, xa, Ly.wqkv, nt, kEpiF32, true, w.part, m->qkvN, nullptr,
-                        0, nullptr, 0, &ns)))
+                        0, nullptr, 0, &ns, l == m->fault_layer)))
       return rc;
     {
       RopeStoreArgs r;
@@ -966,8 +974,22 @@ int enqueue_forward(minfer_model* m, minfer_kv* kv, const int32_t* ids, const in
             (rc = dbg_capture_scales(m, st, "f_scales", w.xa_s, m->nbH, ntp, ntp_call)))
           return rc;
       }
-      if ((rc = gemm_call(m, L, kKGemmGU, xa_r, Ly.wgu, mrows, kEpiSwiGLU, false, nullptr, 0, w.xf,
-                          m->Fp, w.xf_s, ntp, nullptr)))
+      float* s_f32 = nullptr;  // debug capture of the f32 values the SwiGLU epilogue quantizes
+      if (cap) {
+        auto& e = m->dbg["s_f32"];
+        const size_t bytes = (size_t)nt * m->Fp * 4;
+        if (e.second < bytes) {
+          if (e.first) cudaFree(e.first);
+          e.first = nullptr;
+          e.second = 0;
+          CK(cudaMalloc(&e.first, bytes));
+          e.second = bytes;
+        }
+        CK(cudaMemsetAsync(e.first, 0, bytes, st));
+        s_f32 = static_cast<float*>(e.first);  // rows as in "s_codes": the carried rows from 0
+      }
+      if ((rc = gemm_call(m, L, kKGemmGU, xa_r, Ly.wgu, mrows, kEpiSwiGLU, false, s_f32, m->Fp,
+                          w.xf, m->Fp, w.xf_s, ntp, nullptr)))
         return rc;
       if (cap) {
         if ((rc = dbg_capture(m, st, "s_codes", w.xf, (size_t)nt * m->Fp * 2)) ||
@@ -1016,6 +1038,7 @@ int enqueue_forward(minfer_model* m, minfer_kv* kv, const int32_t* ids, const in
         return rc;
       {
         GemvArgs g;
+        g.num_sms = m->num_sms;
         g.wq = Ly.wo_v.q;
         g.ws = Ly.wo_v.s;
         g.N = m->H;
@@ -1044,6 +1067,7 @@ int enqueue_forward(minfer_model* m, minfer_kv* kv, const int32_t* ids, const in
         return rc;
       {
         GemvArgs g;
+        g.num_sms = m->num_sms;
         g.wq = Ly.wgu_v.q;
         g.ws = Ly.wgu_v.s;
         g.N = 2 * m->F;
@@ -1060,6 +1084,7 @@ int enqueue_forward(minfer_model* m, minfer_kv* kv, const int32_t* ids, const in
         return rc;
       {
         GemvArgs g;
+        g.num_sms = m->num_sms;
         g.wq = Ly.wd_v.q;
         g.ws = Ly.wd_v.s;
         g.N = m->H;
@@ -1087,6 +1112,7 @@ int enqueue_forward(minfer_model* m, minfer_kv* kv, const int32_t* ids, const in
       {
         const GemvW& out = hp.tied_embeddings ? m->tok_embd : m->output;
         GemvArgs g;
+        g.num_sms = m->num_sms;
         g.wq = out.q;
         g.ws = out.s;
         g.N = m->V;
@@ -1141,7 +1167,7 @@ int run_forward(minfer_model* m, minfer_kv* kv, const int32_t* ids, const int32_
   if (rc) return rc;
   if ((rc = ensure_logits(m, n_out))) return rc;
   m->dump_on = m->dump_host != nullptr && nt <= m->dump_max_nt;
-  const bool dumps = m->dump_on || m->dbg_layer >= 0;
+  const bool dumps = m->dump_on || m->dbg_layer >= 0 || m->fault_layer >= 0;
   if (dumps) {
     // dumps copy to host memory mid-sequence: run eagerly
     m->ev_used = 0;
@@ -1420,9 +1446,12 @@ int minfer_prefill_n(minfer_model* m, const int32_t* token_ids, const int32_t* p
   CK(cudaMemcpyAsync(m->ws.pos, positions, (size_t)n_tokens * 4, cudaMemcpyHostToDevice, st));
   if ((rc = ensure_logits(m, n_out))) return rc;
   if ((rc = run_forward(m, kv, m->ws.ids, m->ws.pos, n_tokens, n_out, m->ws.logits, st))) return rc;
+  // the caller's buffer is written only when the call succeeded
+  if ((rc = finish_status(m, st))) return rc;
   CK(cudaMemcpyAsync(logits_out, m->ws.logits, (size_t)n_out * m->V * 4, cudaMemcpyDeviceToHost,
                      st));
-  return finish_status(m, st);
+  CK(cudaStreamSynchronize(st));
+  return MINFER_OK;
 }
 
 int minfer_prefill_device(minfer_model* m, const int32_t* d_token_ids, const int32_t* d_positions,
@@ -1835,5 +1864,14 @@ const char* minfer_strerror(int code) {
 }
 
 int minfer_device_status(minfer_model* m) { return m ? m->last_device_status : 0; }
+
+int minfer_debug_fault(minfer_model* m, int layer, int64_t wait_limit_ns) {
+  if (!m || layer < -1 || layer >= m->hp.n_layer || (layer >= 0 && wait_limit_ns <= 0))
+    return MINFER_ERR_ARG;
+  std::lock_guard<std::mutex> lk(g_mu);
+  m->fault_layer = layer;
+  m->fault_wait_ns = layer >= 0 ? (uint64_t)wait_limit_ns : 0;
+  return MINFER_OK;
+}
 
 }  // extern "C"

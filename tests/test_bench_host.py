@@ -49,3 +49,36 @@ def test_profiled_traffic_reads_the_committed_summaries():
         assert isinstance(t, int) and t > 1_000_000
     assert bench.profiled_traffic("gemm_down", "qwen2-0.5b-512") is None
     assert bench.profiled_traffic("gemm_gate_up_swiglu", "no-such-workload") is None
+
+
+def test_forward_roofline_limits():
+    """T* with unlimited bandwidth is the forward's flops at the tensor peak
+    (GEMMs, attention and the lm_head); with unlimited compute it is the
+    algorithmic bytes at the bandwidth, counted here step by step."""
+    for name in ("tiny-32", "qwen2-0.5b-512", "qwen2-1.5b-append-1024"):
+        w = synth.WORKLOADS[name]
+        cfg = w.model
+        nt, p0, n_out = w.n_tokens, w.p0, w.n_out
+        mm, lm, attn = bench.forward_macs(cfg, nt, p0, n_out)
+        t, parts = bench.forward_roofline(cfg, nt, p0, n_out, 1e30, 1.0)
+        assert abs(t - 2 * (mm + lm + attn) / 1e12) <= 1e-9 * t
+        assert parts["memory"] < 1e-12 * t
+        # bytes, one step at a time
+        H, q = cfg.n_embd, cfg.n_head * cfg.head_dim
+        kv, F, L, V = cfg.n_head_kv * cfg.head_dim, cfg.n_ff, cfg.n_layer, cfg.n_vocab
+        e = 34 / 32
+        b = nt * H * 5
+        for layer in range(L):
+            r = n_out if layer == L - 1 else nt
+            b += nt * H * (4 + e)                                      # attn_norm
+            b += (q + 2 * kv) * H * e + nt * H * e + nt * (q + 2 * kv) * 4  # QKV GEMM
+            b += 2 * nt * (q + 2 * kv) * 4                             # RoPE + store
+            b += r * q * 4 + (p0 + nt) * 2 * kv * 4 + r * q * e        # attention
+            b += H * q * e + r * q * e + r * H * 4                     # Wo
+            b += r * H * (12 + e)                                      # residual + ffn_norm
+            b += 2 * F * H * e + r * H * e + r * F * e                 # gate/up + SwiGLU out
+            b += H * F * e + r * F * e + r * H * 4                     # down
+            b += 2 * r * H * 4                                         # residual
+        b += n_out * H * (4 + e) + V * H * e + n_out * V * 4           # final norm, lm_head
+        t, _ = bench.forward_roofline(cfg, nt, p0, n_out, 1.0, 1e30)
+        assert abs(t * 1e9 - b) <= 1e-9 * b, (name, t * 1e9, b)

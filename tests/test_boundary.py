@@ -55,6 +55,10 @@ def test_binding_matches_header(libpath):
     d = _defines()
     for code, name in qp.ERR_NAMES.items():
         assert d["MINFER_" + name] == code
+    for code, name in qp.DEV_NAMES.items():
+        assert d["MINFER_" + name] == code
+    assert sorted(k for k in d if k.startswith("MINFER_DEV_")) == \
+        sorted("MINFER_" + n for n in qp.DEV_NAMES.values())
     assert d["MINFER_F32"] == qp.MINFER_F32 and d["MINFER_Q8_0"] == qp.MINFER_Q8_0
 
 
@@ -79,3 +83,32 @@ def test_create_without_gpu_fails_cleanly(libpath):
     hp = qp.hparams_of(synth.TINY)
     rc = qp.lib().minfer_model_create(ctypes.byref(hp), ctypes.byref(ptr))
     assert rc == -6 and not ptr.value
+
+
+_CITATION = re.compile(r'"09 · Prefill"|"05 · Graph build"|walkthrough index')
+
+
+def test_every_declaration_cites_its_passage():
+    """Each entry point of the header is preceded by a comment that names the
+    passage of the pages defining it (page title and section), or says that
+    the pages have no counterpart.  Declarations that follow one another with
+    no comment between them share the comment above the first."""
+    text = open(HEADER).read()
+    last_comment = ""
+    missing = []
+    seen = []
+    for m in re.finditer(r"/\*.*?\*/|\b(minfer_\w+)\s*\(", text, flags=re.S):
+        if m.group(0).startswith("/*"):
+            last_comment = m.group(0)
+            continue
+        # a declaration: the name follows its return type at the start of a line
+        line = text[text.rfind("\n", 0, m.start()) + 1:m.start()]
+        if not re.fullmatch(r"(int|void|const char\*)\s+", line):
+            continue
+        seen.append(m.group(1))
+        # the comment's text with its line-leading '*' markers removed
+        squashed = " ".join(re.sub(r"\n\s*\*(?!/)", " ", last_comment).split())
+        if not (_CITATION.search(squashed) or "no counterpart" in squashed):
+            missing.append(m.group(1))
+    assert sorted(set(seen)) == _declared()
+    assert not missing, f"declarations without a page citation: {missing}"

@@ -1,6 +1,7 @@
-"""Parity at full size: the 1.5B prompt (2048 tokens), the 7B prompt (4096
-tokens) and the 1.5B append (1024 tokens after 3072 cached ones), run by the
-CUDA library exactly as it is timed, checked stage by stage on sampled rows.
+"""Parity at full size: the 0.5B prompt (512 tokens), the 1.5B prompt (2048
+tokens), the 7B prompt (4096 tokens), the 1.5B append (1024 tokens after 3072
+cached ones), the Qwen3 0.6B prompt and the tiny model, run by the CUDA
+library exactly as it is timed, checked stage by stage on sampled rows.
 
 A full oracle forward at these sizes takes the CPU many minutes, and over 28
 layers any implementation that is not bit-identical to it drifts away from it
@@ -152,6 +153,15 @@ def _check_layer(oracle_mod, g, kv, cfg, layer, pos, rows, tail0=0):
     dg, du = (q8_sum_bound(oracle_mod, fq, fd, *Wt.q8[f"ffn_{x}.weight"], H) for x in ("gate", "up"))
     slack = 1.1 * np.abs(up) * dg + (np.abs(gate) + 0.28) * du + 16 * U * np.abs(s_ref)
     _check_quantized(oracle_mod, sq, sd, s_ref, slack)
+    # the epilogue's own f32 values: within the same bound of the oracle's s,
+    # and their Q8_0 (amax over the block, fp16 scale, rounded codes) is the
+    # oracle's quantization of them, bit for bit
+    s_gpu = _f32(g, "s_f32", nt, nbF * 32)[rows - tail0]
+    assert not np.any(s_gpu[:, cfg.n_ff:]), "SwiGLU padding columns not zero"
+    assert np.all(np.abs(s_gpu[:, :cfg.n_ff] - s_ref) <= slack), "SwiGLU f32 outside its bound"
+    gq, gd = oracle_mod.q8_quantize(s_gpu[:, :cfg.n_ff])
+    assert np.array_equal(sd, gd), "SwiGLU Q8_0 scales differ from the oracle's"
+    assert np.array_equal(sq, gq), "SwiGLU Q8_0 codes differ from the oracle's"
 
     h_out = _f32(g, "h_out", nt, H)[rows]
     _check_sum(oracle_mod, h_out, sq, sd, *Wt.q8["ffn_down.weight"], cfg.n_ff, base=h_mid)
@@ -228,6 +238,19 @@ def _run(qp, oracle_mod, wl, layer_mid, n_rows, seed):
     kv = fresh_cache()
     assert np.array_equal(g.prefill(kv, ids, pos), logits), "graph replay differs"
     kv.free()
+
+
+def test_tiny_32(qp, oracle_mod):
+    """The tiny model (one ragged 32-row tile, partial Q8_0 blocks of the
+    688-wide FFN), both layers."""
+    _run(qp, oracle_mod, synth.WORKLOADS["tiny-32"], 0, 32, 5)
+
+
+def test_qwen2_0_5b_512(qp, oracle_mod):
+    """The benched workload: 24 layers of H 896, 14 query heads of 64 over 2
+    KV heads (7 per group), tied lm_head over 151936 rows; a middle layer and
+    the last layer down to the logits."""
+    _run(qp, oracle_mod, synth.WORKLOADS["qwen2-0.5b-512"], 11, 40, 6)
 
 
 def test_qwen2_1_5b_2048(qp, oracle_mod):

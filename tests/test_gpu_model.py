@@ -272,6 +272,41 @@ def test_q8_0_input_path(qp, oracle_mod):
     check_logits(lg, lo[0], atol=2e-2 * max(1.0, np.abs(lo).max()))
 
 
+def test_bounded_wait_failure_path(qp, tiny_pair):
+    """A device wait that runs out ends the call with an error, not with a
+    hang or with wrong output: the test hook makes layer 0's Q|K|V GEMM
+    withhold one operand stage and shortens every GEMM wait to 100 us.  The
+    call returns MINFER_ERR_DEVICE, the device status names a wait of that
+    GEMM, no K/V row and no logit is written, and the next normal call on the
+    same model and cache succeeds with the oracle's logits."""
+    cfg, g, o = tiny_pair
+    w = synth.WORKLOADS["tiny-32"]
+    ids, pos = w.ids(), w.positions()
+    kv = g.kv(w.n_ctx)
+    kvw = cfg.n_head_kv * cfg.head_dim
+    canary = np.full((w.n_ctx, kvw), np.float32(-3.5))
+    for layer in range(cfg.n_layer):
+        kv.write(layer, 0, 0, canary)
+        kv.write(layer, 1, 0, canary)
+    out = np.full(cfg.n_vocab, np.float32(7.0))
+    g.debug_fault(0, 100_000)
+    try:
+        rc = g.prefill_rc(kv, ids, pos, out)
+    finally:
+        g.debug_fault(-1)
+    assert rc == -8, rc
+    assert qp.DEV_NAMES[g.device_status()] in ("DEV_TIMEOUT_MMA_FULL", "DEV_TIMEOUT_EPILOGUE")
+    assert np.all(out == np.float32(7.0)), "logits written by a failed call"
+    for layer in range(cfg.n_layer):
+        for which in (0, 1):
+            assert np.array_equal(kv.read(layer, which), canary), "K/V written by a failed call"
+    lg = g.prefill(kv, ids, pos)
+    rc, lo, _ = o.prefill(o.kv(w.n_ctx), ids, pos)
+    assert rc == 0
+    check_logits(lg, lo[0])
+    kv.free()
+
+
 def test_missing_tensor_and_shape_errors(qp):
     cfg = synth.TINY
     m = qp.Model(qp.hparams_of(cfg))
@@ -293,37 +328,44 @@ def qwen05_pair(qp, oracle_mod):
 
 
 def test_qwen2_0_5b_512_matches_oracle(qwen05_pair, oracle_mod):
-    """The 0.5B-shaped model at the bench workload (512 tokens, n_ctx 4096).
+    """The 0.5B-shaped model at the bench workload (512 tokens, n_ctx 4096),
+    end to end: a drift report with a regression alarm, not the parity gate.
 
     Over 24 layers any implementation that is not bit-identical to the
     oracle drifts from it: every on-the-fly Q8_0 quantization turns a relative
-    input difference d into about 0.13*sqrt(d) of output difference, so ulp
-    level differences grow to ~2e-2 within a few layers.  The oracle itself
-    shows the same drift against a copy of itself whose attention rounds in
-    float32 instead of float64.  The bound is therefore the larger of the
-    stated tolerance and 2.5x that oracle-vs-oracle floor, per hidden slot and
-    for the logits; the argmax must agree (unless the top-2 gap is below the
-    error).  Tight per-stage checks live in test_gpu_stages.py."""
+    input difference d into about 0.13*sqrt(d) of output difference, so
+    ulp-level differences grow to ~2e-2 within a few layers and stay there.
+    The committed floor (tests/golden/drift_floors.json, written by the
+    oracle alone) is the drift between the oracle and a copy of itself whose
+    attention rounds in float32: one independent, correct rounding of one
+    step.  The GPU rounds every step differently from the oracle (f32 block
+    sums, f32 attention, f32 RMSNorm partial sums), so its drift is of the
+    same size; measured, 1.0-1.5x the floor per slot.  The alarm is 2.5x the
+    committed floor per hidden slot and for the logits (the stated 2e-2 /
+    1e-3 where larger), plus the same argmax.  The parity gate for every
+    configuration is the teacher-forced, stage-by-stage check of
+    test_gpu_fullsize.py."""
+    import json
+    import os
     cfg, g, o = qwen05_pair
     w = synth.WORKLOADS["qwen2-0.5b-512"]
+    with open(os.path.join(os.path.dirname(__file__), "golden", "drift_floors.json")) as f:
+        floor = json.load(f)
+    assert floor["workload"] == w.name
     ids, pos = w.ids(), w.positions()
     lg, lo, dump, ho, kv_g, kv_o = _run_both(cfg, g, o, ids, pos, w.n_ctx)
-    oracle_mod.set_attention_f32(True)
-    try:
-        rc, l32, h32 = o.prefill(o.kv(w.n_ctx), ids, pos, 1, hidden=True)
-    finally:
-        oracle_mod.set_attention_f32(False)
-    assert rc == 0
     nt = w.n_tokens
+    report = []
     for layer in range(cfg.n_layer + 1):
         rows = nt if layer < cfg.n_layer else 1
-        floor = rel_l2(h32[layer, :rows], ho[layer, :rows])
         got = rel_l2(dump[layer, :rows], ho[layer, :rows])
-        assert got <= max(1e-3, 2.5 * floor), (layer, got, floor)
-    floor_abs = float(np.abs(l32[0] - lo).max())
-    floor_rel = rel_l2(l32[0], lo)
-    check_logits(lg, lo, atol=max(2e-2, 2.5 * floor_abs), rtol_l2=max(1e-3, 2.5 * floor_rel))
-    assert int(np.argmax(lg)) == int(np.argmax(lo))
+        report.append(got)
+        assert got <= max(1e-3, 2.5 * floor["hidden_rel_l2"][layer]), (layer, got, floor)
+    check_logits(lg, lo, atol=max(2e-2, 2.5 * floor["logits_max_abs"]),
+                 rtol_l2=max(1e-3, 2.5 * floor["logits_rel_l2"]))
+    assert oracle_mod.argmax(lg) == oracle_mod.argmax(lo) == floor["argmax"]
+    print("hidden rel-L2 drift / floor:",
+          " ".join(f"{a / max(b, 1e-30):.2f}" for a, b in zip(report[1:], floor["hidden_rel_l2"][1:])))
     for layer in (0, cfg.n_layer - 1):
         a = kv_g.read(layer, 0, 0, nt + 8)
         assert not np.any(a[nt:])

@@ -80,8 +80,8 @@ def test_gemm_block_dots_bit_exact(qp, oracle_mod, M, N, K):
 @pytest.mark.parametrize("M,N,K", [(512, 896, 4864), (512, 9728, 896), (2048, 1536, 1536),
                                    (130, 896, 896)])
 def test_gemm_shapes_and_split_k(qp, oracle_mod, M, N, K):
-    """Shapes of the 0.5B/1.5B layers: split-K (down/o), 256-wide tiles
-    (gate/up), several M tiles with a ragged tail."""
+    """Shapes of the 0.5B/1.5B layers: split-K (down/o), a wide N (gate/up),
+    several M tiles with a ragged tail."""
     xq, xd, wq, wd = _q8_pair(oracle_mod, 7 * M + N, M, N, K)
     y = qp.op_gemm(_dev(xq), _dev(xd.view(np.int16)), _dev(wq), _dev(wd.view(np.int16)), K)
     rows = np.unique(np.concatenate([np.arange(0, M, max(1, M // 23)), [M - 1]]))

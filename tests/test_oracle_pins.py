@@ -8,6 +8,7 @@ operand, a wrong head mapping) fails at least one of them.
 """
 import math
 import os
+import sys
 
 import numpy as np
 import pytest
@@ -383,12 +384,38 @@ def test_model_written_slots_and_errors(tiny, synth_mod):
     assert m.prefill(kv, bad, pos)[0] == -3
     for layer in range(cfg.n_layer):
         assert np.array_equal(kv.read(layer, 0), canary)
+    # a repeated position is a bad argument (the pages give every token its
+    # own slot): rejected before any write
+    assert m.prefill(kv, ids, np.array([5, 9, 10, 9, 63], np.int32))[0] == -1
+    for layer in range(cfg.n_layer):
+        assert np.array_equal(kv.read(layer, 0), canary)
+        assert np.array_equal(kv.read(layer, 1), canary)
     assert m.prefill(kv, ids, pos)[0] == 0
     for layer in range(cfg.n_layer):
         for which in (0, 1):
             r = kv.read(layer, which)
             changed = np.where(np.any(r != canary, axis=1))[0]
             assert changed.tolist() == pos.tolist()
+
+
+def test_argmax_brute_force_with_ties(oracle_mod):
+    """The argmax the acceptance bar compares: the largest value, ties to the
+    lowest index (a plain loop over the vector decides)."""
+    rng = np.random.default_rng(11)
+    cases = [np.array([1.0, 3.0, 3.0, 2.0], np.float32),
+             np.array([-5.0, -5.0, -7.0], np.float32),
+             np.array([0.0], np.float32),
+             np.array([2.0, -0.0, 0.0, 2.0], np.float32)]
+    for _ in range(50):
+        x = rng.integers(-4, 5, size=int(rng.integers(1, 300))).astype(np.float32)
+        cases.append(x)
+    cases.append(rng.standard_normal(151936).astype(np.float32))
+    for x in cases:
+        best = 0
+        for i in range(1, x.size):
+            if x[i] > x[best]:
+                best = i
+        assert oracle_mod.argmax(x) == best
 
 
 def test_model_zero_weight_special_case(oracle_mod, synth_mod):
@@ -485,3 +512,25 @@ def test_attention_f32_variant_is_the_same_attention(oracle_mod):
         oracle_mod.set_attention_f32(False)
     assert np.allclose(o32, ref, rtol=2e-5, atol=2e-6)
     assert not np.array_equal(o32, oracle_mod.attention(q, pos, K, V, nh, nkv, hd))
+
+
+def test_committed_drift_floor_is_the_oracles(oracle_mod):
+    """tests/golden/drift_floors.json (the bound the deep end-to-end GPU test
+    scales) is what the oracle gives today: recomputed here, equal within the
+    spread that the host's libm may introduce (last-bit differences of exp /
+    cos / pow grow through the Q8_0 re-quantizations like any other)."""
+    import json
+    sys.path.insert(0, os.path.join(HERE, "golden"))
+    try:
+        import make_drift_floors
+    finally:
+        sys.path.pop(0)
+    with open(os.path.join(HERE, "golden", "drift_floors.json")) as f:
+        want = json.load(f)
+    got = make_drift_floors.floors(want["workload"])
+    assert got["argmax"] == want["argmax"]
+    for a, b in zip(got["hidden_rel_l2"][1:], want["hidden_rel_l2"][1:]):
+        assert 0.75 * b <= a <= 1.25 * b, (a, b)
+    assert got["hidden_rel_l2"][0] == 0.0
+    for k in ("logits_max_abs", "logits_rel_l2"):
+        assert 0.75 * want[k] <= got[k] <= 1.25 * want[k], (k, got[k], want[k])

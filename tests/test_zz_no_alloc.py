@@ -1,16 +1,19 @@
 """The allocation-free GEMM entry point.
 
-minfer_op_gemm_noalloc serves callers that cannot call cudaMalloc: a process
-whose own allocator already holds nearly all device memory, or code that must
-not trigger the device-wide synchronization of cudaFree.  It keeps its operand
-planes and split-K partials in a fixed 32 MiB device array inside the library.
-This file is collected last on purpose, so a run that stops at the first
-failure has run every other test first; it also passes on its own.
-"""
-import ctypes
+minfer_op_gemm_noalloc is for callers that cannot call cudaMalloc: a process
+whose own memory pool reserved nearly all of HBM at start-up, or code that
+must not stall the whole device the way cudaFree does.  It keeps its operand
+planes and split-K partials in a fixed 32 MiB device array inside the library
+and runs on a stream of its own.
 
+This file is collected last on purpose, so a run that stops at the first
+failure has run every other test first; it also passes on its own in a fresh
+process.
+"""
 import numpy as np
 import pytest
+
+from helpers import check_q8_sum
 
 pytestmark = pytest.mark.gpu
 
@@ -33,18 +36,26 @@ def _operands(seed, M, N, K):
     wq[:, K:] = 0
     xd = np.float16(rng.uniform(1e-3, 3e-2, (M, nb))).view(np.uint16)
     wd = np.float16(rng.uniform(1e-4, 1e-3, (N, nb))).view(np.uint16)
-    dev = lambda a: torch.from_numpy(np.ascontiguousarray(a)).cuda()
-    return dev(xq), dev(xd.view(np.int16)), dev(wq), dev(wd.view(np.int16))
+    return xq, xd, wq, wd
 
 
-def test_noalloc_gemm_matches_allocating_gemm_twice(qp):
-    """Two calls in a row (different shapes, the second finds the first's
-    leftovers in the shared array) each match minfer_op_gemm."""
+def _dev(a):
+    return torch.from_numpy(np.ascontiguousarray(a)).cuda()
+
+
+def test_noalloc_gemm_matches_oracle_twice(qp, oracle_mod):
+    """Two calls in a row (different shapes; the second finds the first's
+    leftovers in the shared array), each within the f32 rounding bound of the
+    oracle's Q8_0 matmul on sampled rows, and equal to the allocating entry
+    point's result (same kernels, same split plan)."""
     for seed, (M, N, K) in enumerate([(300, 520, 688), (512, 896, 4864)]):
         xq, xd, wq, wd = _operands(seed, M, N, K)
-        ref = qp.op_gemm(xq, xd, wq, wd, K).cpu().numpy()
-        got = qp.op_gemm_noalloc(xq, xd, wq, wd, K).cpu().numpy()
-        np.testing.assert_allclose(got, ref, rtol=2e-6, atol=2e-6 * np.abs(ref).max())
+        args = (_dev(xq), _dev(xd.view(np.int16)), _dev(wq), _dev(wd.view(np.int16)), K)
+        got = qp.op_gemm_noalloc(*args).cpu().numpy()
+        rows = np.unique(np.concatenate([np.arange(0, M, max(1, M // 37)), [M - 1]]))
+        check_q8_sum(oracle_mod, got[rows], xq[rows], xd[rows], wq, wd, K)
+        ref = qp.op_gemm(*args).cpu().numpy()
+        assert np.array_equal(got, ref)
 
 
 def test_noalloc_gemm_rejects_oversize(qp):
@@ -57,8 +68,10 @@ def test_noalloc_gemm_rejects_oversize(qp):
     wq = torch.zeros((N, nb * 32), dtype=torch.int8, device="cuda")
     wd = torch.zeros((N, nb), dtype=torch.int16, device="cuda")
     y = torch.full((M, N), 5.0, dtype=torch.float32, device="cuda")
-    rc = qp.lib().minfer_op_gemm_noalloc(xq.data_ptr(), xd.data_ptr(), M, wq.data_ptr(),
-                                         wd.data_ptr(), N, K, y.data_ptr())
-    assert rc == -10
-    assert qp.lib().minfer_strerror(rc).decode()
+    for m, n in ((M, N), (2 ** 31, 16), (16, 2 ** 40)):
+        rc = qp.lib().minfer_op_gemm_noalloc(xq.data_ptr(), xd.data_ptr(), m, wq.data_ptr(),
+                                             wd.data_ptr(), n, K, y.data_ptr())
+        assert rc == -10, (m, n, rc)
+    assert qp.lib().minfer_strerror(-10).decode()
+    torch.cuda.synchronize()
     assert bool(torch.all(y == 5.0))
