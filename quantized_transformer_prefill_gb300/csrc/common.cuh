@@ -19,7 +19,8 @@ namespace minfer {
 // try_wait carrying a suspend-time hint: the waiting warp sleeps until the
 // phase completes (or the hint runs out) instead of spinning, so a waiting
 // producer or MMA thread leaves the issue slots of its sub-partition to the
-// epilogue warps that share it.
+// epilogue warps that share it (measured on the forward: dropping the hint
+// costs the GEMMs about 4%).
 constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s
 constexpr uint32_t kMaxPolls = 1u << 24;
 constexpr uint32_t kSuspendHintNs = 1000000u;  // at most 1 ms per poll
@@ -94,16 +95,6 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, int* e
   }
   set_error(err, code);
   return false;
-}
-
-// mbar_wait by every lane of a warp, with one verdict for the whole warp (a
-// lane that saw the phase complete just after another gave up follows the
-// warp), so the .sync.aligned tcgen05 instructions that follow stay
-// convergent.
-__device__ __forceinline__ bool mbar_wait_warp(uint64_t* bar, uint32_t parity, int* err, int code,
-                                               uint64_t limit_ns = kWaitLimitNs) {
-  const bool ok = mbar_wait(bar, parity, err, code, limit_ns);
-  return __all_sync(0xffffffffu, ok);
 }
 
 // The model's status words: [0] input validation (a MINFER error code),
@@ -223,17 +214,6 @@ __device__ __forceinline__ void tmem_ld16x256x4(uint32_t taddr, uint32_t (&r)[16
 __device__ __forceinline__ void tmem_wait_ld() {
   asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 }
-// The same wait, with the 32 destination registers of the load it completes
-// passed through it: every use of them depends on the wait, so the compiler
-// cannot schedule one before it (a plain wait orders memory, not registers).
-__device__ __forceinline__ void tmem_wait_ld_regs(uint32_t (&r)[32]) {
-  asm volatile("tcgen05.wait::ld.sync.aligned;"
-               : "+r"(r[0]),"+r"(r[1]),"+r"(r[2]),"+r"(r[3]),"+r"(r[4]),"+r"(r[5]),"+r"(r[6]),"+r"(r[7]),"+r"(r[8]),"+r"(r[9]),"+r"(r[10]),"+r"(r[11]),"+r"(r[12]),"+r"(r[13]),"+r"(r[14]),"+r"(r[15]),
-                 "+r"(r[16]),"+r"(r[17]),"+r"(r[18]),"+r"(r[19]),"+r"(r[20]),"+r"(r[21]),"+r"(r[22]),"+r"(r[23]),"+r"(r[24]),"+r"(r[25]),"+r"(r[26]),"+r"(r[27]),"+r"(r[28]),"+r"(r[29]),"+r"(r[30]),"+r"(r[31])
-               :
-               : "memory");
-}
-
 // Shared-memory matrix descriptor for a K-major operand tile stored with the
 // 128-byte swizzle (8 rows x 128 B atoms, atoms 1024 B apart).  Fields:
 // start address >> 4 (bits 0-13), leading byte offset >> 4 (16-29, unused for

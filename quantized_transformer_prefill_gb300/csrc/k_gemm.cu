@@ -85,9 +85,6 @@ struct Args {
   int skip_stage;    // test hook: a stage CTA 0's producer withholds (-1: none)
 };
 
-// silu(g) * u = (g / (1 + e^-g)) * u in f32, one correctly rounded division
-// (a reciprocal and two products instead flip measurably more Q8_0 scales of
-// the result against the float64 value)
 __device__ __forceinline__ float silu_mul(float g, float u) {
   return __fmul_rn(__fdiv_rn(g, __fadd_rn(1.0f, expf(-g))), u);
 }
@@ -272,16 +269,14 @@ __global__ void __launch_bounds__(kThreads, 1)
 
       for (int s = s0; s < s1 && ok; ++s, ++it) {
         const int ss = it % C::SSTAGES;
-        if (!mbar_wait_warp(&sfull[ss], (it / C::SSTAGES) & 1, p.err, kDevTimeoutEpilogue,
-                            p.wait_ns)) {
+        if (!mbar_wait(&sfull[ss], (it / C::SSTAGES) & 1, p.err, kDevTimeoutEpilogue, p.wait_ns)) {
           ok = false;
           break;
         }
 #pragma unroll 1
         for (int blk = 0; blk < 2; ++blk) {
           const int slot = sit % C::NSLOT;
-          if (!mbar_wait_warp(&tfull[slot], (sit / C::NSLOT) & 1, p.err, kDevTimeoutEpilogue,
-                              p.wait_ns)) {
+          if (!mbar_wait(&tfull[slot], (sit / C::NSLOT) & 1, p.err, kDevTimeoutEpilogue, p.wait_ns)) {
             ok = false;
             break;
           }
@@ -291,8 +286,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           uint32_t ra[32], rb[32];  // rows g, g+8 and g+16, g+24
           tmem_ld16x256(taddr, ra);
           tmem_ld16x256(taddr + (16u << 16), rb);
-          tmem_wait_ld_regs(ra);
-          tmem_wait_ld_regs(rb);
+          tmem_wait_ld();
           // slot read: hand it back to the MMA issuer
           tc_fence_before();
           __syncwarp();
@@ -309,8 +303,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 for (int e = 0; e < 2; ++e) {
                   const int n = ncol0 + 8 * k + 2 * t4 + e;
                   const uint32_t v = rr < 2 ? ra[4 * k + 2 * rr + e] : rb[4 * k + 2 * (rr - 2) + e];
-                  if (n < p.N)
-                    p.dots[((int64_t)m * p.N + n) * p.nb + b] = __float2int_rn(__uint_as_float(v));
+                  if (n < p.N) p.dots[((int64_t)m * p.N + n) * p.nb + b] = __float2int_rn(__uint_as_float(v));
                 }
             }
           }
@@ -402,7 +395,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   }
 
-  if (warp >= 2) tmem_wait_ld();  // no TMEM load of this warp outlives the allocation
   tc_fence_before();
   __syncthreads();
   tc_fence_after();

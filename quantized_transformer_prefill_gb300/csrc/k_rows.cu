@@ -501,7 +501,9 @@ __global__ void repack_gemm_kernel(const RepackArgs a) {
   for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < total;
        i += (int64_t)gridDim.x * blockDim.x) {
     const int64_t r = i / kpad, k = i % kpad;
-    const int64_t dr = a.interleave ? ((r / 32) * 64 + a.which * 32 + (r % 32)) : (a.dst_row0 + r);
+    const int64_t dr = a.interleave ? ((r / kSwiGluGroup) * 2 * kSwiGluGroup +
+                                       a.which * kSwiGluGroup + (r % kSwiGluGroup))
+                                    : (a.dst_row0 + r);
     a.dst_codes[dr * kpad + k] = __float2half_rn((float)a.q[i]);
     if ((k & 31) == 0) {
       const int b = (int)(k / 32);

@@ -46,6 +46,11 @@ struct GemmOperand {
   int nb = 0;
 };
 
+// Gate/up weights for the SwiGLU epilogue: rows interleaved in groups of
+// kSwiGluGroup gate rows then the kSwiGluGroup up rows of the same outputs,
+// so that one epilogue warp's 64 columns hold matching gate and up values.
+constexpr int kSwiGluGroup = 32;
+
 enum GemmEpilogue : int {
   kEpiF32 = 0,     // out[split][m][n] = sum over the split's K blocks
   kEpiSwiGLU = 1,  // interleaved gate/up columns -> silu(g)*u -> Q8_0 codes + scales
@@ -62,7 +67,8 @@ GemmPlan gemm_plan(int64_t M, int64_t N, int nb, int num_sms, bool allow_split);
 
 // y = A . B^T on the tensor cores.  A: activations (rows = M), B: weights
 // (rows = N).  Epilogue kEpiF32 writes split s to out + s * split_stride.
-// kEpiSwiGLU expects B rows interleaved in groups of 32 gate / 32 up rows and
+// kEpiSwiGLU expects B rows interleaved in groups of kSwiGluGroup gate /
+// kSwiGluGroup up rows and
 // writes codes [M][ldq] fp16 and scales [nbF][ldqs] f32; with `out` set it
 // also writes the f32 values it quantized to out [M][ldo] (debug capture).
 struct GemmLaunch {
@@ -252,7 +258,7 @@ struct RepackArgs {
   float* dst_scales = nullptr;  // [nb][dst_rows_pad]
   int64_t dst_rows_pad = 0;
   int64_t dst_row0 = 0;     // destination row of source row 0 (plain layout)
-  int interleave = 0;       // 1: gate (which=0) / up (which=1) interleave in groups of 32
+  int interleave = 0;       // 1: gate (which=0) / up (which=1) interleave in groups of kSwiGluGroup
   int which = 0;
 };
 cudaError_t repack_gemm_launch(const RepackArgs& a, cudaStream_t stream);
