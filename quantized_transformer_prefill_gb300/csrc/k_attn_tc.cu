@@ -57,6 +57,17 @@ constexpr float kLazyMax = 8.0f;
 // Key tiles accumulated by the tensor core into T before T is folded into R.
 constexpr int kFoldTiles = 4;
 constexpr uint32_t kTcolT = 128;  // TMEM column of T; R follows at kTcolT + hd
+// P (fp16 hi/lo, 64 keys: 32 columns each) after R; with head_dim 64 the Q
+// tile (fp16 hi/lo, 32 columns each) follows P.
+template <int HD>
+struct TcCols {
+  static constexpr uint32_t R = kTcolT + HD;
+  static constexpr uint32_t P = R + HD;
+  static constexpr uint32_t Q = P + kTcKeys;  // used when Q lives in TMEM (HD 64)
+  static constexpr bool kQInTmem = HD == 64;
+  static constexpr uint32_t END = kQInTmem ? Q + HD : P + kTcKeys;
+  static_assert(END <= 512, "TMEM columns");
+};
 
 template <int HD>
 struct TcCfg {
@@ -65,15 +76,14 @@ struct TcCfg {
   static constexpr int Q_BYTES = kTcRows * HD * 2;
   static constexpr int K_BYTES = kTcKeys * HD * 2;
   static constexpr int V_BYTES = HD * kTcKeys * 2;  // V^T tile [hd][64 keys]
-  static constexpr int P_BYTES = kTcRows * kTcKeys * 2;
   static constexpr int STAGES = 2;
   static constexpr int OFF_QH = 0;
   static constexpr int OFF_QL = OFF_QH + Q_BYTES;
   static constexpr int OFF_K = OFF_QL + Q_BYTES;            // stage s: hi, lo
   static constexpr int OFF_V = OFF_K + STAGES * 2 * K_BYTES;  // stage s: hi, lo
-  static constexpr int OFF_P = OFF_V + STAGES * 2 * V_BYTES;  // hi, lo
-  static constexpr int OFF_BAR = OFF_P + 2 * P_BYTES;
-  static constexpr int NBAR = 4 * STAGES + 4 + 3 + 4;
+  static constexpr int OFF_P = OFF_V + STAGES * 2 * V_BYTES;  // end of the V ring (P is in TMEM)
+  static constexpr int OFF_BAR = OFF_P;
+  static constexpr int NBAR = 4 * STAGES + 4 + 3 + 4 + 1;
   static constexpr int OFF_TMEM = OFF_BAR + NBAR * 8;
   static constexpr int SMEM = OFF_TMEM + 16 + 1024;
   // the split-merge partials reuse the K/V rings: o [128 rows][hd], then
@@ -87,7 +97,7 @@ struct TcCfg {
   static_assert(SMEM <= 227 * 1024, "shared memory budget");
   // TMEM columns: S buffers at 0 and 64, the accumulating O part T at 128,
   // the folded part R after it
-  static constexpr uint32_t TCOLS = 128 + 2 * HD <= 256 ? 256 : 512;
+  static constexpr uint32_t TCOLS = 512;
 };
 
 struct TcArgs {
@@ -136,6 +146,16 @@ __device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&r)[32
       "r"(r[29]), "r"(r[30]), "r"(r[31])
       : "memory");
 }
+// 32 lanes x 16 columns of 32-bit TMEM words from registers.
+__device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&r)[16]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], "
+      "{%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};" ::"r"(taddr),
+      "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]),
+      "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]),
+      "r"(r[15])
+      : "memory");
+}
 __device__ __forceinline__ void tmem_wait_st() {
   asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
 }
@@ -163,6 +183,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   uint64_t* qready = oready + 1;
   uint64_t* mdone = qready + 1;  // [2] each issuer's MMAs completed (before TMEM is freed)
   uint64_t* lsum = mdone + 2;    // the two halves of every row have published their sums
+  uint64_t* qtm = lsum + 1;      // the Q tile is in TMEM (head_dim 64)
   uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(smem + C::OFF_TMEM);
   __shared__ int s_maxp;
 
@@ -188,6 +209,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     }
     mbar_init(pready, kSmWarps);
     mbar_init(lsum, kSmWarps);
+    mbar_init(qtm, kSmWarps);
     mbar_init(oready, 1);
     mbar_init(qready, 1);
     mbar_init(&mdone[0], 1);
@@ -228,7 +250,6 @@ __global__ void __launch_bounds__(kTcThreads, 1)
 
   uint8_t* sQh = smem + C::OFF_QH;
   uint8_t* sQl = smem + C::OFF_QL;
-  uint8_t* sP = smem + C::OFF_P;
 
   if (warp == 0) {
     // ---------------------------------------------------------- TMA producer
@@ -277,13 +298,17 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     }
   } else if (warp == 1 || warp == kPvWarp) {
     // ---------------------------------------------------------- MMA issuers
-    // One thread issues about one MMA per 70 cycles whatever its N, so S =
-    // Q.K^T (warp 1) and O += P.V (warp 6) have an issuing thread each.
+    // S = Q.K^T (warp 1) and O += P.V (warp 10) have an issuing thread each.
+    // P, and with head_dim 64 also Q, is the A operand straight from TMEM:
+    // the MMA then reads only K or V^T from shared memory, whose bandwidth
+    // (shared with the TMA writes) bounds these small-N MMAs.
     if (lane == 0 && ntile > 0) {
+      using TC = TcCols<HD>;
       constexpr uint32_t idS = idesc_f16_f32(kTcRows, kTcKeys);
       constexpr uint32_t idO = idesc_f16_f32(kTcRows, HD);
       const uint32_t qh = smem_u32(sQh), ql = smem_u32(sQl);
-      const uint32_t ph = smem_u32(sP), pl = smem_u32(sP + C::P_BYTES);
+      const uint32_t ph = tmem_base + TC::P, pl = tmem_base + TC::P + kTcKeys / 2;
+      const uint32_t tqh = tmem_base + TC::Q, tql = tmem_base + TC::Q + HD / 2;
       const uint32_t tO = tmem_base + kTcolT;
       bool ok = true;
       bool committed = false;
@@ -297,14 +322,20 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         const uint32_t d = tmem_base + (uint32_t)(b * kTcKeys);
 #pragma unroll
         for (int c = 0; c < 3; ++c) {
-          const uint32_t A = c == 2 ? ql : qh;
           const uint32_t B = c == 1 ? kl : kh;
 #pragma unroll
           for (int k = 0; k < HD / 16; ++k) {
             const uint32_t off = (uint32_t)((k & 3) * 32);
-            tc_mma_f16(d, smem_desc_sw128(A + (k >> 2) * C::QSUB + off),
-                       smem_desc_sw128(B + (k >> 2) * C::KSUB + off), idS,
-                       (c == 0 && k == 0) ? 0u : 1u);
+            const uint64_t bd = smem_desc_sw128(B + (k >> 2) * C::KSUB + off);
+            if constexpr (TC::kQInTmem) {
+              // Q in TMEM: 16 fp16 along K = 8 columns per step
+              tc_mma_f16_ts(d, (c == 2 ? tql : tqh) + (uint32_t)(8 * k), bd, idS,
+                            (c == 0 && k == 0) ? 0u : 1u);
+            } else {
+              const uint32_t A = c == 2 ? ql : qh;
+              tc_mma_f16(d, smem_desc_sw128(A + (k >> 2) * C::QSUB + off), bd, idS,
+                         (c == 0 && k == 0) ? 0u : 1u);
+            }
           }
         }
         tc_commit(&sready[b]);
@@ -327,9 +358,10 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           for (int k = 0; k < kTcKeys / 16; ++k) {
             const uint32_t off = (uint32_t)(k * 32);
             // T accumulates over the key tiles since the last fold (rescaled in
-            // place by the softmax warps); the first tile after a fold restarts it
-            tc_mma_f16(tO, smem_desc_sw128(A + off), smem_desc_sw128(B + off), idO,
-                       (j % kFoldTiles == 0 && c == 0 && k == 0) ? 0u : 1u);
+            // place by the softmax warps); the first tile after a fold restarts it.
+            // P in TMEM: 16 keys along K = 8 columns per step.
+            tc_mma_f16_ts(tO, A + (uint32_t)(8 * k), smem_desc_sw128(B + off), idO,
+                          (j % kFoldTiles == 0 && c == 0 && k == 0) ? 0u : 1u);
           }
         }
         tc_commit(oready);
@@ -338,7 +370,11 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         return true;
       };
       if (warp == 1) {
-        ok = mbar_wait(qready, 0, a.err, kDevTimeoutAttn);
+        // Q in shared memory (TMA), or copied from there into TMEM by the
+        // softmax warps
+        ok = TC::kQInTmem ? mbar_wait(qtm, 0, a.err, kDevTimeoutAttn)
+                          : mbar_wait(qready, 0, a.err, kDevTimeoutAttn);
+        if (ok) tc_fence_after();
         for (int j = 0; j < ntile && ok; ++j) ok = issue_s(j);
       } else {
         for (int j = 0; j < ntile && ok; ++j) ok = issue_pv(j);
@@ -369,6 +405,30 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     // scores in log2 units: s2 = (q.k) / sqrt(hd) * log2(e)
     const float sc = __fmul_rn(__fdiv_rn(1.0f, __fsqrt_rn((float)HD)), 1.4426950408889634f);
     bool ok = true;
+    if constexpr (TcCols<HD>::kQInTmem) {
+      if (ntile > 0) {
+        // this thread's half of its row of Q (dims kh*32 .. kh*32+31, hi and
+        // lo) from the swizzled TMA tile into the TMEM columns the S MMA reads
+        ok = mbar_wait(qready, 0, a.err, kDevTimeoutAttn);
+        if (ok) {
+          uint32_t qw[16], ql[16];
+#pragma unroll
+          for (int c8 = 0; c8 < 4; ++c8) {
+            const uint32_t off = sw128_off(rl, kh * 32 + c8 * 8);
+            const uint4 vh = *reinterpret_cast<const uint4*>(sQh + off);
+            const uint4 vl = *reinterpret_cast<const uint4*>(sQl + off);
+            qw[4 * c8] = vh.x, qw[4 * c8 + 1] = vh.y, qw[4 * c8 + 2] = vh.z, qw[4 * c8 + 3] = vh.w;
+            ql[4 * c8] = vl.x, ql[4 * c8 + 1] = vl.y, ql[4 * c8 + 2] = vl.z, ql[4 * c8 + 3] = vl.w;
+          }
+          tmem_st16(tmem_base + lanebase + TcCols<HD>::Q + (uint32_t)(kh * 16), qw);
+          tmem_st16(tmem_base + lanebase + TcCols<HD>::Q + HD / 2 + (uint32_t)(kh * 16), ql);
+          tmem_wait_st();
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(qtm);
+      }
+    }
     for (int j = 0; j < ntile && ok; ++j) {
       const int b = j & 1;
       if (!mbar_wait(&sready[b], (j >> 1) & 1, a.err, kDevTimeoutAttn)) {
@@ -465,15 +525,11 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           tmem_wait_st();
         }
       }
-#pragma unroll
-      for (int c8 = 0; c8 < kTcKeys / 16; ++c8) {
-        const uint32_t off = sw128_off(rl, kh * (kTcKeys / 2) + c8 * 8);
-        *reinterpret_cast<uint4*>(sP + off) =
-            make_uint4(hi[4 * c8], hi[4 * c8 + 1], hi[4 * c8 + 2], hi[4 * c8 + 3]);
-        *reinterpret_cast<uint4*>(sP + C::P_BYTES + off) =
-            make_uint4(lo[4 * c8], lo[4 * c8 + 1], lo[4 * c8 + 2], lo[4 * c8 + 3]);
-      }
-      fence_proxy_async_smem();
+      // this half's P (keys kh*32.. of the row, two fp16 per column) into the
+      // TMEM columns the P.V MMA reads as its A operand
+      tmem_st16(tmem_base + lanebase + TcCols<HD>::P + (uint32_t)(kh * kTcKeys / 4), hi);
+      tmem_st16(tmem_base + lanebase + TcCols<HD>::P + kTcKeys / 2 + (uint32_t)(kh * kTcKeys / 4), lo);
+      tmem_wait_st();
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(pready);
@@ -676,9 +732,10 @@ bool attention_tc_preferred(int rows, int nh, int num_sms) {
 
 int attention_tc_nsplit(int rows, int nh, int num_sms) {
   const int ctas = (rows + kTcRows - 1) / kTcRows * nh;
-  // a key split pays for its merge only when the CTAs are very few
-  if (3 * ctas >= num_sms) return 1;
-  const int ns = (num_sms + ctas - 1) / std::max(ctas, 1);
+  // split the keys when the (row tile, head) pairs leave at least half of the
+  // SMs idle: ns CTAs per pair, one wave (0.5B shape, 512 rows: 56 pairs, 2 splits)
+  if (2 * ctas > num_sms) return 1;
+  const int ns = num_sms / std::max(ctas, 1);
   return ns < 1 ? 1 : (ns > kTcMaxSplits ? kTcMaxSplits : ns);
 }
 

@@ -273,9 +273,21 @@ __global__ void __launch_bounds__(kThreads, 1)
           ok = false;
           break;
         }
-#pragma unroll 1
+        // both blocks of the stage unrolled (the second block's TMEM load and
+        // the first one's FFMAs interleave: 7% fewer cycles per block); each
+        // block's scales are read from shared memory before its slot is waited
+        // for
+#pragma unroll
         for (int blk = 0; blk < 2; ++blk) {
           const int slot = sit % C::NSLOT;
+          const float* sa = sSA + ss * 2 * kBM + blk * kBM + quad * 32 + g;
+          const float* dw = sSB + ss * 2 * BN + blk * BN + half * C::CPW + 2 * t4;
+          float2 w[8];
+#pragma unroll
+          for (int k = 0; k < 8; ++k) w[k] = *reinterpret_cast<const float2*>(dw + 8 * k);
+          float da4[4];
+#pragma unroll
+          for (int rr = 0; rr < 4; ++rr) da4[rr] = sa[8 * rr];
           if (!mbar_wait(&tfull[slot], (sit / C::NSLOT) & 1, p.err, kDevTimeoutEpilogue, p.wait_ns)) {
             ok = false;
             break;
@@ -307,14 +319,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
             }
           }
-          const float* sa = sSA + ss * 2 * kBM + blk * kBM + quad * 32 + g;
-          const float* dw = sSB + ss * 2 * BN + blk * BN + half * C::CPW + 2 * t4;
-          float2 w[8];
-#pragma unroll
-          for (int k = 0; k < 8; ++k) w[k] = *reinterpret_cast<const float2*>(dw + 8 * k);
 #pragma unroll
           for (int rr = 0; rr < 4; ++rr) {
-            const float da = sa[8 * rr];
+            const float da = da4[rr];
             const float2 da2 = make_float2(da, da);
 #pragma unroll
             for (int k = 0; k < 8; ++k) {
