@@ -378,9 +378,10 @@ int minfer_device_status(minfer_model* m);
  * 3.4: the failure must surface as an error, not as wrong output).  While
  * `layer` >= 0, the prefill calls of m run without the recorded graph, every
  * bounded wait of the GEMMs gives up after wait_limit_ns (> 0) instead of
- * 2 s, and the Q|K|V GEMM of that layer withholds one operand stage, so that
- * a wait on it runs out: the call returns MINFER_ERR_DEVICE and
- * minfer_device_status names the wait.  layer = -1 turns it off (the next
+ * 2 s, and the gate/up GEMM of that layer withholds one operand stage, so
+ * that a wait on it runs out: the call returns MINFER_ERR_DEVICE and
+ * minfer_device_status names the wait.  The K/V rows of that layer were
+ * written before the failure point; later layers and the logits are not.  layer = -1 turns it off (the next
  * call runs normally).  MINFER_ERR_ARG for a layer out of range or a
  * non-positive limit. */
 int minfer_debug_fault(minfer_model* m, int layer, int64_t wait_limit_ns);

@@ -206,7 +206,7 @@ class Model:
         check(lib().minfer_debug_layer(self.ptr, layer), "debug_layer")
 
     def debug_fault(self, layer: int, wait_limit_ns: int = 0):
-        """Test hook: layer >= 0 makes that layer's Q|K|V GEMM withhold one
+        """Test hook: layer >= 0 makes that layer's gate/up GEMM withhold one
         operand stage and every GEMM wait give up after wait_limit_ns;
         -1 turns it off."""
         check(lib().minfer_debug_fault(self.ptr, layer, wait_limit_ns), "debug_fault")

@@ -395,7 +395,7 @@ __global__ void __launch_bounds__(1024) rope_store_qknorm_kernel(const RopeStore
 constexpr int kGemvWarps = 8;
 
 template <int R>
-__global__ void __launch_bounds__(32 * kGemvWarps) gemv_kernel(const GemvArgs a) {
+__global__ void __launch_bounds__(32 * kGemvWarps, 2) gemv_kernel(const GemvArgs a) {
   pdl_trigger();
   pdl_wait();
   const int lane = threadIdx.x & 31;
@@ -404,30 +404,40 @@ __global__ void __launch_bounds__(32 * kGemvWarps) gemv_kernel(const GemvArgs a)
   float acc[R];
 #pragma unroll
   for (int r = 0; r < R; ++r) acc[r] = 0.f;
-  for (int64_t c = 0; c < a.kpad; c += 512) {
-    const int64_t k = c + 16 * lane;
-    const bool in = k < a.kpad;
-    const int b = (int)(k >> 5);
-    int4 w[R];
-    float dw[R];
+  // two 512-byte chunks per round: every load of both (all R rows) is issued
+  // before the first dot product
+  for (int64_t c = 0; c < a.kpad; c += 1024) {
+    int4 w[2][R];
+    float dw[2][R];
+    int4 x[2];
+    float dx[2];
 #pragma unroll
-    for (int r = 0; r < R; ++r) {
-      const int64_t n = n0 + r;
-      const bool ok = in && n < a.N;
-      w[r] = ok ? __ldg(reinterpret_cast<const int4*>(a.wq + n * a.kpad + k)) : make_int4(0, 0, 0, 0);
-      dw[r] = ok ? __ldg(a.ws + n * a.nb + b) : 0.f;
-    }
-    const int4 x = in ? *reinterpret_cast<const int4*>(a.xq + k) : make_int4(0, 0, 0, 0);
-    const float dx = in ? a.xs[b] : 0.f;
+    for (int h = 0; h < 2; ++h) {
+      const int64_t k = c + 512 * h + 16 * lane;
+      const bool in = k < a.kpad;
+      const int b = (int)(k >> 5);
 #pragma unroll
-    for (int r = 0; r < R; ++r) {
-      int isum = __dp4a(w[r].x, x.x, 0);
-      isum = __dp4a(w[r].y, x.y, isum);
-      isum = __dp4a(w[r].z, x.z, isum);
-      isum = __dp4a(w[r].w, x.w, isum);
-      isum += __shfl_xor_sync(0xffffffffu, isum, 1);
-      if (!(lane & 1)) acc[r] = fmaf((float)isum, __fmul_rn(dw[r], dx), acc[r]);
+      for (int r = 0; r < R; ++r) {
+        const int64_t n = n0 + r;
+        const bool ok = in && n < a.N;
+        w[h][r] = ok ? __ldg(reinterpret_cast<const int4*>(a.wq + n * a.kpad + k))
+                     : make_int4(0, 0, 0, 0);
+        dw[h][r] = ok ? __ldg(a.ws + n * a.nb + b) : 0.f;
+      }
+      x[h] = in ? *reinterpret_cast<const int4*>(a.xq + k) : make_int4(0, 0, 0, 0);
+      dx[h] = in ? a.xs[b] : 0.f;
     }
+#pragma unroll
+    for (int h = 0; h < 2; ++h)
+#pragma unroll
+      for (int r = 0; r < R; ++r) {
+        int isum = __dp4a(w[h][r].x, x[h].x, 0);
+        isum = __dp4a(w[h][r].y, x[h].y, isum);
+        isum = __dp4a(w[h][r].z, x[h].z, isum);
+        isum = __dp4a(w[h][r].w, x[h].w, isum);
+        isum += __shfl_xor_sync(0xffffffffu, isum, 1);
+        if (!(lane & 1)) acc[r] = fmaf((float)isum, __fmul_rn(dw[h][r], dx[h]), acc[r]);
+      }
   }
 #pragma unroll
   for (int r = 0; r < R; ++r)

@@ -861,7 +861,7 @@ int enqueue_forward(minfer_model* m, minfer_kv* kv, const int32_t* ids, const in
         return rc;
     }
     if ((rc = gemm_call(m, L, kKGemmQKV, xa, Ly.wqkv, nt, kEpiF32, true, w.part, m->qkvN, nullptr,
-                        0, nullptr, 0, &ns, l == m->fault_layer)))
+                        0, nullptr, 0, &ns)))
       return rc;
     {
       RopeStoreArgs r;
@@ -989,7 +989,7 @@ int enqueue_forward(minfer_model* m, minfer_kv* kv, const int32_t* ids, const in
         s_f32 = static_cast<float*>(e.first);  // rows as in "s_codes": the carried rows from 0
       }
       if ((rc = gemm_call(m, L, kKGemmGU, xa_r, Ly.wgu, mrows, kEpiSwiGLU, false, s_f32, m->Fp,
-                          w.xf, m->Fp, w.xf_s, ntp, nullptr)))
+                          w.xf, m->Fp, w.xf_s, ntp, nullptr, l == m->fault_layer)))
         return rc;
       if (cap) {
         if ((rc = dbg_capture(m, st, "s_codes", w.xf, (size_t)nt * m->Fp * 2)) ||

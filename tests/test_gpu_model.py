@@ -274,14 +274,17 @@ def test_q8_0_input_path(qp, oracle_mod):
 
 def test_bounded_wait_failure_path(qp, tiny_pair):
     """A device wait that runs out ends the call with an error, not with a
-    hang or with wrong output: the test hook makes layer 0's Q|K|V GEMM
+    hang or with wrong output: the test hook makes layer 0's gate/up GEMM
     withhold one operand stage and shortens every GEMM wait to 100 us.  The
-    call returns MINFER_ERR_DEVICE, the device status names a wait of that
-    GEMM, no K/V row and no logit is written, and the next normal call on the
-    same model and cache succeeds with the oracle's logits."""
+    call returns MINFER_ERR_DEVICE and the device status names a wait of that
+    GEMM.  Layer 0's K/V rows were written before the failure point (by the
+    Q|K|V GEMM's epilogue) and hold what a clean call writes; the later
+    layers' regions and the caller's logits are untouched; the next normal
+    call on the same model and cache succeeds with the oracle's logits."""
     cfg, g, o = tiny_pair
     w = synth.WORKLOADS["tiny-32"]
     ids, pos = w.ids(), w.positions()
+    nt = w.n_tokens
     kv = g.kv(w.n_ctx)
     kvw = cfg.n_head_kv * cfg.head_dim
     canary = np.full((w.n_ctx, kvw), np.float32(-3.5))
@@ -297,13 +300,18 @@ def test_bounded_wait_failure_path(qp, tiny_pair):
     assert rc == -8, rc
     assert qp.DEV_NAMES[g.device_status()] in ("DEV_TIMEOUT_MMA_FULL", "DEV_TIMEOUT_EPILOGUE")
     assert np.all(out == np.float32(7.0)), "logits written by a failed call"
-    for layer in range(cfg.n_layer):
+    failed = [kv.read(0, which) for which in (0, 1)]
+    for which in (0, 1):
+        assert np.array_equal(failed[which][nt:], canary[nt:]), "rows past the prompt written"
+    for layer in range(1, cfg.n_layer):
         for which in (0, 1):
-            assert np.array_equal(kv.read(layer, which), canary), "K/V written by a failed call"
+            assert np.array_equal(kv.read(layer, which), canary), "K/V written after the failure"
     lg = g.prefill(kv, ids, pos)
     rc, lo, _ = o.prefill(o.kv(w.n_ctx), ids, pos)
     assert rc == 0
     check_logits(lg, lo[0])
+    for which in (0, 1):
+        assert np.array_equal(kv.read(0, which), failed[which]), "the failed call's rows differ"
     kv.free()
 
 
