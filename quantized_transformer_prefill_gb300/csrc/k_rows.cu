@@ -392,7 +392,20 @@ __device__ __forceinline__ void store_q(const RopeStoreArgs& a, int64_t o, float
   }
 }
 
-__global__ void __launch_bounds__(1024) rope_store_kernel(const RopeStoreArgs a) {
+// Two neighbouring dimensions per thread (i, i + 1 of a head's first half,
+// with their partners i + hd/2, i + 1 + hd/2): 8-byte loads and stores, half
+// the threads of one per pair, the same arithmetic element by element.
+__device__ __forceinline__ float2 ld2(const float* p) { return *reinterpret_cast<const float2*>(p); }
+__device__ __forceinline__ float2 add2(float2 a, float2 b) {
+  return make_float2(__fadd_rn(a.x, b.x), __fadd_rn(a.y, b.y));
+}
+__device__ __forceinline__ void split2(float2 v, __half2& hi, __half2& lo) {
+  hi = __floats2half2_rn(v.x, v.y);
+  const float2 hf = __half22float2(hi);
+  lo = __floats2half2_rn(__fsub_rn(v.x, hf.x), __fsub_rn(v.y, hf.y));
+}
+
+__global__ void __launch_bounds__(1024, 2) rope_store_kernel(const RopeStoreArgs a) {
   pdl_trigger();
   pdl_wait();
   const int t = blockIdx.x;
@@ -403,57 +416,73 @@ __global__ void __launch_bounds__(1024) rope_store_kernel(const RopeStoreArgs a)
       status_clear(a.status) && p_in >= 0 && p_in < a.n_ctx;
   const int p = (p_in >= 0 && p_in < a.n_ctx) ? p_in : 0;
   const int half = a.hd >> 1;
-  const int hshift = half == 64 ? 6 : 5;  // head_dim is 64 or 128
+  const int qshift = half == 64 ? 5 : 4;  // head_dim is 64 or 128: half/2 dimension pairs per head
   const int W = (a.nh + 2 * a.nkv) * a.hd;
   const int64_t row = (int64_t)t * W;
-  const int npairs = (a.nh + a.nkv) * half;
+  const int np2 = (a.nh + a.nkv) * (half >> 1);
   const int kw = a.nkv * a.hd;
   const float* cs = a.cos_t + (int64_t)p * half;
   const float* sn = a.sin_t + (int64_t)p * half;
-  for (int pi = threadIdx.x; pi < npairs + kw; pi += blockDim.x) {
-    if (pi < npairs) {
-      const int head = pi >> hshift, i = pi & (half - 1);
+  for (int pi = threadIdx.x; pi < np2 + (kw >> 1); pi += blockDim.x) {
+    if (pi < np2) {
+      const int head = pi >> qshift, i = 2 * (pi & ((half >> 1) - 1));
       const int e0 = head * a.hd + i;
-      float x0 = a.partials[row + e0], x1 = a.partials[row + e0 + half];
+      float2 x0 = ld2(a.partials + row + e0), x1 = ld2(a.partials + row + e0 + half);
       for (int s = 1; s < a.nsplit; ++s) {
         const float* ps = a.partials + s * a.split_stride + row;
-        x0 = __fadd_rn(x0, ps[e0]);
-        x1 = __fadd_rn(x1, ps[e0 + half]);
+        x0 = add2(x0, ld2(ps + e0));
+        x1 = add2(x1, ld2(ps + e0 + half));
       }
       if (a.bias) {
-        x0 = __fadd_rn(x0, a.bias[e0]);
-        x1 = __fadd_rn(x1, a.bias[e0 + half]);
+        x0 = add2(x0, ld2(a.bias + e0));
+        x1 = add2(x1, ld2(a.bias + e0 + half));
       }
-      const float c = cs[i], sv = sn[i];
-      const float v0 = __fsub_rn(__fmul_rn(x0, c), __fmul_rn(x1, sv));
-      const float v1 = __fadd_rn(__fmul_rn(x0, sv), __fmul_rn(x1, c));
+      const float2 c = ld2(cs + i), sv = ld2(sn + i);
+      const float2 v0 = make_float2(__fsub_rn(__fmul_rn(x0.x, c.x), __fmul_rn(x1.x, sv.x)),
+                                    __fsub_rn(__fmul_rn(x0.y, c.y), __fmul_rn(x1.y, sv.y)));
+      const float2 v1 = make_float2(__fadd_rn(__fmul_rn(x0.x, sv.x), __fmul_rn(x1.x, c.x)),
+                                    __fadd_rn(__fmul_rn(x0.y, sv.y), __fmul_rn(x1.y, c.y)));
+      __half2 h0, l0, h1, l1;
+      split2(v0, h0, l0);
+      split2(v1, h1, l1);
       if (head < a.nh) {
-        store_q(a, (int64_t)t * a.nh * a.hd + e0, v0, v1, half);
+        // rotated Q to f32 and, when present, the fp16 hi/lo planes the
+        // tensor-core attention loads by TMA
+        const int64_t o = (int64_t)t * a.nh * a.hd + e0;
+        *reinterpret_cast<float2*>(a.q_out + o) = v0;
+        *reinterpret_cast<float2*>(a.q_out + o + half) = v1;
+        if (a.q_planes[0]) {
+          *reinterpret_cast<__half2*>(a.q_planes[0] + o) = h0;
+          *reinterpret_cast<__half2*>(a.q_planes[0] + o + half) = h1;
+          *reinterpret_cast<__half2*>(a.q_planes[1] + o) = l0;
+          *reinterpret_cast<__half2*>(a.q_planes[1] + o + half) = l1;
+        }
       } else if (write_kv) {
         const int ke = (head - a.nh) * a.hd + i;
         const int64_t o0 = (int64_t)p * kw + ke;
-        a.kreg[o0] = v0;
-        a.kreg[o0 + half] = v1;
-        const __half h0 = __float2half_rn(v0), h1 = __float2half_rn(v1);
-        a.shadow[0][o0] = h0;
-        a.shadow[0][o0 + half] = h1;
-        a.shadow[1][o0] = __float2half_rn(__fsub_rn(v0, __half2float(h0)));
-        a.shadow[1][o0 + half] = __float2half_rn(__fsub_rn(v1, __half2float(h1)));
+        *reinterpret_cast<float2*>(a.kreg + o0) = v0;
+        *reinterpret_cast<float2*>(a.kreg + o0 + half) = v1;
+        *reinterpret_cast<__half2*>(a.shadow[0] + o0) = h0;
+        *reinterpret_cast<__half2*>(a.shadow[0] + o0 + half) = h1;
+        *reinterpret_cast<__half2*>(a.shadow[1] + o0) = l0;
+        *reinterpret_cast<__half2*>(a.shadow[1] + o0 + half) = l1;
       }
     } else if (write_kv) {
-      const int e = pi - npairs;
+      const int e = 2 * (pi - np2);
       const int col = (a.nh + a.nkv) * a.hd + e;
-      float v = a.partials[row + col];
-      for (int s = 1; s < a.nsplit; ++s) v = __fadd_rn(v, a.partials[s * a.split_stride + row + col]);
-      if (a.bias) v = __fadd_rn(v, a.bias[col]);
+      float2 v = ld2(a.partials + row + col);
+      for (int s = 1; s < a.nsplit; ++s) v = add2(v, ld2(a.partials + s * a.split_stride + row + col));
+      if (a.bias) v = add2(v, ld2(a.bias + col));
       const int64_t o0 = (int64_t)p * kw + e;
-      a.vreg[o0] = v;
-      const __half vh = __float2half_rn(v);
-      const __half vl = __float2half_rn(__fsub_rn(v, __half2float(vh)));
-      a.shadow[2][o0] = vh;
-      a.shadow[3][o0] = vl;
-      a.vt[0][e * a.vt_ld + p] = vh;
-      a.vt[1][e * a.vt_ld + p] = vl;
+      *reinterpret_cast<float2*>(a.vreg + o0) = v;
+      __half2 vh, vl;
+      split2(v, vh, vl);
+      *reinterpret_cast<__half2*>(a.shadow[2] + o0) = vh;
+      *reinterpret_cast<__half2*>(a.shadow[3] + o0) = vl;
+      a.vt[0][(int64_t)e * a.vt_ld + p] = __low2half(vh);
+      a.vt[0][(int64_t)(e + 1) * a.vt_ld + p] = __high2half(vh);
+      a.vt[1][(int64_t)e * a.vt_ld + p] = __low2half(vl);
+      a.vt[1][(int64_t)(e + 1) * a.vt_ld + p] = __high2half(vl);
     }
   }
 }
@@ -777,9 +806,9 @@ cudaError_t rope_store_launch(const RopeStoreArgs& a, cudaStream_t st) {
     const int threads = std::min(1024, std::max(128, (W + 31) / 32 * 32));
     return launch_pdl(rope_store_qknorm_kernel, a.nt, threads, smem, st, a);
   }
-  // one thread per (Q/K pair, V element) of the token where that fits a CTA:
-  // every thread's loads go out in one round instead of several
-  const int items = (a.nh + a.nkv) * (a.hd / 2) + a.nkv * a.hd;
+  // one thread per two (Q/K pair, V element)s of the token where that fits a
+  // CTA: every thread's loads go out in one round instead of several
+  const int items = (a.nh + a.nkv) * (a.hd / 4) + a.nkv * a.hd / 2;
   const int threads = std::min(1024, std::max(128, (items + 31) / 32 * 32));
   return launch_pdl(rope_store_kernel, a.nt, threads, 0, st, a);
 }
