@@ -97,6 +97,34 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, int* e
   return false;
 }
 
+// The same wait without the suspend-time hint: the warp keeps polling.  For
+// the warps that do the arithmetic (the GEMM epilogue waiting for a finished
+// TMEM slot), waking the moment the phase completes matters more than the
+// issue slots a poll takes (measured: the 7B GEMMs 2% faster; the producer
+// and MMA-issuer waits keep the hint, which is faster for them).
+__device__ __forceinline__ bool mbar_try_wait_spin(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+__device__ __forceinline__ bool mbar_wait_spin(uint64_t* bar, uint32_t parity, int* err, int code,
+                                               uint64_t limit_ns = kWaitLimitNs) {
+  if (mbar_try_wait_spin(bar, parity)) return true;
+  const uint64_t t0 = global_ns();
+  for (uint32_t i = 0; i < kMaxPolls; ++i) {
+    if (mbar_try_wait_spin(bar, parity)) return true;
+    if (global_ns() - t0 > limit_ns) break;
+  }
+  set_error(err, code);
+  return false;
+}
+
 // The model's status words: [0] input validation (a MINFER error code),
 // [1] the first bounded wait that gave up (a kDev code).  Kernels that write
 // the KV regions or the logits skip those writes unless both are clear.

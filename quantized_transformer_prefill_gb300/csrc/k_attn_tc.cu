@@ -57,15 +57,16 @@ constexpr float kLazyMax = 8.0f;
 // Key tiles accumulated by the tensor core into T before T is folded into R.
 constexpr int kFoldTiles = 4;
 constexpr uint32_t kTcolT = 128;  // TMEM column of T; R follows at kTcolT + hd
-// P (fp16 hi/lo, 64 keys: 32 columns each) after R; with head_dim 64 the Q
-// tile (fp16 hi/lo, 32 columns each) follows P.
+// Two P buffers (fp16 hi/lo, 64 keys: 32 columns each, 64 per buffer) after
+// R, so the softmax of tile j+1 need not wait for the P.V of tile j; with
+// head_dim 64 the Q tile (fp16 hi/lo, 32 columns each) follows them.
 template <int HD>
 struct TcCols {
   static constexpr uint32_t R = kTcolT + HD;
-  static constexpr uint32_t P = R + HD;
-  static constexpr uint32_t Q = P + kTcKeys;  // used when Q lives in TMEM (HD 64)
+  static constexpr uint32_t P = R + HD;         // buffer b at P + b * kTcKeys
+  static constexpr uint32_t Q = P + 2 * kTcKeys;  // used when Q lives in TMEM (HD 64)
   static constexpr bool kQInTmem = HD == 64;
-  static constexpr uint32_t END = kQInTmem ? Q + HD : P + kTcKeys;
+  static constexpr uint32_t END = kQInTmem ? Q + HD : Q;
   static_assert(END <= 512, "TMEM columns");
 };
 
@@ -83,7 +84,7 @@ struct TcCfg {
   static constexpr int OFF_V = OFF_K + STAGES * 2 * K_BYTES;  // stage s: hi, lo
   static constexpr int OFF_P = OFF_V + STAGES * 2 * V_BYTES;  // end of the V ring (P is in TMEM)
   static constexpr int OFF_BAR = OFF_P;
-  static constexpr int NBAR = 4 * STAGES + 4 + 3 + 4 + 1;
+  static constexpr int NBAR = 4 * STAGES + 4 + 3 + 4 + 1 + 2;
   static constexpr int OFF_TMEM = OFF_BAR + NBAR * 8;
   static constexpr int SMEM = OFF_TMEM + 16 + 1024;
   // the split-merge partials reuse the K/V rings: o [128 rows][hd], then
@@ -178,9 +179,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   uint64_t* vempty = vfull + C::STAGES;
   uint64_t* sready = vempty + C::STAGES;  // [2]
   uint64_t* sfree = sready + 2;           // [2]
-  uint64_t* pready = sfree + 2;
-  uint64_t* oready = pready + 1;
-  uint64_t* qready = oready + 1;
+  uint64_t* pready = sfree + 2;   // [2] P buffer b written by the softmax warps
+  uint64_t* oready = pready + 2;  // [2] the P.V that read P buffer b has completed
+  uint64_t* qready = oready + 2;
   uint64_t* mdone = qready + 1;  // [2] each issuer's MMAs completed (before TMEM is freed)
   uint64_t* lsum = mdone + 2;    // the two halves of every row have published their sums
   uint64_t* qtm = lsum + 1;      // the Q tile is in TMEM (head_dim 64)
@@ -207,10 +208,12 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       mbar_init(&sready[b], 1);
       mbar_init(&sfree[b], kSmWarps);
     }
-    mbar_init(pready, kSmWarps);
+    mbar_init(&pready[0], kSmWarps);
+    mbar_init(&pready[1], kSmWarps);
     mbar_init(lsum, kSmWarps);
     mbar_init(qtm, kSmWarps);
-    mbar_init(oready, 1);
+    mbar_init(&oready[0], 1);
+    mbar_init(&oready[1], 1);
     mbar_init(qready, 1);
     mbar_init(&mdone[0], 1);
     mbar_init(&mdone[1], 1);
@@ -307,7 +310,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       constexpr uint32_t idS = idesc_f16_f32(kTcRows, kTcKeys);
       constexpr uint32_t idO = idesc_f16_f32(kTcRows, HD);
       const uint32_t qh = smem_u32(sQh), ql = smem_u32(sQl);
-      const uint32_t ph = tmem_base + TC::P, pl = tmem_base + TC::P + kTcKeys / 2;
+      const uint32_t ph0 = tmem_base + TC::P;  // P buffer b: hi at ph0 + 64 b, lo 32 columns on
       const uint32_t tqh = tmem_base + TC::Q, tql = tmem_base + TC::Q + HD / 2;
       const uint32_t tO = tmem_base + kTcolT;
       bool ok = true;
@@ -344,8 +347,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         return true;
       };
       auto issue_pv = [&](int j) -> bool {
-        const int st = j % C::STAGES;
-        if (!mbar_wait(pready, j & 1, a.err, kDevTimeoutAttn)) return false;
+        const int st = j % C::STAGES, pb = j & 1;
+        if (!mbar_wait(&pready[pb], (j >> 1) & 1, a.err, kDevTimeoutAttn)) return false;
+        const uint32_t ph = ph0 + (uint32_t)(pb * kTcKeys), pl = ph + kTcKeys / 2;
         if (!mbar_wait(&vfull[st], (j / C::STAGES) & 1, a.err, kDevTimeoutAttn)) return false;
         tc_fence_after();
         const uint32_t vh = smem_u32(smem + C::OFF_V + st * 2 * C::V_BYTES);
@@ -364,7 +368,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                           (j % kFoldTiles == 0 && c == 0 && k == 0) ? 0u : 1u);
           }
         }
-        tc_commit(oready);
+        tc_commit(&oready[pb]);
         tc_commit(&vempty[st]);
         committed = true;
         return true;
@@ -487,20 +491,25 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         lo[i] = *reinterpret_cast<const uint32_t*>(&lw);
       }
       l += (l4[0] + l4[1]) + (l4[2] + l4[3]);
-      // the previous P.V has read the P buffer and finished writing O
-      if (j > 0) {
-        if (!mbar_wait(oready, (j - 1) & 1, a.err, kDevTimeoutAttn)) {
+      // O = R + T: T is what the tensor core accumulated since the last fold,
+      // R (TMEM too) the sum of the folded parts.  Every kFoldTiles tiles T is
+      // added into R with round-to-nearest f32 adds, and the next P.V starts T
+      // afresh, so no long sum builds up inside the tensor core.  A fold or a
+      // rescale of O needs the previous P.V to have completed; otherwise only
+      // the P.V two tiles back, which read the P buffer this tile writes.
+      const bool fold = j > 0 && (j % kFoldTiles) == 0;
+      const bool touch_o = j > 0 && (fold || __any_sync(0xffffffffu, resc));
+      const int jw = touch_o ? j - 1 : j - 2;  // the P.V to wait for
+      if (jw >= 0) {
+        if (!mbar_wait(&oready[jw & 1], (jw >> 1) & 1, a.err, kDevTimeoutAttn)) {
           ok = false;
           break;
         }
         tc_fence_after();
-        // O = R + T: T is what the tensor core accumulated since the last fold,
-        // R (TMEM too) the sum of the folded parts.  Every kFoldTiles tiles T is
-        // added into R with round-to-nearest f32 adds, and the next P.V starts
-        // T afresh, so no long sum builds up inside the tensor core.
-        const bool fold = (j % kFoldTiles) == 0;
+      }
+      {
         const bool has_r = j > kFoldTiles;  // an earlier fold wrote R
-        if (fold || __any_sync(0xffffffffu, resc)) {
+        if (touch_o) {
 #pragma unroll
           for (int d0 = 0; d0 < HO; d0 += 32) {
             uint32_t t[32], rr[32];
@@ -527,19 +536,20 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       }
       // this half's P (keys kh*32.. of the row, two fp16 per column) into the
       // TMEM columns the P.V MMA reads as its A operand
-      tmem_st16(tmem_base + lanebase + TcCols<HD>::P + (uint32_t)(kh * kTcKeys / 4), hi);
-      tmem_st16(tmem_base + lanebase + TcCols<HD>::P + kTcKeys / 2 + (uint32_t)(kh * kTcKeys / 4), lo);
+      const uint32_t pcol = TcCols<HD>::P + (uint32_t)((j & 1) * kTcKeys);
+      tmem_st16(tmem_base + lanebase + pcol + (uint32_t)(kh * kTcKeys / 4), hi);
+      tmem_st16(tmem_base + lanebase + pcol + kTcKeys / 2 + (uint32_t)(kh * kTcKeys / 4), lo);
       tmem_wait_st();
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(pready);
+      if (lane == 0) mbar_arrive(&pready[j & 1]);
     }
     // the last P.V completes the O tile
     float o[HO];
 #pragma unroll
     for (int d = 0; d < HO; ++d) o[d] = 0.f;
     if (ok && ntile > 0) {
-      if (!mbar_wait(oready, (ntile - 1) & 1, a.err, kDevTimeoutAttn)) {
+      if (!mbar_wait(&oready[(ntile - 1) & 1], ((ntile - 1) >> 1) & 1, a.err, kDevTimeoutAttn)) {
         ok = false;
       } else {
         tc_fence_after();

@@ -288,7 +288,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           float da4[4];
 #pragma unroll
           for (int rr = 0; rr < 4; ++rr) da4[rr] = sa[8 * rr];
-          if (!mbar_wait(&tfull[slot], (sit / C::NSLOT) & 1, p.err, kDevTimeoutEpilogue, p.wait_ns)) {
+          if (!mbar_wait_spin(&tfull[slot], (sit / C::NSLOT) & 1, p.err, kDevTimeoutEpilogue, p.wait_ns)) {
             ok = false;
             break;
           }
