@@ -44,10 +44,11 @@ def test_per_token_matmul_work_and_lm_head_of_the_shapes():
 
 
 def test_profiled_traffic_reads_the_committed_summaries():
-    for kernel in ("gemm_gate_up_swiglu", "attention", "rmsnorm_quant"):
+    for kernel in ("gemm_gate_up_swiglu", "attention", "rmsnorm_quant", "gemm_qkv", "gemm_o",
+                   "gemm_down", "rope_kv_store", "lm_head_gemv"):
         t = bench.profiled_traffic(kernel, "qwen2-0.5b-512")
         assert isinstance(t, int) and t > 1_000_000
-    assert bench.profiled_traffic("gemm_down", "qwen2-0.5b-512") is None
+    assert bench.profiled_traffic("embed", "qwen2-0.5b-512") is None
     assert bench.profiled_traffic("gemm_gate_up_swiglu", "no-such-workload") is None
 
 
