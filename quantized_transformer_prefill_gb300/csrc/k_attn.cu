@@ -500,7 +500,204 @@ __global__ void kv_shadow_kernel(const float* __restrict__ k, const float* __res
   }
 }
 
+// ---------------------------------------------------------------- one query row
+// A call with a single query row (a one-token call, the last row of a prompt)
+// has almost no work per KV head: the tiled kernel's 16-row MMA tiles and its
+// cluster merge are all latency there.  This kernel deals the keys 0..pos of
+// each KV head to up to gridDim.x CTAs (about kRowKeys keys each).  A CTA
+// stages a chunk of kRowKeys K and V rows of the f32 regions in shared memory
+// (every load in flight at once); warp h then scores the chunk for query head
+// h of the group, one key per lane, in f32 on the CUDA cores, keeps the
+// softmax online across chunks and accumulates P.V with lane l holding dims
+// l + 32 j.  The CTA leaves (max, sum, unnormalized O) in a global scratch;
+// the CTA that finishes last for the KV head (an atomic ticket: nothing
+// waits) merges the shares, normalizes and quantizes the group's 32-blocks.
+constexpr int kRowKeys = 32;  // keys per chunk, and per CTA the split count aims at
+constexpr int kRowThreadsA = 256;
+
+__device__ __forceinline__ float warp_sum(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  return v;
+}
+
+template <int HD>
+__global__ void __launch_bounds__(kRowThreadsA) attn_row_kernel(const AttnArgs a, const AttnOut out) {
+  constexpr int DPL = HD / 32;  // dims per lane
+  constexpr int C4 = HD / 4;    // float4 per row
+  __shared__ float ks[kRowKeys][HD + 1];  // +1: lane = key reads a column without bank conflicts
+  __shared__ __align__(16) float vs[kRowKeys][HD];
+  __shared__ float qs[8][HD];
+  __shared__ unsigned s_last;
+  pdl_trigger();
+  pdl_wait();
+
+  const int G = a.nh / a.nkv;
+  const int g = blockIdx.y;
+  const int split = blockIdx.x;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int r = a.r0;
+  const int64_t kw = (int64_t)a.nkv * HD;
+  const int64_t qw = (int64_t)a.nh * HD;
+  // the group's query rows load next to the position they do not depend on
+  for (int i = tid; i < G * HD; i += kRowThreadsA)
+    qs[i / HD][i % HD] = a.q[(int64_t)r * qw + (int64_t)g * G * HD + i];
+  int p = a.pos[r];
+  p = p < 0 ? -1 : (p >= a.n_ctx ? a.n_ctx - 1 : p);
+  const int nkeys = p + 1;
+  // CTAs beyond the splits this position needs leave at once (and take no ticket)
+  int ns = (nkeys + kRowKeys - 1) / kRowKeys;
+  ns = ns < 1 ? 1 : (ns > (int)gridDim.x ? (int)gridDim.x : ns);
+  if (split >= ns) return;
+  const int share = (nkeys + ns - 1) / ns;
+  const int kbeg = split * share;
+  const int kend = min(nkeys, kbeg + share);
+  // scores in log2 units: s = (q.k) / sqrt(hd) * log2(e)
+  const float sc = __fmul_rn(__fdiv_rn(1.0f, __fsqrt_rn((float)HD)), 1.4426950408889634f);
+
+  float m = -INFINITY, l = 0.f, o[DPL];
+#pragma unroll
+  for (int j = 0; j < DPL; ++j) o[j] = 0.f;
+
+  for (int k0 = kbeg; k0 < kend; k0 += kRowKeys) {
+    const int nc = min(kRowKeys, kend - k0);
+    for (int i = tid; i < kRowKeys * C4; i += kRowThreadsA) {
+      const int kk = i / C4, c = i % C4;
+      float4 kx = make_float4(0.f, 0.f, 0.f, 0.f), vx = kx;
+      if (kk < nc) {
+        const int64_t off = (int64_t)(k0 + kk) * kw + (int64_t)g * HD + 4 * c;
+        kx = *reinterpret_cast<const float4*>(a.kreg + off);
+        vx = *reinterpret_cast<const float4*>(a.vreg + off);
+      }
+      ks[kk][4 * c] = kx.x;
+      ks[kk][4 * c + 1] = kx.y;
+      ks[kk][4 * c + 2] = kx.z;
+      ks[kk][4 * c + 3] = kx.w;
+      *reinterpret_cast<float4*>(&vs[kk][4 * c]) = vx;
+    }
+    __syncthreads();
+    if (warp < G) {
+      const int h = warp;
+      float d4[4] = {0.f, 0.f, 0.f, 0.f};  // four partial dots: shorter dependency chains
+#pragma unroll 8
+      for (int d = 0; d < HD; d += 4) {
+#pragma unroll
+        for (int e = 0; e < 4; ++e) d4[e] = fmaf(qs[h][d + e], ks[lane][d + e], d4[e]);
+      }
+      const float dot = __fadd_rn(__fadd_rn(d4[0], d4[1]), __fadd_rn(d4[2], d4[3]));
+      const float s = lane < nc ? __fmul_rn(dot, sc) : -INFINITY;
+      const float m_new = fmaxf(m, warp_max(s));
+      const float corr = m == -INFINITY ? 1.f : exp2f(m - m_new);
+      const float pk = lane < nc ? exp2f(s - m_new) : 0.f;
+      l = __fadd_rn(__fmul_rn(l, corr), warp_sum(pk));
+      m = m_new;
+#pragma unroll
+      for (int j = 0; j < DPL; ++j) o[j] *= corr;
+      for (int kk = 0; kk < nc; ++kk) {
+        const float pb = __shfl_sync(0xffffffffu, pk, kk);
+#pragma unroll
+        for (int j = 0; j < DPL; ++j) o[j] = fmaf(pb, vs[kk][lane + 32 * j], o[j]);
+      }
+    }
+    __syncthreads();  // the next chunk overwrites ks / vs
+  }
+
+  // this CTA's share of head warp: unnormalized O and (max, sum)
+  const int64_t slot = (int64_t)g * gridDim.x + split;
+  const int64_t ml_base = (int64_t)a.nkv * gridDim.x * 8 * HD;
+  if (warp < G) {
+    float* po = a.row_part + slot * 8 * HD + warp * HD;
+#pragma unroll
+    for (int j = 0; j < DPL; ++j) po[lane + 32 * j] = o[j];
+    if (lane == 0) {
+      a.row_part[ml_base + slot * 16 + 2 * warp] = m;
+      a.row_part[ml_base + slot * 16 + 2 * warp + 1] = l;
+    }
+  }
+  __threadfence();
+  __syncthreads();
+  if (tid == 0) s_last = atomicAdd(a.row_ticket + g, 1u) == (unsigned)(ns - 1);
+  __syncthreads();
+  if (!s_last) return;
+  __threadfence();
+  if (tid == 0) a.row_ticket[g] = 0u;  // every CTA of this head has drawn its ticket
+  if (warp >= G) return;
+
+  // merge (the last CTA of the head), warp h for query head h: lane s holds
+  // the (max, sum) of splits s, s + 32, ... (ns <= 128); weights exp2(m_s - M)
+  const int h = warp;
+  const float* gml = a.row_part + ml_base + (int64_t)g * gridDim.x * 16 + 2 * h;
+  const float* gpo = a.row_part + (int64_t)g * gridDim.x * 8 * HD + h * HD + lane;
+  float ms[4], ls[4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const int sidx = lane + 32 * i;
+    ms[i] = sidx < ns ? __ldcg(gml + sidx * 16) : -INFINITY;
+    ls[i] = sidx < ns ? __ldcg(gml + sidx * 16 + 1) : 0.f;
+  }
+  const float M = warp_max(fmaxf(fmaxf(ms[0], ms[1]), fmaxf(ms[2], ms[3])));
+  float ws[4], lsum = 0.f;
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    ws[i] = ms[i] == -INFINITY ? 0.f : exp2f(ms[i] - M);
+    lsum = fmaf(ls[i], ws[i], lsum);
+  }
+  const float L = warp_sum(lsum);
+  float acc[DPL];
+#pragma unroll
+  for (int j = 0; j < DPL; ++j) acc[j] = 0.f;
+  for (int s0 = 0; s0 < ns; s0 += 8) {
+    float x[8][DPL];  // eight splits' loads in flight
+#pragma unroll
+    for (int u = 0; u < 8; ++u)
+#pragma unroll
+      for (int j = 0; j < DPL; ++j)
+        x[u][j] = s0 + u < ns ? __ldcg(gpo + (int64_t)(s0 + u) * 8 * HD + 32 * j) : 0.f;
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+      const int sidx = s0 + u;
+      if (sidx >= ns) break;  // warp-uniform
+      const int q4 = sidx >> 5;
+      const float wsel = q4 == 0 ? ws[0] : (q4 == 1 ? ws[1] : (q4 == 2 ? ws[2] : ws[3]));
+      const float w = __shfl_sync(0xffffffffu, wsel, sidx & 31);
+#pragma unroll
+      for (int j = 0; j < DPL; ++j) acc[j] = fmaf(x[u][j], w, acc[j]);
+    }
+  }
+  const float il = L > 0.f ? __fdiv_rn(1.0f, L) : 0.f;
+  // Q8_0: block j of head h is dims 32 j .. 32 j + 31, one per lane
+  const int q = a.nh * HD;
+  const int nb = q / 32;
+  const int64_t orow = r - out.row_base;
+#pragma unroll
+  for (int j = 0; j < DPL; ++j) {
+    const float v = __fmul_rn(acc[j], il);
+    const int k = (g * G + h) * HD + 32 * j + lane;  // element of the output row
+    const int b = k / 32;
+    const float amax = warp_max(fabsf(v));
+    const float dd = __fdiv_rn(amax, 127.0f);
+    const float code = q8_code(v, q8_inv(dd));
+    if (out.f32) out.f32[(int64_t)r * q + k] = v;
+    const float d16 = __half2float(__float2half_rn(dd));
+    if (out.q8) {
+      out.q8[orow * (int64_t)nb * 32 + k] = (int8_t)code;
+      if (lane == 0) out.s8[orow * nb + b] = d16;
+    } else {
+      out.q16[orow * out.ldq + k] = __float2half_rn(code);
+      if (lane == 0) out.s16[(int64_t)b * out.ldqs + orow] = d16;
+    }
+  }
+}
+
 }  // namespace
+
+int attn_row_splits(int n_ctx, int nkv, int num_sms) {
+  int s = (n_ctx + kRowKeys - 1) / kRowKeys;
+  int cap = 2 * num_sms / (nkv > 0 ? nkv : 1);
+  if (cap > kAttnRowMaxSplits) cap = kAttnRowMaxSplits;
+  if (cap < 1) cap = 1;
+  return s < 1 ? 1 : (s > cap ? cap : s);
+}
 
 // 16-row tiles per CTA: enough to give the CTA 8 warps when a KV group has
 // few query heads.
@@ -549,6 +746,22 @@ cudaError_t attention_launch(const AttnArgs& a, const AttnOut& out, cudaStream_t
   if (a.nh % a.nkv != 0 || G > 8 || a.nsplit < 1 || a.nsplit > kMaxSplits)
     return cudaErrorInvalidValue;
   const bool gemv = out.q8 != nullptr;
+  if (rows == 1 && a.kreg && a.vreg && a.row_part && a.row_ticket && a.row_splits >= 1 &&
+      a.row_splits <= kAttnRowMaxSplits && reinterpret_cast<uintptr_t>(a.kreg) % 16 == 0 &&
+      reinterpret_cast<uintptr_t>(a.vreg) % 16 == 0) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)a.row_splits, (unsigned)a.nkv, 1);
+    cfg.blockDim = dim3(kRowThreadsA);
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    if (a.hd == 64) return cudaLaunchKernelEx(&cfg, attn_row_kernel<64>, a, out);
+    if (a.hd == 128) return cudaLaunchKernelEx(&cfg, attn_row_kernel<128>, a, out);
+    return cudaErrorInvalidValue;
+  }
   if (a.hd == 64) return gemv ? launch_attn<64, true>(a, out, rows, st) : launch_attn<64, false>(a, out, rows, st);
   if (a.hd == 128)
     return gemv ? launch_attn<128, true>(a, out, rows, st) : launch_attn<128, false>(a, out, rows, st);

@@ -171,14 +171,13 @@ __global__ void __launch_bounds__(kRowThreads) row_quant_kernel(const RowQuantAr
 // issued once per 4 blocks instead of once per block.  Same arithmetic as
 // row_quant_kernel element by element (partials summed in split order, then
 // the residual add; the sum of squares as float-float pairs; y = (x * r) * w).
-template <bool kGemvOut, int PER4>
-__global__ void __launch_bounds__(kRowThreads) row_quant4_kernel(const RowQuantArgs a) {
-  pdl_trigger();
-  pdl_wait();
+// kCG: read h through L2 only (h was written by other CTAs of the running
+// grid: the one-row GEMV's fused norm).
+template <bool kGemvOut, int PER4, bool kCG>
+__device__ __forceinline__ void row_quant4_row(const RowQuantArgs& a, const int64_t r) {
   __shared__ float red_hi[kRowThreads / 32], red_lo[kRowThreads / 32];
   __shared__ float s_scale;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int64_t r = blockIdx.x;
   const int64_t hr = a.row_offset + r;
   const int64_t n = a.n;
   const int64_t nc = n >> 2;  // float4 chunks of the row
@@ -189,7 +188,8 @@ __global__ void __launch_bounds__(kRowThreads) row_quant4_kernel(const RowQuantA
 #pragma unroll
   for (int i = 0; i < PER4; ++i) {
     const int64_t c = tid + (int64_t)kRowThreads * i;
-    x[i] = c < nc ? *reinterpret_cast<const float4*>(hrow + 4 * c) : make_float4(0.f, 0.f, 0.f, 0.f);
+    const float4* src = reinterpret_cast<const float4*>(hrow + 4 * c);
+    x[i] = c < nc ? (kCG ? __ldcg(src) : *src) : make_float4(0.f, 0.f, 0.f, 0.f);
   }
   if (a.nsplit > 0) {
     float4 o[PER4];
@@ -305,6 +305,13 @@ __global__ void __launch_bounds__(kRowThreads) row_quant4_kernel(const RowQuantA
       if (first) a.s16[(int64_t)b * a.ldqs + r] = __half2float(d16);
     }
   }
+}
+
+template <bool kGemvOut, int PER4>
+__global__ void __launch_bounds__(kRowThreads) row_quant4_kernel(const RowQuantArgs a) {
+  pdl_trigger();
+  pdl_wait();
+  row_quant4_row<kGemvOut, PER4, false>(a, blockIdx.x);
 }
 
 template <bool kGemvOut>
@@ -570,42 +577,50 @@ __global__ void __launch_bounds__(1024) rope_store_qknorm_kernel(const RopeStore
 }
 
 // ---------------------------------------------------------------- one-row GEMV
-// y[n] = sum_b dw[n][b] * dx[b] * dot_b, one output row n at a time per warp
-// slot.  Lane l reads bytes 16 l .. 16 l + 15 of each 512-byte chunk of a
-// row's codes (half of a Q8_0 block, coalesced across the warp); dp4a gives
-// the integer partial and the lane pair (l, l ^ 1) adds up the block's exact
-// int32 dot, which the even lane scales by dw * dx.  A warp owns R rows and
-// issues every load of all of them before any arithmetic, so R times more
-// bytes are in flight per lane than with one row per warp: the kernel is
-// bound by HBM, and the number of bytes in flight sets how close it gets.
+// y[n] = sum_b dw[n][b] * dx[b] * dot_b.  A warp owns R output rows; lane l
+// reads bytes 16 l .. 16 l + 15 of each 512-byte chunk of a row's codes (half
+// of a Q8_0 block, coalesced across the warp); dp4a gives the integer partial
+// and the lane pair (l, l ^ 1) adds up the block's exact int32 dot, which the
+// even lane scales by dw * dx.  Every load of a round (U chunks of all R
+// rows, U = 4 for R = 1 and 2 above) is issued before the first dp4a: the
+// kernel is bound by HBM, and the bytes in flight per warp (R * U * 512) set
+// how close it gets.
+//
+// Fused one-row epilogues (grid-wide, wait-free):
+//  - swiglu: the rows are gate/up interleaved in groups of 32, so CTA j (8
+//    warps x 8 rows) holds the gate and up sums of outputs 32 j .. 32 j + 31;
+//    it quantizes silu(g) * u of them (Q8_0) into q8/s8 and writes no y;
+//  - norm_w: after its rows are written each CTA takes a ticket; the CTA that
+//    draws the last one RMS-normalizes y[0:N] and quantizes it (Q8_0) into
+//    q8/s8, with the row kernel's arithmetic, and returns the ticket to zero.
 constexpr int kGemvWarps = 8;
 
+__device__ __forceinline__ float silu_mul_row(float g, float u) {
+  return __fmul_rn(__fdiv_rn(g, __fadd_rn(1.0f, expf(-g))), u);
+}
+
+// The dot products of R rows (rows[r] < 0: none) with the activation row:
+// after the call every lane holds the full sum of each row in acc[r].
 template <int R>
-__global__ void __launch_bounds__(32 * kGemvWarps, 2) gemv_kernel(const GemvArgs a) {
-  pdl_trigger();
-  pdl_wait();
+__device__ __forceinline__ void gemv_dot(const GemvArgs& a, const int64_t (&rows)[R], float (&acc)[R]) {
+  constexpr int U = R >= 2 ? 2 : 4;  // 512-byte chunks per round
   const int lane = threadIdx.x & 31;
-  const int64_t n0 = ((int64_t)blockIdx.x * kGemvWarps + (threadIdx.x >> 5)) * R;
-  if (n0 >= a.N) return;
-  float acc[R];
 #pragma unroll
   for (int r = 0; r < R; ++r) acc[r] = 0.f;
-  // two 512-byte chunks per round: every load of both (all R rows) is issued
-  // before the first dot product
-  for (int64_t c = 0; c < a.kpad; c += 1024) {
-    int4 w[2][R];
-    float dw[2][R];
-    int4 x[2];
-    float dx[2];
+  for (int64_t c = 0; c < a.kpad; c += 512 * U) {
+    int4 w[U][R];
+    float dw[U][R];
+    int4 x[U];
+    float dx[U];
 #pragma unroll
-    for (int h = 0; h < 2; ++h) {
+    for (int h = 0; h < U; ++h) {
       const int64_t k = c + 512 * h + 16 * lane;
       const bool in = k < a.kpad;
       const int b = (int)(k >> 5);
 #pragma unroll
       for (int r = 0; r < R; ++r) {
-        const int64_t n = n0 + r;
-        const bool ok = in && n < a.N;
+        const int64_t n = rows[r];
+        const bool ok = in && n >= 0;
         w[h][r] = ok ? __ldg(reinterpret_cast<const int4*>(a.wq + n * a.kpad + k))
                      : make_int4(0, 0, 0, 0);
         dw[h][r] = ok ? __ldg(a.ws + n * a.nb + b) : 0.f;
@@ -614,7 +629,7 @@ __global__ void __launch_bounds__(32 * kGemvWarps, 2) gemv_kernel(const GemvArgs
       dx[h] = in ? a.xs[b] : 0.f;
     }
 #pragma unroll
-    for (int h = 0; h < 2; ++h)
+    for (int h = 0; h < U; ++h)
 #pragma unroll
       for (int r = 0; r < R; ++r) {
         int isum = __dp4a(w[h][r].x, x[h].x, 0);
@@ -629,34 +644,140 @@ __global__ void __launch_bounds__(32 * kGemvWarps, 2) gemv_kernel(const GemvArgs
   for (int r = 0; r < R; ++r)
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) acc[r] += __shfl_xor_sync(0xffffffffu, acc[r], o);
-  if (lane < R && n0 + lane < a.N) {
-    if (!status_clear(a.status)) return;
-    float v = acc[0];
+}
+
+template <int R>
+__global__ void __launch_bounds__(32 * kGemvWarps, R >= 4 ? 2 : (R == 2 ? 4 : 3)) gemv_kernel(const GemvArgs a) {
+  __shared__ float part[kGemvWarps][8];
+  __shared__ unsigned s_last;
+  pdl_trigger();
+  pdl_wait();
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int64_t n0 = ((int64_t)blockIdx.x * kGemvWarps + warp) * R;
+  float acc[R];
+  int64_t rows[R];
 #pragma unroll
-    for (int r = 1; r < R; ++r)
-      if (lane == r) v = acc[r];
-    const int64_t n = n0 + lane;
-    a.y[n] = a.resid ? __fadd_rn(a.resid[n], v) : v;
+  for (int r = 0; r < R; ++r) rows[r] = n0 + r < a.N ? n0 + r : -1;
+  gemv_dot<R>(a, rows, acc);
+  float v = acc[0];  // lane r < R: the sum of row n0 + r
+#pragma unroll
+  for (int r = 1; r < R; ++r)
+    if (lane == r) v = acc[r];
+  const int64_t n = n0 + lane;
+  if (a.swiglu) {
+    // part[w][r] = row 8 w + r of the CTA: gate rows in warps 0-3, up in 4-7
+    if (lane < R) part[warp][lane] = v;
+    __syncthreads();
+    if (warp == 0) {
+      const float gsum = part[lane >> 3][lane & 7];
+      const float usum = part[4 + (lane >> 3)][lane & 7];
+      const float sv = silu_mul_row(gsum, usum);
+      const float amax = warp_max(fabsf(sv));
+      const float d = __fdiv_rn(amax, 127.0f);
+      a.q8[(int64_t)blockIdx.x * 32 + lane] = (int8_t)q8_code(sv, q8_inv(d));
+      if (lane == 0) a.s8[blockIdx.x] = __half2float(__float2half_rn(d));
+    }
+    return;
+  }
+  if (lane < R && n < a.N && status_clear(a.status)) a.y[n] = a.resid ? __fadd_rn(a.resid[n], v) : v;
+  if (a.norm_w) {
+    __threadfence();  // this CTA's rows of y, device-wide, before its ticket
+    __syncthreads();
+    if (threadIdx.x == 0) s_last = atomicAdd(a.ticket, 1u) == gridDim.x - 1;
+    __syncthreads();
+    if (!s_last) return;
+    __threadfence();
+    RowQuantArgs rq;
+    rq.h = a.y;
+    rq.norm_w = a.norm_w;
+    rq.eps = a.eps;
+    rq.rows = 1;
+    rq.n = a.N;
+    rq.q8 = a.q8;
+    rq.s8 = a.s8;
+    row_quant4_row<true, 4, true>(rq, 0);
+    if (threadIdx.x == 0) *a.ticket = 0u;
   }
 }
 
-__global__ void swiglu_quant_row_kernel(const float* __restrict__ gu, int64_t F, int8_t* q,
-                                        float* s) {
+// The one-row QKV GEMV with the RoPE/store of its token in the same kernel.
+// A warp's four rows are two neighbouring dimension pairs (i, i + 1 and their
+// partners i + hd/2, i + 1 + hd/2) of one Q or K head, or four V dimensions,
+// so the rotation needs only the warp's own sums.  The raw sums still go to y;
+// bias, rotation, the region and plane writes are rope_store_kernel's
+// arithmetic element by element.
+__global__ void __launch_bounds__(32 * kGemvWarps, 2) gemv_rope_kernel(const GemvArgs a,
+                                                                      const RopeStoreArgs ra) {
   pdl_trigger();
   pdl_wait();
-  const int lane = threadIdx.x & 31;
-  const int64_t nb = (F + 31) / 32;
-  for (int64_t b = threadIdx.x >> 5; b < nb; b += blockDim.x >> 5) {
-    const int64_t j = b * 32 + lane;
-    float v = 0.f;
-    if (j < F) {
-      const float g = gu[j], u = gu[F + j];
-      v = __fmul_rn(__fdiv_rn(g, __fadd_rn(1.0f, expf(-g))), u);
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int hd = ra.hd, half = hd >> 1;
+  const int64_t unit = (int64_t)blockIdx.x * kGemvWarps + warp;
+  const int64_t urope = (int64_t)(ra.nh + ra.nkv) * half / 2;  // units of Q and K heads
+  const int64_t units = a.N / 4;
+  const bool live = unit < units, rope = unit < urope;
+  int hh = 0, i0 = 0;
+  int64_t rows[4];
+  if (rope) {
+    hh = (int)(2 * unit / half);
+    i0 = (int)(2 * unit % half);
+    const int64_t base = (int64_t)hh * hd + i0;
+    rows[0] = base;
+    rows[1] = base + 1;
+    rows[2] = base + half;
+    rows[3] = base + half + 1;
+  } else {
+    const int64_t base = (int64_t)(ra.nh + ra.nkv) * hd + 4 * (unit - urope);
+#pragma unroll
+    for (int r = 0; r < 4; ++r) rows[r] = live ? base + r : -1;
+  }
+  float acc[4];
+  gemv_dot<4>(a, rows, acc);
+  const int r4 = lane & 3;
+  const float v = r4 == 0 ? acc[0] : (r4 == 1 ? acc[1] : (r4 == 2 ? acc[2] : acc[3]));
+  const int64_t row = r4 == 0 ? rows[0] : (r4 == 1 ? rows[1] : (r4 == 2 ? rows[2] : rows[3]));
+  float x = v;
+  if (live && ra.bias) x = __fadd_rn(x, ra.bias[row]);
+  const float xp = __shfl_xor_sync(0xffffffffu, x, 2);  // the pair partner (lanes 0<->2, 1<->3)
+  if (!live || lane >= 4) return;
+  a.y[row] = v;
+  const int p_in = ra.pos[0];
+  const bool write_kv = status_clear(ra.status) && p_in >= 0 && p_in < ra.n_ctx;
+  const int p = (p_in >= 0 && p_in < ra.n_ctx) ? p_in : 0;
+  const int64_t kw = (int64_t)ra.nkv * hd;
+  if (rope) {
+    const int i = i0 + (lane & 1);
+    const float c = ra.cos_t[(int64_t)p * half + i], sn = ra.sin_t[(int64_t)p * half + i];
+    const bool first = lane < 2;
+    const float x0 = first ? x : xp, x1 = first ? xp : x;
+    const float val = first ? __fsub_rn(__fmul_rn(x0, c), __fmul_rn(x1, sn))
+                            : __fadd_rn(__fmul_rn(x0, sn), __fmul_rn(x1, c));
+    const int e = first ? i : i + half;  // dimension within the head
+    const __half hi = __float2half_rn(val);
+    const __half lo = __float2half_rn(__fsub_rn(val, __half2float(hi)));
+    if (hh < ra.nh) {
+      const int64_t o = (int64_t)hh * hd + e;
+      ra.q_out[o] = val;
+      if (ra.q_planes[0]) {
+        ra.q_planes[0][o] = hi;
+        ra.q_planes[1][o] = lo;
+      }
+    } else if (write_kv) {
+      const int64_t o0 = (int64_t)p * kw + (int64_t)(hh - ra.nh) * hd + e;
+      ra.kreg[o0] = val;
+      ra.shadow[0][o0] = hi;
+      ra.shadow[1][o0] = lo;
     }
-    const float amax = warp_max(fabsf(v));
-    const float d = __fdiv_rn(amax, 127.0f);
-    q[j] = (int8_t)q8_code(v, q8_inv(d));
-    if (lane == 0) s[b] = __half2float(__float2half_rn(d));
+  } else if (write_kv) {
+    const int64_t e = row - (int64_t)(ra.nh + ra.nkv) * hd;
+    const int64_t o0 = (int64_t)p * kw + e;
+    const __half hi = __float2half_rn(x);
+    const __half lo = __float2half_rn(__fsub_rn(x, __half2float(hi)));
+    ra.vreg[o0] = x;
+    ra.shadow[2][o0] = hi;
+    ra.shadow[3][o0] = lo;
+    ra.vt[0][e * ra.vt_ld + p] = hi;
+    ra.vt[1][e * ra.vt_ld + p] = lo;
   }
 }
 
@@ -735,14 +856,21 @@ __global__ void copy_if_ok_kernel(const float* __restrict__ src, float* dst, int
     dst[i] = src[i];
 }
 
+// interleave: source row r goes to row (r / 32) * 64 + which * 32 + r % 32
+// (gate and up rows of the same 32 outputs side by side), else to row r.
 __global__ void repack_gemv_kernel(const int8_t* __restrict__ q, const uint16_t* __restrict__ dbits,
-                                   int64_t rows, int nb, int8_t* dst_q, float* dst_s) {
+                                   int64_t rows, int nb, int8_t* dst_q, float* dst_s, int interleave,
+                                   int which) {
   const int64_t kpad = (int64_t)nb * 32;
   const int64_t total = rows * kpad;
   for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < total;
        i += (int64_t)gridDim.x * blockDim.x) {
-    dst_q[i] = q[i];
-    if ((i & 31) == 0) dst_s[i / 32] = __half2float(__ushort_as_half(dbits[i / 32]));
+    const int64_t r = i / kpad, k = i % kpad;
+    const int64_t dr = interleave ? (r / kSwiGluGroup) * 2 * kSwiGluGroup + which * kSwiGluGroup +
+                                        r % kSwiGluGroup
+                                  : r;
+    dst_q[dr * kpad + k] = q[i];
+    if ((k & 31) == 0) dst_s[dr * nb + k / 32] = __half2float(__ushort_as_half(dbits[i / 32]));
   }
 }
 
@@ -814,6 +942,13 @@ cudaError_t rope_store_launch(const RopeStoreArgs& a, cudaStream_t st) {
 }
 
 cudaError_t gemv_launch(const GemvArgs& a, cudaStream_t st) {
+  if (a.swiglu) {
+    // one CTA per 32 outputs: 64 interleaved gate/up rows, 8 per warp
+    if (a.N % 64 != 0 || !a.q8 || !a.s8) return cudaErrorInvalidValue;
+    return launch_pdl(gemv_kernel<8>, (unsigned)(a.N / 64), 32 * kGemvWarps, 0, st, a);
+  }
+  if (a.norm_w && (!a.ticket || !gemv_norm_fusable(a.N, a.y, a.norm_w, a.q8)))
+    return cudaErrorInvalidValue;
   // the most rows per warp that still gives every SM two CTAs
   const int64_t per_cta[4] = {8 * kGemvWarps, 4 * kGemvWarps, 2 * kGemvWarps, kGemvWarps};
   int pick = 3;
@@ -831,6 +966,20 @@ cudaError_t gemv_launch(const GemvArgs& a, cudaStream_t st) {
   }
 }
 
+cudaError_t gemv_rope_launch(const GemvArgs& a, const RopeStoreArgs& r, cudaStream_t st) {
+  if (r.nt != 1 || r.q_norm || r.nsplit != 1 || (r.hd != 64 && r.hd != 128) ||
+      a.N != (int64_t)(r.nh + 2 * r.nkv) * r.hd)
+    return cudaErrorInvalidValue;
+  const int64_t units = a.N / 4;
+  return launch_pdl(gemv_rope_kernel, (unsigned)((units + kGemvWarps - 1) / kGemvWarps),
+                    32 * kGemvWarps, 0, st, a, r);
+}
+
+bool gemv_norm_fusable(int64_t N, const float* y, const float* norm_w, const int8_t* q8) {
+  return N % 32 == 0 && N / 4 <= 4 * kRowThreads && reinterpret_cast<uintptr_t>(y) % 16 == 0 &&
+         reinterpret_cast<uintptr_t>(norm_w) % 16 == 0 && reinterpret_cast<uintptr_t>(q8) % 4 == 0;
+}
+
 cudaError_t gemv_to_gemm_launch(const int8_t* q, const float* sc, int64_t rows, int nb,
                                 __half* codes, float* scales, int64_t rows_pad, cudaStream_t st) {
   gemv_to_gemm_kernel<<<grid_for(rows * nb * 32, 256), 256, 0, st>>>(q, sc, rows, nb, codes, scales,
@@ -842,11 +991,6 @@ cudaError_t copy_if_ok_launch(const float* src, float* dst, int64_t n, const int
                               cudaStream_t st) {
   return launch_pdl(copy_if_ok_kernel, (unsigned)std::min<int64_t>((n + 255) / 256, 4096), 256, 0,
                     st, src, dst, n, status);
-}
-
-cudaError_t swiglu_quant_row_launch(const float* gu, int64_t F, int8_t* q, float* s,
-                                    cudaStream_t st) {
-  return launch_pdl(swiglu_quant_row_kernel, 1, 1024, 0, st, gu, F, q, s);
 }
 
 cudaError_t quantize_rows_launch(const float* x, int64_t rows, int64_t n, int8_t* q,
@@ -869,8 +1013,10 @@ cudaError_t repack_gemm_launch(const RepackArgs& a, cudaStream_t st) {
 }
 
 cudaError_t repack_gemv_launch(const int8_t* q, const uint16_t* dbits, int64_t rows, int nb,
-                               int8_t* dst_q, float* dst_s, cudaStream_t st) {
-  repack_gemv_kernel<<<grid_for(rows * nb * 32, 256), 256, 0, st>>>(q, dbits, rows, nb, dst_q, dst_s);
+                               int8_t* dst_q, float* dst_s, int interleave, int which,
+                               cudaStream_t st) {
+  repack_gemv_kernel<<<grid_for(rows * nb * 32, 256), 256, 0, st>>>(q, dbits, rows, nb, dst_q, dst_s,
+                                                                    interleave, which);
   return cudaGetLastError();
 }
 

@@ -162,6 +162,10 @@ struct RopeStoreArgs {
   float eps = 0.f;
 };
 cudaError_t rope_store_launch(const RopeStoreArgs& a, cudaStream_t stream);
+struct GemvArgs;
+// One token, no QK-norm: the QKV GEMV (g: y = the raw Q|K|V sums) and the
+// RoPE/store of r (partials = g.y, nsplit 1) in one kernel.
+cudaError_t gemv_rope_launch(const GemvArgs& g, const RopeStoreArgs& r, cudaStream_t stream);
 
 // Causal GQA attention of query rows [r0, r1) over the fp16 hi/lo shadow
 // planes of a layer's K/V regions, split along the keys (ksplit keys per
@@ -177,7 +181,21 @@ struct AttnArgs {
   int nh = 0, nkv = 0, hd = 0;
   int n_ctx = 0;   // positions are clamped into [0, n_ctx) before any region read
   int nsplit = 1;  // key splits (CTAs per cluster), 1..8
+  // One-row calls (r1 - r0 == 1) run the split-key CUDA-core kernel when these
+  // are set: the f32 K/V regions [n_ctx][nkv*hd], a scratch of
+  // attn_row_scratch_floats() floats and nkv zero-initialized tickets (left at
+  // zero); row_splits = attn_row_splits(n_ctx, nkv, num_sms).
+  const float* kreg = nullptr;
+  const float* vreg = nullptr;
+  float* row_part = nullptr;
+  unsigned* row_ticket = nullptr;
+  int row_splits = 0;
 };
+constexpr int kAttnRowMaxSplits = 128;
+int attn_row_splits(int n_ctx, int nkv, int num_sms);
+inline size_t attn_row_scratch_floats(int nkv, int hd) {
+  return (size_t)nkv * kAttnRowMaxSplits * (8 * (size_t)hd + 16);
+}
 // Where the attention output goes: Q8_0 codes in the GEMM layout (q16 [rows][ldq]
 // fp16 + s16 [nb][ldqs]) or the GEMV layout (q8 [rows][nb*32] + s8 [rows][nb]);
 // output row index = query row - row_base.  f32 (optional): [nt][nh*hd].
@@ -226,19 +244,30 @@ struct GemvArgs {
   const float* resid = nullptr;  // y = resid + W.x when set (may alias y)
   const int* status = nullptr;   // the model's two status words: no write of y unless both are 0
   int num_sms = 152;             // rows per warp are chosen to give every SM two CTAs
+  // Fused one-row epilogues (q8 [nb*32] codes + s8 [nb] f32 scales of the result):
+  // swiglu: rows are gate/up interleaved in groups of 32 (N = 2 * F padded to
+  //   a multiple of 64); q8/s8 get the Q8_0 of silu(gate) * up; y is not written.
+  // norm_w: y is written, then the last CTA to finish writes the Q8_0 of
+  //   RMSNorm(y) * norm_w (eps) into q8/s8; ticket: a zero-initialized counter,
+  //   left at zero.  Needs gemv_norm_fusable().
+  int swiglu = 0;
+  const float* norm_w = nullptr;
+  float eps = 0.f;
+  int8_t* q8 = nullptr;
+  float* s8 = nullptr;
+  unsigned* ticket = nullptr;
 };
 cudaError_t gemv_launch(const GemvArgs& a, cudaStream_t stream);
+// Whether a norm can ride the GEMV's last CTA: whole Q8_0 blocks, N <= 4096,
+// 16-byte aligned y and norm_w, 4-byte aligned q8.
+bool gemv_norm_fusable(int64_t N, const float* y, const float* norm_w, const int8_t* q8);
 
-// s = silu(g) * u for one row of F outputs (g = y[0:F], u = y[F:2F]) -> Q8_0
-// int8 codes [nbF*32] + f32 scales [nbF].
 // int8 [rows][nb*32] + f32 [rows][nb] (GEMV layout) -> fp16 codes + block-major scales.
 cudaError_t gemv_to_gemm_launch(const int8_t* q, const float* sc, int64_t rows, int nb,
                                 __half* codes, float* scales, int64_t rows_pad, cudaStream_t stream);
 // dst[0:n] = src[0:n] when both status words are 0.
 cudaError_t copy_if_ok_launch(const float* src, float* dst, int64_t n, const int* status,
                               cudaStream_t stream);
-cudaError_t swiglu_quant_row_launch(const float* gu, int64_t F, int8_t* q, float* s,
-                                    cudaStream_t stream);
 
 // ---------------------------------------------------------------- load-time kernels
 // f32 rows -> Q8_0 (int8 codes [rows][nb*32] + fp16 scale bits [rows][nb]).
@@ -262,9 +291,12 @@ struct RepackArgs {
   int which = 0;
 };
 cudaError_t repack_gemm_launch(const RepackArgs& a, cudaStream_t stream);
-// int8 codes + fp16 bits -> GEMV planes (int8 codes copy + f32 scales [rows][nb]).
+// int8 codes + fp16 bits -> GEMV planes (int8 codes copy + f32 scales [rows][nb]);
+// interleave = 1: source row r lands on row (r / 32) * 64 + which * 32 + r % 32
+// (the fused SwiGLU GEMV's gate/up layout).
 cudaError_t repack_gemv_launch(const int8_t* q, const uint16_t* dbits, int64_t rows, int nb,
-                               int8_t* dst_q, float* dst_s, cudaStream_t stream);
+                               int8_t* dst_q, float* dst_s, int interleave, int which,
+                               cudaStream_t stream);
 // GEMM planes -> canonical int8 codes / fp16 bits (tests).
 cudaError_t gemm_plane_to_q8_launch(const __half* codes, const float* scales, int64_t rows,
                                     int64_t rows_pad, int nb, int8_t* q, uint16_t* dbits,

@@ -163,14 +163,18 @@ struct Workspace {
   float* h_last = nullptr;   // [H]
   int8_t* t_q = nullptr;     // [max kpad] one-row codes
   float* t_s = nullptr;      // [max nb]
-  float* gu = nullptr;       // [2F]
+  int8_t* t_q2 = nullptr;    // [Fp] one-row SwiGLU codes
+  float* t_s2 = nullptr;     // [nbF]
+  float* arow = nullptr;     // one-row attention scratch
+  unsigned* tickets = nullptr;  // [kTickets] zero-initialized counters of the one-row kernels
   float* logits = nullptr;   // [logits_rows][V]
   int logits_rows = 0;
   float* lm_out = nullptr;   // [logits_rows][V]: lm_head GEMM output before the status-gated copy
   int ntp = 0;
   void release() {
     dfree(ids); dfree(pos); dfree(h); dfree(xa); dfree(xa_s); dfree(xf); dfree(xf_s);
-    dfree(part); dfree(qrot); dfree(qpl); dfree(att); dfree(h_last); dfree(t_q); dfree(t_s); dfree(gu);
+    dfree(part); dfree(qrot); dfree(qpl); dfree(att); dfree(h_last); dfree(t_q); dfree(t_s);
+    dfree(t_q2); dfree(t_s2); dfree(arow); dfree(tickets);
     dfree(logits); dfree(lm_out);
     logits_rows = 0;
     max_nt = 0;
@@ -178,14 +182,18 @@ struct Workspace {
 };
 
 constexpr int kMaxSplits = 8;
+// tickets: [0, nkv) the one-row attention's heads, then the fused norms of the
+// o and down GEMVs
+constexpr int kTicketNormO = 0, kTicketNormDown = 1;
+constexpr int kTicketsFixed = 2;
 
 enum KClass : int {
   kKValidate, kKEmbed, kKRowQuant, kKGemmQKV, kKRope, kKAttn, kKGemmO, kKGemmGU, kKGemmDown,
-  kKTailGemv, kKTailSwiglu, kKLmHead, kNumKClass
+  kKTailGemv, kKLmHead, kNumKClass
 };
 const char* kClassNames[kNumKClass] = {
     "validate", "embed", "rmsnorm_quant", "gemm_qkv", "rope_kv_store", "attention", "gemm_o",
-    "gemm_gate_up_swiglu", "gemm_down", "tail_gemv", "tail_swiglu", "lm_head_gemv"};
+    "gemm_gate_up_swiglu", "gemm_down", "tail_gemv", "lm_head_gemv"};
 
 }  // namespace
 
@@ -335,9 +343,10 @@ int to_gemm(minfer_model* m, int64_t rows, int nb, GemmW& w, int64_t row0, int i
   return MINFER_OK;
 }
 
-int to_gemv(minfer_model* m, int64_t rows, int nb, GemvW& w, int64_t row0) {
+int to_gemv(minfer_model* m, int64_t rows, int nb, GemvW& w, int64_t row0, int interleave = 0,
+            int which = 0) {
   CK(repack_gemv_launch(m->stage_q, m->stage_d, rows, nb, w.q + row0 * nb * 32, w.s + row0 * nb,
-                        m->stream));
+                        interleave, which, m->stream));
   return MINFER_OK;
 }
 
@@ -386,7 +395,7 @@ int model_alloc(minfer_model* m) {
         (rc = L.wgu.alloc(2 * m->Fp, m->nbH)) || (rc = L.wd.alloc(m->H, m->nbF)))
       return rc;
     if ((rc = L.wqkv_v.alloc(m->qkvN, m->nbH)) || (rc = L.wo_v.alloc(m->H, m->nbq)) ||
-        (rc = L.wgu_v.alloc(2 * m->F, m->nbH)) || (rc = L.wd_v.alloc(m->H, m->nbF)))
+        (rc = L.wgu_v.alloc(2 * m->Fp, m->nbH)) || (rc = L.wd_v.alloc(m->H, m->nbF)))
       return rc;
   }
   if ((rc = dalloc(&m->d_status, 4))) return rc;
@@ -474,7 +483,7 @@ int set_tensor(minfer_model* m, const minfer_tensor* t) {
       if (!mat_ok(m->H, m->F)) return MINFER_ERR_SHAPE;
       if ((rc = stage_matrix(m, t))) return rc;
       if ((rc = to_gemm(m, m->F, m->nbH, L.wgu, 0, 1, which))) return rc;
-      rc = to_gemv(m, m->F, m->nbH, L.wgu_v, which * m->F);
+      rc = to_gemv(m, m->F, m->nbH, L.wgu_v, 0, 1, which);
     } else if (k == "ffn_down.weight") {
       if (!mat_ok(m->F, m->H)) return MINFER_ERR_SHAPE;
       if ((rc = stage_matrix(m, t))) return rc;
@@ -536,7 +545,10 @@ int ensure_workspace(minfer_model* m, int nt) {
       (rc = dalloc(&w.qpl, 2 * nt * m->q)) ||
       (rc = dalloc(&w.att, nt * m->q)) || (rc = dalloc(&w.h_last, m->H)) ||
       (rc = dalloc(&w.t_q, std::max<int64_t>(kx, m->Fp))) ||
-      (rc = dalloc(&w.t_s, std::max(nbx, m->nbF))) || (rc = dalloc(&w.gu, 2 * m->F)) ||
+      (rc = dalloc(&w.t_s, std::max(nbx, m->nbF))) || (rc = dalloc(&w.t_q2, m->Fp)) ||
+      (rc = dalloc(&w.t_s2, m->nbF)) ||
+      (rc = dalloc(&w.arow, attn_row_scratch_floats(m->hp.n_head_kv, m->hp.head_dim))) ||
+      (rc = dalloc(&w.tickets, (size_t)kTicketsFixed + m->hp.n_head_kv)) ||
       (rc = dalloc(&w.logits, m->V)))
     return rc;
   w.logits_rows = 1;
@@ -664,28 +676,80 @@ void dump_hidden(minfer_model* m, cudaStream_t st, int slot, const float* src, i
 // n_tokens = 1): every projection is a one-row GEMV over the int8 layout,
 // which reads each weight byte once -- the work is bound by HBM, and the
 // tensor-core GEMM would pad the one row to 128.
+// ------------------------------------------------------------------ one-row stages
+// Shared by single-token calls and the last row of a prompt: every projection
+// is a GEMV over the one-row Q8_0 activation.
+
+GemvArgs row_gemv(const minfer_model* m, const GemvW& W, int64_t N, int nb, const int8_t* xq,
+                  const float* xs, float* y, const float* resid) {
+  GemvArgs g;
+  g.num_sms = m->num_sms;
+  g.wq = W.q;
+  g.ws = W.s;
+  g.N = N;
+  g.nb = nb;
+  g.kpad = (int64_t)nb * 32;
+  g.xq = xq;
+  g.xs = xs;
+  g.y = y;
+  g.resid = resid;
+  return g;
+}
+
+// y = resid + W.x, then RMSNorm(y) * norm_w quantized (Q8_0) into the one-row
+// codes t_q/t_s: inside the GEMV's last CTA where the shape allows, else by
+// the row kernel after it.
+int row_gemv_norm(minfer_model* m, Launcher& L, GemvArgs g, const float* norm_w, int ticket,
+                  cudaStream_t st) {
+  Workspace& w = m->ws;
+  if (gemv_norm_fusable(g.N, g.y, norm_w, w.t_q)) {
+    g.norm_w = norm_w;
+    g.eps = m->hp.rms_eps;
+    g.q8 = w.t_q;
+    g.s8 = w.t_s;
+    g.ticket = w.tickets + ticket;
+    LAUNCH(kKTailGemv, gemv_launch(g, st));
+    return MINFER_OK;
+  }
+  LAUNCH(kKTailGemv, gemv_launch(g, st));
+  RowQuantArgs r;
+  r.h = g.y;
+  r.norm_w = norm_w;
+  r.eps = m->hp.rms_eps;
+  r.rows = 1;
+  r.n = g.N;
+  r.q8 = w.t_q;
+  r.s8 = w.t_s;
+  LAUNCH(kKRowQuant, row_quant_launch(r, st));
+  return MINFER_OK;
+}
+
+// gate/up GEMV with the SwiGLU and its Q8_0 in the same kernel: t_q/t_s in,
+// t_q2/t_s2 out.
+int row_gemv_swiglu(minfer_model* m, Launcher& L, const GemvW& W, cudaStream_t st) {
+  Workspace& w = m->ws;
+  GemvArgs g = row_gemv(m, W, 2 * m->Fp, m->nbH, w.t_q, w.t_s, nullptr, nullptr);
+  g.swiglu = 1;
+  g.q8 = w.t_q2;
+  g.s8 = w.t_s2;
+  LAUNCH(kKTailGemv, gemv_launch(g, st));
+  return MINFER_OK;
+}
+
+// The one-row attention kernel's inputs on top of the tiled kernel's.
+void row_attention_args(const minfer_model* m, const minfer_kv* kv, int l, AttnArgs* at) {
+  at->kreg = kv->k(l);
+  at->vreg = kv->v(l);
+  at->row_part = m->ws.arow;
+  at->row_ticket = m->ws.tickets + kTicketsFixed;
+  at->row_splits = attn_row_splits(kv->n_ctx, m->hp.n_head_kv, m->num_sms);
+}
+
 int enqueue_decode(minfer_model* m, minfer_kv* kv, const int32_t* ids, const int32_t* pos,
                    float* logits, cudaStream_t st, bool prof, bool dumps) {
   const auto& hp = m->hp;
   Workspace& w = m->ws;
   Launcher L{m, st, prof};
-  auto gemv = [&](int cls, const GemvW& W, int64_t N, int nb, float* y, const float* resid,
-                  const int* status) -> int {
-    GemvArgs g;
-    g.num_sms = m->num_sms;
-    g.wq = W.q;
-    g.ws = W.s;
-    g.N = N;
-    g.nb = nb;
-    g.kpad = (int64_t)nb * 32;
-    g.xq = w.t_q;
-    g.xs = w.t_s;
-    g.y = y;
-    g.resid = resid;
-    g.status = status;
-    LAUNCH(cls, gemv_launch(g, st));
-    return MINFER_OK;
-  };
   auto norm_quant = [&](const float* norm_w) -> int {
     RowQuantArgs r;
     r.h = w.h;
@@ -725,8 +789,6 @@ int enqueue_decode(minfer_model* m, minfer_kv* kv, const int32_t* ids, const int
           (rc = cap_q8("x_q8", "x_s8", m->nbH)))
         return rc;
     }
-    if ((rc = gemv(kKTailGemv, Ly.wqkv_v, m->qkvN, m->nbH, w.part, nullptr, nullptr))) return rc;
-    if (cap && (rc = dbg_capture(m, st, "qkv", w.part, (size_t)m->qkvN * 4))) return rc;
     {
       RopeStoreArgs r;
       r.partials = w.part;
@@ -752,8 +814,16 @@ int enqueue_decode(minfer_model* m, minfer_kv* kv, const int32_t* ids, const int
         r.k_norm = Ly.k_norm;
         r.eps = hp.rms_eps;
       }
-      LAUNCH(kKRope, rope_store_launch(r, st));
+      // Q|K|V sums -> w.part; RoPE/store in the same kernel unless QK-norm
+      const GemvArgs gq = row_gemv(m, Ly.wqkv_v, m->qkvN, m->nbH, w.t_q, w.t_s, w.part, nullptr);
+      if (!hp.qk_norm) {
+        LAUNCH(kKTailGemv, gemv_rope_launch(gq, r, st));
+      } else {
+        LAUNCH(kKTailGemv, gemv_launch(gq, st));
+        LAUNCH(kKRope, rope_store_launch(r, st));
+      }
     }
+    if (cap && (rc = dbg_capture(m, st, "qkv", w.part, (size_t)m->qkvN * 4))) return rc;
     {
       AttnArgs at;
       at.q = w.qrot;
@@ -769,6 +839,7 @@ int enqueue_decode(minfer_model* m, minfer_kv* kv, const int32_t* ids, const int
       at.hd = hp.head_dim;
       at.n_ctx = kv->n_ctx;
       at.nsplit = attention_nsplit(1, at.nkv, m->num_sms, at.nh / at.nkv);
+      row_attention_args(m, kv, l, &at);
       AttnOut ao;
       ao.f32 = (m->debug_f32 || cap) ? w.att : nullptr;
       ao.q8 = w.t_q;
@@ -779,20 +850,30 @@ int enqueue_decode(minfer_model* m, minfer_kv* kv, const int32_t* ids, const int
                 (rc = dbg_capture(m, st, "att", w.att, (size_t)m->q * 4)) ||
                 (rc = cap_q8("att_q8", "att_s8", m->nbq))))
       return rc;
-    if ((rc = gemv(kKTailGemv, Ly.wo_v, m->H, m->nbq, w.h, w.h, nullptr))) return rc;
+    // o projection + residual, ffn_norm -> t_q/t_s
+    if ((rc = row_gemv_norm(m, L, row_gemv(m, Ly.wo_v, m->H, m->nbq, w.t_q, w.t_s, w.h, w.h),
+                            Ly.ffn_norm, kTicketNormO, st)))
+      return rc;
     if (cap && (rc = dbg_capture(m, st, "h_mid", w.h, (size_t)m->H * 4))) return rc;
-    if ((rc = norm_quant(Ly.ffn_norm))) return rc;
     if (cap && (rc = cap_q8("f_q8", "f_s8", m->nbH))) return rc;
-    if ((rc = gemv(kKTailGemv, Ly.wgu_v, 2 * m->F, m->nbH, w.gu, nullptr, nullptr))) return rc;
-    LAUNCH(kKTailSwiglu, swiglu_quant_row_launch(w.gu, m->F, w.t_q, w.t_s, st));
-    if (cap && (rc = cap_q8("s_q8", "s_s8", m->nbF))) return rc;
-    if ((rc = gemv(kKTailGemv, Ly.wd_v, m->H, m->nbF, w.h, w.h, nullptr))) return rc;
+    // gate/up + SwiGLU -> t_q2/t_s2
+    if ((rc = row_gemv_swiglu(m, L, Ly.wgu_v, st))) return rc;
+    if (cap && ((rc = dbg_capture(m, st, "s_q8", w.t_q2, (size_t)m->nbF * 32)) ||
+                (rc = dbg_capture(m, st, "s_s8", w.t_s2, (size_t)m->nbF * 4))))
+      return rc;
+    // down + residual, the next norm (attn_norm of the next layer, or the output norm)
+    if ((rc = row_gemv_norm(m, L, row_gemv(m, Ly.wd_v, m->H, m->nbF, w.t_q2, w.t_s2, w.h, w.h),
+                            l + 1 < hp.n_layer ? m->layers[l + 1].attn_norm : m->out_norm,
+                            kTicketNormDown, st)))
+      return rc;
     if (cap && (rc = dbg_capture(m, st, "h_out", w.h, (size_t)m->H * 4))) return rc;
     if (dumps) dump_hidden(m, st, l + 1, w.h, 1);
-    if ((rc = norm_quant(l + 1 < hp.n_layer ? m->layers[l + 1].attn_norm : m->out_norm))) return rc;
   }
   const GemvW& out = hp.tied_embeddings ? m->tok_embd : m->output;
-  return gemv(kKLmHead, out, m->V, m->nbH, logits, nullptr, m->d_status);
+  GemvArgs g = row_gemv(m, out, m->V, m->nbH, w.t_q, w.t_s, logits, nullptr);
+  g.status = m->d_status;
+  LAUNCH(kKLmHead, gemv_launch(g, st));
+  return MINFER_OK;
 }
 
 // Enqueue one forward.  ids/pos/logits are device pointers.
@@ -922,6 +1003,7 @@ int enqueue_forward(minfer_model* m, minfer_kv* kv, const int32_t* ids, const in
     at.hd = hp.head_dim;
     at.n_ctx = kv->n_ctx;
     at.nsplit = attention_nsplit(at.r1 - at.r0, at.nkv, m->num_sms, at.nh / at.nkv);
+    if (tail1) row_attention_args(m, kv, l, &at);
     AttnOut ao;
     ao.f32 = (m->debug_f32 || cap) ? w.att : nullptr;
     if (!tail1) {
@@ -1036,91 +1118,31 @@ int enqueue_forward(minfer_model* m, minfer_kv* kv, const int32_t* ids, const in
           (rc = cap_row("att_q8", w.t_q, (size_t)m->nbq * 32)) ||
           (rc = cap_row("att_s8", w.t_s, (size_t)m->nbq * 4)))
         return rc;
-      {
-        GemvArgs g;
-        g.num_sms = m->num_sms;
-        g.wq = Ly.wo_v.q;
-        g.ws = Ly.wo_v.s;
-        g.N = m->H;
-        g.nb = m->nbq;
-        g.kpad = (int64_t)m->nbq * 32;
-        g.xq = w.t_q;
-        g.xs = w.t_s;
-        g.y = w.h_last;
-        g.resid = w.h + last_row * m->H;
-        LAUNCH(kKTailGemv, gemv_launch(g, st));
-      }
-      if ((rc = cap_row("h_mid", w.h_last, (size_t)m->H * 4))) return rc;
-      {
-        RowQuantArgs r;
-        r.h = w.h_last;
-        r.norm_w = Ly.ffn_norm;
-        r.eps = hp.rms_eps;
-        r.rows = 1;
-        r.n = m->H;
-        r.q8 = w.t_q;
-        r.s8 = w.t_s;
-        LAUNCH(kKRowQuant, row_quant_launch(r, st));
-      }
-      if ((rc = cap_row("f_q8", w.t_q, (size_t)m->nbH * 32)) ||
+      // o projection + residual of the last row, ffn_norm -> t_q/t_s
+      if ((rc = row_gemv_norm(m, L,
+                              row_gemv(m, Ly.wo_v, m->H, m->nbq, w.t_q, w.t_s, w.h_last,
+                                       w.h + last_row * m->H),
+                              Ly.ffn_norm, kTicketNormO, st)))
+        return rc;
+      if ((rc = cap_row("h_mid", w.h_last, (size_t)m->H * 4)) ||
+          (rc = cap_row("f_q8", w.t_q, (size_t)m->nbH * 32)) ||
           (rc = cap_row("f_s8", w.t_s, (size_t)m->nbH * 4)))
         return rc;
-      {
-        GemvArgs g;
-        g.num_sms = m->num_sms;
-        g.wq = Ly.wgu_v.q;
-        g.ws = Ly.wgu_v.s;
-        g.N = 2 * m->F;
-        g.nb = m->nbH;
-        g.kpad = (int64_t)m->nbH * 32;
-        g.xq = w.t_q;
-        g.xs = w.t_s;
-        g.y = w.gu;
-        LAUNCH(kKTailGemv, gemv_launch(g, st));
-      }
-      LAUNCH(kKTailSwiglu, swiglu_quant_row_launch(w.gu, m->F, w.t_q, w.t_s, st));
-      if ((rc = cap_row("s_q8", w.t_q, (size_t)m->nbF * 32)) ||
-          (rc = cap_row("s_s8", w.t_s, (size_t)m->nbF * 4)))
+      // gate/up + SwiGLU -> t_q2/t_s2
+      if ((rc = row_gemv_swiglu(m, L, Ly.wgu_v, st))) return rc;
+      if ((rc = cap_row("s_q8", w.t_q2, (size_t)m->nbF * 32)) ||
+          (rc = cap_row("s_s8", w.t_s2, (size_t)m->nbF * 4)))
         return rc;
-      {
-        GemvArgs g;
-        g.num_sms = m->num_sms;
-        g.wq = Ly.wd_v.q;
-        g.ws = Ly.wd_v.s;
-        g.N = m->H;
-        g.nb = m->nbF;
-        g.kpad = (int64_t)m->nbF * 32;
-        g.xq = w.t_q;
-        g.xs = w.t_s;
-        g.y = w.h_last;
-        g.resid = w.h_last;
-        LAUNCH(kKTailGemv, gemv_launch(g, st));
-      }
+      // down + residual, output norm -> t_q/t_s
+      if ((rc = row_gemv_norm(m, L,
+                              row_gemv(m, Ly.wd_v, m->H, m->nbF, w.t_q2, w.t_s2, w.h_last, w.h_last),
+                              m->out_norm, kTicketNormDown, st)))
+        return rc;
       if ((rc = cap_row("h_out", w.h_last, (size_t)m->H * 4))) return rc;
       if (dumps) dump_hidden(m, st, l + 1, w.h_last, 1);
       {
-        RowQuantArgs r;
-        r.h = w.h_last;
-        r.norm_w = m->out_norm;
-        r.eps = hp.rms_eps;
-        r.rows = 1;
-        r.n = m->H;
-        r.q8 = w.t_q;
-        r.s8 = w.t_s;
-        LAUNCH(kKRowQuant, row_quant_launch(r, st));
-      }
-      {
         const GemvW& out = hp.tied_embeddings ? m->tok_embd : m->output;
-        GemvArgs g;
-        g.num_sms = m->num_sms;
-        g.wq = out.q;
-        g.ws = out.s;
-        g.N = m->V;
-        g.nb = m->nbH;
-        g.kpad = (int64_t)m->nbH * 32;
-        g.xq = w.t_q;
-        g.xs = w.t_s;
-        g.y = logits;
+        GemvArgs g = row_gemv(m, out, m->V, m->nbH, w.t_q, w.t_s, logits, nullptr);
         g.status = m->d_status;
         LAUNCH(kKLmHead, gemv_launch(g, st));
       }
@@ -1705,6 +1727,18 @@ int minfer_op_attention(const float* d_q, const int32_t* d_pos, int nt, const fl
   if (!rc) rc = dalloc(&qpl, (size_t)2 * nt * q);
   if (!rc) rc = dalloc(&q16, (size_t)nt * q);
   if (!rc) rc = dalloc(&s16, (size_t)(q / 32) * nt);
+  // one query row: the split-key kernel, straight from the f32 regions
+  float* rpart = nullptr;
+  unsigned* rtick = nullptr;
+  if (!rc && nt == 1) rc = dalloc(&rpart, attn_row_scratch_floats(n_head_kv, head_dim));
+  if (!rc && nt == 1) rc = dalloc(&rtick, (size_t)n_head_kv);
+  if (!rc && nt == 1) {
+    a.kreg = d_k;
+    a.vreg = d_v;
+    a.row_part = rpart;
+    a.row_ticket = rtick;
+    a.row_splits = attn_row_splits(n_ctx, n_head_kv, num_sms);
+  }
   cudaError_t e = cudaSuccess;
   if (!rc) {
     __half* planes[4];
@@ -1746,6 +1780,8 @@ int minfer_op_attention(const float* d_q, const int32_t* d_pos, int nt, const fl
   dfree(qpl);
   dfree(q16);
   dfree(s16);
+  dfree(rpart);
+  dfree(rtick);
   if (rc) return rc;
   CK(e);
   return MINFER_OK;

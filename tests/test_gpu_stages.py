@@ -139,6 +139,31 @@ def test_attention_vs_oracle(qp, oracle_mod, nh, nkv, hd, nt, n_ctx, p0):
     assert err <= 2e-5 * max(1.0, np.abs(ref).max()), err
 
 
+@pytest.mark.parametrize("nh,nkv,hd,n_ctx,p,grow", [
+    (14, 2, 64, 4096, 0, False), (14, 2, 64, 4096, 31, False), (14, 2, 64, 4096, 32, False),
+    (14, 2, 64, 4096, 512, False), (14, 2, 64, 4096, 4095, True),
+    (14, 2, 64, 16384, 16383, True),   # 128 CTAs of 128 keys: two chunks each
+    (28, 4, 128, 8192, 8191, True),    # 76 CTAs of ~108 keys
+    (28, 4, 128, 8192, 700, False), (12, 2, 128, 600, 599, False), (16, 8, 128, 256, 200, False),
+    (4, 2, 64, 64, 63, False), (16, 16, 64, 100, 57, True)])
+def test_attention_one_row_vs_oracle(qp, oracle_mod, nh, nkv, hd, n_ctx, p, grow):
+    """One query row (a single-token call, the last row of a prompt): the keys
+    0..p of each KV head are dealt to many CTAs, each keeps an online softmax
+    over chunks of keys, and the last CTA of the head merges the shares.  Keys
+    that grow along the sequence make the chunk rescaling and the merge
+    weights differ from one."""
+    rng = np.random.default_rng(n_ctx + p + hd)
+    q = rng.normal(0, 1, (1, nh * hd)).astype(np.float32)
+    scale = (1.0 + np.arange(n_ctx) / 256.0).astype(np.float32)[:, None] if grow else 1.0
+    K = (rng.normal(0, 1, (n_ctx, nkv * hd)) * scale).astype(np.float32)
+    V = rng.normal(0, 1, (n_ctx, nkv * hd)).astype(np.float32)
+    pos = np.array([p], np.int32)
+    o = qp.op_attention(_dev(q), _dev(pos), _dev(K), _dev(V), nh, nkv, hd).cpu().numpy()
+    ref = oracle_mod.attention(q, pos, K, V, nh, nkv, hd)
+    err = np.abs(o - ref).max()
+    assert err <= 2e-5 * max(1.0, np.abs(ref).max()), err
+
+
 @pytest.mark.parametrize("nh,nkv,hd,nt", [(14, 2, 64, 384), (12, 2, 128, 300)])
 def test_attention_rising_scores_vs_oracle(qp, oracle_mod, nh, nkv, hd, nt):
     """Keys that grow with their position push every row's running max up
