@@ -502,17 +502,19 @@ __global__ void kv_shadow_kernel(const float* __restrict__ k, const float* __res
 
 // ---------------------------------------------------------------- one query row
 // A call with a single query row (a one-token call, the last row of a prompt)
-// has almost no work per KV head: the tiled kernel's 16-row MMA tiles and its
-// cluster merge are all latency there.  This kernel deals the keys 0..pos of
-// each KV head to up to gridDim.x CTAs (about kRowKeys keys each).  A CTA
-// stages a chunk of kRowKeys K and V rows of the f32 regions in shared memory
-// (every load in flight at once); warp h then scores the chunk for query head
-// h of the group, one key per lane, in f32 on the CUDA cores, keeps the
-// softmax online across chunks and accumulates P.V with lane l holding dims
-// l + 32 j.  The CTA leaves (max, sum, unnormalized O) in a global scratch;
-// the CTA that finishes last for the KV head (an atomic ticket: nothing
-// waits) merges the shares, normalizes and quantizes the group's 32-blocks.
-constexpr int kRowKeys = 32;  // keys per chunk, and per CTA the split count aims at
+// has almost no work per KV head: the tiled kernel's 16-row MMA tiles are all
+// latency there.  Here one thread-block cluster of CS CTAs (16 where the
+// device allows that non-portable size, else 8) serves a KV head; CTA c takes
+// the c-th share of the keys 0..pos.  A CTA walks its
+// share in chunks of kRowKeys K and V rows of the f32 regions, staged in
+// shared memory (the next chunk's loads are in flight while the current one
+// is scored); warp h scores the chunk for query head h of the group, one key
+// per lane, in f32 on the CUDA cores, keeps the softmax online and
+// accumulates P.V with lane l holding dims l + 32 j.  After a cluster barrier
+// CTA h merges head h from its peers' (max, sum, O) through distributed
+// shared memory, normalizes and quantizes; a second barrier keeps every CTA
+// alive until its partials have been read.
+constexpr int kRowKeys = 32;    // keys per chunk
 constexpr int kRowThreadsA = 256;
 
 __device__ __forceinline__ float warp_sum(float v) {
@@ -521,20 +523,25 @@ __device__ __forceinline__ float warp_sum(float v) {
   return v;
 }
 
-template <int HD>
+template <int HD, int CS>
 __global__ void __launch_bounds__(kRowThreadsA) attn_row_kernel(const AttnArgs a, const AttnOut out) {
-  constexpr int DPL = HD / 32;  // dims per lane
-  constexpr int C4 = HD / 4;    // float4 per row
+  static_assert(CS >= 8, "CTA h merges query head h < G <= 8");
+  constexpr int DPL = HD / 32;                      // dims per lane
+  constexpr int C4 = HD / 4;                        // float4 per row
+  constexpr int PER = kRowKeys * C4 / kRowThreadsA;  // float4 of K (and of V) per thread and chunk
+  static_assert(PER * kRowThreadsA == kRowKeys * C4, "whole chunks per thread");
   __shared__ float ks[kRowKeys][HD + 1];  // +1: lane = key reads a column without bank conflicts
   __shared__ __align__(16) float vs[kRowKeys][HD];
   __shared__ float qs[8][HD];
-  __shared__ unsigned s_last;
+  __shared__ float po[8][HD];  // this CTA's unnormalized O, per query head of the group
+  __shared__ float pml[8][2];  // and its (max, sum)
   pdl_trigger();
   pdl_wait();
 
   const int G = a.nh / a.nkv;
   const int g = blockIdx.y;
-  const int split = blockIdx.x;
+  const int split = (int)cluster_rank();
+  const int ns = CS;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int r = a.r0;
   const int64_t kw = (int64_t)a.nkv * HD;
@@ -545,37 +552,47 @@ __global__ void __launch_bounds__(kRowThreadsA) attn_row_kernel(const AttnArgs a
   int p = a.pos[r];
   p = p < 0 ? -1 : (p >= a.n_ctx ? a.n_ctx - 1 : p);
   const int nkeys = p + 1;
-  // CTAs beyond the splits this position needs leave at once (and take no ticket)
-  int ns = (nkeys + kRowKeys - 1) / kRowKeys;
-  ns = ns < 1 ? 1 : (ns > (int)gridDim.x ? (int)gridDim.x : ns);
-  if (split >= ns) return;
   const int share = (nkeys + ns - 1) / ns;
-  const int kbeg = split * share;
+  const int kbeg = min(nkeys, split * share);
   const int kend = min(nkeys, kbeg + share);
+  const int nchunks = (kend - kbeg + kRowKeys - 1) / kRowKeys;
   // scores in log2 units: s = (q.k) / sqrt(hd) * log2(e)
   const float sc = __fmul_rn(__fdiv_rn(1.0f, __fsqrt_rn((float)HD)), 1.4426950408889634f);
+
+  float4 kr[PER], vr[PER];  // the next chunk, in flight
+  auto load_chunk = [&](int k0) {
+#pragma unroll
+    for (int i = 0; i < PER; ++i) {
+      const int idx = tid + kRowThreadsA * i;
+      const int kk = idx / C4, c = idx % C4;
+      kr[i] = vr[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+      if (k0 + kk < kend) {
+        const int64_t off = (int64_t)(k0 + kk) * kw + (int64_t)g * HD + 4 * c;
+        kr[i] = *reinterpret_cast<const float4*>(a.kreg + off);
+        vr[i] = *reinterpret_cast<const float4*>(a.vreg + off);
+      }
+    }
+  };
+  if (nchunks > 0) load_chunk(kbeg);
 
   float m = -INFINITY, l = 0.f, o[DPL];
 #pragma unroll
   for (int j = 0; j < DPL; ++j) o[j] = 0.f;
-
-  for (int k0 = kbeg; k0 < kend; k0 += kRowKeys) {
+  for (int ci = 0; ci < nchunks; ++ci) {
+    const int k0 = kbeg + ci * kRowKeys;
     const int nc = min(kRowKeys, kend - k0);
-    for (int i = tid; i < kRowKeys * C4; i += kRowThreadsA) {
-      const int kk = i / C4, c = i % C4;
-      float4 kx = make_float4(0.f, 0.f, 0.f, 0.f), vx = kx;
-      if (kk < nc) {
-        const int64_t off = (int64_t)(k0 + kk) * kw + (int64_t)g * HD + 4 * c;
-        kx = *reinterpret_cast<const float4*>(a.kreg + off);
-        vx = *reinterpret_cast<const float4*>(a.vreg + off);
-      }
-      ks[kk][4 * c] = kx.x;
-      ks[kk][4 * c + 1] = kx.y;
-      ks[kk][4 * c + 2] = kx.z;
-      ks[kk][4 * c + 3] = kx.w;
-      *reinterpret_cast<float4*>(&vs[kk][4 * c]) = vx;
+#pragma unroll
+    for (int i = 0; i < PER; ++i) {
+      const int idx = tid + kRowThreadsA * i;
+      const int kk = idx / C4, c = idx % C4;
+      ks[kk][4 * c] = kr[i].x;
+      ks[kk][4 * c + 1] = kr[i].y;
+      ks[kk][4 * c + 2] = kr[i].z;
+      ks[kk][4 * c + 3] = kr[i].w;
+      *reinterpret_cast<float4*>(&vs[kk][4 * c]) = vr[i];
     }
     __syncthreads();
+    if (ci + 1 < nchunks) load_chunk(k0 + kRowKeys);
     if (warp < G) {
       const int h = warp;
       float d4[4] = {0.f, 0.f, 0.f, 0.f};  // four partial dots: shorter dependency chains
@@ -601,103 +618,74 @@ __global__ void __launch_bounds__(kRowThreadsA) attn_row_kernel(const AttnArgs a
     }
     __syncthreads();  // the next chunk overwrites ks / vs
   }
-
-  // this CTA's share of head warp: unnormalized O and (max, sum)
-  const int64_t slot = (int64_t)g * gridDim.x + split;
-  const int64_t ml_base = (int64_t)a.nkv * gridDim.x * 8 * HD;
   if (warp < G) {
-    float* po = a.row_part + slot * 8 * HD + warp * HD;
 #pragma unroll
-    for (int j = 0; j < DPL; ++j) po[lane + 32 * j] = o[j];
+    for (int j = 0; j < DPL; ++j) po[warp][lane + 32 * j] = o[j];
     if (lane == 0) {
-      a.row_part[ml_base + slot * 16 + 2 * warp] = m;
-      a.row_part[ml_base + slot * 16 + 2 * warp + 1] = l;
+      pml[warp][0] = m;
+      pml[warp][1] = l;
     }
   }
-  __threadfence();
-  __syncthreads();
-  if (tid == 0) s_last = atomicAdd(a.row_ticket + g, 1u) == (unsigned)(ns - 1);
-  __syncthreads();
-  if (!s_last) return;
-  __threadfence();
-  if (tid == 0) a.row_ticket[g] = 0u;  // every CTA of this head has drawn its ticket
-  if (warp >= G) return;
+  cluster_sync_all();  // every CTA's partials are visible to the cluster
 
-  // merge (the last CTA of the head), warp h for query head h: lane s holds
-  // the (max, sum) of splits s, s + 32, ... (ns <= 128); weights exp2(m_s - M)
-  const int h = warp;
-  const float* gml = a.row_part + ml_base + (int64_t)g * gridDim.x * 16 + 2 * h;
-  const float* gpo = a.row_part + (int64_t)g * gridDim.x * 8 * HD + h * HD + lane;
-  float ms[4], ls[4];
+  if (split < G && warp == 0) {
+    // merge head h = split from the ns CTAs: weights exp2(m_s - M), then 1 / L
+    const int h = split;
+    const uint32_t ml_s = smem_u32(&pml[h][0]);
+    float ms[CS], ls[CS];
 #pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    const int sidx = lane + 32 * i;
-    ms[i] = sidx < ns ? __ldcg(gml + sidx * 16) : -INFINITY;
-    ls[i] = sidx < ns ? __ldcg(gml + sidx * 16 + 1) : 0.f;
-  }
-  const float M = warp_max(fmaxf(fmaxf(ms[0], ms[1]), fmaxf(ms[2], ms[3])));
-  float ws[4], lsum = 0.f;
+    for (int c = 0; c < CS; ++c) {
+      const float2 v = ld_peer2(peer_addr(ml_s, (uint32_t)c));
+      ms[c] = v.x;
+      ls[c] = v.y;
+    }
+    float x[CS][DPL];
 #pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    ws[i] = ms[i] == -INFINITY ? 0.f : exp2f(ms[i] - M);
-    lsum = fmaf(ls[i], ws[i], lsum);
-  }
-  const float L = warp_sum(lsum);
-  float acc[DPL];
-#pragma unroll
-  for (int j = 0; j < DPL; ++j) acc[j] = 0.f;
-  for (int s0 = 0; s0 < ns; s0 += 8) {
-    float x[8][DPL];  // eight splits' loads in flight
-#pragma unroll
-    for (int u = 0; u < 8; ++u)
+    for (int c = 0; c < CS; ++c)
 #pragma unroll
       for (int j = 0; j < DPL; ++j)
-        x[u][j] = s0 + u < ns ? __ldcg(gpo + (int64_t)(s0 + u) * 8 * HD + 32 * j) : 0.f;
+        x[c][j] = ld_peer(peer_addr(smem_u32(&po[h][lane + 32 * j]), (uint32_t)c));
+    float M = -INFINITY;
 #pragma unroll
-    for (int u = 0; u < 8; ++u) {
-      const int sidx = s0 + u;
-      if (sidx >= ns) break;  // warp-uniform
-      const int q4 = sidx >> 5;
-      const float wsel = q4 == 0 ? ws[0] : (q4 == 1 ? ws[1] : (q4 == 2 ? ws[2] : ws[3]));
-      const float w = __shfl_sync(0xffffffffu, wsel, sidx & 31);
+    for (int c = 0; c < CS; ++c) M = fmaxf(M, ms[c]);
+    float L = 0.f, acc[DPL];
 #pragma unroll
-      for (int j = 0; j < DPL; ++j) acc[j] = fmaf(x[u][j], w, acc[j]);
+    for (int j = 0; j < DPL; ++j) acc[j] = 0.f;
+#pragma unroll
+    for (int c = 0; c < CS; ++c) {
+      const float w = ms[c] == -INFINITY ? 0.f : exp2f(ms[c] - M);
+      L = fmaf(ls[c], w, L);
+#pragma unroll
+      for (int j = 0; j < DPL; ++j) acc[j] = fmaf(x[c][j], w, acc[j]);
+    }
+    const float il = L > 0.f ? __fdiv_rn(1.0f, L) : 0.f;
+    // Q8_0: block j of head h is dims 32 j .. 32 j + 31, one per lane
+    const int q = a.nh * HD;
+    const int nb = q / 32;
+    const int64_t orow = r - out.row_base;
+#pragma unroll
+    for (int j = 0; j < DPL; ++j) {
+      const float v = __fmul_rn(acc[j], il);
+      const int k = (g * G + h) * HD + 32 * j + lane;  // element of the output row
+      const int b = k / 32;
+      const float amax = warp_max(fabsf(v));
+      const float dd = __fdiv_rn(amax, 127.0f);
+      const float code = q8_code(v, q8_inv(dd));
+      if (out.f32) out.f32[(int64_t)r * q + k] = v;
+      const float d16 = __half2float(__float2half_rn(dd));
+      if (out.q8) {
+        out.q8[orow * (int64_t)nb * 32 + k] = (int8_t)code;
+        if (lane == 0) out.s8[orow * nb + b] = d16;
+      } else {
+        out.q16[orow * out.ldq + k] = __float2half_rn(code);
+        if (lane == 0) out.s16[(int64_t)b * out.ldqs + orow] = d16;
+      }
     }
   }
-  const float il = L > 0.f ? __fdiv_rn(1.0f, L) : 0.f;
-  // Q8_0: block j of head h is dims 32 j .. 32 j + 31, one per lane
-  const int q = a.nh * HD;
-  const int nb = q / 32;
-  const int64_t orow = r - out.row_base;
-#pragma unroll
-  for (int j = 0; j < DPL; ++j) {
-    const float v = __fmul_rn(acc[j], il);
-    const int k = (g * G + h) * HD + 32 * j + lane;  // element of the output row
-    const int b = k / 32;
-    const float amax = warp_max(fabsf(v));
-    const float dd = __fdiv_rn(amax, 127.0f);
-    const float code = q8_code(v, q8_inv(dd));
-    if (out.f32) out.f32[(int64_t)r * q + k] = v;
-    const float d16 = __half2float(__float2half_rn(dd));
-    if (out.q8) {
-      out.q8[orow * (int64_t)nb * 32 + k] = (int8_t)code;
-      if (lane == 0) out.s8[orow * nb + b] = d16;
-    } else {
-      out.q16[orow * out.ldq + k] = __float2half_rn(code);
-      if (lane == 0) out.s16[(int64_t)b * out.ldqs + orow] = d16;
-    }
-  }
+  cluster_sync_all();  // peers may still be reading this CTA's partials
 }
 
 }  // namespace
-
-int attn_row_splits(int n_ctx, int nkv, int num_sms) {
-  int s = (n_ctx + kRowKeys - 1) / kRowKeys;
-  int cap = 2 * num_sms / (nkv > 0 ? nkv : 1);
-  if (cap > kAttnRowMaxSplits) cap = kAttnRowMaxSplits;
-  if (cap < 1) cap = 1;
-  return s < 1 ? 1 : (s > cap ? cap : s);
-}
 
 // 16-row tiles per CTA: enough to give the CTA 8 warps when a KV group has
 // few query heads.
@@ -746,20 +734,40 @@ cudaError_t attention_launch(const AttnArgs& a, const AttnOut& out, cudaStream_t
   if (a.nh % a.nkv != 0 || G > 8 || a.nsplit < 1 || a.nsplit > kMaxSplits)
     return cudaErrorInvalidValue;
   const bool gemv = out.q8 != nullptr;
-  if (rows == 1 && a.kreg && a.vreg && a.row_part && a.row_ticket && a.row_splits >= 1 &&
-      a.row_splits <= kAttnRowMaxSplits && reinterpret_cast<uintptr_t>(a.kreg) % 16 == 0 &&
-      reinterpret_cast<uintptr_t>(a.vreg) % 16 == 0) {
+  if (rows == 1 && a.kreg && a.vreg && reinterpret_cast<uintptr_t>(a.kreg) % 16 == 0 &&
+      reinterpret_cast<uintptr_t>(a.vreg) % 16 == 0 && ((int64_t)a.nkv * a.hd) % 4 == 0) {
+    // 16 CTAs per cluster where the device allows that size (measured faster
+    // than 8 on both single-token shapes), else the portable 8
+    static int cs = 0;
+    if (cs == 0) {
+      cs = 16;
+      if (cudaFuncSetAttribute(attn_row_kernel<64, 16>, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) !=
+              cudaSuccess ||
+          cudaFuncSetAttribute(attn_row_kernel<128, 16>, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) !=
+              cudaSuccess) {
+        (void)cudaGetLastError();
+        cs = 8;
+      }
+    }
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3((unsigned)a.row_splits, (unsigned)a.nkv, 1);
+    cfg.gridDim = dim3((unsigned)cs, (unsigned)a.nkv, 1);
     cfg.blockDim = dim3(kRowThreadsA);
     cfg.stream = st;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cudaLaunchAttribute attr[2];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = (unsigned)cs;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[1].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
-    cfg.numAttrs = 1;
-    if (a.hd == 64) return cudaLaunchKernelEx(&cfg, attn_row_kernel<64>, a, out);
-    if (a.hd == 128) return cudaLaunchKernelEx(&cfg, attn_row_kernel<128>, a, out);
+    cfg.numAttrs = 2;
+    if (a.hd == 64)
+      return cs == 16 ? cudaLaunchKernelEx(&cfg, attn_row_kernel<64, 16>, a, out)
+                      : cudaLaunchKernelEx(&cfg, attn_row_kernel<64, 8>, a, out);
+    if (a.hd == 128)
+      return cs == 16 ? cudaLaunchKernelEx(&cfg, attn_row_kernel<128, 16>, a, out)
+                      : cudaLaunchKernelEx(&cfg, attn_row_kernel<128, 8>, a, out);
     return cudaErrorInvalidValue;
   }
   if (a.hd == 64) return gemv ? launch_attn<64, true>(a, out, rows, st) : launch_attn<64, false>(a, out, rows, st);

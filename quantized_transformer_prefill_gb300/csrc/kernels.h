@@ -181,21 +181,12 @@ struct AttnArgs {
   int nh = 0, nkv = 0, hd = 0;
   int n_ctx = 0;   // positions are clamped into [0, n_ctx) before any region read
   int nsplit = 1;  // key splits (CTAs per cluster), 1..8
-  // One-row calls (r1 - r0 == 1) run the split-key CUDA-core kernel when these
-  // are set: the f32 K/V regions [n_ctx][nkv*hd], a scratch of
-  // attn_row_scratch_floats() floats and nkv zero-initialized tickets (left at
-  // zero); row_splits = attn_row_splits(n_ctx, nkv, num_sms).
+  // One-row calls (r1 - r0 == 1) run the CUDA-core kernel of one thread-block
+  // cluster per KV head when the f32 K/V regions [n_ctx][nkv*hd] are given
+  // (16-byte aligned).
   const float* kreg = nullptr;
   const float* vreg = nullptr;
-  float* row_part = nullptr;
-  unsigned* row_ticket = nullptr;
-  int row_splits = 0;
 };
-constexpr int kAttnRowMaxSplits = 128;
-int attn_row_splits(int n_ctx, int nkv, int num_sms);
-inline size_t attn_row_scratch_floats(int nkv, int hd) {
-  return (size_t)nkv * kAttnRowMaxSplits * (8 * (size_t)hd + 16);
-}
 // Where the attention output goes: Q8_0 codes in the GEMM layout (q16 [rows][ldq]
 // fp16 + s16 [nb][ldqs]) or the GEMV layout (q8 [rows][nb*32] + s8 [rows][nb]);
 // output row index = query row - row_base.  f32 (optional): [nt][nh*hd].

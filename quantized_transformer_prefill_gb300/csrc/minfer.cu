@@ -165,8 +165,7 @@ struct Workspace {
   float* t_s = nullptr;      // [max nb]
   int8_t* t_q2 = nullptr;    // [Fp] one-row SwiGLU codes
   float* t_s2 = nullptr;     // [nbF]
-  float* arow = nullptr;     // one-row attention scratch
-  unsigned* tickets = nullptr;  // [kTickets] zero-initialized counters of the one-row kernels
+  unsigned* tickets = nullptr;  // [kTickets] zero-initialized counters of the fused one-row norms
   float* logits = nullptr;   // [logits_rows][V]
   int logits_rows = 0;
   float* lm_out = nullptr;   // [logits_rows][V]: lm_head GEMM output before the status-gated copy
@@ -174,7 +173,7 @@ struct Workspace {
   void release() {
     dfree(ids); dfree(pos); dfree(h); dfree(xa); dfree(xa_s); dfree(xf); dfree(xf_s);
     dfree(part); dfree(qrot); dfree(qpl); dfree(att); dfree(h_last); dfree(t_q); dfree(t_s);
-    dfree(t_q2); dfree(t_s2); dfree(arow); dfree(tickets);
+    dfree(t_q2); dfree(t_s2); dfree(tickets);
     dfree(logits); dfree(lm_out);
     logits_rows = 0;
     max_nt = 0;
@@ -182,10 +181,9 @@ struct Workspace {
 };
 
 constexpr int kMaxSplits = 8;
-// tickets: [0, nkv) the one-row attention's heads, then the fused norms of the
-// o and down GEMVs
+// tickets of the fused norms of the one-row o and down GEMVs
 constexpr int kTicketNormO = 0, kTicketNormDown = 1;
-constexpr int kTicketsFixed = 2;
+constexpr int kTickets = 2;
 
 enum KClass : int {
   kKValidate, kKEmbed, kKRowQuant, kKGemmQKV, kKRope, kKAttn, kKGemmO, kKGemmGU, kKGemmDown,
@@ -547,8 +545,7 @@ int ensure_workspace(minfer_model* m, int nt) {
       (rc = dalloc(&w.t_q, std::max<int64_t>(kx, m->Fp))) ||
       (rc = dalloc(&w.t_s, std::max(nbx, m->nbF))) || (rc = dalloc(&w.t_q2, m->Fp)) ||
       (rc = dalloc(&w.t_s2, m->nbF)) ||
-      (rc = dalloc(&w.arow, attn_row_scratch_floats(m->hp.n_head_kv, m->hp.head_dim))) ||
-      (rc = dalloc(&w.tickets, (size_t)kTicketsFixed + m->hp.n_head_kv)) ||
+      (rc = dalloc(&w.tickets, (size_t)kTickets)) ||
       (rc = dalloc(&w.logits, m->V)))
     return rc;
   w.logits_rows = 1;
@@ -737,12 +734,9 @@ int row_gemv_swiglu(minfer_model* m, Launcher& L, const GemvW& W, cudaStream_t s
 }
 
 // The one-row attention kernel's inputs on top of the tiled kernel's.
-void row_attention_args(const minfer_model* m, const minfer_kv* kv, int l, AttnArgs* at) {
+void row_attention_args(const minfer_kv* kv, int l, AttnArgs* at) {
   at->kreg = kv->k(l);
   at->vreg = kv->v(l);
-  at->row_part = m->ws.arow;
-  at->row_ticket = m->ws.tickets + kTicketsFixed;
-  at->row_splits = attn_row_splits(kv->n_ctx, m->hp.n_head_kv, m->num_sms);
 }
 
 int enqueue_decode(minfer_model* m, minfer_kv* kv, const int32_t* ids, const int32_t* pos,
@@ -839,7 +833,7 @@ int enqueue_decode(minfer_model* m, minfer_kv* kv, const int32_t* ids, const int
       at.hd = hp.head_dim;
       at.n_ctx = kv->n_ctx;
       at.nsplit = attention_nsplit(1, at.nkv, m->num_sms, at.nh / at.nkv);
-      row_attention_args(m, kv, l, &at);
+      row_attention_args(kv, l, &at);
       AttnOut ao;
       ao.f32 = (m->debug_f32 || cap) ? w.att : nullptr;
       ao.q8 = w.t_q;
@@ -1003,7 +997,7 @@ int enqueue_forward(minfer_model* m, minfer_kv* kv, const int32_t* ids, const in
     at.hd = hp.head_dim;
     at.n_ctx = kv->n_ctx;
     at.nsplit = attention_nsplit(at.r1 - at.r0, at.nkv, m->num_sms, at.nh / at.nkv);
-    if (tail1) row_attention_args(m, kv, l, &at);
+    if (tail1) row_attention_args(kv, l, &at);
     AttnOut ao;
     ao.f32 = (m->debug_f32 || cap) ? w.att : nullptr;
     if (!tail1) {
@@ -1727,17 +1721,10 @@ int minfer_op_attention(const float* d_q, const int32_t* d_pos, int nt, const fl
   if (!rc) rc = dalloc(&qpl, (size_t)2 * nt * q);
   if (!rc) rc = dalloc(&q16, (size_t)nt * q);
   if (!rc) rc = dalloc(&s16, (size_t)(q / 32) * nt);
-  // one query row: the split-key kernel, straight from the f32 regions
-  float* rpart = nullptr;
-  unsigned* rtick = nullptr;
-  if (!rc && nt == 1) rc = dalloc(&rpart, attn_row_scratch_floats(n_head_kv, head_dim));
-  if (!rc && nt == 1) rc = dalloc(&rtick, (size_t)n_head_kv);
-  if (!rc && nt == 1) {
+  // one query row: the cluster kernel, straight from the f32 regions
+  if (nt == 1) {
     a.kreg = d_k;
     a.vreg = d_v;
-    a.row_part = rpart;
-    a.row_ticket = rtick;
-    a.row_splits = attn_row_splits(n_ctx, n_head_kv, num_sms);
   }
   cudaError_t e = cudaSuccess;
   if (!rc) {
@@ -1780,8 +1767,6 @@ int minfer_op_attention(const float* d_q, const int32_t* d_pos, int nt, const fl
   dfree(qpl);
   dfree(q16);
   dfree(s16);
-  dfree(rpart);
-  dfree(rtick);
   if (rc) return rc;
   CK(e);
   return MINFER_OK;
