@@ -496,14 +496,15 @@ __global__ void __launch_bounds__(1024, 2) rope_store_kernel(const RopeStoreArgs
 
 // Qwen3: the same with the per-head QK RMSNorm between the bias and RoPE
 // ("05 · Graph build", section 3.2, FusedQkvNorm).  One CTA per token: the
-// Q and K sums go to shared memory, one warp per head takes the mean of
-// squares in double (the scale is rounded to f32 once, as in every RMSNorm
-// here), then the pairs are normalized, weighted and rotated.
+// Q and K sums go to shared memory, one warp per head takes the sum of
+// squares as float-float pairs and the scale 1 / sqrt(mean + eps) in double,
+// rounded to f32 once (as in every RMSNorm here), then the pairs are
+// normalized, weighted and rotated.
 constexpr int kMaxQkHeads = 128;
 
 __global__ void __launch_bounds__(1024) rope_store_qknorm_kernel(const RopeStoreArgs a) {
   extern __shared__ float xs[];  // [(nh + nkv) * hd]
-  __shared__ float rs[kMaxQkHeads];
+  __shared__ float rs[kMaxQkHeads], rl[kMaxQkHeads];  // per head: (hi, lo) sum of squares, then the scale
   pdl_trigger();
   pdl_wait();
   const int t = blockIdx.x;
@@ -538,14 +539,34 @@ __global__ void __launch_bounds__(1024) rope_store_qknorm_kernel(const RopeStore
   __syncthreads();
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, nwarps = blockDim.x >> 5;
   for (int hh = warp; hh < nheads; hh += nwarps) {
-    double ss = 0.0;
+    // the head's sum of squares as float-float pairs (as in the row kernel):
+    // the double pipe of this part is too slow for a sum per element
+    float hi = 0.f, lo = 0.f;
     for (int i = lane; i < a.hd; i += 32) {
-      const double x = (double)xs[hh * a.hd + i];
-      ss += x * x;
+      const float x = xs[hh * a.hd + i];
+      const float sq = __fmul_rn(x, x);
+      ff_add(hi, lo, sq, fmaf(x, x, -sq));
     }
 #pragma unroll
-    for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
-    if (lane == 0) rs[hh] = (float)(1.0 / sqrt(ss / (double)a.hd + (double)a.eps));
+    for (int o = 16; o > 0; o >>= 1) {
+      const float bhi = __shfl_xor_sync(0xffffffffu, hi, o);
+      const float blo = __shfl_xor_sync(0xffffffffu, lo, o);
+      ff_add(hi, lo, bhi, blo);
+    }
+    if (lane == 0) {
+      rs[hh] = hi;
+      rl[hh] = lo;
+    }
+  }
+  __syncthreads();
+  // the scales of all heads side by side in the lanes of warp 0: the double
+  // divisions and square roots go through that pipe once per warp, not once
+  // per head
+  if (warp == 0) {
+    for (int hh = lane; hh < nheads; hh += 32) {
+      const double ss = (double)rs[hh] + (double)rl[hh];
+      rs[hh] = (float)(1.0 / sqrt(ss / (double)a.hd + (double)a.eps));
+    }
   }
   __syncthreads();
   const float* cs = a.cos_t + (int64_t)p * half;
