@@ -37,6 +37,43 @@ __device__ __forceinline__ void ff_add(float& hi, float& lo, float bhi, float bl
   lo = __fsub_rn(e, __fsub_rn(hi, s));
 }
 
+// The RMSNorm scale 1 / sqrt(ss / n + eps), rounded to f32, from the sum of
+// squares ss held as a float-float pair (hi, lo), in f32 arithmetic only (the
+// double pipe of this part is slow, and the scale sits on every row's critical
+// path): v = ss / n + eps as a float-float pair (the exact remainder of the
+// division by fma), the hardware reciprocal square root of its high part,
+// then two Newton-Raphson steps y <- y + y (1 - v y^2) / 2 for 1/sqrt carried
+// in float-float, so the result is within a few 2^-47 of the exact value and
+// rounds to f32 like a float64 evaluation except that close to a boundary.
+__device__ __forceinline__ float rms_scale(float hi, float lo, float n, float eps) {
+  const float q1 = __fdiv_rn(hi, n);
+  const float r1 = fmaf(-q1, n, hi);  // hi - q1 n, exact
+  const float q2 = __fdiv_rn(__fadd_rn(r1, lo), n);
+  float vh, vl;
+  two_sum(q1, q2, vh, vl);
+  ff_add(vh, vl, eps, 0.f);
+  if (!(vh > 0.f)) return __frcp_rn(__fsqrt_rn(vh));  // v = 0: inf, as in float64
+  float yh = rsqrtf(vh), yl = 0.f;
+#pragma unroll
+  for (int it = 0; it < 2; ++it) {
+    // y^2 = s + se (yl's share to first order)
+    const float s = __fmul_rn(yh, yh);
+    const float se = fmaf(yh, yh, -s) + 2.0f * yh * yl;
+    // v y^2 = t + te
+    const float t = __fmul_rn(vh, s);
+    const float te = fmaf(vh, s, -t) + (vh * se + vl * s);
+    // e = 1 - v y^2 (1 - t is exact: t is close to 1)
+    const float e = __fsub_rn(1.0f - t, te);
+    // y += y e / 2 as a float-float pair
+    const float c = __fmul_rn(0.5f * yh, e) + 0.5f * yl * e;
+    float nh, nl;
+    two_sum(yh, c, nh, nl);
+    yl = nl + yl;
+    two_sum(nh, yl, yh, yl);
+  }
+  return yh;
+}
+
 // ---------------------------------------------------------------- row quant
 // One CTA of 256 threads per row; thread i holds elements i + 256 k (k < PER,
 // all loads issued before any arithmetic).  In step k, warp w holds block
@@ -132,8 +169,7 @@ __global__ void __launch_bounds__(kRowThreads) row_quant_kernel(const RowQuantAr
     if (tid == 0) {
       float h2 = red_hi[0], l2 = red_lo[0];
       for (int w = 1; w < kRowThreads / 32; ++w) ff_add(h2, l2, red_hi[w], red_lo[w]);
-      const double ss = (double)h2 + (double)l2;
-      s_scale = (float)(1.0 / sqrt(ss / (double)n + (double)a.eps));
+      s_scale = rms_scale(h2, l2, (float)n, a.eps);
     }
     __syncthreads();
     scale = s_scale;
@@ -254,8 +290,7 @@ __device__ __forceinline__ void row_quant4_row(const RowQuantArgs& a, const int6
     if (tid == 0) {
       float h2 = red_hi[0], l2 = red_lo[0];
       for (int w = 1; w < kRowThreads / 32; ++w) ff_add(h2, l2, red_hi[w], red_lo[w]);
-      const double ss = (double)h2 + (double)l2;
-      s_scale = (float)(1.0 / sqrt(ss / (double)n + (double)a.eps));
+      s_scale = rms_scale(h2, l2, (float)n, a.eps);
     }
     __syncthreads();
     scale = s_scale;
@@ -497,9 +532,8 @@ __global__ void __launch_bounds__(1024, 2) rope_store_kernel(const RopeStoreArgs
 // Qwen3: the same with the per-head QK RMSNorm between the bias and RoPE
 // ("05 · Graph build", section 3.2, FusedQkvNorm).  One CTA per token: the
 // Q and K sums go to shared memory, one warp per head takes the sum of
-// squares as float-float pairs and the scale 1 / sqrt(mean + eps) in double,
-// rounded to f32 once (as in every RMSNorm here), then the pairs are
-// normalized, weighted and rotated.
+// squares as float-float pairs, warp 0 turns every head's sum into its scale
+// (rms_scale), then the pairs are normalized, weighted and rotated.
 constexpr int kMaxQkHeads = 128;
 
 __global__ void __launch_bounds__(1024) rope_store_qknorm_kernel(const RopeStoreArgs a) {
@@ -559,15 +593,9 @@ __global__ void __launch_bounds__(1024) rope_store_qknorm_kernel(const RopeStore
     }
   }
   __syncthreads();
-  // the scales of all heads side by side in the lanes of warp 0: the double
-  // divisions and square roots go through that pipe once per warp, not once
-  // per head
-  if (warp == 0) {
-    for (int hh = lane; hh < nheads; hh += 32) {
-      const double ss = (double)rs[hh] + (double)rl[hh];
-      rs[hh] = (float)(1.0 / sqrt(ss / (double)a.hd + (double)a.eps));
-    }
-  }
+  // the scales of all heads side by side in the lanes of warp 0
+  if (warp == 0)
+    for (int hh = lane; hh < nheads; hh += 32) rs[hh] = rms_scale(rs[hh], rl[hh], (float)a.hd, a.eps);
   __syncthreads();
   const float* cs = a.cos_t + (int64_t)p * half;
   const float* sn = a.sin_t + (int64_t)p * half;
