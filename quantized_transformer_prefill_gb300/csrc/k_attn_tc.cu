@@ -127,9 +127,17 @@ __device__ __forceinline__ uint32_t peer_addr_tc(uint32_t saddr, uint32_t rank) 
   asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(saddr), "r"(rank));
   return r;
 }
-__device__ __forceinline__ float ld_peer_tc(uint32_t addr) {
-  float v;
-  asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(addr) : "memory");
+__device__ __forceinline__ float2 ld_peer2_tc(uint32_t addr) {
+  float2 v;
+  asm volatile("ld.shared::cluster.v2.f32 {%0, %1}, [%2];" : "=f"(v.x), "=f"(v.y) : "r"(addr) : "memory");
+  return v;
+}
+__device__ __forceinline__ float4 ld_peer4_tc(uint32_t addr) {
+  float4 v;
+  asm volatile("ld.shared::cluster.v4.f32 {%0, %1, %2, %3}, [%4];"
+               : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
+               : "r"(addr)
+               : "memory");
   return v;
 }
 
@@ -641,79 +649,111 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   if (ns > 1) {
     __syncthreads();
     cluster_sync_tc();
-    // merge: CTA `split` takes rows rl = split, split + ns, ...; one warp per
-    // row, each lane VPL consecutive dims (a 32-block spans 32 / VPL lanes)
-    constexpr int VPL = HD / 32;
-    constexpr int LPB = 32 / VPL;  // lanes per 32-block
+    // merge: CTA `split` takes rows rl = split, split + ns, ...; TPR threads
+    // per row, 16 consecutive dims each (a 32-block spans two neighbouring
+    // threads), so every row of the CTA merges at once: each thread loads the
+    // (max, sum) of every split and its 16 values of every split, combines them
+    // and quantizes its half block
+    constexpr int TPR = HD / 16;
     const uint32_t po_s = smem_u32(smem + C::OFF_K);
     const int q = a.nh * HD;
     const int nb = q / 32;
-    for (int rl = split + warp * ns; rl < kTcRows; rl += ns * (kTcThreads / 32)) {
+    const int nrows = (kTcRows - split + ns - 1) / ns;
+    const int items = nrows * TPR;
+    for (int base = 0; base < items; base += kTcThreads) {  // CTA-uniform bound
+      const int idx = base + (int)threadIdx.x;
+      const int part = idx % TPR;
+      const int rl = split + ns * (idx / TPR);
       const int r = rbase + rl;
-      if (r >= a.r1) continue;  // warp-uniform
-      // every remote load of the row in flight at once: (max, sum) of split
-      // `lane` and this lane's values of every split
-      float ms = -INFINITY, ls = 0.f;
-      if (lane < ns) {
-        const uint32_t ml = peer_addr_tc(po_s + (uint32_t)((C::PART_ML + rl * 2) * 4), (uint32_t)lane);
-        ms = ld_peer_tc(ml);
-        ls = ld_peer_tc(ml + 4);
-      }
-      float xs[kTcMaxSplits][VPL];
+      const bool valid = idx < items && r < a.r1;  // equal on both threads of a block
+      float y[16];
 #pragma unroll
-      for (int sdx = 0; sdx < kTcMaxSplits; ++sdx) {
-        if (sdx < ns) {
-          const uint32_t pa =
-              peer_addr_tc(po_s + (uint32_t)((rl * HD + lane * VPL) * 4), (uint32_t)sdx);
+      for (int i = 0; i < 16; ++i) y[i] = 0.f;
+      float amax = 0.f;
+      if (valid) {
+        float ms[kTcMaxSplits], ls[kTcMaxSplits];
+        float4 xs[kTcMaxSplits][4];
 #pragma unroll
-          for (int i = 0; i < VPL; ++i) xs[sdx][i] = ld_peer_tc(pa + 4u * i);
+        for (int sdx = 0; sdx < kTcMaxSplits; ++sdx) {
+          ms[sdx] = -INFINITY;
+          ls[sdx] = 0.f;
+          if (sdx < ns) {
+            const float2 ml = ld_peer2_tc(
+                peer_addr_tc(po_s + (uint32_t)((C::PART_ML + rl * 2) * 4), (uint32_t)sdx));
+            ms[sdx] = ml.x;
+            ls[sdx] = ml.y;
+            const uint32_t pa =
+                peer_addr_tc(po_s + (uint32_t)((rl * HD + part * 16) * 4), (uint32_t)sdx);
+#pragma unroll
+            for (int i = 0; i < 4; ++i) xs[sdx][i] = ld_peer4_tc(pa + 16u * i);
+          }
+        }
+        float M = -INFINITY;
+#pragma unroll
+        for (int sdx = 0; sdx < kTcMaxSplits; ++sdx)
+          if (sdx < ns) M = fmaxf(M, ms[sdx]);
+        float L = 0.f;
+#pragma unroll
+        for (int sdx = 0; sdx < kTcMaxSplits; ++sdx) {
+          if (sdx < ns) {
+            const float w = ms[sdx] != -INFINITY ? exp2f(ms[sdx] - M) : 0.f;
+            L = fmaf(w, ls[sdx], L);
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+              y[4 * i + 0] = fmaf(xs[sdx][i].x, w, y[4 * i + 0]);
+              y[4 * i + 1] = fmaf(xs[sdx][i].y, w, y[4 * i + 1]);
+              y[4 * i + 2] = fmaf(xs[sdx][i].z, w, y[4 * i + 2]);
+              y[4 * i + 3] = fmaf(xs[sdx][i].w, w, y[4 * i + 3]);
+            }
+          }
+        }
+        const float inv = L > 0.f ? __fdiv_rn(1.0f, L) : 0.f;
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+          y[i] = __fmul_rn(y[i], inv);
+          amax = fmaxf(amax, fabsf(y[i]));
         }
       }
-      float M = ms;
+      amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
+      if (valid) {
+        const int k0 = h * HD + part * 16;  // first element of this thread in the output row
+        const int blk = k0 / 32;
+        if (out.f32)
 #pragma unroll
-      for (int o2 = 16; o2 > 0; o2 >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o2));
-      const float wl = (lane < ns && ms != -INFINITY) ? exp2f(ms - M) : 0.f;
-      float L = wl * ls;
+          for (int i = 0; i < 16; i += 4)
+            *reinterpret_cast<float4*>(out.f32 + (int64_t)r * q + k0 + i) =
+                make_float4(y[i], y[i + 1], y[i + 2], y[i + 3]);
+        const float dd = __fdiv_rn(amax, 127.0f);
+        const float id = q8_inv(dd);
+        const float d16 = __half2float(__float2half_rn(dd));
+        const int64_t orow = r - out.row_base;
+        if (kGemvOut) {
+          uint32_t wv[4];
 #pragma unroll
-      for (int o2 = 16; o2 > 0; o2 >>= 1) L += __shfl_xor_sync(0xffffffffu, L, o2);
-      float y[VPL];
+          for (int i = 0; i < 4; ++i)
+            wv[i] = (uint32_t)(uint8_t)(int8_t)q8_code(y[4 * i], id) |
+                    ((uint32_t)(uint8_t)(int8_t)q8_code(y[4 * i + 1], id) << 8) |
+                    ((uint32_t)(uint8_t)(int8_t)q8_code(y[4 * i + 2], id) << 16) |
+                    ((uint32_t)(uint8_t)(int8_t)q8_code(y[4 * i + 3], id) << 24);
+          *reinterpret_cast<uint4*>(out.q8 + orow * (int64_t)nb * 32 + k0) =
+              make_uint4(wv[0], wv[1], wv[2], wv[3]);
+          if ((part & 1) == 0) out.s8[orow * nb + blk] = d16;
+        } else {
 #pragma unroll
-      for (int i = 0; i < VPL; ++i) y[i] = 0.f;
-#pragma unroll
-      for (int sdx = 0; sdx < kTcMaxSplits; ++sdx) {
-        const float w = __shfl_sync(0xffffffffu, wl, sdx);
-        if (sdx < ns)
-#pragma unroll
-          for (int i = 0; i < VPL; ++i) y[i] = fmaf(xs[sdx][i], w, y[i]);
-      }
-      const float inv = L > 0.f ? __fdiv_rn(1.0f, L) : 0.f;
-      float amax = 0.f;
-#pragma unroll
-      for (int i = 0; i < VPL; ++i) {
-        y[i] = __fmul_rn(y[i], inv);
-        amax = fmaxf(amax, fabsf(y[i]));
-      }
-#pragma unroll
-      for (int o2 = 1; o2 < LPB; o2 <<= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o2));
-      const int k0 = h * HD + lane * VPL;  // first element of this lane in the output row
-      const int blk = k0 / 32;
-      if (out.f32)
-#pragma unroll
-        for (int i = 0; i < VPL; ++i) out.f32[(int64_t)r * q + k0 + i] = y[i];
-      const float dd = __fdiv_rn(amax, 127.0f);
-      const float id = q8_inv(dd);
-      const float d16 = __half2float(__float2half_rn(dd));
-      const int64_t orow = r - out.row_base;
-      if (kGemvOut) {
-#pragma unroll
-        for (int i = 0; i < VPL; ++i) out.q8[orow * (int64_t)nb * 32 + k0 + i] = (int8_t)q8_code(y[i], id);
-        if ((lane % LPB) == 0) out.s8[orow * nb + blk] = d16;
-      } else {
-#pragma unroll
-        for (int i = 0; i < VPL; i += 2)
-          *reinterpret_cast<__half2*>(out.q16 + orow * out.ldq + k0 + i) =
-              __floats2half2_rn(q8_code(y[i], id), q8_code(y[i + 1], id));
-        if ((lane % LPB) == 0) out.s16[(int64_t)blk * out.ldqs + orow] = d16;
+          for (int i = 0; i < 16; i += 8) {
+            uint4 w;
+            __half2 c0 = __floats2half2_rn(q8_code(y[i], id), q8_code(y[i + 1], id));
+            __half2 c1 = __floats2half2_rn(q8_code(y[i + 2], id), q8_code(y[i + 3], id));
+            __half2 c2 = __floats2half2_rn(q8_code(y[i + 4], id), q8_code(y[i + 5], id));
+            __half2 c3 = __floats2half2_rn(q8_code(y[i + 6], id), q8_code(y[i + 7], id));
+            w.x = *reinterpret_cast<uint32_t*>(&c0);
+            w.y = *reinterpret_cast<uint32_t*>(&c1);
+            w.z = *reinterpret_cast<uint32_t*>(&c2);
+            w.w = *reinterpret_cast<uint32_t*>(&c3);
+            *reinterpret_cast<uint4*>(out.q16 + orow * out.ldq + k0 + i) = w;
+          }
+          if ((part & 1) == 0) out.s16[(int64_t)blk * out.ldqs + orow] = d16;
+        }
       }
     }
     cluster_sync_tc();  // peers may still be reading this CTA's partials
