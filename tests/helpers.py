@@ -107,4 +107,18 @@ def check_q8_requant(oracle_mod, codes, scales, ref, slack):
     flips = (diff > 0) & same_scale
     assert np.all(dist[flips] <= tol_t[flips] + 1e-3), "code flip away from a rounding boundary"
     assert flips.mean() <= 2e-3, flips.mean()
-    assert (scales != od).mean() <= 2e-3
+    # a block's fp16 scale may differ from the oracle's only by one fp16 step,
+    # and only where the oracle's d = amax/127 lies within the f32 error of
+    # amax (the block's largest slack, over 127) of the rounding boundary
+    # between the two fp16 values
+    sc = np.asarray(scales)[:, :nb]
+    off = sc != od[:, :nb]
+    if off.any():
+        g16, o16 = sc[off].astype(np.int32), od[:, :nb][off].astype(np.int32)
+        assert np.all(np.abs(g16 - o16) == 1), "scale off by more than one fp16 step"
+        f16 = lambda b: np.asarray(b, dtype=np.uint16).view(np.float16).astype(np.float64)
+        mid = 0.5 * (f16(sc[off]) + f16(od[:, :nb][off]))
+        dref = amax[:, :, 0][off] / 127.0
+        smax = sl.reshape(rows, nb, 32).max(axis=2)[off]
+        assert np.all(np.abs(dref - mid) <= smax / 127.0 * (1 + 1e-3) + 2.0 ** -22 * dref), \
+            "scale differs away from an fp16 rounding boundary"

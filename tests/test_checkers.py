@@ -65,3 +65,21 @@ def test_requant_checker(oracle_mod):
     assert _raises(check_q8_requant, oracle_mod, q2, d, ref, slack)
     q3, d3 = oracle_mod.q8_quantize((ref * 1.01).astype(np.float32))   # a scaled output
     assert _raises(check_q8_requant, oracle_mod, q3, d3, ref, slack)
+    # one block's scale one fp16 step off, its d far from a rounding boundary
+    f16 = lambda b: np.asarray(b, dtype=np.uint16).view(np.float16).astype(np.float64)
+    amax = np.abs(np.pad(ref, ((0, 0), (0, 4)))).reshape(8, 22, 32).max(axis=2)
+    frac = (amax / 127.0 - f16(d)) / (f16(d + 1) - f16(d))
+    r, b = np.argwhere(np.abs(frac) < 0.2)[0]
+    d4 = d.copy()
+    d4[r, b] += 1
+    assert _raises(check_q8_requant, oracle_mod, q, d4, ref, slack)
+    # the same step where d sits on the boundary within the slack passes
+    ref5 = ref.copy()
+    blk = ref5[r, 32 * b:32 * b + 32]
+    k = int(np.argmax(np.abs(blk)))
+    mid = 0.5 * (f16(d[r, b]) + f16(d[r, b] + 1))
+    blk[k] = np.sign(blk[k]) * mid * 127.0   # amax / 127 exactly on the boundary
+    q5, d5 = oracle_mod.q8_quantize(ref5.astype(np.float32))
+    d6 = d5.copy()
+    d6[r, b] = d5[r, b] + 1 if f16(d5[r, b]) < mid else d5[r, b] - 1
+    check_q8_requant(oracle_mod, q5, d6, ref5, 4e-6 * np.abs(ref5))
