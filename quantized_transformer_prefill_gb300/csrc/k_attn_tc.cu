@@ -198,9 +198,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int G = a.nh / a.nkv;
-  const int ns = (int)gridDim.z;
+  const int ns = (int)gridDim.x;
   const int split = (int)cluster_rank_tc();
-  const int tile = (int)gridDim.x - 1 - (int)blockIdx.x;  // longest rows first
+  const int tile = (int)gridDim.z - 1 - (int)blockIdx.z;  // longest rows first
   const int h = blockIdx.y;
   const int g = h / G;
   const int rbase = a.r0 + tile * kTcRows;
@@ -821,15 +821,18 @@ cudaError_t launch_tc(const AttnArgs& a, const AttnOut& out, int ns, int* err, c
   t.err = err;
   const int rows = a.r1 - a.r0;
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3((rows + kTcRows - 1) / kTcRows, a.nh, ns);
+  // the cluster's CTAs (key splits) along x, heads along y, row tiles along z
+  // with the longest rows first, so that every head's longest tiles start in
+  // the first wave
+  cfg.gridDim = dim3(ns, a.nh, (rows + kTcRows - 1) / kTcRows);
   cfg.blockDim = dim3(kTcThreads);
   cfg.dynamicSmemBytes = C::SMEM;
   cfg.stream = st;
   cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = 1;
+  attr[0].val.clusterDim.x = ns;
   attr[0].val.clusterDim.y = 1;
-  attr[0].val.clusterDim.z = ns;
+  attr[0].val.clusterDim.z = 1;
   attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
