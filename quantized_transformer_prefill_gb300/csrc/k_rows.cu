@@ -423,8 +423,10 @@ __global__ void validate_kernel(const int32_t* __restrict__ ids, const int32_t* 
 // when present, the fp16 hi/lo planes the tensor-core attention loads by TMA.
 __device__ __forceinline__ void store_q(const RopeStoreArgs& a, int64_t o, float v0, float v1,
                                         int half) {
-  a.q_out[o] = v0;
-  a.q_out[o + half] = v1;
+  if (a.q_out) {
+    a.q_out[o] = v0;
+    a.q_out[o + half] = v1;
+  }
   if (a.q_planes[0]) {
     const __half h0 = __float2half_rn(v0), h1 = __float2half_rn(v1);
     a.q_planes[0][o] = h0;
@@ -491,8 +493,10 @@ __global__ void __launch_bounds__(1024, 2) rope_store_kernel(const RopeStoreArgs
         // rotated Q to f32 and, when present, the fp16 hi/lo planes the
         // tensor-core attention loads by TMA
         const int64_t o = (int64_t)t * a.nh * a.hd + e0;
-        *reinterpret_cast<float2*>(a.q_out + o) = v0;
-        *reinterpret_cast<float2*>(a.q_out + o + half) = v1;
+        if (a.q_out) {
+          *reinterpret_cast<float2*>(a.q_out + o) = v0;
+          *reinterpret_cast<float2*>(a.q_out + o + half) = v1;
+        }
         if (a.q_planes[0]) {
           *reinterpret_cast<__half2*>(a.q_planes[0] + o) = h0;
           *reinterpret_cast<__half2*>(a.q_planes[0] + o + half) = h1;

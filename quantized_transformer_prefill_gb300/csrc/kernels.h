@@ -148,7 +148,7 @@ struct RopeStoreArgs {
   int n_ctx = 0;                 // rows of the regions and of the cos/sin tables
   const float* cos_t = nullptr;  // [n_ctx][hd/2]
   const float* sin_t = nullptr;
-  float* q_out = nullptr;  // [nt][nh*hd]
+  float* q_out = nullptr;  // [nt][nh*hd]; null: only the fp16 planes of Q are written
   float* kreg = nullptr;   // [n_ctx][nkv*hd]
   float* vreg = nullptr;
   __half* shadow[4] = {nullptr, nullptr, nullptr, nullptr};  // fp16 hi/lo copies of K, V

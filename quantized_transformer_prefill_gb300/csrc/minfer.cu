@@ -938,6 +938,25 @@ int enqueue_forward(minfer_model* m, minfer_kv* kv, const int32_t* ids, const in
     if ((rc = gemm_call(m, L, kKGemmQKV, xa, Ly.wqkv, nt, kEpiF32, true, w.part, m->qkvN, nullptr,
                         0, nullptr, 0, &ns)))
       return rc;
+    AttnArgs at;
+    at.q = w.qrot;
+    at.qp[0] = w.qpl;
+    at.qp[1] = w.qpl + (int64_t)w.max_nt * m->q;
+    at.pos = pos;
+    at.r0 = r0;
+    at.r1 = nt;
+    for (int i = 0; i < 4; ++i) at.shadow[i] = kv->plane(l, i);
+    at.vt[0] = kv->vtp(l, 0);
+    at.vt[1] = kv->vtp(l, 1);
+    at.vt_ld = kv->vt_ld;
+    at.nh = hp.n_head;
+    at.nkv = hp.n_head_kv;
+    at.hd = hp.head_dim;
+    at.n_ctx = kv->n_ctx;
+    at.nsplit = attention_nsplit(at.r1 - at.r0, at.nkv, m->num_sms, at.nh / at.nkv);
+    if (tail1) row_attention_args(kv, l, &at);
+    const bool attn_tc =
+        attention_tc_supported(at) && attention_tc_preferred(at.r1 - at.r0, at.nh, m->num_sms);
     {
       RopeStoreArgs r;
       r.partials = w.part;
@@ -952,7 +971,9 @@ int enqueue_forward(minfer_model* m, minfer_kv* kv, const int32_t* ids, const in
       r.n_ctx = kv->n_ctx;
       r.cos_t = kv->cos_t;
       r.sin_t = kv->sin_t;
-      r.q_out = w.qrot;
+      // the rotated Q in f32 is read by the CUDA-core attention kernels and the
+      // debug captures; the tensor-core attention reads only its fp16 hi/lo planes
+      r.q_out = (attn_tc && !cap && !m->debug_f32) ? nullptr : w.qrot;
       r.q_planes[0] = w.qpl;
       r.q_planes[1] = w.qpl + (int64_t)w.max_nt * m->q;
       r.kreg = kv->k(l);
@@ -981,23 +1002,6 @@ int enqueue_forward(minfer_model* m, minfer_kv* kv, const int32_t* ids, const in
                            static_cast<float*>(e.first), st));
       if (cap_all && (rc = dbg_capture(m, st, "qrot", w.qrot, (size_t)nt * m->q * 4))) return rc;
     }
-    AttnArgs at;
-    at.q = w.qrot;
-    at.qp[0] = w.qpl;
-    at.qp[1] = w.qpl + (int64_t)w.max_nt * m->q;
-    at.pos = pos;
-    at.r0 = r0;
-    at.r1 = nt;
-    for (int i = 0; i < 4; ++i) at.shadow[i] = kv->plane(l, i);
-    at.vt[0] = kv->vtp(l, 0);
-    at.vt[1] = kv->vtp(l, 1);
-    at.vt_ld = kv->vt_ld;
-    at.nh = hp.n_head;
-    at.nkv = hp.n_head_kv;
-    at.hd = hp.head_dim;
-    at.n_ctx = kv->n_ctx;
-    at.nsplit = attention_nsplit(at.r1 - at.r0, at.nkv, m->num_sms, at.nh / at.nkv);
-    if (tail1) row_attention_args(kv, l, &at);
     AttnOut ao;
     ao.f32 = (m->debug_f32 || cap) ? w.att : nullptr;
     if (!tail1) {
@@ -1011,7 +1015,7 @@ int enqueue_forward(minfer_model* m, minfer_kv* kv, const int32_t* ids, const in
       ao.s8 = w.t_s;
       ao.row_base = nt - 1;
     }
-    if (attention_tc_supported(at) && attention_tc_preferred(at.r1 - at.r0, at.nh, m->num_sms))
+    if (attn_tc)
       LAUNCH(kKAttn, attention_tc_launch(at, ao, m->num_sms, m->d_status + 1, st));
     else
       LAUNCH(kKAttn, attention_launch(at, ao, st));
