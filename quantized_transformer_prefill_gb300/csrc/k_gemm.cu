@@ -46,9 +46,10 @@ constexpr int kThreads = 64 + 32 * kEpiWarps;
 
 template <int BN>
 struct Cfg {
-  // five stages of A/B (10 K blocks in flight): measured 1-2% faster than
-  // six on the 1.5B and 7B shapes, equal on the 0.5B ones
-  static constexpr int STAGES = 5;
+  // four stages of A/B (8 K blocks in flight), measured against 3, 5 and 6:
+  // six is 1-2% slower on the 1.5B and 7B shapes, three 1.5% slower on
+  // 1.5B/2048, five 0.4% slower on the 0.5B forward
+  static constexpr int STAGES = 4;
   static constexpr int SSTAGES = 8;
   static constexpr int NSLOT = 512 / BN;
   static constexpr int CPW = BN / 2;  // columns per epilogue thread
