@@ -8,6 +8,8 @@ tolerances derived from f32 arithmetic.
 import numpy as np
 import pytest
 
+from helpers import U, check_q8_requant, q8_sum_bound
+
 pytestmark = pytest.mark.gpu
 
 torch = pytest.importorskip("torch")
@@ -101,17 +103,22 @@ def test_gemm_swiglu_quantize(qp, oracle_mod, M, F, K):
     uq, ud = oracle_mod.q8_quantize(u)
     sq, sd = qp.op_gemm_swiglu(_dev(xq), _dev(xd.view(np.int16)), _dev(gq), _dev(gd.view(np.int16)),
                                _dev(uq), _dev(ud.view(np.int16)), F, K)
-    gg = oracle_mod.matmul_q8(xq, xd, gq, gd, K)
-    uu = oracle_mod.matmul_q8(xq, xd, uq, ud, K)
-    oq, od = oracle_mod.q8_quantize(oracle_mod.swiglu(gg, uu))
+    gg = oracle_mod.matmul_q8(xq, xd, gq, gd, K).astype(np.float64)
+    uu = oracle_mod.matmul_q8(xq, xd, uq, ud, K).astype(np.float64)
+    s_ref = oracle_mod.swiglu(gg, uu)
+    oq, od = oracle_mod.q8_quantize(s_ref)
     sq = sq.cpu().numpy()
     sd = sd.cpu().numpy().view(np.uint16)
-    # the f32 sums differ from the oracle's float64 ones in the last bits, so
-    # a code can land on the other side of a rounding boundary: at most one
-    # step, rarely; scales match unless amax sits on an fp16 boundary
-    diff = np.abs(sq.astype(np.int32) - oq.astype(np.int32))
-    assert diff.max() <= 1 and (diff > 0).mean() < 1e-3
-    assert (sd != od).mean() < 1e-3
+    # the GPU's gate/up are f32 block sums (error dg, du within their bounds);
+    # silu' <= 1.1 and |silu(g)| <= |g| + 0.28 carry them into s = silu(g) u,
+    # plus the f32 arithmetic of silu and of the product (10 units of
+    # roundoff; 16 allowed): a code or a scale may then differ from the
+    # oracle's own quantization only across a rounding boundary within that
+    # bound
+    dg = q8_sum_bound(oracle_mod, xq, xd, gq, gd, K)
+    du = q8_sum_bound(oracle_mod, xq, xd, uq, ud, K)
+    slack = 1.1 * np.abs(uu) * dg + (np.abs(gg) + 0.28) * du + 16 * U * np.abs(s_ref)
+    check_q8_requant(oracle_mod, sq, sd, s_ref, slack)
     deq = oracle_mod.q8_dequantize(sq, sd, F)
     ref = oracle_mod.q8_dequantize(oq, od, F)
     assert np.linalg.norm(deq - ref) <= 1e-3 * np.linalg.norm(ref)
