@@ -86,6 +86,7 @@ struct Args {
   int* err;
   uint64_t wait_ns;  // time limit of every bounded wait
   int skip_stage;    // test hook: a stage CTA 0's producer withholds (-1: none)
+  int b_pre;         // B written by no kernel in flight: its first loads precede the grid wait
 };
 
 // silu(g) * u = g / (1 + exp(-g)) * u in f32: expf (2 ulp), the add, the
@@ -148,9 +149,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem_base = *tmem_holder;
-  // set-up above overlaps the previous kernel; global memory only after it
+  // set-up above overlaps the previous kernel; global memory only after it,
+  // except the producer's first B loads when B is static (below)
   pdl_trigger();
-  pdl_wait();
+  if (warp != 0) pdl_wait();
 
   const int total = p.m_tiles * p.n_tiles * p.splits;
 
@@ -159,6 +161,25 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (lane == 0) {
       int it = 0, n_ab = 0, n_s = 0;  // stages issued; A/B loads and scale loads in flight
       bool ok = true;
+      // the first stages' B tiles and B scales (weights) before the wait for
+      // the previous kernel: their ring slots are free at the start, and the
+      // stage barriers complete once the A halves follow
+      int npre = 0;
+      if (p.b_pre && (int)blockIdx.x < total) {
+        const int rest = (int)blockIdx.x / p.m_tiles;
+        const int ntile = rest % p.n_tiles;
+        const int s0 = (rest / p.n_tiles) * p.stages_per_split;
+        const int s1 = min(p.n_stages, s0 + p.stages_per_split);
+        npre = min(C::STAGES, s1 - s0);
+        for (int j = 0; j < npre; ++j) {
+          if (j == p.skip_stage && blockIdx.x == 0) continue;
+          mbar_arrive_expect_tx(&full[j], C::STAGE_TX);
+          tma_load_2d(sB + j * C::B_BYTES, &tmB, &full[j], (s0 + j) * kBK, ntile * BN);
+          mbar_arrive_expect_tx(&sfull[j], C::SCALE_TX);
+          tma_load_2d(sSB + j * (C::SB_BYTES / 4), &tmSB, &sfull[j], ntile * BN, 2 * (s0 + j));
+        }
+      }
+      pdl_wait();
       for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
         const int mt = t % p.m_tiles;
         const int rest = t / p.m_tiles;
@@ -175,18 +196,19 @@ __global__ void __launch_bounds__(kThreads, 1)
           // test hook: withhold this stage (no loads, no arrival), so the
           // consumers' bounded waits on it run out
           if (it == p.skip_stage && blockIdx.x == 0) continue;
-          mbar_arrive_expect_tx(&full[st], C::STAGE_TX);
+          const bool pre = it < npre;  // B half already issued
+          if (!pre) mbar_arrive_expect_tx(&full[st], C::STAGE_TX);
           tma_load_2d(sA + st * C::A_BYTES, &tmA, &full[st], s * kBK, mt * kBM);
-          tma_load_2d(sB + st * C::B_BYTES, &tmB, &full[st], s * kBK, ntile * BN);
+          if (!pre) tma_load_2d(sB + st * C::B_BYTES, &tmB, &full[st], s * kBK, ntile * BN);
           n_ab = it + 1;
           const int ss = it % C::SSTAGES;
           if (!mbar_wait(&sempty[ss], ((it / C::SSTAGES) & 1) ^ 1, p.err, kDevTimeoutTmaEmpty, p.wait_ns)) {
             ok = false;
             break;
           }
-          mbar_arrive_expect_tx(&sfull[ss], C::SCALE_TX);
+          if (!pre) mbar_arrive_expect_tx(&sfull[ss], C::SCALE_TX);
           tma_load_2d(sSA + ss * (C::SA_BYTES / 4), &tmSA, &sfull[ss], mt * kBM, 2 * s);
-          tma_load_2d(sSB + ss * (C::SB_BYTES / 4), &tmSB, &sfull[ss], ntile * BN, 2 * s);
+          if (!pre) tma_load_2d(sSB + ss * (C::SB_BYTES / 4), &tmSB, &sfull[ss], ntile * BN, 2 * s);
           n_s = it + 1;
         }
       }
@@ -479,6 +501,7 @@ cudaError_t launch_bn(const GemmLaunch& g, const GemmMaps& maps, int num_sms, cu
   a.err = g.err;
   a.wait_ns = g.wait_ns ? g.wait_ns : kWaitLimitNs;
   a.skip_stage = g.skip_stage;
+  a.b_pre = g.b_static ? 1 : 0;
   const int total = a.m_tiles * a.n_tiles * a.splits;
   const int grid = std::max(1, std::min(total, num_sms));
   return launch_pdl(gemm_q8_kernel<BN, EPI>, grid, kThreads, C::SMEM, st, maps.a, maps.b, maps.sa,

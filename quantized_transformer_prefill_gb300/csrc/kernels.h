@@ -85,6 +85,10 @@ struct GemmLaunch {
   int64_t n_out_cols = 0;  // kEpiSwiGLU: padded count of SwiGLU outputs
   int32_t* dots = nullptr;
   int* err = nullptr;
+  // B (codes and scales) is written by no kernel that may still be running
+  // (weights uploaded before the call): the first stages' B loads then start
+  // before the wait for the previous kernel of the stream
+  bool b_static = false;
   // test hook (off by default): the time limit of every bounded wait (0: the
   // default) and one K stage that CTA 0's producer withholds (-1: none), so
   // that the MMA issuer's wait on it runs out

@@ -613,6 +613,7 @@ int gemm_call(minfer_model* m, Launcher& L, int cls, const GemmOperand& A, const
   g.ldqs = ldqs;
   g.n_out_cols = m->Fp;
   g.err = m->d_status + 1;
+  g.b_static = true;  // the model's weights, uploaded (and synchronized) at load
   if (m->fault_layer >= 0) {
     g.wait_ns = m->fault_wait_ns;
     if (fault) g.skip_stage = 0;
