@@ -678,6 +678,15 @@ __device__ __forceinline__ void gemv_dot(const GemvArgs& a, const int64_t (&rows
                      : make_int4(0, 0, 0, 0);
         dw[h][r] = ok ? __ldg(a.ws + n * a.nb + b) : 0.f;
       }
+    }
+    // static weights: their first round is in flight before the wait for the
+    // kernel that wrote the activation row
+    if (c == 0 && a.w_static) pdl_wait();
+#pragma unroll
+    for (int h = 0; h < U; ++h) {
+      const int64_t k = c + 512 * h + 16 * lane;
+      const bool in = k < a.kpad;
+      const int b = (int)(k >> 5);
       x[h] = in ? *reinterpret_cast<const int4*>(a.xq + k) : make_int4(0, 0, 0, 0);
       dx[h] = in ? a.xs[b] : 0.f;
     }
@@ -704,7 +713,7 @@ __global__ void __launch_bounds__(32 * kGemvWarps, R >= 4 ? 2 : (R == 2 ? 4 : 3)
   __shared__ float part[kGemvWarps][8];
   __shared__ unsigned s_last;
   pdl_trigger();
-  pdl_wait();
+  if (!a.w_static) pdl_wait();  // else inside gemv_dot, after the first weight loads
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int64_t n0 = ((int64_t)blockIdx.x * kGemvWarps + warp) * R;
   float acc[R];
@@ -762,7 +771,7 @@ __global__ void __launch_bounds__(32 * kGemvWarps, R >= 4 ? 2 : (R == 2 ? 4 : 3)
 __global__ void __launch_bounds__(32 * kGemvWarps, 2) gemv_rope_kernel(const GemvArgs a,
                                                                       const RopeStoreArgs ra) {
   pdl_trigger();
-  pdl_wait();
+  if (!a.w_static) pdl_wait();  // else inside gemv_dot, after the first weight loads
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int hd = ra.hd, half = hd >> 1;
   const int64_t unit = (int64_t)blockIdx.x * kGemvWarps + warp;

@@ -251,6 +251,10 @@ struct GemvArgs {
   int8_t* q8 = nullptr;
   float* s8 = nullptr;
   unsigned* ticket = nullptr;
+  // the weights are written by no kernel that may still be running (uploaded
+  // before the call): the first round of weight loads then starts before the
+  // wait for the previous kernel of the stream
+  int w_static = 0;
 };
 cudaError_t gemv_launch(const GemvArgs& a, cudaStream_t stream);
 // Whether a norm can ride the GEMV's last CTA: whole Q8_0 blocks, N <= 4096,

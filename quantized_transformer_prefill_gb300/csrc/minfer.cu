@@ -691,6 +691,7 @@ GemvArgs row_gemv(const minfer_model* m, const GemvW& W, int64_t N, int nb, cons
   g.xs = xs;
   g.y = y;
   g.resid = resid;
+  g.w_static = 1;  // the model's weights, uploaded (and synchronized) at load
   return g;
 }
 
