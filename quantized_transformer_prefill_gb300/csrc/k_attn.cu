@@ -536,7 +536,6 @@ __global__ void __launch_bounds__(kRowThreadsA) attn_row_kernel(const AttnArgs a
   __shared__ float po[8][HD];  // this CTA's unnormalized O, per query head of the group
   __shared__ float pml[8][2];  // and its (max, sum)
   pdl_trigger();
-  pdl_wait();
 
   const int G = a.nh / a.nkv;
   const int g = blockIdx.y;
@@ -546,10 +545,7 @@ __global__ void __launch_bounds__(kRowThreadsA) attn_row_kernel(const AttnArgs a
   const int r = a.r0;
   const int64_t kw = (int64_t)a.nkv * HD;
   const int64_t qw = (int64_t)a.nh * HD;
-  // the group's query rows load next to the position they do not depend on
-  for (int i = tid; i < G * HD; i += kRowThreadsA)
-    qs[i / HD][i % HD] = a.q[(int64_t)r * qw + (int64_t)g * G * HD + i];
-  int p = a.pos[r];
+  int p = a.pos[r];  // the positions are the call's input, written before any kernel
   p = p < 0 ? -1 : (p >= a.n_ctx ? a.n_ctx - 1 : p);
   const int nkeys = p + 1;
   const int share = (nkeys + ns - 1) / ns;
@@ -573,7 +569,15 @@ __global__ void __launch_bounds__(kRowThreadsA) attn_row_kernel(const AttnArgs a
       }
     }
   };
-  if (nchunks > 0) load_chunk(kbeg);
+  // the first chunk before the wait for the previous kernel when none of its
+  // rows is the one that kernel wrote (row p)
+  const bool early = a.kv_static_below && nchunks > 0 && min(kbeg + kRowKeys, kend) <= p;
+  if (early) load_chunk(kbeg);
+  pdl_wait();
+  // the group's query rows load next to the chunk
+  for (int i = tid; i < G * HD; i += kRowThreadsA)
+    qs[i / HD][i % HD] = a.q[(int64_t)r * qw + (int64_t)g * G * HD + i];
+  if (nchunks > 0 && !early) load_chunk(kbeg);
 
   float m = -INFINITY, l = 0.f, o[DPL];
 #pragma unroll

@@ -190,6 +190,10 @@ struct AttnArgs {
   // (16-byte aligned).
   const float* kreg = nullptr;
   const float* vreg = nullptr;
+  // One-row kernel: the region rows below the query's position were written
+  // by earlier calls (a single-token call), not by a kernel that may still be
+  // running, so the first chunk of them loads before the grid wait.
+  int kv_static_below = 0;
 };
 // Where the attention output goes: Q8_0 codes in the GEMM layout (q16 [rows][ldq]
 // fp16 + s16 [nb][ldqs]) or the GEMV layout (q8 [rows][nb*32] + s8 [rows][nb]);

@@ -827,15 +827,16 @@ int enqueue_decode(minfer_model* m, minfer_kv* kv, const int32_t* ids, const int
       at.r0 = 0;
       at.r1 = 1;
       for (int i = 0; i < 4; ++i) at.shadow[i] = kv->plane(l, i);
-    at.vt[0] = kv->vtp(l, 0);
-    at.vt[1] = kv->vtp(l, 1);
-    at.vt_ld = kv->vt_ld;
+      at.vt[0] = kv->vtp(l, 0);
+      at.vt[1] = kv->vtp(l, 1);
+      at.vt_ld = kv->vt_ld;
       at.nh = hp.n_head;
       at.nkv = hp.n_head_kv;
       at.hd = hp.head_dim;
       at.n_ctx = kv->n_ctx;
       at.nsplit = attention_nsplit(1, at.nkv, m->num_sms, at.nh / at.nkv);
       row_attention_args(kv, l, &at);
+      at.kv_static_below = 1;  // rows below the token's position: earlier calls
       AttnOut ao;
       ao.f32 = (m->debug_f32 || cap) ? w.att : nullptr;
       ao.q8 = w.t_q;
