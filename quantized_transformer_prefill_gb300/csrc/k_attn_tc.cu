@@ -58,15 +58,14 @@ constexpr float kLazyMax = 8.0f;
 constexpr int kFoldTiles = 4;
 constexpr uint32_t kTcolT = 128;  // TMEM column of T; R follows at kTcolT + hd
 // Two P buffers (fp16 hi/lo, 64 keys: 32 columns each, 64 per buffer) after
-// R, so the softmax of tile j+1 need not wait for the P.V of tile j; with
-// head_dim 64 the Q tile (fp16 hi/lo, 32 columns each) follows them.
+// R, so the softmax of tile j+1 need not wait for the P.V of tile j.  (The Q
+// tile stays in shared memory: copying it into TMEM as the S MMA's A operand,
+// as P is for P.V, cost 0.3% of the 0.5B forward in the copy's latency.)
 template <int HD>
 struct TcCols {
   static constexpr uint32_t R = kTcolT + HD;
-  static constexpr uint32_t P = R + HD;         // buffer b at P + b * kTcKeys
-  static constexpr uint32_t Q = P + 2 * kTcKeys;  // used when Q lives in TMEM (HD 64)
-  static constexpr bool kQInTmem = HD == 64;
-  static constexpr uint32_t END = kQInTmem ? Q + HD : Q;
+  static constexpr uint32_t P = R + HD;  // buffer b at P + b * kTcKeys
+  static constexpr uint32_t END = P + 2 * kTcKeys;
   static_assert(END <= 512, "TMEM columns");
 };
 
@@ -106,12 +105,6 @@ struct TcArgs {
   int r0, r1, nh, nkv, n_ctx;
   int* err;
 };
-
-// Byte offset of element (row, k) in a K-major, 128-byte-swizzled tile whose
-// rows are 64 fp16 wide (chunk of 8 halves XOR row % 8, as TMA writes it).
-__device__ __forceinline__ uint32_t sw128_off(int row, int k) {
-  return (uint32_t)(row * 128 + (((k >> 3) ^ (row & 7)) << 4) + ((k & 7) << 1));
-}
 
 __device__ __forceinline__ uint32_t cluster_rank_tc() {
   uint32_t r;
@@ -192,7 +185,6 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   uint64_t* qready = oready + 2;
   uint64_t* mdone = qready + 1;  // [2] each issuer's MMAs completed (before TMEM is freed)
   uint64_t* lsum = mdone + 2;    // the two halves of every row have published their sums
-  uint64_t* qtm = lsum + 1;      // the Q tile is in TMEM (head_dim 64)
   uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(smem + C::OFF_TMEM);
   __shared__ int s_maxp;
 
@@ -219,7 +211,6 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     mbar_init(&pready[0], kSmWarps);
     mbar_init(&pready[1], kSmWarps);
     mbar_init(lsum, kSmWarps);
-    mbar_init(qtm, kSmWarps);
     mbar_init(&oready[0], 1);
     mbar_init(&oready[1], 1);
     mbar_init(qready, 1);
@@ -243,14 +234,16 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   tc_fence_after();
   const uint32_t tmem_base = *tmem_holder;
   pdl_trigger();
-  pdl_wait();
 
   auto clamp_pos = [&](int r) -> int {
     if (r >= a.r1) return -1;
     const int p = a.pos[r];
     return p < 0 ? -1 : (p >= a.n_ctx ? a.n_ctx - 1 : p);
   };
+  // the positions are the call's input, written before any kernel: their max
+  // is taken while the previous kernel finishes
   if (threadIdx.x < kTcRows) atomicMax(&s_maxp, clamp_pos(rbase + threadIdx.x));
+  pdl_wait();
   __syncthreads();
   const int nkeys = s_maxp + 1;
   int share = (nkeys + ns - 1) / ns;
@@ -310,16 +303,14 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   } else if (warp == 1 || warp == kPvWarp) {
     // ---------------------------------------------------------- MMA issuers
     // S = Q.K^T (warp 1) and O += P.V (warp 10) have an issuing thread each.
-    // P, and with head_dim 64 also Q, is the A operand straight from TMEM:
-    // the MMA then reads only K or V^T from shared memory, whose bandwidth
-    // (shared with the TMA writes) bounds these small-N MMAs.
+    // P is the A operand of P.V straight from TMEM: that MMA then reads only
+    // V^T from shared memory; S reads Q and K from shared memory.
     if (lane == 0 && ntile > 0) {
       using TC = TcCols<HD>;
       constexpr uint32_t idS = idesc_f16_f32(kTcRows, kTcKeys);
       constexpr uint32_t idO = idesc_f16_f32(kTcRows, HD);
       const uint32_t qh = smem_u32(sQh), ql = smem_u32(sQl);
       const uint32_t ph0 = tmem_base + TC::P;  // P buffer b: hi at ph0 + 64 b, lo 32 columns on
-      const uint32_t tqh = tmem_base + TC::Q, tql = tmem_base + TC::Q + HD / 2;
       const uint32_t tO = tmem_base + kTcolT;
       bool ok = true;
       bool committed = false;
@@ -338,15 +329,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           for (int k = 0; k < HD / 16; ++k) {
             const uint32_t off = (uint32_t)((k & 3) * 32);
             const uint64_t bd = smem_desc_sw128(B + (k >> 2) * C::KSUB + off);
-            if constexpr (TC::kQInTmem) {
-              // Q in TMEM: 16 fp16 along K = 8 columns per step
-              tc_mma_f16_ts(d, (c == 2 ? tql : tqh) + (uint32_t)(8 * k), bd, idS,
-                            (c == 0 && k == 0) ? 0u : 1u);
-            } else {
-              const uint32_t A = c == 2 ? ql : qh;
-              tc_mma_f16(d, smem_desc_sw128(A + (k >> 2) * C::QSUB + off), bd, idS,
-                         (c == 0 && k == 0) ? 0u : 1u);
-            }
+            const uint32_t A = c == 2 ? ql : qh;
+            tc_mma_f16(d, smem_desc_sw128(A + (k >> 2) * C::QSUB + off), bd, idS,
+                       (c == 0 && k == 0) ? 0u : 1u);
           }
         }
         tc_commit(&sready[b]);
@@ -382,10 +367,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         return true;
       };
       if (warp == 1) {
-        // Q in shared memory (TMA), or copied from there into TMEM by the
-        // softmax warps
-        ok = TC::kQInTmem ? mbar_wait(qtm, 0, a.err, kDevTimeoutAttn)
-                          : mbar_wait(qready, 0, a.err, kDevTimeoutAttn);
+        // Q in shared memory (TMA)
+        ok = mbar_wait(qready, 0, a.err, kDevTimeoutAttn);
         if (ok) tc_fence_after();
         for (int j = 0; j < ntile && ok; ++j) ok = issue_s(j);
       } else {
@@ -417,30 +400,6 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     // scores in log2 units: s2 = (q.k) / sqrt(hd) * log2(e)
     const float sc = __fmul_rn(__fdiv_rn(1.0f, __fsqrt_rn((float)HD)), 1.4426950408889634f);
     bool ok = true;
-    if constexpr (TcCols<HD>::kQInTmem) {
-      if (ntile > 0) {
-        // this thread's half of its row of Q (dims kh*32 .. kh*32+31, hi and
-        // lo) from the swizzled TMA tile into the TMEM columns the S MMA reads
-        ok = mbar_wait(qready, 0, a.err, kDevTimeoutAttn);
-        if (ok) {
-          uint32_t qw[16], ql[16];
-#pragma unroll
-          for (int c8 = 0; c8 < 4; ++c8) {
-            const uint32_t off = sw128_off(rl, kh * 32 + c8 * 8);
-            const uint4 vh = *reinterpret_cast<const uint4*>(sQh + off);
-            const uint4 vl = *reinterpret_cast<const uint4*>(sQl + off);
-            qw[4 * c8] = vh.x, qw[4 * c8 + 1] = vh.y, qw[4 * c8 + 2] = vh.z, qw[4 * c8 + 3] = vh.w;
-            ql[4 * c8] = vl.x, ql[4 * c8 + 1] = vl.y, ql[4 * c8 + 2] = vl.z, ql[4 * c8 + 3] = vl.w;
-          }
-          tmem_st16(tmem_base + lanebase + TcCols<HD>::Q + (uint32_t)(kh * 16), qw);
-          tmem_st16(tmem_base + lanebase + TcCols<HD>::Q + HD / 2 + (uint32_t)(kh * 16), ql);
-          tmem_wait_st();
-        }
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(qtm);
-      }
-    }
     for (int j = 0; j < ntile && ok; ++j) {
       const int b = j & 1;
       if (!mbar_wait(&sready[b], (j >> 1) & 1, a.err, kDevTimeoutAttn)) {
