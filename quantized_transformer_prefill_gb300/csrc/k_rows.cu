@@ -220,12 +220,16 @@ __device__ __forceinline__ void row_quant4_row(const RowQuantArgs& a, const int6
   const int nb = (int)(n >> 5);
   float* hrow = a.h + hr * n;
 
-  float4 x[PER4];
+  float4 x[PER4], w4[PER4];
 #pragma unroll
   for (int i = 0; i < PER4; ++i) {
     const int64_t c = tid + (int64_t)kRowThreads * i;
     const float4* src = reinterpret_cast<const float4*>(hrow + 4 * c);
     x[i] = c < nc ? (kCG ? __ldcg(src) : *src) : make_float4(0.f, 0.f, 0.f, 0.f);
+    // the norm weights load with the row, ahead of the stores of h (which the
+    // compiler cannot move them past)
+    w4[i] = (a.norm_w && c < nc) ? *reinterpret_cast<const float4*>(a.norm_w + 4 * c)
+                                 : make_float4(0.f, 0.f, 0.f, 0.f);
   }
   if (a.nsplit > 0) {
     float4 o[PER4];
@@ -303,9 +307,7 @@ __device__ __forceinline__ void row_quant4_row(const RowQuantArgs& a, const int6
     const bool in = c < nc;
     float y[4] = {x[i].x, x[i].y, x[i].z, x[i].w};
     if (a.norm_w) {
-      const float4 w4 = in ? *reinterpret_cast<const float4*>(a.norm_w + 4 * c)
-                           : make_float4(0.f, 0.f, 0.f, 0.f);
-      const float wv[4] = {w4.x, w4.y, w4.z, w4.w};
+      const float wv[4] = {w4[i].x, w4[i].y, w4[i].z, w4[i].w};
 #pragma unroll
       for (int e = 0; e < 4; ++e) y[e] = in ? __fmul_rn(__fmul_rn(y[e], scale), wv[e]) : 0.f;
     }
@@ -451,9 +453,11 @@ __device__ __forceinline__ void split2(float2 v, __half2& hi, __half2& lo) {
 
 __global__ void __launch_bounds__(1024, 2) rope_store_kernel(const RopeStoreArgs a) {
   pdl_trigger();
-  pdl_wait();
   const int t = blockIdx.x;
+  // the position is the call's input, written before any kernel: read while
+  // the previous kernel finishes, so the table rows load with the sums
   const int p_in = a.pos[t];
+  pdl_wait();
   // an out-of-range position is reported by validation; it only selects a
   // table row here (clamped) and never a region row
   const bool write_kv =
@@ -544,9 +548,9 @@ __global__ void __launch_bounds__(1024) rope_store_qknorm_kernel(const RopeStore
   extern __shared__ float xs[];  // [(nh + nkv) * hd]
   __shared__ float rs[kMaxQkHeads], rl[kMaxQkHeads];  // per head: (hi, lo) sum of squares, then the scale
   pdl_trigger();
-  pdl_wait();
   const int t = blockIdx.x;
-  const int p_in = a.pos[t];
+  const int p_in = a.pos[t];  // the call's input: read before the wait, as above
+  pdl_wait();
   const bool write_kv =
       status_clear(a.status) && p_in >= 0 && p_in < a.n_ctx;
   const int p = (p_in >= 0 && p_in < a.n_ctx) ? p_in : 0;
